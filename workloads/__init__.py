@@ -1,0 +1,164 @@
+"""Seeded synthetic inputs for the fused normalization + GEMM path.
+
+This module is data plumbing shared by the tests, the bench and the oracle
+checks.  It holds the workload table (shapes, epsilons, distributions) and the
+seeded generators, and none of the method's arithmetic: no norm, no matmul.
+
+Workloads (all bf16, row-major; "N(0, s)" means standard deviation s):
+
+* ``cfg1``  Lazy Pre-RMSNorm GEMM, no affine: A[256,512] rows N(0,1) times a
+  per-row scale log-uniform in [0.1, 10]; B[512,128] N(0, 1/sqrt(512));
+  eps 1e-6.
+* ``cfg2_n64`` / ``cfg2_n128``  GEMM + post-LayerNorm with affine:
+  A[16384,1024] N(0,1); B[1024,N] N(0,1/32); gamma 1+N(0,0.1); beta N(0,0.1);
+  eps 1e-5.
+* ``cfg3``  Lazy Pre-RMSNorm GEMM, LLM-shaped: A[8192,4096] N(0,1) times a
+  log-uniform row scale; B[4096,4096] N(0,1/64); eps 1e-6.
+* ``cfg4_n{1024,4096,8192}_{ln,rms}``  GEMM + post-norm over a cluster of CTAs
+  along N: A[16384,2048] N(0,1); B[2048,N] N(0,1/45); LayerNorm with gamma and
+  beta, or RMSNorm with gamma only; eps 1e-5.
+* ``cfg5``  pre-RMSNorm (eps 1e-6, no affine) and post-LayerNorm (gamma, beta,
+  eps 1e-5) in one kernel: A[65536,256] N(0,1) with 1% of rows (655 rows,
+  drawn without replacement) scaled by 100; B[256,256] N(0,1/16).
+
+Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
+float32 in the order A, row scale, outlier rows, B, gamma, beta, then rounded
+once to bf16 (round to nearest even) by ``torch.Tensor.to(torch.bfloat16)``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str                 # "prenorm" | "postnorm" | "gemm"
+    M: int
+    K: int
+    N: int
+    b_std: float
+    eps: float = 1e-5
+    norm: Optional[str] = None        # "layernorm" | "rmsnorm" (postnorm only)
+    gamma: bool = False
+    beta: bool = False
+    pre_rmsnorm: bool = False         # cfg5: pre-RMSNorm scale before the post-norm
+    pre_eps: float = 1e-6
+    a_row_scale: bool = False         # log-uniform [0.1, 10] per-row scale on A
+    a_outlier_frac: float = 0.0       # fraction of rows of A multiplied by 100
+    description: str = ""
+
+    def scaled(self, **kw) -> "Workload":
+        """Same distributions at other sizes (used by the small parity cases)."""
+        return replace(self, **kw)
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """A + B + C in bf16, plus gamma/beta and the fp32 row statistics."""
+        b = 2.0 * (self.M * self.K + self.K * self.N + self.M * self.N)
+        if self.gamma:
+            b += 2.0 * self.N
+        if self.beta:
+            b += 2.0 * self.N
+        nstats = 0
+        if self.kind == "prenorm":
+            nstats = 1
+        elif self.kind == "postnorm":
+            nstats = 2 if self.norm == "layernorm" else 1
+            if self.pre_rmsnorm:
+                nstats += 1
+        return b + 4.0 * self.M * nstats
+
+
+def _cfg4(n: int, norm: str) -> Workload:
+    return Workload(
+        name=f"cfg4_n{n}_{'ln' if norm == 'layernorm' else 'rms'}",
+        kind="postnorm", M=16384, K=2048, N=n, b_std=1.0 / 45.0, eps=1e-5,
+        norm=norm, gamma=True, beta=(norm == "layernorm"),
+        description=f"GEMM + post-{norm} over a CTA cluster along N, "
+                    f"A[16384,2048] @ B[2048,{n}]")
+
+
+WORKLOADS: dict[str, Workload] = {w.name: w for w in [
+    Workload("cfg1", "prenorm", M=256, K=512, N=128, b_std=1.0 / math.sqrt(512.0),
+             eps=1e-6, a_row_scale=True,
+             description="Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128]"),
+    Workload("cfg2_n64", "postnorm", M=16384, K=1024, N=64, b_std=1.0 / 32.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True,
+             description="GEMM + post-LayerNorm(affine), A[16384,1024] @ B[1024,64]"),
+    Workload("cfg2_n128", "postnorm", M=16384, K=1024, N=128, b_std=1.0 / 32.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True,
+             description="GEMM + post-LayerNorm(affine), A[16384,1024] @ B[1024,128]"),
+    Workload("cfg3", "prenorm", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-6,
+             a_row_scale=True,
+             description="Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096]"),
+    _cfg4(1024, "layernorm"), _cfg4(1024, "rmsnorm"),
+    _cfg4(4096, "layernorm"), _cfg4(4096, "rmsnorm"),
+    _cfg4(8192, "layernorm"), _cfg4(8192, "rmsnorm"),
+    Workload("cfg5", "postnorm", M=65536, K=256, N=256, b_std=1.0 / 16.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True, pre_rmsnorm=True, pre_eps=1e-6,
+             a_outlier_frac=0.01,
+             description="pre-RMSNorm + GEMM + post-LayerNorm(affine) in one kernel, "
+                         "A[65536,256] @ B[256,256]"),
+]}
+
+
+def outlier_rows(M: int, frac: float, rng: np.random.Generator) -> np.ndarray:
+    """floor(frac*M) distinct row indices, sorted."""
+    n = int(math.floor(frac * M))
+    if n == 0:
+        return np.zeros(0, dtype=np.int64)
+    return np.sort(rng.choice(M, size=n, replace=False)).astype(np.int64)
+
+
+def make_inputs(w: Workload, seed: int = 0) -> dict:
+    """CPU bf16 tensors A[M,K], B[K,N] and optional gamma[N], beta[N].
+
+    Also returns the drawn ``row_scale`` (float32, or None) and ``outliers``
+    (row indices) so tests can reason about the structure of A.
+    """
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((w.M, w.K), dtype=np.float32)
+    row_scale = None
+    if w.a_row_scale:
+        lo, hi = math.log(0.1), math.log(10.0)
+        row_scale = np.exp(rng.uniform(lo, hi, size=w.M)).astype(np.float32)
+        a *= row_scale[:, None]
+    outl = outlier_rows(w.M, w.a_outlier_frac, rng)
+    if outl.size:
+        a[outl] *= np.float32(100.0)
+    b = rng.standard_normal((w.K, w.N), dtype=np.float32) * np.float32(w.b_std)
+    gamma = beta = None
+    if w.gamma:
+        gamma = np.float32(1.0) + np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32)
+    if w.beta:
+        beta = np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32)
+
+    def bf16(x):
+        return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
+
+    return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta),
+            "row_scale": row_scale, "outliers": outl}
+
+
+def make_rows_inputs(w: Workload, rows: np.ndarray, seed: int = 0) -> dict:
+    """The full-size inputs restricted to ``rows`` of A (for sampled checks)."""
+    d = make_inputs(w, seed)
+    d["A"] = d["A"][torch.from_numpy(np.asarray(rows, dtype=np.int64))].contiguous()
+    return d
+
+
+def to_f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
+    """Exact widening of a bf16/fp32 CPU tensor to a float64 numpy array."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()
