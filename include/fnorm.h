@@ -1,0 +1,192 @@
+/*
+ * fnorm.h — C ABI of libfnorm: row normalization fused into a tcgen05 GEMM
+ * on GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [FNF-ru] "Free normalization fusion" (aixai.ru blog, Russian summary of
+ *            the PyTorch post "Towards Free Normalization").
+ *   [FNF-es] "PyTorch: normalización casi gratis fusionando kernels"
+ *            (noticias.mechatronicstore.cl).
+ *   [TFN]    "Towards Free Normalization: Fusing Normalization into GEMM and
+ *            Attention Kernels – PyTorch" (news.8syncdev.com abstract).
+ *   [ATB]    Ascend ATB RMSNorm-fusion article (gsyq.cn), sections 1.1-1.2
+ *            (textbook LayerNorm and RMSNorm definitions).
+ *
+ * Conventions shared by every entry point
+ *   - Matrices are row-major and contiguous.  A is [M,K], B is [K,N],
+ *     C is [M,N], X and Y are [M,N].  Element type is bfloat16, passed as its
+ *     16-bit storage (fnorm_bf16).  Accumulation is fp32; row statistics are
+ *     fp32 arrays of length M.
+ *   - Every pointer is DEVICE memory on the current CUDA device, owned by
+ *     the caller.  The library never frees, retains or allocates per call.
+ *     Base addresses of A, B, C, X and Y must be 16-byte aligned; gamma and
+ *     beta 2-byte aligned for fnorm_gemm_postnorm and 16-byte aligned for
+ *     fnorm_rmsnorm / fnorm_layernorm; fp32 statistic outputs 4-byte aligned.
+ *     A misaligned pointer is an argument error.
+ *   - Sizes: M >= 0 (M == 0 is a valid empty call that does nothing);
+ *     N >= 8 and K >= 8, both multiples of 8 (16-byte row pitch for the
+ *     tensor-memory-access engine); M, N, K < 2^31.
+ *   - eps > 0 and finite.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on that stream: no host synchronisation happens inside
+ *     them and they can be captured into a CUDA graph after the first call on
+ *     a device has returned (that first call loads the device code).
+ *   - A call returns FNORM_OK once its kernels are enqueued.  Argument errors
+ *     return FNORM_ERR_INVALID_ARG and launch nothing; shapes the kernels do
+ *     not implement return FNORM_ERR_UNSUPPORTED; CUDA launch errors return
+ *     FNORM_ERR_CUDA.  fnorm_last_error() then describes the failure.
+ *   - Every wait inside the kernels is bounded (fnorm_set_wait_limit_ns).  A
+ *     wait that runs out makes the kernel stop early and record a device
+ *     status word; fnorm_check_status() reports it as FNORM_ERR_TIMEOUT.
+ *   - NaN and Inf inputs are not supported (results are unspecified).
+ */
+#ifndef FNORM_H
+#define FNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fnorm_bf16;  /* bfloat16 storage */
+
+typedef enum {
+  FNORM_OK = 0,
+  FNORM_ERR_INVALID_ARG = 1,
+  FNORM_ERR_UNSUPPORTED = 2,
+  FNORM_ERR_CUDA = 3,
+  FNORM_ERR_TIMEOUT = 4
+} fnorm_status_t;
+
+typedef enum {
+  FNORM_RMSNORM = 0,
+  FNORM_LAYERNORM = 1
+} fnorm_norm_t;
+
+/*
+ * fnorm_gemm — C = A @ B, bf16 in and out, fp32 accumulate.
+ *   The plain tiled GEMM ([FNF-ru] "Why normalization is a performance
+ *   problem": the GEMM tiles over M and N, so no tile sees a whole row).  It
+ *   shares the tcgen05 mainloop with the fused kernels and is the GEMM half
+ *   of the unfused comparison.
+ */
+fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
+                          int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * fnorm_lazy_prenorm_gemm — C = rmsnorm(A) @ B, RMSNorm without affine,
+ * computed as (A @ B) * rstd(A).
+ *   [FNF-ru] "Lazy Pre-Norm"; [FNF-es] "Lazy Pre-Norm: el truco matemático".
+ *   rstd[m] = 1 / sqrt((1/K) * sum_k A[m,k]^2 + eps), summed in fp32 from the
+ *   A tiles already staged in shared memory while the tensor cores run, and
+ *   applied to the fp32 accumulator before the bf16 rounding of C.
+ *   rstd_out: [M] fp32 device array, or NULL to skip it.
+ *   There is deliberately no gamma/beta: a per-column affine does not commute
+ *   with the GEMM ([FNF-ru] "Lazy Pre-Norm" limits and FAQ).
+ */
+fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
+                                       int64_t M, int64_t N, int64_t K, float eps,
+                                       float* rstd_out, void* stream);
+
+/*
+ * fnorm_gemm_postnorm — C = norm(A @ B) * gamma + beta (epilogue post-norm).
+ *   [FNF-ru] "Multi-CTA Norm Fusion"; [FNF-es] "El problema del tiling";
+ *   definitions from [ATB] 1.1 (LayerNorm, biased variance) and 1.2 (RMSNorm).
+ *   The norm is taken over the fp32 accumulator of each row.  When N is wider
+ *   than one CTA's tile, the CTAs of a thread-block cluster that share a
+ *   128-row block split the row along N, exchange per-row partial statistics
+ *   through distributed shared memory and each normalises its own slice.
+ *   norm:        FNORM_LAYERNORM or FNORM_RMSNORM.
+ *   gamma, beta: [N] bf16 device arrays, or NULL (gamma = 1, beta = 0).
+ *   eps:         epsilon of the post-norm, inside the square root.
+ *   pre_rmsnorm: 0 or 1.  With 1 the kernel first applies a lazy pre-RMSNorm
+ *                of A without affine (epsilon pre_eps), i.e. it computes
+ *                norm(rmsnorm(A) @ B) in one kernel; pre_eps is ignored with 0.
+ *   mean_out:    [M] fp32, LayerNorm only (must be NULL for RMSNorm), or NULL.
+ *   rstd_out:    [M] fp32 rstd of the post-norm, or NULL.
+ *   pre_rstd_out:[M] fp32 rstd of the pre-norm (pre_rmsnorm == 1 only), or NULL.
+ *   N up to 8192 (FNORM_ERR_UNSUPPORTED beyond).
+ */
+fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
+                                   int64_t M, int64_t N, int64_t K, fnorm_norm_t norm,
+                                   const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                   int pre_rmsnorm, float pre_eps,
+                                   float* mean_out, float* rstd_out, float* pre_rstd_out,
+                                   void* stream);
+
+/*
+ * fnorm_rmsnorm — standalone row RMSNorm, Y = X / sqrt(mean(X^2) + eps) * gamma.
+ *   [ATB] 1.2.  The unfused comparison kernel ([FNF-ru] FAQ: a standalone norm
+ *   stays memory-bound however well it is written).  gamma: [N] or NULL.
+ *   rstd_out: [M] fp32 or NULL.
+ */
+fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N,
+                             const fnorm_bf16* gamma, float eps, float* rstd_out, void* stream);
+
+/*
+ * fnorm_layernorm — standalone row LayerNorm,
+ *   Y = (X - mean) / sqrt(var + eps) * gamma + beta, biased variance ([ATB] 1.1).
+ *   gamma, beta: [N] or NULL.  mean_out, rstd_out: [M] fp32 or NULL.
+ */
+fnorm_status_t fnorm_layernorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N,
+                               const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                               float* mean_out, float* rstd_out, void* stream);
+
+/*
+ * fnorm_check_status — synchronise `stream`, then read and clear the device
+ * status word of the current device.  Returns FNORM_ERR_TIMEOUT if a kernel
+ * gave up on a bounded wait since the last check, FNORM_ERR_CUDA if the
+ * stream reported an error, else FNORM_OK.
+ */
+fnorm_status_t fnorm_check_status(void* stream);
+
+/*
+ * fnorm_last_error — message describing the last failing call on this host
+ * thread ("" if none).  The pointer stays valid until the next call on the
+ * same thread.
+ */
+const char* fnorm_last_error(void);
+
+/*
+ * fnorm_set_wait_limit_ns — upper bound, in nanoseconds of GPU global time,
+ * on every wait inside the kernels launched after this call (process-wide;
+ * default 2e9 = 2 s).  0 restores the default.
+ */
+fnorm_status_t fnorm_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * fnorm_postnorm_plan — how fnorm_gemm_postnorm splits a row of width N:
+ * *cluster receives the CTAs per cluster along N and *cols_per_cta the
+ * columns each CTA owns (a multiple of 64).  Returns FNORM_ERR_UNSUPPORTED if
+ * N is too wide.  Host only; launches nothing.
+ */
+fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta);
+
+/*
+ * fnorm_set_postnorm_cluster — force the cluster size used by
+ * fnorm_gemm_postnorm (1, 2, 4, 8 or 16; 0 = automatic, the default).  A
+ * testing and tuning knob: results agree across cluster sizes up to fp32
+ * summation order.  Process-wide.  A forced size that cannot hold the row
+ * makes later calls return FNORM_ERR_UNSUPPORTED.
+ */
+fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size);
+
+/*
+ * fnorm_debug_wait_timeout — failure-detection self test.  Launches one small
+ * kernel that waits, with a bound of limit_ns, on a barrier that nothing
+ * arrives on; the wait runs out, the kernel records a timeout in the device
+ * status word and returns.  fnorm_check_status(stream) then returns
+ * FNORM_ERR_TIMEOUT and the CUDA context stays usable.  limit_ns is clamped
+ * to [1e3, 1e10].
+ */
+fnorm_status_t fnorm_debug_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fnorm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FNORM_H */

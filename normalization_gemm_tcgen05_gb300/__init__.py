@@ -1,0 +1,283 @@
+"""Row normalization fused into a tcgen05 GEMM on GB300 (sm_103a).
+
+Thin Python binding of ``libfnorm.so`` (C ABI: ``include/fnorm.h``).  The
+functions here only marshal arguments: they check dtypes and shapes, allocate
+outputs with PyTorch and pass raw device pointers and the current CUDA stream
+to the library.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback of any kind, and a missing or unloadable library
+raises ``FnormError``.
+
+Forms (see the header for the full contract):
+
+* ``gemm(A, B)``                      C = A @ B
+* ``lazy_prenorm_gemm(A, B, eps)``    C = rmsnorm(A) @ B = (A @ B) * rstd(A)
+* ``gemm_postnorm(A, B, norm, ...)``  C = norm(A @ B) * gamma + beta, optionally
+  norm(rmsnorm(A) @ B); rows wider than one CTA tile are split over a cluster
+* ``rmsnorm(X)`` / ``layernorm(X)``   standalone row norms (unfused comparison)
+
+``lib()`` returns the ctypes handle with every entry point declared, for
+callers that want the raw C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "gemm_postnorm", "rmsnorm",
+    "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
+    "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfnorm.so")
+
+RMSNORM = 0
+LAYERNORM = 1
+_NORMS = {"rmsnorm": RMSNORM, "layernorm": LAYERNORM, RMSNORM: RMSNORM, LAYERNORM: LAYERNORM}
+
+OK, INVALID_ARG, UNSUPPORTED, CUDA_ERROR, TIMEOUT = 0, 1, 2, 3, 4
+_STATUS = {0: "FNORM_OK", 1: "FNORM_ERR_INVALID_ARG", 2: "FNORM_ERR_UNSUPPORTED", 3: "FNORM_ERR_CUDA",
+           4: "FNORM_ERR_TIMEOUT"}
+
+
+class FnormError(RuntimeError):
+    """A libfnorm call failed; ``status`` holds the fnorm_status_t code."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_c_status = ctypes.c_int
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+
+# name -> (restype, argtypes); the C ABI of include/fnorm.h
+_SIGNATURES = {
+    "fnorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _p]),
+    "fnorm_lazy_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _f32, _p, _p]),
+    "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
+                                        ctypes.c_int, _f32, _p, _p, _p, _p]),
+    "fnorm_rmsnorm": (_c_status, [_p, _p, _i64, _i64, _p, _f32, _p, _p]),
+    "fnorm_layernorm": (_c_status, [_p, _p, _i64, _i64, _p, _p, _f32, _p, _p, _p]),
+    "fnorm_check_status": (_c_status, [_p]),
+    "fnorm_last_error": (ctypes.c_char_p, []),
+    "fnorm_set_wait_limit_ns": (_c_status, [ctypes.c_uint64]),
+    "fnorm_postnorm_plan": (_c_status, [_i64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "fnorm_set_postnorm_cluster": (_c_status, [ctypes.c_int]),
+    "fnorm_debug_wait_timeout": (_c_status, [ctypes.c_uint64, _p]),
+    "fnorm_version": (ctypes.c_int, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfnorm.so (once) and declare its entry points."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FnormError(CUDA_ERROR, f"{LIB_PATH} is not built; build it with "
+                                         "`python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def last_error() -> str:
+    msg = lib().fnorm_last_error()
+    return msg.decode() if msg else ""
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise FnormError(status, last_error())
+
+
+def version() -> int:
+    return lib().fnorm_version()
+
+
+# --------------------------------------------------------------------------
+# argument marshalling
+# --------------------------------------------------------------------------
+def _mat(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16 (got {t.dtype})")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (got shape {tuple(t.shape)})")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    return t
+
+
+def _vec(t: Optional[torch.Tensor], n: int, name: str, device) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.dtype != torch.bfloat16 or t.dim() != 1 or t.numel() != n:
+        raise ValueError(f"{name} must be a bfloat16 vector of length {n}")
+    if not t.is_cuda or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor on {device}")
+    return t
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _out(out: Optional[torch.Tensor], shape, device, name="out") -> torch.Tensor:
+    if out is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    _mat(out, name)
+    if tuple(out.shape) != tuple(shape) or out.device != device:
+        raise ValueError(f"{name} must have shape {tuple(shape)} on {device}")
+    return out
+
+
+def _stat(M: int, device) -> torch.Tensor:
+    return torch.empty(M, dtype=torch.float32, device=device)
+
+
+def _ab(A, B):
+    _mat(A, "A")
+    _mat(B, "B")
+    if A.shape[1] != B.shape[0]:
+        raise ValueError(f"inner dimensions differ: A {tuple(A.shape)} @ B {tuple(B.shape)}")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+    return A.shape[0], B.shape[1], A.shape[1]
+
+
+# --------------------------------------------------------------------------
+# public functions
+# --------------------------------------------------------------------------
+def gemm(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """C = A @ B (bf16 in/out, fp32 accumulate) on the tcgen05 mainloop."""
+    M, N, K = _ab(A, B)
+    C = _out(out, (M, N), A.device)
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(A.device)))
+    return C
+
+
+def lazy_prenorm_gemm(A: torch.Tensor, B: torch.Tensor, eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+                      return_rstd: bool = False):
+    """C = rmsnorm(A) @ B (RMSNorm without affine) computed as (A @ B) * rstd(A).
+
+    With ``return_rstd`` also returns the fp32 rstd[M] of the rows of A.
+    """
+    M, N, K = _ab(A, B)
+    C = _out(out, (M, N), A.device)
+    rstd = _stat(M, A.device) if return_rstd else None
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_lazy_prenorm_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, float(eps), _ptr(rstd),
+                                             _stream(A.device)))
+    return (C, rstd) if return_rstd else C
+
+
+def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Optional[torch.Tensor] = None,
+                  beta: Optional[torch.Tensor] = None, eps: float = 1e-5, pre_rmsnorm: bool = False,
+                  pre_eps: float = 1e-6, out: Optional[torch.Tensor] = None, return_stats: bool = False):
+    """C = norm(A @ B) * gamma + beta, or norm(rmsnorm(A) @ B) * gamma + beta.
+
+    ``norm`` is "layernorm" or "rmsnorm".  With ``return_stats`` also returns a
+    dict of fp32 [M] tensors: "rstd", "mean" (LayerNorm) and "pre_rstd"
+    (``pre_rmsnorm``).
+    """
+    M, N, K = _ab(A, B)
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    nid = _NORMS[norm]
+    gamma = _vec(gamma, N, "gamma", A.device)
+    beta = _vec(beta, N, "beta", A.device)
+    C = _out(out, (M, N), A.device)
+    stats = {}
+    if return_stats:
+        stats["rstd"] = _stat(M, A.device)
+        stats["mean"] = _stat(M, A.device) if nid == LAYERNORM else None
+        stats["pre_rstd"] = _stat(M, A.device) if pre_rmsnorm else None
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_gemm_postnorm(
+            _ptr(A), _ptr(B), _ptr(C), M, N, K, nid, _ptr(gamma), _ptr(beta), float(eps),
+            1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
+            _ptr(stats.get("pre_rstd")), _stream(A.device)))
+    return (C, stats) if return_stats else C
+
+
+def rmsnorm(X: torch.Tensor, gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
+            out: Optional[torch.Tensor] = None, return_rstd: bool = False):
+    """Standalone row RMSNorm (the unfused comparison kernel)."""
+    _mat(X, "X")
+    M, N = X.shape
+    gamma = _vec(gamma, N, "gamma", X.device)
+    Y = _out(out, (M, N), X.device)
+    rstd = _stat(M, X.device) if return_rstd else None
+    with torch.cuda.device(X.device):
+        _check(lib().fnorm_rmsnorm(_ptr(X), _ptr(Y), M, N, _ptr(gamma), float(eps), _ptr(rstd),
+                                   _stream(X.device)))
+    return (Y, rstd) if return_rstd else Y
+
+
+def layernorm(X: torch.Tensor, gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None,
+              eps: float = 1e-5, out: Optional[torch.Tensor] = None, return_stats: bool = False):
+    """Standalone row LayerNorm (the unfused comparison kernel)."""
+    _mat(X, "X")
+    M, N = X.shape
+    gamma = _vec(gamma, N, "gamma", X.device)
+    beta = _vec(beta, N, "beta", X.device)
+    Y = _out(out, (M, N), X.device)
+    mean = _stat(M, X.device) if return_stats else None
+    rstd = _stat(M, X.device) if return_stats else None
+    with torch.cuda.device(X.device):
+        _check(lib().fnorm_layernorm(_ptr(X), _ptr(Y), M, N, _ptr(gamma), _ptr(beta), float(eps), _ptr(mean),
+                                     _ptr(rstd), _stream(X.device)))
+    return (Y, {"mean": mean, "rstd": rstd}) if return_stats else Y
+
+
+def check_status(device=None) -> None:
+    """Synchronise the current stream and raise FnormError if a kernel timed out."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().fnorm_check_status(_stream(dev)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _check(lib().fnorm_set_wait_limit_ns(int(ns)))
+
+
+def postnorm_plan(N: int) -> tuple[int, int]:
+    """(CTAs per cluster along N, columns per CTA) used by gemm_postnorm for width N."""
+    c = ctypes.c_int(0)
+    w = ctypes.c_int(0)
+    _check(lib().fnorm_postnorm_plan(int(N), ctypes.byref(c), ctypes.byref(w)))
+    return c.value, w.value
+
+
+def set_postnorm_cluster(cluster_size: int) -> None:
+    """Force the post-norm cluster size (0 = automatic)."""
+    _check(lib().fnorm_set_postnorm_cluster(int(cluster_size)))
+
+
+def debug_wait_timeout(limit_ns: int = 50_000_000, device=None) -> None:
+    """Launch the bounded-wait self test (see fnorm_debug_wait_timeout)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().fnorm_debug_wait_timeout(int(limit_ns), _stream(dev)))

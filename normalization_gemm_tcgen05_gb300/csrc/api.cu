@@ -1,0 +1,273 @@
+// api.cu — the extern "C" entry points of libfnorm (declared in
+// include/fnorm.h): argument validation, the plan (tile widths, cluster size)
+// and dispatch to the kernels.  No entry point allocates memory or
+// synchronises the host, except fnorm_check_status, whose job is to.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "fused_gemm.cuh"
+#include "internal.h"
+
+namespace fnorm {
+const char* last_error_cstr();
+void clear_error();
+void set_wait_limit(uint64_t ns);
+fnorm_status_t read_and_clear_status(cudaStream_t stream);
+
+namespace {
+std::atomic<int> g_forced_cluster{0};
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+
+fnorm_status_t bad(const char* msg) {
+  set_error("%s", msg);
+  return FNORM_ERR_INVALID_ARG;
+}
+
+fnorm_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || M > kMaxDim) return bad("M must be in [0, 2^31)");
+  if (N < 8 || N > kMaxDim || N % 8 != 0) return bad("N must be a multiple of 8 in [8, 2^31)");
+  if (K < 8 || K > kMaxDim || K % 8 != 0) return bad("K must be a multiple of 8 in [8, 2^31)");
+  return FNORM_OK;
+}
+
+fnorm_status_t check_eps(float eps, const char* name) {
+  if (!(eps > 0.0f) || !std::isfinite(eps)) {
+    set_error("%s must be finite and > 0", name);
+    return FNORM_ERR_INVALID_ARG;
+  }
+  return FNORM_OK;
+}
+
+fnorm_status_t check_ptr(const void* p, const char* name, uintptr_t align, bool optional) {
+  if (p == nullptr) {
+    if (optional) return FNORM_OK;
+    set_error("%s must not be NULL", name);
+    return FNORM_ERR_INVALID_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(p) % align != 0) {
+    set_error("%s must be %u-byte aligned", name, (unsigned)align);
+    return FNORM_ERR_INVALID_ARG;
+  }
+  return FNORM_OK;
+}
+
+#define FN_TRY(expr)                      \
+  do {                                    \
+    fnorm_status_t s_ = (expr);           \
+    if (s_ != FNORM_OK) return s_;        \
+  } while (0)
+
+int round64(int64_t x) { return static_cast<int>((x + 63) / 64 * 64); }
+
+int gemm_tile_n(int64_t N) { return N <= 64 ? 64 : (N <= 128 ? 128 : 256); }
+
+// How a post-norm row of width N is split: cluster size, subtile width and
+// subtiles per CTA.  Automatic plans prefer one accumulator subtile per CTA
+// (tensor memory double buffered, so a tile's epilogue overlaps the next
+// tile's MMAs) on clusters of up to 8, then two 256-column subtiles per CTA on
+// clusters of 8 or 16.  Returns FNORM_ERR_UNSUPPORTED when nothing holds N.
+fnorm_status_t plan_postnorm(int64_t N, int forced, int* cluster, int* bn_sub, int* nsub) {
+  auto one_sub = [&](int c) -> bool {
+    const int64_t w = (N + c - 1) / c;  // columns per CTA
+    if (w > 256 || c > 8) return false;
+    *cluster = c;
+    *bn_sub = (c == 1) ? round64(w) : (w <= 128 ? 128 : 256);
+    *nsub = 1;
+    return true;
+  };
+  auto two_sub = [&](int c) -> bool {
+    const int64_t w = (N + c - 1) / c;
+    if (w > 512 || c < 2) return false;
+    *cluster = c, *bn_sub = 256, *nsub = 2;
+    return true;
+  };
+  if (forced != 0) {
+    if (one_sub(forced) || two_sub(forced)) return FNORM_OK;
+    set_error("a row of %lld columns does not fit a forced cluster of %d CTAs", (long long)N, forced);
+    return FNORM_ERR_UNSUPPORTED;
+  }
+  for (int c : {1, 2, 4, 8})
+    if (one_sub(c)) return FNORM_OK;
+  for (int c : {8, 16})
+    if (two_sub(c)) return FNORM_OK;
+  set_error("post-norm rows are limited to 8192 columns (got %lld)", (long long)N);
+  return FNORM_ERR_UNSUPPORTED;
+}
+
+FusedLaunch base_launch(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, void* stream) {
+  FusedLaunch L{};
+  L.A = A;
+  L.B = B;
+  L.C = C;
+  L.M = static_cast<int>(M);
+  L.N = static_cast<int>(N);
+  L.K = static_cast<int>(K);
+  L.nsub = 1;
+  L.cluster = 1;
+  L.eps = 1.0f;
+  L.pre_eps = 1.0f;
+  L.stream = static_cast<cudaStream_t>(stream);
+  return L;
+}
+
+}  // namespace
+
+int forced_postnorm_cluster() { return g_forced_cluster.load(std::memory_order_relaxed); }
+
+}  // namespace fnorm
+
+using namespace fnorm;
+
+extern "C" {
+
+fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M, int64_t N,
+                          int64_t K, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  L.mode = 0;
+  L.bn_sub = gemm_tile_n(N);
+  return launch_fused_plain(L);
+}
+
+fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
+                                       int64_t N, int64_t K, float eps, float* rstd_out, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  FN_TRY(check_eps(eps, "eps"));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  L.mode = MODE_PRE;
+  L.bn_sub = gemm_tile_n(N);
+  L.pre_eps = eps;
+  L.rstd_out = rstd_out;
+  return launch_fused_plain(L);
+}
+
+fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
+                                   int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                   const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
+                                   float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  if (pre_rmsnorm != 0 && pre_rmsnorm != 1) return bad("pre_rmsnorm must be 0 or 1");
+  FN_TRY(check_eps(eps, "eps"));
+  if (pre_rmsnorm) FN_TRY(check_eps(pre_eps, "pre_eps"));
+  if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
+  if (!pre_rmsnorm && pre_rstd_out != nullptr) return bad("pre_rstd_out needs pre_rmsnorm = 1");
+  int cluster = 1, bn_sub = 64, nsub = 1;
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &cluster, &bn_sub, &nsub));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 2, true));
+  FN_TRY(check_ptr(beta, "beta", 2, true));
+  FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  FN_TRY(check_ptr(pre_rstd_out, "pre_rstd_out", 4, true));
+  FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  L.mode = MODE_POST | (norm == FNORM_LAYERNORM ? MODE_LN : 0) | (pre_rmsnorm ? MODE_PRE : 0);
+  L.bn_sub = bn_sub;
+  L.nsub = nsub;
+  L.cluster = cluster;
+  L.eps = eps;
+  L.pre_eps = pre_rmsnorm ? pre_eps : 1.0f;
+  L.gamma = gamma;
+  L.beta = beta;
+  L.mean_out = mean_out;
+  L.rstd_out = rstd_out;
+  L.pre_rstd_out = pre_rstd_out;
+  return cluster == 1 ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
+}
+
+fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
+                             float eps, float* rstd_out, void* stream) {
+  clear_error();
+  if (M < 0 || M > kMaxDim) return bad("M must be in [0, 2^31)");
+  if (N < 8 || N % 8 != 0 || N > 32768) return bad("N must be a multiple of 8 in [8, 32768]");
+  FN_TRY(check_eps(eps, "eps"));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(X, "X", 16, false));
+  FN_TRY(check_ptr(Y, "Y", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  return launch_rownorm(X, Y, static_cast<int>(M), static_cast<int>(N), false, gamma, nullptr, eps, nullptr,
+                        rstd_out, static_cast<cudaStream_t>(stream));
+}
+
+fnorm_status_t fnorm_layernorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
+                               const fnorm_bf16* beta, float eps, float* mean_out, float* rstd_out,
+                               void* stream) {
+  clear_error();
+  if (M < 0 || M > kMaxDim) return bad("M must be in [0, 2^31)");
+  if (N < 8 || N % 8 != 0 || N > 32768) return bad("N must be a multiple of 8 in [8, 32768]");
+  FN_TRY(check_eps(eps, "eps"));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(X, "X", 16, false));
+  FN_TRY(check_ptr(Y, "Y", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
+  FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  return launch_rownorm(X, Y, static_cast<int>(M), static_cast<int>(N), true, gamma, beta, eps, mean_out,
+                        rstd_out, static_cast<cudaStream_t>(stream));
+}
+
+fnorm_status_t fnorm_check_status(void* stream) {
+  clear_error();
+  return read_and_clear_status(static_cast<cudaStream_t>(stream));
+}
+
+const char* fnorm_last_error(void) { return last_error_cstr(); }
+
+fnorm_status_t fnorm_set_wait_limit_ns(uint64_t ns) {
+  clear_error();
+  if (ns == 0) ns = 2000000000ull;
+  if (ns < 1000ull) ns = 1000ull;
+  if (ns > 60000000000ull) ns = 60000000000ull;
+  set_wait_limit(ns);
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta) {
+  clear_error();
+  if (cluster == nullptr || cols_per_cta == nullptr) return bad("output pointers must not be NULL");
+  if (N < 8 || N > kMaxDim || N % 8 != 0) return bad("N must be a multiple of 8 in [8, 2^31)");
+  int c = 1, bn = 64, ns = 1;
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &c, &bn, &ns));
+  *cluster = c;
+  *cols_per_cta = bn * ns;
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size) {
+  clear_error();
+  if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 &&
+      cluster_size != 16)
+    return bad("cluster size must be 0 (automatic), 1, 2, 4, 8 or 16");
+  g_forced_cluster.store(cluster_size, std::memory_order_relaxed);
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_debug_wait_timeout(uint64_t limit_ns, void* stream) {
+  clear_error();
+  if (limit_ns < 1000ull) limit_ns = 1000ull;
+  if (limit_ns > 10000000000ull) limit_ns = 10000000000ull;
+  return launch_wait_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+int fnorm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// internal.h — host-side declarations shared by the translation units of
+// libfnorm (not part of the public C ABI, which is include/fnorm.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fnorm.h"
+
+namespace fnorm {
+
+// thread-local error message (returned by fnorm_last_error)
+void set_error(const char* fmt, ...);
+fnorm_status_t cuda_fail(cudaError_t e, const char* what);
+
+struct DeviceInfo {
+  int id;
+  int num_sms;
+  uint32_t* status;  // device status word of this device
+};
+
+// Properties of the current device, cached per device.  The first call on a
+// device also resolves the address of its status word.
+fnorm_status_t current_device(DeviceInfo* out);
+
+uint64_t wait_limit_ns();
+int forced_postnorm_cluster();
+
+// 2-D row-major bf16 tensor map: `inner` elements per row (contiguous),
+// `outer` rows, `pitch_bytes` between rows; box of box_inner x box_outer.
+fnorm_status_t encode_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                                   uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                                   CUtensorMapSwizzle swizzle);
+
+struct FusedLaunch {
+  const void* A;
+  const void* B;
+  void* C;
+  int M, N, K;
+  int mode;     // MODE_* bits of fused_gemm.cuh (cluster bits are set by the planner)
+  int bn_sub;   // UMMA N of one accumulator subtile (64..256, multiple of 64)
+  int nsub;     // accumulator subtiles per CTA tile (1 or 2)
+  int cluster;  // CTAs per cluster along N (post-norm), else 1
+  float eps, pre_eps;
+  const void* gamma;
+  const void* beta;
+  float* mean_out;
+  float* rstd_out;
+  float* pre_rstd_out;
+  cudaStream_t stream;
+};
+
+// instantiation sets (one translation unit each)
+fnorm_status_t launch_fused_plain(const FusedLaunch& L);          // GEMM, Lazy Pre-Norm
+fnorm_status_t launch_fused_post_single(const FusedLaunch& L);    // post-norm, one CTA per row block
+fnorm_status_t launch_fused_post_cluster(const FusedLaunch& L);   // post-norm over a cluster
+
+fnorm_status_t launch_rownorm(const void* X, void* Y, int M, int N, bool layernorm, const void* gamma,
+                              const void* beta, float eps, float* mean_out, float* rstd_out,
+                              cudaStream_t stream);
+
+fnorm_status_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fnorm

@@ -8,3 +8,11 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests need the in-tree library; build it once if it is missing
+    if any(item.get_closest_marker("gpu") for item in items):
+        from normalization_gemm_tcgen05_gb300 import build as _b
+        if not os.path.exists(_b.LIB_PATH):
+            _b.build()

@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute launched).
+
+* libfnorm.so loads and exports every function include/fnorm.h declares;
+* argument validation returns FNORM_ERR_INVALID_ARG / FNORM_ERR_UNSUPPORTED
+  before touching the device (fake non-NULL pointers are never dereferenced);
+* the post-norm planner's cluster choices.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    import normalization_gemm_tcgen05_gb300 as fn
+    return fn.lib()
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "fnorm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fnorm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _header_functions()
+    for required in ("fnorm_gemm", "fnorm_lazy_prenorm_gemm", "fnorm_gemm_postnorm", "fnorm_rmsnorm",
+                     "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import normalization_gemm_tcgen05_gb300 as fn
+    names = _header_functions()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in fnorm.h but not exported"
+    assert sorted(fn.EXPORTED_SYMBOLS) == names, "binding and header disagree"
+    assert L.fnorm_version() == 100
+
+
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("M,N,K", [(-1, 64, 64), (128, 60, 64), (128, 64, 60), (128, 0, 64), (128, 64, 0),
+                                   (1 << 31, 64, 64)])
+def test_gemm_rejects_bad_sizes(L, M, N, K):
+    assert L.fnorm_gemm(FAKE, FAKE, FAKE, M, N, K, None) == 1
+    assert L.fnorm_last_error()
+
+
+def test_gemm_rejects_null_and_misaligned(L):
+    assert L.fnorm_gemm(None, FAKE, FAKE, 128, 64, 64, None) == 1
+    assert b"A" in L.fnorm_last_error()
+    assert L.fnorm_gemm(FAKE, ctypes.c_void_p(0x10008), FAKE, 128, 64, 64, None) == 1
+    assert b"aligned" in L.fnorm_last_error()
+
+
+def test_prenorm_rejects_bad_eps(L):
+    for eps in (0.0, -1.0, float("inf"), float("nan")):
+        assert L.fnorm_lazy_prenorm_gemm(FAKE, FAKE, FAKE, 128, 64, 64, eps, None, None) == 1
+
+
+def test_postnorm_argument_rules(L):
+    f = L.fnorm_gemm_postnorm
+    # unknown norm
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 7, None, None, 1e-5, 0, 1e-6, None, None, None, None) == 1
+    # mean_out with RMSNorm
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 0, None, None, 1e-5, 0, 1e-6, FAKE, None, None, None) == 1
+    # pre_rstd_out without the pre-norm
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, FAKE, None) == 1
+    # pre_rmsnorm flag out of range and a bad pre_eps
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, 2, 1e-6, None, None, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, 1, 0.0, None, None, None, None) == 1
+    # rows wider than any plan
+    assert f(FAKE, FAKE, FAKE, 128, 16384, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None, None) == 2
+
+
+def test_norm_rejects_bad_sizes(L):
+    assert L.fnorm_rmsnorm(FAKE, FAKE, 16, 12, None, 1e-6, None, None) == 1
+    assert L.fnorm_layernorm(FAKE, FAKE, 16, 65536, None, None, 1e-5, None, None, None) == 1
+    assert L.fnorm_layernorm(FAKE, FAKE, 16, 64, ctypes.c_void_p(0x10002), None, 1e-5, None, None, None) == 1
+
+
+@pytest.mark.parametrize("N,cluster,cols", [(8, 1, 64), (64, 1, 64), (128, 1, 128), (200, 1, 256), (256, 1, 256),
+                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (2048, 8, 256),
+                                            (3000, 8, 512), (4096, 8, 512), (8192, 16, 512)])
+def test_postnorm_plan(L, N, cluster, cols):
+    import normalization_gemm_tcgen05_gb300 as fn
+    assert fn.postnorm_plan(N) == (cluster, cols)
+
+
+def test_forced_cluster(L):
+    import normalization_gemm_tcgen05_gb300 as fn
+    try:
+        fn.set_postnorm_cluster(8)
+        assert fn.postnorm_plan(1024) == (8, 128)
+        fn.set_postnorm_cluster(16)
+        assert fn.postnorm_plan(1024) == (16, 512)
+        fn.set_postnorm_cluster(1)
+        with pytest.raises(fn.FnormError):
+            fn.postnorm_plan(1024)
+        with pytest.raises(fn.FnormError):
+            fn.set_postnorm_cluster(3)
+    finally:
+        fn.set_postnorm_cluster(0)
+    assert fn.postnorm_plan(1024) == (4, 256)
+
+
+def test_wait_limit_setter(L):
+    assert L.fnorm_set_wait_limit_ns(0) == 0
+    assert L.fnorm_set_wait_limit_ns(5_000_000) == 0
+    assert L.fnorm_set_wait_limit_ns(0) == 0
+
+
+def test_product_path_has_no_fallback():
+    # the binding must fail loudly when the library cannot be loaded
+    import normalization_gemm_tcgen05_gb300 as fn
+    src = open(fn.__file__).read()
+    assert "oracle" not in src.replace("no fallback", "")
+    saved = fn._lib, fn.LIB_PATH
+    try:
+        fn._lib = None
+        fn.LIB_PATH = os.path.join(ROOT, "does-not-exist.so")
+        with pytest.raises(fn.FnormError):
+            fn.lib()
+    finally:
+        fn._lib, fn.LIB_PATH = saved

@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA path (through the C ABI binding) against the fp64 oracle.
+
+Small cases the oracle finishes in seconds, spanning several tiles, ragged
+tails in M, N and K, every post-norm cluster plan, the degenerate rows of the
+method (zero rows, constant rows, outlier rows) and empty inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normalization_gemm_tcgen05_gb300 as fn
+import oracle
+from gpu_util import assert_mean_close, assert_out_close, assert_rstd_close, np64
+from workloads import WORKLOADS, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _case(base: str, seed: int, **kw):
+    w = WORKLOADS[base].scaled(**kw)
+    return w, make_inputs(w, seed)
+
+
+def _dev(t):
+    return None if t is None else t.to(DEV)
+
+
+# ----------------------------------------------------------------------------
+# plain GEMM (the unfused comparison's GEMM half, same mainloop)
+# ----------------------------------------------------------------------------
+GEMM_SHAPES = [(128, 64, 64), (256, 128, 512), (200, 136, 72), (300, 256, 1000), (129, 320, 64),
+               (1, 8, 8), (513, 520, 264), (384, 1024, 2048), (1000, 4096, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES, ids=lambda v: str(v))
+def test_gemm(M, N, K):
+    w, d = _case("cfg3", M * 7 + N, M=M, N=N, K=K, b_std=1.0 / np.sqrt(K), a_row_scale=False)
+    C = fn.gemm(_dev(d["A"]), _dev(d["B"]))
+    assert_out_close(C, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])), f"gemm {M}x{N}x{K}")
+    fn.check_status(DEV)
+
+
+def test_gemm_identity_B():
+    # B = I: C must reproduce A exactly (every product is exact in fp32)
+    w, d = _case("cfg3", 3, M=256, N=192, K=192, a_row_scale=False)
+    eye = torch.eye(192, dtype=torch.bfloat16)
+    C = fn.gemm(_dev(d["A"]), _dev(eye))
+    assert torch.equal(C.cpu(), d["A"]), "A @ I != A"
+
+
+# ----------------------------------------------------------------------------
+# Lazy Pre-RMSNorm GEMM
+# ----------------------------------------------------------------------------
+PRE_SHAPES = [(256, 128, 512), (200, 64, 72), (333, 256, 1024), (128, 520, 256), (1, 8, 8), (640, 4096, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", PRE_SHAPES, ids=lambda v: str(v))
+def test_lazy_prenorm(M, N, K):
+    w, d = _case("cfg1", M + 11 * K, M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    C, rstd = fn.lazy_prenorm_gemm(_dev(d["A"]), _dev(d["B"]), w.eps, return_rstd=True)
+    Cr, rr = oracle.lazy_prenorm_gemm(to_f64(d["A"]), to_f64(d["B"]), w.eps)
+    assert_out_close(C, Cr, "prenorm C")
+    assert_rstd_close(rstd, rr, "prenorm rstd")
+    fn.check_status(DEV)
+
+
+def test_lazy_prenorm_cfg1_exact_config():
+    w = WORKLOADS["cfg1"]
+    d = make_inputs(w, 0)
+    C, rstd = fn.lazy_prenorm_gemm(_dev(d["A"]), _dev(d["B"]), w.eps, return_rstd=True)
+    Cr, rr = oracle.lazy_prenorm_gemm(to_f64(d["A"]), to_f64(d["B"]), w.eps)
+    assert_out_close(C, Cr)
+    assert_rstd_close(rstd, rr)
+
+
+def test_lazy_prenorm_special_rows():
+    # zero row -> rstd = 1/sqrt(eps) and C row = 0; constant row c -> rstd = 1/sqrt(c^2 + eps)
+    w, d = _case("cfg1", 5, M=300, N=128, K=512)
+    A = d["A"].clone()
+    A[7] = 0
+    A[8] = 3.0
+    A[299] = -0.5
+    eps = 1e-2
+    C, rstd = fn.lazy_prenorm_gemm(_dev(A), _dev(d["B"]), eps, return_rstd=True)
+    Cr, rr = oracle.lazy_prenorm_gemm(to_f64(A), to_f64(d["B"]), eps)
+    assert_out_close(C, Cr)
+    assert_rstd_close(rstd, rr)
+    r = np64(rstd)
+    assert abs(r[7] - 1 / np.sqrt(eps)) <= 1e-4 / np.sqrt(eps)
+    assert abs(r[8] - 1 / np.sqrt(9 + eps)) <= 1e-4 / np.sqrt(9 + eps)
+    assert np.all(np64(C)[7] == 0)
+
+
+def test_lazy_prenorm_identity_B_is_rmsnorm():
+    # B = I reduces the fused form to the standalone RMSNorm (both kernels)
+    w, d = _case("cfg1", 6, M=256, N=256, K=256)
+    eye = torch.eye(256, dtype=torch.bfloat16)
+    C = fn.lazy_prenorm_gemm(_dev(d["A"]), _dev(eye), w.eps)
+    Y = fn.rmsnorm(_dev(d["A"]), None, w.eps)
+    ref, _ = oracle.rmsnorm(to_f64(d["A"]), None, None, w.eps)
+    assert_out_close(C, ref, "prenorm with B = I")
+    assert_out_close(Y, ref, "standalone rmsnorm")
+
+
+# ----------------------------------------------------------------------------
+# GEMM + post-norm, one CTA per row block (N <= 256)
+# ----------------------------------------------------------------------------
+POST1 = [("layernorm", 64), ("layernorm", 128), ("rmsnorm", 64), ("rmsnorm", 128), ("layernorm", 192),
+         ("layernorm", 256), ("rmsnorm", 256), ("layernorm", 200), ("rmsnorm", 8)]
+
+
+def _post(w, d, norm, pre=False, affine=True):
+    gamma = d["gamma"] if affine else None
+    beta = d["beta"] if (affine and norm == "layernorm") else None
+    C, st = fn.gemm_postnorm(_dev(d["A"]), _dev(d["B"]), norm, _dev(gamma), _dev(beta), w.eps,
+                             pre_rmsnorm=pre, pre_eps=w.pre_eps, return_stats=True)
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), norm, to_f64(gamma), to_f64(beta), w.eps,
+                               pre_rmsnorm=pre, pre_eps=w.pre_eps)
+    assert_out_close(C, ref["C"], f"post-{norm} C")
+    assert_rstd_close(st["rstd"], ref["rstd"], f"post-{norm} rstd")
+    if norm == "layernorm":
+        assert_mean_close(st["mean"], ref["mean"], ref["rstd"], "post-LN mean")
+    if pre:
+        assert_rstd_close(st["pre_rstd"], ref["pre_rstd"], "pre rstd")
+    fn.check_status(DEV)
+    return C, st
+
+
+@pytest.mark.parametrize("norm,N", POST1, ids=lambda v: str(v))
+def test_postnorm_single_cta(norm, N):
+    w, d = _case("cfg2_n64", N + 3, M=1000, N=N, K=1024)
+    assert fn.postnorm_plan(N)[0] == 1
+    _post(w, d, norm)
+
+
+def test_postnorm_no_affine_and_ragged_K():
+    w, d = _case("cfg2_n128", 9, M=257, N=128, K=200)
+    _post(w, d, "layernorm", affine=False)
+    _post(w, d, "rmsnorm", affine=False)
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_pre_and_post_in_one_kernel(norm):
+    w, d = _case("cfg5", 12, M=1500)
+    assert d["outliers"].size == 15
+    _post(w, d, norm, pre=True)
+
+
+# ----------------------------------------------------------------------------
+# GEMM + post-norm over a cluster along N (DSMEM row-statistics exchange)
+# ----------------------------------------------------------------------------
+CLUSTER_N = [320, 512, 1024, 2048, 3000, 4096, 8192]
+
+
+@pytest.mark.parametrize("N", CLUSTER_N)
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_postnorm_cluster(norm, N):
+    w, d = _case("cfg4_n1024_ln", N + (norm == "rmsnorm"), M=300, N=N, K=256)
+    c, cols = fn.postnorm_plan(N)
+    assert c > 1 and c * cols >= N
+    _post(w, d, norm)
+
+
+def test_postnorm_cluster_with_pre():
+    w, d = _case("cfg5", 13, M=400, N=2048, K=256)
+    _post(w, d, "layernorm", pre=True)
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_cluster_sizes_agree(norm):
+    # the statistics split into per-CTA partials: cluster sizes 4, 8 and 16 must
+    # give the same row statistics up to fp32 summation order
+    w, d = _case("cfg4_n1024_ln", 21, M=256, N=1024, K=512)
+    outs = {}
+    try:
+        for c in (4, 8, 16):
+            fn.set_postnorm_cluster(c)
+            assert fn.postnorm_plan(1024)[0] == c
+            outs[c] = _post(w, d, norm)
+    finally:
+        fn.set_postnorm_cluster(0)
+    r4 = np64(outs[4][1]["rstd"])
+    for c in (8, 16):
+        rc = np64(outs[c][1]["rstd"])
+        assert np.max(np.abs(rc - r4) / r4) < 1e-5, f"cluster {c} rstd differs from cluster 4"
+
+
+def test_cluster_size_one_vs_two_small_N():
+    w, d = _case("cfg2_n128", 22, M=384, N=256, K=512)
+    try:
+        fn.set_postnorm_cluster(1)
+        C1, s1 = _post(w, d, "layernorm")
+        fn.set_postnorm_cluster(2)
+        C2, s2 = _post(w, d, "layernorm")
+    finally:
+        fn.set_postnorm_cluster(0)
+    assert np.max(np.abs(np64(s1["rstd"]) - np64(s2["rstd"])) / np64(s1["rstd"])) < 1e-5
+
+
+# ----------------------------------------------------------------------------
+# standalone norms (unfused comparison kernels)
+# ----------------------------------------------------------------------------
+NORM_SHAPES = [(1000, 64), (1000, 128), (257, 1024), (64, 4096), (33, 8192), (7, 8), (100, 1000), (3, 32768)]
+
+
+@pytest.mark.parametrize("M,N", NORM_SHAPES, ids=lambda v: str(v))
+def test_standalone_norms(M, N):
+    w, d = _case("cfg2_n64", M + N, M=1, K=8, N=N)
+    rng = np.random.default_rng(M * 31 + N)
+    X = torch.from_numpy((rng.standard_normal((M, N)) * 2 + 0.5).astype(np.float32)).to(torch.bfloat16)
+    Y, st = fn.layernorm(_dev(X), _dev(d["gamma"]), _dev(d["beta"]), 1e-5, return_stats=True)
+    ref, mu, r = oracle.layernorm(to_f64(X), to_f64(d["gamma"]), to_f64(d["beta"]), 1e-5)
+    assert_out_close(Y, ref, "layernorm")
+    assert_rstd_close(st["rstd"], r)
+    assert_mean_close(st["mean"], mu, r)
+    Y, rs = fn.rmsnorm(_dev(X), _dev(d["gamma"]), 1e-6, return_rstd=True)
+    ref, r = oracle.rmsnorm(to_f64(X), to_f64(d["gamma"]), None, 1e-6)
+    assert_out_close(Y, ref, "rmsnorm")
+    assert_rstd_close(rs, r)
+
+
+# ----------------------------------------------------------------------------
+# edge cases and failure detection
+# ----------------------------------------------------------------------------
+def test_empty_M_is_a_no_op():
+    A = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    B = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    assert fn.gemm(A, B).shape == (0, 128)
+    assert fn.lazy_prenorm_gemm(A, B).shape == (0, 128)
+    assert fn.gemm_postnorm(A, B, "rmsnorm").shape == (0, 128)
+    assert fn.rmsnorm(A).shape == (0, 64)
+    fn.check_status(DEV)
+
+
+def test_invalid_arguments_launch_nothing():
+    A = torch.randn(128, 60, device=DEV).to(torch.bfloat16)   # K not a multiple of 8
+    B = torch.randn(60, 64, device=DEV).to(torch.bfloat16)
+    with pytest.raises(fn.FnormError) as e:
+        fn.gemm(A, B)
+    assert e.value.status == fn.INVALID_ARG
+    A = torch.randn(128, 64, device=DEV).to(torch.bfloat16)
+    B = torch.randn(64, 64, device=DEV).to(torch.bfloat16)
+    with pytest.raises(fn.FnormError) as e:
+        fn.lazy_prenorm_gemm(A, B, eps=0.0)
+    assert e.value.status == fn.INVALID_ARG
+    Bw = torch.randn(64, 16384, device=DEV).to(torch.bfloat16)
+    with pytest.raises(fn.FnormError) as e:
+        fn.gemm_postnorm(A, Bw, "layernorm")
+    assert e.value.status == fn.UNSUPPORTED
+    fn.check_status(DEV)
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    fn.debug_wait_timeout(20_000_000, DEV)          # a wait nothing will satisfy, 20 ms bound
+    with pytest.raises(fn.FnormError) as e:
+        fn.check_status(DEV)
+    assert e.value.status == fn.TIMEOUT
+    fn.check_status(DEV)                            # cleared
+    w, d = _case("cfg1", 30, M=128, N=64, K=64)     # the context is still usable
+    C = fn.gemm(_dev(d["A"]), _dev(d["B"]))
+    assert_out_close(C, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])))
+    fn.check_status(DEV)
+
+
+def test_stream_and_graph_capture():
+    # calls run on the caller's stream and replay from a CUDA graph
+    w, d = _case("cfg2_n128", 31, M=512, N=128, K=1024)
+    A, B, g, b = _dev(d["A"]), _dev(d["B"]), _dev(d["gamma"]), _dev(d["beta"])
+    out = torch.empty((512, 128), dtype=torch.bfloat16, device=DEV)
+    fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps, out=out)   # first call loads the kernels
+    torch.cuda.synchronize()
+    ref = out.clone()
+    out.zero_()
+    s = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
