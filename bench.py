@@ -1,0 +1,575 @@
+"""Benchmark of the fused normalization + GEMM path on one GB300 (or N replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload cfg2|cfg1|cfg3|cfg4|cfg5|all]
+
+Default workload (one JSON line on stdout): GEMM + post-LayerNorm with affine,
+A[16384,1024] @ B[1024,N] for N = 64 and N = 128 (both launches make one step).
+Metric: fused norm-GEMM TFLOP/s (2*M*N*K per launch), with the roofline of the
+dominant kernel, the fraction of the unfused norm's latency that fusion hides,
+an end-to-end number through the public API with host buffers, and the fp64
+oracle timed on the host cores.
+
+Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
+bracketed by a barrier and torch.cuda.synchronize() on both sides and timed
+with CUDA events on the launching stream.  Inputs and outputs rotate over R
+copies whose total exceeds 2x the L2 cache, so no step reads what the previous
+one left in L2.  Under torchrun every rank runs the same per-GPU workload (weak
+scaling, independent replicas: rows of the path never interact) and the time
+is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+if "OPENBLAS_NUM_THREADS" not in os.environ and "OMP_NUM_THREADS" not in os.environ:
+    _ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    os.environ["OPENBLAS_NUM_THREADS"] = str(_ncores)
+    os.environ["OMP_NUM_THREADS"] = str(_ncores)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "fused norm-GEMM TFLOP/s and % of roofline; % unfused-norm latency hidden (1×GB300)"
+
+GROUPS = {
+    "cfg1": ["cfg1"],
+    "cfg2": ["cfg2_n64", "cfg2_n128"],
+    "cfg3": ["cfg3"],
+    "cfg4": ["cfg4_n1024_ln", "cfg4_n1024_rms", "cfg4_n4096_ln", "cfg4_n4096_rms", "cfg4_n8192_ln",
+             "cfg4_n8192_rms"],
+    "cfg5": ["cfg5"],
+}
+GROUP_TEXT = {
+    "cfg1": "Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128], eps 1e-6",
+    "cfg2": "GEMM + post-LayerNorm(affine), A[16384,1024] @ B[1024,N], N in {64,128}, eps 1e-5",
+    "cfg3": "Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], eps 1e-6",
+    "cfg4": "GEMM + post-LayerNorm and post-RMSNorm over a CTA cluster, A[16384,2048] @ B[2048,N], "
+            "N in {1024,4096,8192}",
+    "cfg5": "pre-RMSNorm + GEMM + post-LayerNorm(affine) in one kernel, A[65536,256] @ B[256,256]",
+}
+KERNEL_SOURCES = ["fused_gemm.cuh", "ptx.cuh", "fused_launch.cuh", "rownorm.cu"]
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (N > 1 under torchrun: independent replicas)
+# --------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar (a time) over all ranks."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "normalization_gemm_tcgen05_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic(name: str):
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when it is missing or was taken on kernel sources other than these."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self) -> dict:
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 250.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, label in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                               ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(label)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+class Case:
+    """One sub-workload on the device: R rotating copies of its buffers."""
+
+    def __init__(self, w: Workload, device, l2_bytes: int, seed: int = 0):
+        import normalization_gemm_tcgen05_gb300 as fn
+        self.fn = fn
+        self.w = w
+        self.dev = device
+        d = make_inputs(w, seed)
+        self.host = d
+        fp = 2 * (w.M * w.K + w.K * w.N + 2 * w.M * w.N)
+        self.R = max(2, math.ceil(2 * l2_bytes / fp))
+        self.A = [d["A"].to(device) for _ in range(self.R)]
+        self.B = [d["B"].to(device) for _ in range(self.R)]
+        self.g = None if d["gamma"] is None else d["gamma"].to(device)
+        self.b = None if d["beta"] is None else d["beta"].to(device)
+        self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
+        self.Y = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
+        nst = 3
+        self.stats = [[torch.empty(w.M, dtype=torch.float32, device=device) for _ in range(nst)]
+                      for _ in range(self.R)]
+        # the unfused norm reads a C produced by the GEMM: rotate it too
+        self.Rn = max(2, math.ceil(2 * l2_bytes / (4 * w.M * w.N)))
+        self.Cn = [torch.randn((w.M, w.N), device=device).to(torch.bfloat16) for _ in range(self.Rn)]
+        self.Yn = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.Rn)]
+        self.An = self.A  # the pre-norm's input rotates with A
+
+    # one launch of the fused kernel on copy i
+    def fused(self, i: int):
+        w, fn, j = self.w, self.fn, i % self.R
+        st = self.stats[j]
+        if w.kind == "prenorm":
+            fn.lazy_prenorm_gemm(self.A[j], self.B[j], w.eps, out=self.C[j])
+        elif w.kind == "postnorm":
+            fn.gemm_postnorm(self.A[j], self.B[j], w.norm, self.g, self.b, w.eps, pre_rmsnorm=w.pre_rmsnorm,
+                             pre_eps=w.pre_eps, out=self.C[j])
+        else:
+            fn.gemm(self.A[j], self.B[j], out=self.C[j])
+        del st
+
+    def gemm_only(self, i: int):
+        j = i % self.R
+        self.fn.gemm(self.A[j], self.B[j], out=self.C[j])
+
+    def norm_only(self, i: int):
+        """The standalone norm kernel(s) the fusion replaces, on rotating inputs."""
+        w, fn, j = self.w, self.fn, i % self.Rn
+        if w.kind == "prenorm":
+            k = i % self.R
+            fn.rmsnorm(self.A[k], None, w.eps, out=self._pre_out(k))
+        else:
+            if w.pre_rmsnorm:
+                k = i % self.R
+                fn.rmsnorm(self.A[k], None, w.pre_eps, out=self._pre_out(k))
+            if w.norm == "layernorm":
+                fn.layernorm(self.Cn[j], self.g, self.b, w.eps, out=self.Yn[j])
+            else:
+                fn.rmsnorm(self.Cn[j], self.g, w.eps, out=self.Yn[j])
+
+    def unfused_pipeline(self, i: int):
+        """GEMM and the standalone norm(s) back to back, as an unfused model runs them."""
+        w, fn, j = self.w, self.fn, i % self.R
+        if w.kind == "prenorm":
+            fn.rmsnorm(self.A[j], None, w.eps, out=self._pre_out(j))
+            fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+        else:
+            if w.pre_rmsnorm:
+                fn.rmsnorm(self.A[j], None, w.pre_eps, out=self._pre_out(j))
+                fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+            else:
+                fn.gemm(self.A[j], self.B[j], out=self.C[j])
+            if w.norm == "layernorm":
+                fn.layernorm(self.C[j], self.g, self.b, w.eps, out=self.Y[j])
+            else:
+                fn.rmsnorm(self.C[j], self.g, w.eps, out=self.Y[j])
+
+    _pre = None
+
+    def _pre_out(self, j):
+        if self._pre is None:
+            self._pre = [torch.empty((self.w.M, self.w.K), dtype=torch.bfloat16, device=self.dev)
+                         for _ in range(self.R)]
+        return self._pre[j]
+
+    def launches_per_call(self, what: str) -> int:
+        w = self.w
+        if what == "fused" or what == "gemm":
+            return 1
+        if what == "norm":
+            return 1 + (1 if (w.kind == "postnorm" and w.pre_rmsnorm) else 0)
+        return 2 + (1 if (w.kind == "postnorm" and w.pre_rmsnorm) else 0)
+
+
+def time_graph(step, K: int, stream, world: int, device, chunk: int = 200) -> float:
+    """Capture `step(i)` for i in [0, K) into CUDA graphs and time one replay of
+    all of them; returns seconds (max over ranks)."""
+    graphs = []
+    i = 0
+    with torch.cuda.stream(stream):
+        while i < K:
+            n = min(chunk, K - i)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(i, i + n):
+                    step(k)
+            graphs.append(g)
+            i += n
+        for g in graphs:          # one untimed replay: graph upload
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    del graphs
+    return max_over_ranks(t, world, device)
+
+
+def run_ours(args, names, world, rank, local):
+    import normalization_gemm_tcgen05_gb300 as fn
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    peaks = load_peaks()
+    cases = [Case(WORKLOADS[n], device, l2) for n in names]
+    stream = torch.cuda.Stream(device)
+    K, W = args.steps, args.warmup
+
+    for c in cases:                      # warm-up (loads kernels, first-use set-up)
+        for i in range(W):
+            c.fused(i)
+            c.gemm_only(i)
+            c.norm_only(i)
+            c.unfused_pipeline(i)
+    torch.cuda.synchronize()
+    fn.check_status(device)
+
+    with ClockSampler(local) as clk:
+        fused_t = [time_graph(c.fused, K, stream, world, device) for c in cases]
+        gemm_t = [time_graph(c.gemm_only, K, stream, world, device) for c in cases]
+        norm_t = [time_graph(c.norm_only, K, stream, world, device) for c in cases]
+        pipe_t = [time_graph(c.unfused_pipeline, K, stream, world, device) for c in cases]
+    fn.check_status(device)
+
+    # ---- end to end through the public API with pinned host buffers ----
+    e2e = run_e2e(cases, K, W, world, device)
+
+    flops_step = sum(c.w.flops for c in cases)
+    t_step = sum(fused_t) / K
+    value = world * flops_step / t_step / 1e12
+    dom = max(range(len(cases)), key=lambda k: fused_t[k])
+    dc = cases[dom]
+    per_launch = fused_t[dom] / K
+    ai = dc.w.flops / dc.w.algorithmic_bytes
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai < ridge:
+        achieved = dc.w.algorithmic_bytes / per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = dc.w.flops / per_launch / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = load_traffic(dc.w.name)
+    roof["kernel"] = f"fused kernel, {dc.w.name}"
+    roof["algorithmic_bytes"] = dc.w.algorithmic_bytes
+    roof["peak_source"] = peaks["source"] + (" (burst)" if roof["bound"] == "tensor" else "")
+
+    hidden = {}
+    for k, c in enumerate(cases):
+        tf, tg, tn, tp = fused_t[k] / K, gemm_t[k] / K, norm_t[k] / K, pipe_t[k] / K
+        hidden[c.w.name] = {
+            "t_fused_us": round(tf * 1e6, 3), "t_gemm_us": round(tg * 1e6, 3), "t_norm_us": round(tn * 1e6, 3),
+            "t_unfused_pipeline_us": round(tp * 1e6, 3),
+            "hidden_vs_standalone_norm": round((tg + tn - tf) / tn, 4),
+            "hidden_vs_pipeline": round((tp - tf) / (tp - tg), 4) if tp > tg else None,
+            "fused_tflops": round(c.w.flops / tf / 1e12, 2),
+            "fused_gbs": round(c.w.algorithmic_bytes / tf / 1e9, 1),
+        }
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(t_step * 1e3, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded inputs with the workload table's shapes and distributions",
+        "config": {"workload": args.workload + ": " + GROUP_TEXT.get(args.workload, ""),
+                   "sub_workloads": names, "l2": f"inputs/outputs rotate over >= 2x L2 ({l2 >> 20} MiB)",
+                   "timing": "CUDA graphs of K launches, CUDA events on the launching stream",
+                   "parallelism": f"{world} independent replica(s)"},
+        "roofline": roof,
+        "latency_hidden": hidden,
+        "e2e": e2e,
+        "gpu_launches": K * len(cases),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(names, args.cpu_seconds)
+    return line
+
+
+def run_e2e(cases, K, W, world, device) -> dict:
+    """K steps through the public API: H2D copy of every input from pinned
+    host memory, the fused call, D2H copy of the output, per step."""
+    import normalization_gemm_tcgen05_gb300 as fn
+    host = []
+    for c in cases:
+        hA = c.host["A"].pin_memory()
+        hB = c.host["B"].pin_memory()
+        hg = None if c.host["gamma"] is None else c.host["gamma"].pin_memory()
+        hb = None if c.host["beta"] is None else c.host["beta"].pin_memory()
+        hC = torch.empty((c.w.M, c.w.N), dtype=torch.bfloat16).pin_memory()
+        host.append((hA, hB, hg, hb, hC))
+    h2d = sum(t.numel() * t.element_size() for h in host for t in h[:4] if t is not None)
+    d2h = sum(h[4].numel() * h[4].element_size() for h in host)
+
+    def step():
+        for c, (hA, hB, hg, hb, hC) in zip(cases, host):
+            dA, dB = c.A[0], c.B[0]
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            if hg is not None:
+                c.g.copy_(hg, non_blocking=True)
+            if hb is not None:
+                c.b.copy_(hb, non_blocking=True)
+            w = c.w
+            if w.kind == "prenorm":
+                fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
+            else:
+                fn.gemm_postnorm(dA, dB, w.norm, c.g, c.b, w.eps, pre_rmsnorm=w.pre_rmsnorm, pre_eps=w.pre_eps,
+                                 out=c.C[0])
+            hC.copy_(c.C[0], non_blocking=True)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    flops = sum(c.w.flops for c in cases)
+    return {"value": round(world * K * flops / t / 1e12, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(t / K * 1e3, 4)}
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+def oracle_step(w: Workload, d: dict, rows: np.ndarray):
+    import oracle
+    A = d["A64"][rows]
+    if w.kind == "prenorm":
+        oracle.lazy_prenorm_gemm(A, d["B64"], w.eps)
+    elif w.kind == "postnorm":
+        oracle.gemm_postnorm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps, pre_rmsnorm=w.pre_rmsnorm,
+                             pre_eps=w.pre_eps)
+    else:
+        oracle.gemm(A, d["B64"])
+
+
+def _oracle_inputs(names):
+    from workloads import to_f64
+    out = []
+    for n in names:
+        w = WORKLOADS[n]
+        d = make_inputs(w, 0)
+        out.append((w, {"A64": to_f64(d["A"]), "B64": to_f64(d["B"]), "g64": to_f64(d["gamma"]),
+                        "b64": to_f64(d["beta"])}))
+    return out
+
+
+def _cores() -> int:
+    v = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else (os.cpu_count() or 1)
+
+
+def _sample_rows(w: Workload, budget_flops: float) -> np.ndarray:
+    per_row = 2.0 * w.N * w.K
+    n = int(max(1, min(w.M, budget_flops // per_row)))
+    return np.linspace(0, w.M - 1, n).astype(np.int64)
+
+
+def cpu_baseline(names, seconds: float) -> dict:
+    """The fp64 oracle as it stands, on a bounded row sample of each sub-workload."""
+    inputs = _oracle_inputs(names)
+    flops = 0.0
+    t_total = 0.0
+    samples = []
+    for w, d in inputs:
+        rows = _sample_rows(w, 4e9)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle_step(w, d, rows)
+            reps += 1
+            if time.perf_counter() - t0 >= seconds / len(inputs):
+                break
+        dt = time.perf_counter() - t0
+        flops += reps * 2.0 * len(rows) * w.N * w.K
+        t_total += dt
+        samples.append(f"{w.name}: {reps} x {len(rows)} of {w.M} rows")
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": "; ".join(samples) + " (fp64 numpy oracle, all N columns of each sampled row)"}
+
+
+def run_reference(args, names, world, rank):
+    """--impl reference: the oracle on the host cores, K timed steps each a bounded row sample."""
+    if world > 1 and rank != 0:
+        return None
+    inputs = _oracle_inputs(names)
+    budget = 2e9 / len(inputs)
+    sampled = [(w, d, _sample_rows(w, budget)) for w, d in inputs]
+    for _ in range(args.warmup):
+        for w, d, rows in sampled:
+            oracle_step(w, d, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for w, d, rows in sampled:
+            oracle_step(w, d, rows)
+    t = time.perf_counter() - t0
+    flops = args.steps * sum(2.0 * len(rows) * w.N * w.K for w, d, rows in sampled)
+    value = flops / t / 1e12
+    sample = "; ".join(f"{w.name}: {len(rows)} of {w.M} rows" for w, d, rows in sampled)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded inputs with the workload table's shapes and distributions",
+        "config": {"workload": args.workload + ": " + GROUP_TEXT.get(args.workload, ""), "sub_workloads": names},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                         "sample": sample + " per step (fp64 numpy oracle on the host cores)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="cfg2", choices=sorted(GROUPS) + ["all"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "ours":
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device (the fused path has no CPU fallback)")
+        torch.cuda.set_device(local)
+        init_dist(world, "nccl")
+    groups = sorted(GROUPS) if args.workload == "all" else [args.workload]
+    for gname in groups:
+        args.workload = gname
+        names = GROUPS[gname]
+        if args.impl == "reference":
+            line = run_reference(args, names, world, rank)
+        else:
+            line = run_ours(args, names, world, rank, local)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
