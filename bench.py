@@ -539,6 +539,19 @@ def run_reference(args, names, world, rank):
     }
 
 
+def profile_case(args):
+    """Eager launches of one kernel on one sub-workload (a small, bounded ncu target)."""
+    import normalization_gemm_tcgen05_gb300 as fn
+    device = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(device)
+    c = Case(WORKLOADS[args.profile_case], device, int(getattr(props, "L2_cache_size", 126 * 2**20)))
+    step = {"fused": c.fused, "gemm": c.gemm_only, "norm": c.norm_only}[args.profile_kernel]
+    for i in range(args.warmup + args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    fn.check_status(device)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -548,10 +561,16 @@ def main(argv=None):
     ap.add_argument("--workload", default="cfg2", choices=sorted(GROUPS) + ["all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-case", default=None, choices=sorted(WORKLOADS),
+                    help="for ncu: run W + K eager launches of one kernel of one sub-workload and exit")
+    ap.add_argument("--profile-kernel", default="fused", choices=["fused", "gemm", "norm"])
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.impl == "ours":
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA device (the fused path has no CPU fallback)")

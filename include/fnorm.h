@@ -19,10 +19,9 @@
  *     fp32 arrays of length M.
  *   - Every pointer is DEVICE memory on the current CUDA device, owned by
  *     the caller.  The library never frees, retains or allocates per call.
- *     Base addresses of A, B, C, X and Y must be 16-byte aligned; gamma and
- *     beta 2-byte aligned for fnorm_gemm_postnorm and 16-byte aligned for
- *     fnorm_rmsnorm / fnorm_layernorm; fp32 statistic outputs 4-byte aligned.
- *     A misaligned pointer is an argument error.
+ *     Base addresses of A, B, C, X, Y, gamma and beta must be 16-byte
+ *     aligned; fp32 statistic outputs 4-byte aligned.  A misaligned pointer
+ *     is an argument error.
  *   - Sizes: M >= 0 (M == 0 is a valid empty call that does nothing);
  *     N >= 8 and K >= 8, both multiples of 8 (16-byte row pitch for the
  *     tensor-memory-access engine); M, N, K < 2^31.
@@ -30,7 +29,11 @@
  *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *     asynchronous on that stream: no host synchronisation happens inside
  *     them and they can be captured into a CUDA graph after the first call on
- *     a device has returned (that first call loads the device code).
+ *     a device has returned (that first call loads the device code).  Kernels
+ *     are launched with programmatic stream serialisation: their set-up may
+ *     overlap the previous kernel in the stream, and every global memory
+ *     access waits for that kernel to complete (environment variable
+ *     FNORM_PDL=0 turns this off).
  *   - A call returns FNORM_OK once its kernels are enqueued.  Argument errors
  *     return FNORM_ERR_INVALID_ARG and launch nothing; shapes the kernels do
  *     not implement return FNORM_ERR_UNSUPPORTED; CUDA launch errors return
@@ -93,10 +96,16 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
  * fnorm_gemm_postnorm — C = norm(A @ B) * gamma + beta (epilogue post-norm).
  *   [FNF-ru] "Multi-CTA Norm Fusion"; [FNF-es] "El problema del tiling";
  *   definitions from [ATB] 1.1 (LayerNorm, biased variance) and 1.2 (RMSNorm).
- *   The norm is taken over the fp32 accumulator of each row.  When N is wider
- *   than one CTA's tile, the CTAs of a thread-block cluster that share a
- *   128-row block split the row along N, exchange per-row partial statistics
- *   through distributed shared memory and each normalises its own slice.
+ *   The row statistics are taken over the fp32 accumulator of each row.  When
+ *   N is wider than one CTA's tile, the CTAs of a thread-block cluster that
+ *   share a 128-row block split the row along N, exchange per-row partial
+ *   statistics through distributed shared memory and each normalises its own
+ *   slice (fnorm_postnorm_plan reports the split).  Rows wider than the
+ *   cluster's tensor memory (N > 1024 by default) use a spill layout: each
+ *   CTA writes its un-normalised slices to C in bf16, then normalises them in
+ *   place once the statistics are known; those outputs are normalised from
+ *   bf16-rounded values (relative error <= 2^-9 of the value before the norm).
+ *   C is therefore also read by this call.
  *   norm:        FNORM_LAYERNORM or FNORM_RMSNORM.
  *   gamma, beta: [N] bf16 device arrays, or NULL (gamma = 1, beta = 0).
  *   eps:         epsilon of the post-norm, inside the square root.
@@ -106,7 +115,6 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
  *   mean_out:    [M] fp32, LayerNorm only (must be NULL for RMSNorm), or NULL.
  *   rstd_out:    [M] fp32 rstd of the post-norm, or NULL.
  *   pre_rstd_out:[M] fp32 rstd of the pre-norm (pre_rmsnorm == 1 only), or NULL.
- *   N up to 8192 (FNORM_ERR_UNSUPPORTED beyond).
  */
 fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
                                    int64_t M, int64_t N, int64_t K, fnorm_norm_t norm,
@@ -158,17 +166,18 @@ fnorm_status_t fnorm_set_wait_limit_ns(uint64_t ns);
 /*
  * fnorm_postnorm_plan — how fnorm_gemm_postnorm splits a row of width N:
  * *cluster receives the CTAs per cluster along N and *cols_per_cta the
- * columns each CTA owns (a multiple of 64).  Returns FNORM_ERR_UNSUPPORTED if
- * N is too wide.  Host only; launches nothing.
+ * columns each CTA owns (a multiple of 64; more than 256 means the spill
+ * layout).  Host only; launches nothing.
  */
 fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta);
 
 /*
  * fnorm_set_postnorm_cluster — force the cluster size used by
- * fnorm_gemm_postnorm (1, 2, 4, 8 or 16; 0 = automatic, the default).  A
- * testing and tuning knob: results agree across cluster sizes up to fp32
+ * fnorm_gemm_postnorm (1, 2, 4 or 8; 0 = automatic, the default).  A testing
+ * and tuning knob: statistics agree across cluster sizes up to fp32
  * summation order.  Process-wide.  A forced size that cannot hold the row
- * makes later calls return FNORM_ERR_UNSUPPORTED.
+ * (8 CTAs hold at most 128 columns each) makes later calls return
+ * FNORM_ERR_UNSUPPORTED.
  */
 fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size);
 

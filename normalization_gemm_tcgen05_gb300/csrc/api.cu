@@ -63,36 +63,58 @@ int round64(int64_t x) { return static_cast<int>((x + 63) / 64 * 64); }
 
 int gemm_tile_n(int64_t N) { return N <= 64 ? 64 : (N <= 128 ? 128 : 256); }
 
-// How a post-norm row of width N is split: cluster size, subtile width and
-// subtiles per CTA.  Automatic plans prefer one accumulator subtile per CTA
-// (tensor memory double buffered, so a tile's epilogue overlaps the next
-// tile's MMAs) on clusters of up to 8, then two 256-column subtiles per CTA on
-// clusters of 8 or 16.  Returns FNORM_ERR_UNSUPPORTED when nothing holds N.
-fnorm_status_t plan_postnorm(int64_t N, int forced, int* cluster, int* bn_sub, int* nsub) {
-  auto one_sub = [&](int c) -> bool {
+// Keep all of B in shared memory when it is one tile wide (N <= bn), at most
+// 128 KB, and each CTA will visit several row blocks (more row blocks than
+// SMs), so B is read once per CTA instead of once per tile.
+bool want_resident_b(int64_t M, int64_t N, int64_t K, int bn) {
+  DeviceInfo dev;
+  if (current_device(&dev) != FNORM_OK) return false;
+  const int64_t kb_max = 131072 / (64LL * bn * 2);
+  return N <= bn && (K + 63) / 64 <= kb_max && (M + 127) / 128 > dev.num_sms;
+}
+
+// How a post-norm row of width N is laid out over the CTAs.
+//   N <= 256:     one CTA per row block holds the whole row in tensor memory
+//                 (tile width N rounded up to 64);
+//   N <= 1024:    resident cluster of 2 or 4 CTAs, each holding one 128- or
+//                 256-column slice in tensor memory;
+//   wider rows:   spill layout on a cluster of kSpillCluster CTAs, each owning
+//                 S = ceil(N / (cluster * 256)) slices of 256 columns.
+// A forced cluster size c keeps the resident layout when each CTA's share fits
+// one tile (256 columns for c <= 4, 128 for c = 8), else uses the spill layout
+// (c <= 4).
+constexpr int kSpillCluster = 4;
+
+struct PostPlan {
+  int cluster, bn, slices;
+  bool spill;
+};
+
+fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl) {
+  auto resident = [&](int c) -> bool {
     const int64_t w = (N + c - 1) / c;  // columns per CTA
-    if (w > 256 || c > 8) return false;
-    *cluster = c;
-    *bn_sub = (c == 1) ? round64(w) : (w <= 128 ? 128 : 256);
-    *nsub = 1;
+    if (w > 256 || (c > 4 && w > 128)) return false;
+    pl->cluster = c;
+    pl->bn = (c == 1) ? round64(w) : (w <= 128 ? 128 : 256);
+    pl->slices = 1;
+    pl->spill = false;
     return true;
   };
-  auto two_sub = [&](int c) -> bool {
-    const int64_t w = (N + c - 1) / c;
-    if (w > 512 || c < 2) return false;
-    *cluster = c, *bn_sub = 256, *nsub = 2;
+  auto spill = [&](int c) -> bool {
+    const int64_t s = (N + 256LL * c - 1) / (256LL * c);
+    if (c > 4 || s > (1 << 20)) return false;
+    pl->cluster = c, pl->bn = 256, pl->slices = static_cast<int>(s), pl->spill = true;
     return true;
   };
   if (forced != 0) {
-    if (one_sub(forced) || two_sub(forced)) return FNORM_OK;
+    if (resident(forced) || spill(forced)) return FNORM_OK;
     set_error("a row of %lld columns does not fit a forced cluster of %d CTAs", (long long)N, forced);
     return FNORM_ERR_UNSUPPORTED;
   }
-  for (int c : {1, 2, 4, 8})
-    if (one_sub(c)) return FNORM_OK;
-  for (int c : {8, 16})
-    if (two_sub(c)) return FNORM_OK;
-  set_error("post-norm rows are limited to 8192 columns (got %lld)", (long long)N);
+  for (int c : {1, 2, 4})
+    if (resident(c)) return FNORM_OK;
+  if (spill(kSpillCluster)) return FNORM_OK;
+  set_error("post-norm row of %lld columns is too wide", (long long)N);
   return FNORM_ERR_UNSUPPORTED;
 }
 
@@ -104,7 +126,9 @@ FusedLaunch base_launch(const void* A, const void* B, void* C, int64_t M, int64_
   L.M = static_cast<int>(M);
   L.N = static_cast<int>(N);
   L.K = static_cast<int>(K);
-  L.nsub = 1;
+  L.slices = 1;
+  L.spill = false;
+  L.bres = false;
   L.cluster = 1;
   L.eps = 1.0f;
   L.pre_eps = 1.0f;
@@ -132,7 +156,8 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
   FN_TRY(check_ptr(C, "C", 16, false));
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   L.mode = 0;
-  L.bn_sub = gemm_tile_n(N);
+  L.bn = gemm_tile_n(N);
+  L.bres = want_resident_b(M, N, K, L.bn);
   return launch_fused_plain(L);
 }
 
@@ -148,7 +173,8 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   L.mode = MODE_PRE;
-  L.bn_sub = gemm_tile_n(N);
+  L.bn = gemm_tile_n(N);
+  L.bres = want_resident_b(M, N, K, L.bn);
   L.pre_eps = eps;
   L.rstd_out = rstd_out;
   return launch_fused_plain(L);
@@ -166,22 +192,24 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   if (pre_rmsnorm) FN_TRY(check_eps(pre_eps, "pre_eps"));
   if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
   if (!pre_rmsnorm && pre_rstd_out != nullptr) return bad("pre_rstd_out needs pre_rmsnorm = 1");
-  int cluster = 1, bn_sub = 64, nsub = 1;
-  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &cluster, &bn_sub, &nsub));
+  PostPlan plan{};
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
   if (M == 0) return FNORM_OK;
   FN_TRY(check_ptr(A, "A", 16, false));
   FN_TRY(check_ptr(B, "B", 16, false));
   FN_TRY(check_ptr(C, "C", 16, false));
-  FN_TRY(check_ptr(gamma, "gamma", 2, true));
-  FN_TRY(check_ptr(beta, "beta", 2, true));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
   FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
   FN_TRY(check_ptr(pre_rstd_out, "pre_rstd_out", 4, true));
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   L.mode = MODE_POST | (norm == FNORM_LAYERNORM ? MODE_LN : 0) | (pre_rmsnorm ? MODE_PRE : 0);
-  L.bn_sub = bn_sub;
-  L.nsub = nsub;
-  L.cluster = cluster;
+  L.bn = plan.bn;
+  L.slices = plan.slices;
+  L.spill = plan.spill;
+  L.cluster = plan.cluster;
+  L.bres = (plan.cluster == 1 && !plan.spill) && want_resident_b(M, N, K, plan.bn);
   L.eps = eps;
   L.pre_eps = pre_rmsnorm ? pre_eps : 1.0f;
   L.gamma = gamma;
@@ -189,7 +217,7 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   L.mean_out = mean_out;
   L.rstd_out = rstd_out;
   L.pre_rstd_out = pre_rstd_out;
-  return cluster == 1 ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
+  return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
 }
 
 fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
@@ -245,18 +273,17 @@ fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta) {
   clear_error();
   if (cluster == nullptr || cols_per_cta == nullptr) return bad("output pointers must not be NULL");
   if (N < 8 || N > kMaxDim || N % 8 != 0) return bad("N must be a multiple of 8 in [8, 2^31)");
-  int c = 1, bn = 64, ns = 1;
-  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &c, &bn, &ns));
-  *cluster = c;
-  *cols_per_cta = bn * ns;
+  PostPlan plan{};
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
+  *cluster = plan.cluster;
+  *cols_per_cta = plan.bn * plan.slices;
   return FNORM_OK;
 }
 
 fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size) {
   clear_error();
-  if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 &&
-      cluster_size != 16)
-    return bad("cluster size must be 0 (automatic), 1, 2, 4, 8 or 16");
+  if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8)
+    return bad("cluster size must be 0 (automatic), 1, 2, 4 or 8");
   g_forced_cluster.store(cluster_size, std::memory_order_relaxed);
   return FNORM_OK;
 }

@@ -8,28 +8,46 @@
 //     shared memory by a dedicated norm warpgroup while the tensor cores run,
 //     and rstd scales the fp32 accumulator in the epilogue ([FNF-ru] "Lazy
 //     Pre-Norm"; [FNF-es] "Lazy Pre-Norm: el truco matemático");
-//   * epilogue post-norm, C = norm(A @ B) * gamma + beta, LayerNorm or RMSNorm.
-//     When a row is wider than one CTA tile, the CTAs of a cluster split it
-//     along N, push per-row partial statistics (count is implicit, mean and
-//     M2 for LayerNorm, sum of squares for RMSNorm) to every peer through
-//     distributed shared memory, combine them in rank order and normalise
-//     their own slice ([FNF-ru] "Multi-CTA Norm Fusion": the norm splits into
-//     a row reduction and an element-wise step, and only the reduction needs
-//     the whole row, one scalar per row to exchange);
+//   * epilogue post-norm, C = norm(A @ B) * gamma + beta, LayerNorm or RMSNorm
+//     ([FNF-ru] "Multi-CTA Norm Fusion": a norm is a row reduction plus an
+//     element-wise step, only the reduction needs the whole row, and its
+//     result is one scalar per row).  Three layouts of a row block:
+//       - resident, one CTA: the CTA's accumulator spans the whole row;
+//       - resident, cluster: the CTAs of a cluster split the row along N, each
+//         keeps its slice in tensor memory, pushes its per-row partial
+//         statistics to every peer through distributed shared memory, combines
+//         them in rank order and normalises its slice;
+//       - spill, cluster: each CTA owns S slices of 256 columns, computed one
+//         after another in double-buffered tensor memory; each slice is written
+//         to C un-normalised while its statistics accumulate, and once the row
+//         block's statistics are exchanged the slices are re-read from L2 and
+//         normalised in place while the next row block's MMAs run.  Rows of
+//         any width, on small clusters.
 //   * both at once: norm(rmsnorm(A) @ B).
 //
-// Warp roles (one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A [128 x BK] and B [BK x BN_CTA] tiles into an
-//               S-stage shared-memory ring (128-byte swizzle).
+// Warp roles (one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: A [128 x 64] and B [64 x BN] tiles into an
+//               S-stage shared-memory ring (128-byte swizzle), or A only when
+//               all of B is resident in shared memory.
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, M = 128,
-//               N = BN_SUB, K = 16, accumulators in tensor memory, double
-//               buffered when a tile needs at most half of it.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator in register subtiles
-//               of 32 or 64 columns, statistics, normalise / scale, bf16,
-//               swizzled shared-memory staging and TMA stores.
-//   warps 6-9   (Lazy Pre-Norm only) sum of squares of the staged A rows.
+//               N = BN, K = 16, fp32 accumulators in tensor memory, double
+//               buffered.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter: warps 2-5 own the
+//               first BN/2 columns of a tile, warps 6-9 the second half.
+//               tcgen05.ld of 32-column register subtiles, statistics (the two
+//               halves combine theirs through shared memory), normalise /
+//               scale, bf16, swizzled shared-memory staging, TMA stores.
+//   warps 10-13 Lazy Pre-Norm: sum of squares of the staged A rows; spill
+//               layout (without Lazy Pre-Norm): the in-place normalisation of
+//               finished row blocks, from L2.
 // A stage is released when the MMA commit and (for Lazy Pre-Norm) the four
 // norm warps have all arrived on its "empty" barrier.
+//
+// LayerNorm statistics are one pass of shifted sums per column range: with k0
+// the row's first value in the range, s1 = sum(x - k0), s2 = sum((x - k0)^2),
+// mean = k0 + s1/n, M2 = s2 - s1^2/n (k0 is a sample of the row, so the
+// subtraction does not cancel catastrophically); ranges combine by the
+// parallel-variance rule M2 = sum M2_i + sum n_i (mean_i - mean)^2.
 #pragma once
 
 #include "ptx.cuh"
@@ -40,16 +58,19 @@ enum : int {
   MODE_PRE = 1,       // lazy pre-RMSNorm of A (sum of squares + epilogue scale)
   MODE_POST = 2,      // post-norm of the accumulator rows
   MODE_LN = 4,        // post-norm is LayerNorm (else RMSNorm)
-  MODE_CLUSTER = 8,   // rows split over a cluster of up to 8 CTAs along N
-  MODE_CL16 = 16,     // ... of up to 16 CTAs (non-portable cluster size)
+  MODE_CLUSTER = 8,   // rows split over a cluster of CTAs along N
+  MODE_SPILL = 16,    // spill layout: S slices per CTA, normalised from L2
+  MODE_BRES = 32,     // all of B (K x BN, <= 128 KB) resident in shared memory
 };
 
 struct FusedParams {
   int M, N, K;
-  int cluster;  // CTAs per cluster along N (1 without MODE_CLUSTER)
+  int cluster;      // CTAs per cluster along N (1 without MODE_CLUSTER)
+  int slices;       // S: BN-column slices per CTA and row block (1 unless MODE_SPILL)
   float eps, pre_eps;
   const __nv_bfloat16* gamma;
   const __nv_bfloat16* beta;
+  __nv_bfloat16* C;  // the output, re-read by the spill layout
   float* mean_out;
   float* rstd_out;
   float* pre_rstd_out;
@@ -63,7 +84,7 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
   return p;
 }
 
-template <int STAGES_, int BN_CTA, int CLMAX>
+template <int STAGES_, int GB, int CLMAX>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -72,64 +93,154 @@ struct Aux {
   uint64_t ss_full[2];
   uint64_t ss_empty[2];
   uint64_t xbar[2];
+  uint64_t nstat_full[2];
+  uint64_t nstat_empty[2];
+  uint64_t ebar[2];  // bounded group barrier of the eight epilogue warps
   uint64_t teardown;
+  uint64_t bres_full;
   uint32_t tmem_base;
   int abort_flag;
+  int nstat_m0[2];
+  int nstat_c0[2];
   float ss[2][128];
-  float gam[BN_CTA];
-  float bet[BN_CTA];
+  float2 nstat[2][128];
+  float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
+  float gam[GB];
+  float bet[GB];
   float2 xstat[2][CLMAX > 0 ? CLMAX : 1][128];
 };
 
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
 constexpr int kMaxStages = 8;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kBoxBytes = 32 * 64;  // one [32 rows x 32 columns] bf16 store box
 
-template <int BN_SUB_, int NSUB_, int BK_, int MODE_>
+template <int BN_, int MODE_, int CLMAX_ = 0>
 struct KCfg {
-  static constexpr int BN_SUB = BN_SUB_, NSUB = NSUB_, BK = BK_, MODE = MODE_;
+  static constexpr int BN = BN_, MODE = MODE_, BK = 64, BM = 128;
   static constexpr bool PRE = (MODE & MODE_PRE) != 0;
   static constexpr bool POST = (MODE & MODE_POST) != 0;
   static constexpr bool LN = (MODE & MODE_LN) != 0;
-  static constexpr bool CLUSTER = (MODE & (MODE_CLUSTER | MODE_CL16)) != 0;
-  static constexpr int CLMAX = (MODE & MODE_CL16) ? 16 : (CLUSTER ? 8 : 0);
-  static constexpr int BM = 128;
-  static constexpr int BN_CTA = BN_SUB * NSUB;
-  static constexpr int NBUF = (NSUB == 1) ? 2 : 1;  // accumulator buffers in TMEM
-  static constexpr int TMEM_COLS = pow2_at_least(NBUF * BN_CTA, 32);
+  static constexpr bool CLUSTER = (MODE & MODE_CLUSTER) != 0;
+  static constexpr bool SPILL = (MODE & MODE_SPILL) != 0;
+  static constexpr bool BRES = (MODE & MODE_BRES) != 0;
+  // the spill layout's in-place normalisation runs in its own warps (10-13)
+  // unless those warps compute the Lazy Pre-Norm sums of squares
+  static constexpr bool NORMW = SPILL && !PRE;
+  static constexpr bool AUXW = PRE || NORMW;  // warps 10-13 present
+  static constexpr int HALF = BN / 2;          // columns per epilogue half
+  static constexpr int NCH = HALF / 32;        // 32-column subtiles per half
+  static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
+  static constexpr int GB = (POST && !SPILL) ? BN : 1;  // gamma/beta kept in shared memory
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BK * BN_CTA * 2;
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t STG_BYTES = 4 * 2 * 4096;  // 4 epilogue warps x 2 buffers x [32 x 64] bf16
-  static constexpr uint32_t AUX_BYTES = (sizeof(Aux<kMaxStages, BN_CTA, CLMAX>) + 15) / 16 * 16;
-  static constexpr int STAGES_FIT = (int)((kSmemLimit - 1024 - STG_BYTES - AUX_BYTES) / STAGE_BYTES);
-  static constexpr int STAGES = STAGES_FIT < kMaxStages ? STAGES_FIT : kMaxStages;
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;
-  static constexpr int NUM_THREADS = 32 * (2 + 4 + (PRE ? 4 : 0));
-  static constexpr uint32_t SW_A = (BK == 64) ? kSwizzle128B : kSwizzle64B;
-  static constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN_SUB, true);
+  static constexpr uint32_t B_BYTES = BK * BN * 2;
+  // resident B: up to 128 KB, i.e. KB_MAX k-blocks of [64 x BN]
+  static constexpr int KB_MAX = BRES ? (int)(131072u / B_BYTES) : 0;
+  static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES);
+  static constexpr uint32_t AUX_BYTES = (sizeof(Aux<kMaxStages, GB, CLMAX>) + 15) / 16 * 16;
+  // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
+  // that buys a pipeline stage below 4
+  static constexpr int stages_with(int bufs) {
+    return (int)((kSmemLimit - 1024 - BRES_BYTES - kEpiWarps * bufs * kBoxBytes - AUX_BYTES) / STAGE_BYTES);
+  }
+  static constexpr int STG_BUFS = (stages_with(2) < 4 && stages_with(1) > stages_with(2)) ? 1 : 2;
+  static constexpr uint32_t STG_BYTES = kEpiWarps * STG_BUFS * kBoxBytes;
+  static constexpr int STAGES = stages_with(STG_BUFS) < kMaxStages ? stages_with(STG_BUFS) : kMaxStages;
+  static constexpr uint32_t SMEM_BYTES = 1024 + BRES_BYTES + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;
+  static constexpr int NUM_THREADS = 32 * (2 + kEpiWarps + (AUXW ? 4 : 0));
+  static constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, true);
 
-  static_assert(BK == 64 || BK == 32, "BK must be 64 (128B swizzle) or 32 (64B swizzle)");
-  static_assert(BN_SUB % 64 == 0 && BN_SUB >= 64 && BN_SUB <= 256, "UMMA N in 64..256, step 64");
-  static_assert(NSUB == 1 || NSUB == 2, "one or two accumulator subtiles per tile");
-  static_assert(NBUF * BN_CTA <= 512, "tensor memory holds 512 fp32 columns");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage ring");
-  static_assert(!(PRE && !POST) || !CLUSTER, "Lazy Pre-Norm alone never needs a cluster");
+  static_assert(!SPILL || (BN == 256 && POST && CLUSTER), "spill layout: 256-column slices, post-norm, cluster");
+  static_assert(!CLUSTER || (POST && CLMAX_ >= 1 && CLMAX_ <= 8), "clusters serve the post-norm, up to 8 CTAs");
+  static_assert(!BRES || !CLUSTER, "resident B serves one CTA per row block");
 };
+
+// Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
+// (columns c0..c0+255) of C, re-read from L2.  Lane l owns columns
+// c0+8l..c0+8l+7; mean and rstd of row r0+i are held by lane lane_off+i.
+template <bool LN>
+__device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, int nrows, int lane_off, int c0,
+                                                float mean, float rstd, int lane) {
+  const int col = c0 + lane * 8;
+  const bool colok = col < p.N;
+  float gv[8], bv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    gv[j] = 1.0f;
+    bv[j] = 0.0f;
+  }
+  if (colok && p.gamma != nullptr) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p.gamma + col);
+    gv[0] = bf16_lo(u.x); gv[1] = bf16_hi(u.x); gv[2] = bf16_lo(u.y); gv[3] = bf16_hi(u.y);
+    gv[4] = bf16_lo(u.z); gv[5] = bf16_hi(u.z); gv[6] = bf16_lo(u.w); gv[7] = bf16_hi(u.w);
+  }
+  if (colok && p.beta != nullptr) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p.beta + col);
+    bv[0] = bf16_lo(u.x); bv[1] = bf16_hi(u.x); bv[2] = bf16_lo(u.y); bv[3] = bf16_hi(u.y);
+    bv[4] = bf16_lo(u.z); bv[5] = bf16_hi(u.z); bv[6] = bf16_lo(u.w); bv[7] = bf16_hi(u.w);
+  }
+#pragma unroll 1
+  for (int rr = 0; rr < nrows; rr += 8) {
+    uint4 v[8];  // eight rows of loads in flight per lane
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int m = r0 + rr + u;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (colok && rr + u < nrows && m < p.M) v[u] = ld_global_cg_v4(p.C + static_cast<size_t>(m) * p.N + col);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float mu = __shfl_sync(0xffffffffu, mean, (lane_off + rr + u) & 31);
+      const float rs = __shfl_sync(0xffffffffu, rstd, (lane_off + rr + u) & 31);
+      const int m = r0 + rr + u;
+      if (colok && rr + u < nrows && m < p.M) {
+        const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float x0 = bf16_lo(in[h]), x1 = bf16_hi(in[h]);
+          const float y0 = (LN ? (x0 - mu) : x0) * rs * gv[2 * h] + bv[2 * h];
+          const float y1 = (LN ? (x1 - mu) : x1) * rs * gv[2 * h + 1] + bv[2 * h + 1];
+          o[h] = pack_bf16x2(y0, y1);
+        }
+        st_global_v4(p.C + static_cast<size_t>(m) * p.N + col, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    }
+  }
+}
+
+// Parallel-variance combination: fold (mean_b, m2_b) over nb values into
+// (mean, m2) over n values.
+__device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n, float mean_b, float m2_b,
+                                                float nb) {
+  if (nb <= 0.0f) return;
+  const float nn = n + nb;
+  const float d = mean_b - mean;
+  mean += d * (nb / nn);
+  m2 += m2_b + d * d * (n * nb / nn);
+  n = nn;
+}
 
 // ---------------------------------------------------------------------------
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
-  constexpr int BK = Cfg::BK, BN_SUB = Cfg::BN_SUB, NSUB = Cfg::NSUB, BN_CTA = Cfg::BN_CTA;
-  constexpr int STAGES = Cfg::STAGES, NBUF = Cfg::NBUF;
-  constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER;
+  constexpr int BK = Cfg::BK, BN = Cfg::BN, STAGES = Cfg::STAGES, HALF = Cfg::HALF, NCH = Cfg::NCH;
+  constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER, SPILL = Cfg::SPILL;
+  constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, BN_CTA, Cfg::CLMAX>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  const uint32_t base = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+  const uint32_t base0 = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+  const uint32_t bres_base = base0;                     // resident B (MODE_BRES)
+  const uint32_t base = base0 + Cfg::BRES_BYTES;        // the stage ring
   uint8_t* smem = smem_raw + (base - raw_addr);
   const uint32_t stg_base = base + STAGES * STAGE_BYTES;
   AuxT* aux = reinterpret_cast<AuxT*>(smem + STAGES * STAGE_BYTES + Cfg::STG_BYTES);
@@ -138,11 +249,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int M = p.M, N = p.N, K = p.K;
   const int C = CLUSTER ? p.cluster : 1;
+  const int S = SPILL ? p.slices : 1;
   const int rank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
   const int num_m = (M + Cfg::BM - 1) / Cfg::BM;
-  const int group_cols = BN_CTA * C;
+  const int cta_cols = S * BN;
+  const int group_cols = cta_cols * C;
   const int ngroups = (N + group_cols - 1) / group_cols;
-  const int total = num_m * ngroups;
+  const int total = num_m * ngroups;  // row blocks (x column groups) to visit
   const int cid = static_cast<int>(blockIdx.x) / C;
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_kb = (K + BK - 1) / BK;
@@ -157,12 +270,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&aux->acc_full[b]), 1);
-      mbar_init(smem_u32(&aux->acc_empty[b]), 4);
+      mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->ss_full[b]), 128);
-      mbar_init(smem_u32(&aux->ss_empty[b]), 128);
+      mbar_init(smem_u32(&aux->ss_empty[b]), 32 * kEpiWarps);
       mbar_init(smem_u32(&aux->xbar[b]), 1);
+      mbar_init(smem_u32(&aux->nstat_full[b]), 32 * kEpiWarps);
+      mbar_init(smem_u32(&aux->nstat_empty[b]), 128);
+      mbar_init(smem_u32(&aux->ebar[b]), 32 * kEpiWarps);
     }
     mbar_init(smem_u32(&aux->teardown), 1);
+    mbar_init(smem_u32(&aux->bres_full), 1);
     aux->abort_flag = 0;
     fence_mbar_init();
   }
@@ -175,46 +292,54 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     tmem_alloc(smem_u32(&aux->tmem_base), Cfg::TMEM_COLS);
     tmem_relinquish();
   }
-  if (POST && warp >= 2 && warp < 6) {
-    // post-norm CTAs own a fixed column slice: the whole row fits the cluster
-    const int n0 = rank * BN_CTA;
-    for (int j = static_cast<int>(threadIdx.x) - 64; j < BN_CTA; j += 128) {
-      const int n = n0 + j;
-      aux->gam[j] = (p.gamma != nullptr && n < N) ? __bfloat162float(p.gamma[n]) : 1.0f;
-      aux->bet[j] = (p.beta != nullptr && n < N) ? __bfloat162float(p.beta[n]) : 0.0f;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (CLUSTER) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_base;
+  // Set-up above overlaps the previous grid in the stream; every global
+  // access below comes after it has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, filled = 0, fill_par = 0;
       bool ok = true;
+      if (BRES && cid < total) {
+        // all of B once: num_kb k-blocks x BN/64 chunks of [64 x 64]
+        const uint32_t bf = smem_u32(&aux->bres_full);
+        mbar_arrive_expect_tx(bf, static_cast<uint32_t>(num_kb) * Cfg::B_BYTES);
+        for (int kb = 0; kb < num_kb; ++kb)
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(bres_base + kb * Cfg::B_BYTES + c * (BK * 128), &tmB, c * 64, kb * BK, bf);
+      }
       for (int t = cid; t < total && ok; t += ncl) {
         const int m0 = (t / ngroups) * Cfg::BM;
-        const int n0 = ((t % ngroups) * C + rank) * BN_CTA;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&aux->full[stage]);
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          tma_load_2d(sa, &tmA, kb * BK, m0, full);
-          const uint32_t sb = sa + A_BYTES;
+        for (int s = 0; s < S && ok; ++s) {
+          const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN;
+          for (int kb = 0; kb < num_kb; ++kb) {
+            if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&aux->full[stage]);
+            mbar_arrive_expect_tx(full, STAGE_BYTES);
+            const uint32_t sa = base + stage * STAGE_BYTES;
+            tma_load_2d(sa, &tmA, kb * BK, m0, full);
+            if (!BRES) {
+              const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int c = 0; c < BN_CTA / 64; ++c) tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
-          filled |= 1u << stage;
-          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+            }
+            filled |= 1u << stage;
+            fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
@@ -222,6 +347,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u)
           mbar_wait<false, true>(wc, smem_u32(&aux->full[s]), (fill_par >> s) & 1u, kSiteTeardown);
+      if (BRES && cid < total) mbar_wait<false, true>(wc, smem_u32(&aux->bres_full), 0, kSiteTeardown);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -229,241 +355,434 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl, ++it) {
-        const int buf = (NBUF == 2) ? (it & 1) : 0;
-        const uint32_t aph = static_cast<uint32_t>((NBUF == 2) ? (it >> 1) : it) & 1u;
-        if (!mbar_wait(wc, smem_u32(&aux->acc_empty[buf]), aph ^ 1u, kSiteMma)) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * BN_CTA);
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(wc, smem_u32(&aux->full[stage]), phase, kSiteMma)) {
+      if (BRES && cid < total) ok = mbar_wait(wc, smem_u32(&aux->bres_full), 0, kSiteMma);
+      for (int t = cid; t < total && ok; t += ncl) {
+        for (int s = 0; s < S && ok; ++s, ++it) {
+          const int buf = it & 1;
+          const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+          if (!mbar_wait(wc, smem_u32(&aux->acc_empty[buf]), aph ^ 1u, kSiteMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * BN);
+          for (int kb = 0; kb < num_kb; ++kb) {
+            if (!mbar_wait(wc, smem_u32(&aux->full[stage]), phase, kSiteMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = base + stage * STAGE_BYTES;
+            const uint32_t sb = BRES ? bres_base + kb * Cfg::B_BYTES : sa + A_BYTES;
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            // A: K-major, rows of BK*2 bytes, 8-row groups BK*16 bytes apart;
-            // a K step of 16 elements is 32 bytes inside the swizzle row.
-            const uint64_t da = make_smem_desc(sa + ks * 32, 16, 8 * BK * 2, Cfg::SW_A);
-#pragma unroll
-            for (int sub = 0; sub < NSUB; ++sub) {
-              // B: MN-major, 64-column chunks of BK rows x 128 bytes;
-              // LBO = chunk stride along N, SBO = 8-row group stride along K;
-              // a K step of 16 rows is 2048 bytes.
-              const uint64_t db = make_smem_desc(sb + sub * (BN_SUB / 64) * (BK * 128) + ks * (16 * 128),
-                                                 BK * 128, 1024, kSwizzle128B);
-              umma_bf16(d0 + sub * BN_SUB, da, db, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+            for (int ks = 0; ks < BK / 16; ++ks) {
+              // A: K-major, 128-byte rows, 8-row groups 1024 bytes apart; a K step
+              // of 16 elements is 32 bytes inside the swizzled row.
+              const uint64_t da = make_smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
+              // B: MN-major, 64-column chunks of 64 rows x 128 bytes; LBO = chunk
+              // stride along N, SBO = 8-row group stride along K; a K step of 16
+              // rows is 2048 bytes.
+              const uint64_t db = make_smem_desc(sb + ks * (16 * 128), BK * 128, 1024, kSwizzle128B);
+              umma_bf16(d0, da, db, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&aux->empty[stage]));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
             }
           }
-          umma_commit(smem_u32(&aux->empty[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (ok) umma_commit(smem_u32(&aux->acc_full[buf]));
         }
-        if (ok) umma_commit(smem_u32(&aux->acc_full[buf]));
       }
       // every MMA issued has completed before tensor memory is released
       umma_commit(smem_u32(&aux->teardown));
       mbar_wait<false, true>(wc, smem_u32(&aux->teardown), 0, kSiteTeardown);
     }
-  } else if (warp < 6) {
-    // ======================= epilogue =======================
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;
-    const uint32_t stg = stg_base + static_cast<uint32_t>(warp - 2) * 8192u;
+  } else if (warp < 2 + kEpiWarps) {
+    // ======================= epilogue (8 warps) =======================
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;     // column half of each tile
+    const int row = q * 32 + lane;     // tile row of this thread
+    const int etid = static_cast<int>(threadIdx.x) - 64;  // 0..255
+    const uint32_t stg = stg_base + static_cast<uint32_t>(warp - 2) * (Cfg::STG_BUFS * kBoxBytes);
     uint32_t sbuf = 0;
     int it = 0;
-    for (int t = cid; t < total; t += ncl, ++it) {
+
+    if (POST && !SPILL) {
+      // resident post-norm CTAs own one fixed BN-column slice of every row
+      const int n0 = rank * BN;
+      for (int j = etid; j < BN; j += 32 * kEpiWarps) {
+        const int n = n0 + j;
+        aux->gam[j] = (p.gamma != nullptr && n < N) ? __bfloat162float(p.gamma[n]) : 1.0f;
+        aux->bet[j] = (p.beta != nullptr && n < N) ? __bfloat162float(p.beta[n]) : 0.0f;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
+    }
+
+    // stage one [32 rows x 32 columns] bf16 box of this warp's rows (64-byte
+    // swizzle) and store it with TMA
+    auto store_box = [&](const uint32_t (&w)[16], int col0, int m0) {
+      const uint32_t sbase = stg + sbuf * kBoxBytes;
+      if (lane == 0) {
+        if (Cfg::STG_BUFS == 2) bulk_wait_read<1>();  // the store that used this buffer has read it
+        else bulk_wait_read<0>();
+      }
+      __syncwarp();
+      // row `lane` of the box: 16-byte chunk ch sits at chunk (ch ^ ((row >> 1) & 3))
+      const uint32_t rbase = sbase + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t a = rbase + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * ch]), "r"(w[4 * ch + 1]),
+                     "r"(w[4 * ch + 2]), "r"(w[4 * ch + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (m0 + q * 32 < M) tma_store_2d(&tmC, sbase, col0, m0 + q * 32);
+        bulk_commit();
+      }
+      if (Cfg::STG_BUFS == 2) sbuf ^= 1u;
+    };
+
+    // barrier of the eight epilogue warps on an mbarrier, so that it is
+    // bounded like every other wait (returns false if it gave up)
+    int esn = 0;
+    auto esync = [&]() -> bool {
+      const int b = esn & 1;
+      mbar_arrive(smem_u32(&aux->ebar[b]));
+      const bool r =
+          mbar_wait_warp(wc, smem_u32(&aux->ebar[b]), static_cast<uint32_t>(esn >> 1) & 1u, kSiteEpilogue);
+      ++esn;
+      return r;
+    };
+
+    // combine this row's partial statistics of the two column halves, in
+    // half order (identical in both halves)
+    auto combine_halves = [&](float& part0, float& part1, float nh0, float nh1) -> bool {
+      const int hp = esn & 1;
+      aux->hstat[hp][h][row] = make_float2(part0, part1);
+      if (!esync()) return false;
+      const float2 a = aux->hstat[hp][0][row];
+      const float2 b = aux->hstat[hp][1][row];
+      if (LN) {
+        float mean = 0.0f, m2 = 0.0f, n = 0.0f;
+        combine_mean_m2(mean, m2, n, a.x, a.y, nh0);
+        combine_mean_m2(mean, m2, n, b.x, b.y, nh1);
+        part0 = mean;
+        part1 = m2;
+      } else {
+        part0 = a.x + b.x;
+        part1 = 0.0f;
+      }
+      return true;
+    };
+
+    // exchange (part0, part1) of this row with the cluster and combine them
+    // in rank order; half 0 pushes, both halves wait and combine; returns
+    // false if the wait gave up
+    auto exchange = [&](float& part0, float& part1, int g, int xit) -> bool {
+      const int xp = xit & 1;
+      const uint32_t xb = smem_u32(&aux->xbar[xp]);
+      if (etid == 0) mbar_arrive_expect_tx(xb, static_cast<uint32_t>(C) * 128u * 8u);
+      if (h == 0) {
+        const uint32_t mine = smem_u32(&aux->xstat[xp][rank][row]);
+        for (int r2 = 0; r2 < C; ++r2) st_async_f32x2(mapa_shared(mine, r2), part0, part1, mapa_shared(xb, r2));
+      }
+      if (!mbar_wait_warp<true>(wc, xb, static_cast<uint32_t>(xit >> 1) & 1u, kSiteExchange)) return false;
+      float n_acc = 0.0f, m_acc = 0.0f, q_acc = 0.0f;
+      for (int r2 = 0; r2 < C; ++r2) {
+        const float2 v = aux->xstat[xp][r2][row];
+        const int nq = min(max(N - (g * C + r2) * cta_cols, 0), cta_cols);
+        if (LN) combine_mean_m2(m_acc, q_acc, n_acc, v.x, v.y, static_cast<float>(nq));
+        else q_acc += v.x;
+      }
+      part0 = LN ? m_acc : q_acc;
+      part1 = q_acc;
+      return true;
+    };
+
+    // spill-layout state: running shifted sums of this half over the current
+    // row block, and (inline normalisation only) the pending row block
+    float k0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f;
+    bool pend = false;
+    int pm0 = 0, pc0 = 0, pnext = 0;
+    float pmean = 0.0f, prstd = 1.0f;
+    int xit = 0;  // row-block statistics completed so far
+    bool ok = true;
+
+    for (int t = cid; t < total && ok; t += ncl) {
       const int m0 = (t / ngroups) * Cfg::BM;
       const int g = t % ngroups;
-      const int n0 = (g * C + rank) * BN_CTA;
-      const int buf = (NBUF == 2) ? (it & 1) : 0;
-      const uint32_t aph = static_cast<uint32_t>((NBUF == 2) ? (it >> 1) : it) & 1u;
-      if (!mbar_wait_warp(wc, smem_u32(&aux->acc_full[buf]), aph, kSiteEpilogue)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN_CTA);
-
-      // ---- lazy pre-norm scale: rstd of the A row ----
-      float pre = 1.0f;
-      if (PRE) {
-        const int sb = it & 1;
-        if (!mbar_wait_warp(wc, smem_u32(&aux->ss_full[sb]), static_cast<uint32_t>(it >> 1) & 1u, kSiteEpilogue))
+      for (int s = 0; s < S && ok; ++s, ++it) {
+        const int n0 = (g * C + rank) * cta_cols + s * BN;  // first column of the tile
+        const int c0h = n0 + h * HALF;                      // first column of this half
+        const int buf = it & 1;
+        const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait_warp(wc, smem_u32(&aux->acc_full[buf]), aph, kSiteEpilogue)) {
+          ok = false;
           break;
-        const float ss = aux->ss[sb][row];
-        mbar_arrive(smem_u32(&aux->ss_empty[sb]));
-        pre = rsqrtf(ss / static_cast<float>(K) + p.pre_eps);
-      }
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(buf * BN + h * HALF);
 
-      // ---- post-norm statistics ----
-      float mean = 0.0f, rstd = 1.0f;
-      if (POST) {
-        const int nvalid = min(max(N - n0, 0), BN_CTA);
-        float part0 = 0.0f, part1 = 0.0f;  // LN: (mean, M2) of the slice; RMS: (sum x^2, 0)
-        {
-          float s[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int c = 0; c < BN_CTA / 32; ++c) {
-            if (c * 32 >= nvalid) break;
+        // ---- lazy pre-norm scale: rstd of the A row ----
+        float pre = 1.0f;
+        if (PRE) {
+          const int sb = it & 1;
+          if (!mbar_wait_warp(wc, smem_u32(&aux->ss_full[sb]), static_cast<uint32_t>(it >> 1) & 1u,
+                              kSiteEpilogue)) {
+            ok = false;
+            break;
+          }
+          const float ss = aux->ss[sb][row];
+          mbar_arrive(smem_u32(&aux->ss_empty[sb]));
+          pre = rsqrtf(ss / static_cast<float>(K) + p.pre_eps);
+        }
+        const int nvh = min(max(N - c0h, 0), HALF);  // valid columns of this half
+
+        if (SPILL) {
+          // ---- pass 1: statistics + un-normalised (pre-scaled) bf16 slice to C ----
+          if (s == 0) sum1 = sum2 = 0.0f;
+          for (int c = 0; c < NCH; ++c) {
+            if (c * 32 >= nvh) break;
             uint32_t r[32];
             tmem_ld_32x32b_x32(tb + c * 32, r);
             tmem_ld_wait();
             reg_fence(r);
-            const int lim = nvalid - c * 32;
+            if (LN && s == 0 && c == 0) k0 = __uint_as_float(r[0]) * pre;
+            uint32_t w[16];
+            float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
+            const int lim = nvh - c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float v0 = __uint_as_float(r[j]) * pre, v1 = __uint_as_float(r[j + 1]) * pre;
+              const float d0 = LN ? v0 - k0 : v0, d1 = LN ? v1 - k0 : v1;
+              if (j < lim) { a1[0] += d0; a2[0] = fmaf(d0, d0, a2[0]); }
+              if (j + 1 < lim) { a1[1] += d1; a2[1] = fmaf(d1, d1, a2[1]); }
+              w[j >> 1] = pack_bf16x2(v0, v1);
+            }
+            sum1 += a1[0] + a1[1];
+            sum2 += a2[0] + a2[1];
+            store_box(w, c0h + c * 32, m0);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
+
+          // ---- (inline) one slice of the pending row block's normalisation ----
+          if (!NORMW && pend) {
+            normalize_slice<LN>(p, pm0 + q * 32 + 16 * h, 16, 16 * h, pc0 + pnext * BN, pmean, prstd, lane);
+            if (++pnext == S) pend = false;
+          }
+          if (s == S - 1) {
+            // ---- row block complete: statistics, exchange, then hand it over ----
+            const int cbase = (g * C + rank) * cta_cols;
+            float nh[2] = {0.f, 0.f};
+            for (int s2 = 0; s2 < S; ++s2)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+                nh[hh] += static_cast<float>(min(max(N - (cbase + s2 * BN + hh * HALF), 0), HALF));
+            const float nmine = nh[h];
+            float part0, part1;
+            if (LN) {
+              part0 = nmine > 0.0f ? k0 + sum1 / nmine : 0.0f;
+              part1 = nmine > 0.0f ? fmaxf(sum2 - sum1 * sum1 / nmine, 0.0f) : 0.0f;
+            } else {
+              part0 = sum2;
+              part1 = 0.0f;
+            }
+            if (!combine_halves(part0, part1, nh[0], nh[1]) || !exchange(part0, part1, g, xit)) {
+              ok = false;
+              break;
+            }
+            ++xit;
+            const float mean = LN ? part0 : 0.0f;
+            const float rstd = rsqrtf((LN ? part1 : part0) / static_cast<float>(N) + p.eps);
+            const int m = m0 + row;
+            if (h == 0 && rank == 0 && g == 0 && m < M) {
+              if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
+              if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
+              if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
+            }
+            if (NORMW) {
+              // hand the row block to the normaliser warps
+              const int nb = xit - 1;
+              const int b = nb & 1;
+              if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_empty[b]), (static_cast<uint32_t>(nb >> 1) & 1u) ^ 1u,
+                                  kSiteEpilogue)) {
+                ok = false;
+                break;
+              }
+              // this warp's un-normalised stores are complete and visible
+              // before they are read back
+              if (lane == 0) {
+                bulk_wait<0>();
+                fence_proxy_async_global();
+              }
+              __syncwarp();
+              if (h == 0) aux->nstat[b][row] = make_float2(mean, rstd);
+              if (etid == 0) {
+                aux->nstat_m0[b] = m0;
+                aux->nstat_c0[b] = cbase;
+              }
+              mbar_arrive(smem_u32(&aux->nstat_full[b]));
+            } else {
+              while (pend) {  // (only when S == 1 would anything remain)
+                normalize_slice<LN>(p, pm0 + q * 32 + 16 * h, 16, 16 * h, pc0 + pnext * BN, pmean, prstd, lane);
+                if (++pnext == S) pend = false;
+              }
+              // both halves' stores of this block are complete before either
+              // half re-reads rows the other half wrote
+              if (lane == 0) {
+                bulk_wait<0>();
+                fence_proxy_async_global();
+              }
+              if (!esync()) {
+                ok = false;
+                break;
+              }
+              pend = true;
+              pm0 = m0;
+              pc0 = cbase;
+              pnext = 0;
+              pmean = mean;
+              prstd = rstd;
+            }
+          }
+          continue;
+        }
+
+        // ---- resident layouts: statistics straight from tensor memory ----
+        float mean = 0.0f, rstd = 1.0f;
+        if (POST) {
+          float kk = 0.0f;
+          float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
+          for (int c = 0; c < NCH; ++c) {
+            if (c * 32 >= nvh) break;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + c * 32, r);
+            tmem_ld_wait();
+            reg_fence(r);
+            if (LN && c == 0) kk = __uint_as_float(r[0]) * pre;
+            const int lim = nvh - c * 32;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float v = __uint_as_float(r[j]) * pre;
-              const float add = LN ? v : v * v;
-              s[j & 3] += (j < lim) ? add : 0.0f;
+              const float d = LN ? v - kk : v;
+              if (j < lim) {
+                a1[j & 1] += d;
+                a2[j & 1] = fmaf(d, d, a2[j & 1]);
+              }
             }
           }
-          const float tot = (s[0] + s[1]) + (s[2] + s[3]);
+          const float s1 = a1[0] + a1[1], s2 = a2[0] + a2[1];
+          const float nf = static_cast<float>(nvh);
+          float part0, part1;
           if (LN) {
-            const float m_loc = nvalid > 0 ? tot / static_cast<float>(nvalid) : 0.0f;
-            float d2[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int c = 0; c < BN_CTA / 32; ++c) {
-              if (c * 32 >= nvalid) break;
-              uint32_t r[32];
-              tmem_ld_32x32b_x32(tb + c * 32, r);
-              tmem_ld_wait();
-              reg_fence(r);
-              const int lim = nvalid - c * 32;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float d = __uint_as_float(r[j]) * pre - m_loc;
-                d2[j & 3] += (j < lim) ? d * d : 0.0f;
-              }
-            }
-            part0 = m_loc;
-            part1 = (d2[0] + d2[1]) + (d2[2] + d2[3]);
+            part0 = nvh > 0 ? kk + s1 / nf : 0.0f;
+            part1 = nvh > 0 ? fmaxf(s2 - s1 * s1 / nf, 0.0f) : 0.0f;
           } else {
-            part0 = tot;
+            part0 = s2;
+            part1 = 0.0f;
           }
-        }
-        if (CLUSTER) {
-          // push (part0, part1) for this row to every CTA of the cluster
-          const int xp = it & 1;
-          const uint32_t xb = smem_u32(&aux->xbar[xp]);
-          if (threadIdx.x == 64) mbar_arrive_expect_tx(xb, static_cast<uint32_t>(C) * 128u * 8u);
-          const uint32_t mine = smem_u32(&aux->xstat[xp][rank][row]);
-          for (int r2 = 0; r2 < C; ++r2)
-            st_async_f32x2(mapa_shared(mine, r2), part0, part1, mapa_shared(xb, r2));
-          if (!mbar_wait_warp<true>(wc, xb, static_cast<uint32_t>(it >> 1) & 1u, kSiteExchange)) break;
-          // combine the slices in rank order (identical on every CTA)
-          float n_acc = 0.0f, m_acc = 0.0f, q_acc = 0.0f;
-          for (int r2 = 0; r2 < C; ++r2) {
-            const float2 v = aux->xstat[xp][r2][row];
-            const int nq = min(max(N - (g * C + r2) * BN_CTA, 0), BN_CTA);
-            if (LN) {
-              if (nq > 0) {
-                const float nqf = static_cast<float>(nq);
-                const float nn = n_acc + nqf;
-                const float d = v.x - m_acc;
-                m_acc += d * (nqf / nn);
-                q_acc += v.y + d * d * (n_acc * nqf / nn);
-                n_acc = nn;
-              }
-            } else {
-              q_acc += v.x;
+          const float n_h0 = static_cast<float>(min(max(N - n0, 0), HALF));
+          const float n_h1 = static_cast<float>(min(max(N - n0 - HALF, 0), HALF));
+          if (!combine_halves(part0, part1, n_h0, n_h1)) {
+            ok = false;
+            break;
+          }
+          if (CLUSTER) {
+            if (!exchange(part0, part1, g, xit)) {
+              ok = false;
+              break;
             }
+            ++xit;
           }
-          part0 = LN ? m_acc : q_acc;
-          part1 = q_acc;
+          if (LN) {
+            mean = part0;
+            rstd = rsqrtf(part1 / static_cast<float>(N) + p.eps);
+          } else {
+            rstd = rsqrtf(part0 / static_cast<float>(N) + p.eps);
+          }
         }
-        if (LN) {
-          mean = part0;
-          rstd = rsqrtf(part1 / static_cast<float>(N) + p.eps);
-        } else {
-          rstd = rsqrtf(part0 / static_cast<float>(N) + p.eps);
-        }
-      }
 
-      // ---- normalise / scale, bf16, stage, TMA store: 64 columns at a time ----
-      for (int c = 0; c < BN_CTA / 64; ++c) {
-        const int col0 = n0 + c * 64;
-        if (col0 >= N) break;
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tb + c * 64, r0);
-        tmem_ld_32x32b_x32(tb + c * 64 + 32, r1);
-        tmem_ld_wait();
-        reg_fence(r0);
-        reg_fence(r1);
-        uint32_t w[32];
+        // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
+        for (int c = 0; c < NCH; ++c) {
+          const int col0 = c0h + c * 32;
+          if (col0 >= N) break;
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tb + c * 32, r);
+          tmem_ld_wait();
+          reg_fence(r);
+          uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float y0 = __uint_as_float(r0[j]) * pre, y1 = __uint_as_float(r0[j + 1]) * pre;
-          if (POST) {
-            const int cj = c * 64 + j;
-            y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
-            y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
+          for (int j = 0; j < 32; j += 2) {
+            float y0 = __uint_as_float(r[j]) * pre, y1 = __uint_as_float(r[j + 1]) * pre;
+            if (POST) {
+              const int cj = h * HALF + c * 32 + j;
+              y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
+              y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
+            }
+            w[j >> 1] = pack_bf16x2(y0, y1);
           }
-          w[j >> 1] = pack_bf16x2(y0, y1);
+          store_box(w, col0, m0);
         }
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float y0 = __uint_as_float(r1[j]) * pre, y1 = __uint_as_float(r1[j + 1]) * pre;
-          if (POST) {
-            const int cj = c * 64 + 32 + j;
-            y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
-            y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
-          }
-          w[16 + (j >> 1)] = pack_bf16x2(y0, y1);
-        }
-        const uint32_t sbase = stg + sbuf * 4096u;
-        if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+        tc_fence_before();
         __syncwarp();
-        // row `lane` of a [32 x 64] bf16 box, 128-byte swizzle: 16-byte chunk
-        // ch of the row sits at chunk (ch ^ (row & 7))
-        const uint32_t rbase = sbase + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t a = rbase + (static_cast<uint32_t>(ch ^ (lane & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * ch]), "r"(w[4 * ch + 1]),
-                       "r"(w[4 * ch + 2]), "r"(w[4 * ch + 3])
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (m0 + q * 32 < M) tma_store_2d(&tmC, sbase, col0, m0 + q * 32);
-          bulk_commit();
-        }
-        sbuf ^= 1u;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
+        if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
 
-      // ---- row statistics ----
-      const int m = m0 + row;
-      if (m < M) {
-        if (POST) {
-          if (rank == 0) {
-            if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
-            if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
-            if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
+        // ---- row statistics ----
+        const int m = m0 + row;
+        if (h == 0 && m < M) {
+          if (POST) {
+            if (rank == 0) {
+              if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
+              if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
+              if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
+            }
+          } else if (PRE) {
+            if (g == 0 && p.rstd_out != nullptr) p.rstd_out[m] = pre;
           }
-        } else if (PRE) {
-          if (g == 0 && p.rstd_out != nullptr) p.rstd_out[m] = pre;
         }
       }
     }
-    if (lane == 0) bulk_wait<0>();
-  } else {
+    if (SPILL && !NORMW && ok) {
+      while (pend) {  // the last row block
+        normalize_slice<LN>(p, pm0 + q * 32 + 16 * h, 16, 16 * h, pc0 + pnext * BN, pmean, prstd, lane);
+        if (++pnext == S) pend = false;
+      }
+    }
+    if (lane == 0) bulk_wait_read<0>();  // staging is read; the writes complete with the grid
+  } else if (NORMW) {
+    // ======================= normaliser warps (spill layout) =======================
+    const int k = warp - (2 + kEpiWarps);  // rows 32k..32k+31 of each row block
+    int nb = 0;
+    for (int t = cid; t < total; t += ncl, ++nb) {
+      const int b = nb & 1;
+      if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_full[b]), static_cast<uint32_t>(nb >> 1) & 1u, kSiteEpilogue))
+        break;
+      const float2 st = aux->nstat[b][k * 32 + lane];
+      const int m0 = aux->nstat_m0[b];
+      const int c0 = aux->nstat_c0[b];
+      mbar_arrive(smem_u32(&aux->nstat_empty[b]));
+      for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
+    }
+  } else if (PRE) {
     // ======================= norm warps (Lazy Pre-Norm) =======================
-    if (PRE) {
-      const int row = (warp - 6) * 32 + lane;
-      constexpr int ROW_BYTES = BK * 2;
-      constexpr int CHUNKS = ROW_BYTES / 16;
-      // swizzle phase of this row: chunk index XOR (row address bits 7..)
-      const int swz = ((row * ROW_BYTES) >> 7) & (CHUNKS - 1);
-      uint32_t stage = 0, phase = 0;
-      int it = 0;
-      for (int t = cid; t < total; t += ncl, ++it) {
+    const int row = (warp - (2 + kEpiWarps)) * 32 + lane;
+    constexpr int ROW_BYTES = BK * 2;
+    constexpr int CHUNKS = ROW_BYTES / 16;
+    // swizzle phase of this row: chunk index XOR (row address bits 7..9)
+    const int swz = ((row * ROW_BYTES) >> 7) & (CHUNKS - 1);
+    uint32_t stage = 0, phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = cid; t < total && ok; t += ncl) {
+      for (int s = 0; s < S && ok; ++s, ++it) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_warp(wc, smem_u32(&aux->full[stage]), phase, kSiteNorm)) {
             ok = false;
@@ -494,8 +813,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
         if (!ok) break;
         const int sb = it & 1;
-        if (!mbar_wait_warp(wc, smem_u32(&aux->ss_empty[sb]), (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, kSiteNorm))
+        if (!mbar_wait_warp(wc, smem_u32(&aux->ss_empty[sb]), (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u,
+                            kSiteNorm)) {
+          ok = false;
           break;
+        }
         aux->ss[sb][row] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         mbar_arrive(smem_u32(&aux->ss_full[sb]));
       }

@@ -1,6 +1,6 @@
 // fused_launch.cuh — host launch of one instantiation of fused_gemm_kernel:
 // tensor maps, persistent grid sizing (one CTA per SM, or as many clusters as
-// can be co-resident), cluster attributes.
+// can be co-resident), cluster and programmatic-dependent-launch attributes.
 #pragma once
 
 #include <atomic>
@@ -21,22 +21,24 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   if (!((configured.load(std::memory_order_acquire) >> dev.id) & 1ull)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-    if (Cfg::CLMAX > 8) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
-    }
     configured.fetch_or(1ull << dev.id, std::memory_order_acq_rel);
   }
+  if (Cfg::BRES && (L.N > Cfg::BN || (L.K + Cfg::BK - 1) / Cfg::BK > Cfg::KB_MAX)) {
+    set_error("internal: resident-B kernel given N %d, K %d", L.N, L.K);
+    return FNORM_ERR_UNSUPPORTED;
+  }
 
+  // A [M,K] in [128 x 64] boxes; B [K,N] in [64 x 64] boxes (MN-major for the
+  // MMA); C [M,N] in [32 x 32] store boxes (64-byte rows)
   CUtensorMap ta, tb, tc;
   st = encode_tmap_bf16_2d(&ta, L.A, (uint64_t)L.K, (uint64_t)L.M, (uint64_t)L.K * 2, Cfg::BK, Cfg::BM,
-                           Cfg::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FNORM_OK) return st;
   st = encode_tmap_bf16_2d(&tb, L.B, (uint64_t)L.N, (uint64_t)L.K, (uint64_t)L.N * 2, 64, Cfg::BK,
                            CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FNORM_OK) return st;
-  st = encode_tmap_bf16_2d(&tc, L.C, (uint64_t)L.N, (uint64_t)L.M, (uint64_t)L.N * 2, 64, 32,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+  st = encode_tmap_bf16_2d(&tc, L.C, (uint64_t)L.N, (uint64_t)L.M, (uint64_t)L.N * 2, 32, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != FNORM_OK) return st;
 
   FusedParams p;
@@ -44,10 +46,12 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.N = L.N;
   p.K = L.K;
   p.cluster = Cfg::CLUSTER ? L.cluster : 1;
+  p.slices = Cfg::SPILL ? L.slices : 1;
   p.eps = L.eps;
   p.pre_eps = L.pre_eps;
   p.gamma = static_cast<const __nv_bfloat16*>(L.gamma);
   p.beta = static_cast<const __nv_bfloat16*>(L.beta);
+  p.C = static_cast<__nv_bfloat16*>(L.C);
   p.mean_out = L.mean_out;
   p.rstd_out = L.rstd_out;
   p.pre_rstd_out = L.pre_rstd_out;
@@ -56,32 +60,43 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
 
   const int C = p.cluster;
   const int num_m = (L.M + Cfg::BM - 1) / Cfg::BM;
-  const int group_cols = Cfg::BN_CTA * C;
+  const int group_cols = Cfg::BN * p.slices * C;
   const int ngroups = (L.N + group_cols - 1) / group_cols;
   const long long total = (long long)num_m * ngroups;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (pdl_enabled()) {
+    // the kernel's set-up may overlap the previous grid; its first global
+    // access waits for that grid (griddepcontrol.wait)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   if (Cfg::CLUSTER) {
     if (C < 1 || C > Cfg::CLMAX) {
       set_error("cluster size %d outside 1..%d for this kernel", C, Cfg::CLMAX);
       return FNORM_ERR_UNSUPPORTED;
     }
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute& ca = attr[cfg.numAttrs++];
+    ca.id = cudaLaunchAttributeClusterDimension;
+    ca.val.clusterDim.x = (unsigned)C;
+    ca.val.clusterDim.y = 1;
+    ca.val.clusterDim.z = 1;
     // co-resident clusters, cached per device and cluster size
-    static std::atomic<int> max_clusters[64][17];
+    static std::atomic<int> max_clusters[64][9];
     int mc = max_clusters[dev.id][C].load(std::memory_order_relaxed);
     if (mc == 0) {
-      cfg.gridDim = dim3((unsigned)C, 1, 1);
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, (void*)kern, &cfg);
+      cudaLaunchConfig_t q = cfg;  // occupancy query: the cluster attribute only
+      q.gridDim = dim3((unsigned)C, 1, 1);
+      q.attrs = &ca;
+      q.numAttrs = 1;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, (void*)kern, &q);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
       if (mc <= 0) {
         set_error("no cluster of %d CTAs (%u bytes of shared memory each) fits on this device", C,

@@ -1,22 +1,31 @@
 // fused_plain.cu — instantiations of the fused kernel for the plain GEMM and
-// the Lazy Pre-RMSNorm GEMM (one CTA per 128 x BN tile, persistent).
+// the Lazy Pre-RMSNorm GEMM (one CTA per 128 x BN tile, persistent), with B
+// streamed per k-block or, for N <= BN and short K, resident in shared memory.
 #include "fused_launch.cuh"
 
 namespace fnorm {
 
+namespace {
+template <int BN>
+fnorm_status_t by_mode(const FusedLaunch& L, bool pre) {
+  if (L.bres) return pre ? launch_cfg<KCfg<BN, MODE_PRE | MODE_BRES>>(L) : launch_cfg<KCfg<BN, MODE_BRES>>(L);
+  return pre ? launch_cfg<KCfg<BN, MODE_PRE>>(L) : launch_cfg<KCfg<BN, 0>>(L);
+}
+}  // namespace
+
 fnorm_status_t launch_fused_plain(const FusedLaunch& L) {
   const bool pre = (L.mode & MODE_PRE) != 0;
-  if (L.nsub != 1 || (L.mode & ~MODE_PRE) != 0) {
-    set_error("internal: unexpected plain-GEMM plan (mode %d, nsub %d)", L.mode, L.nsub);
+  if ((L.mode & ~MODE_PRE) != 0 || L.spill || L.cluster != 1) {
+    set_error("internal: unexpected plain-GEMM plan (mode %d)", L.mode);
     return FNORM_ERR_UNSUPPORTED;
   }
-  switch (L.bn_sub) {
-    case 64:  return pre ? launch_cfg<KCfg<64, 1, 64, MODE_PRE>>(L) : launch_cfg<KCfg<64, 1, 64, 0>>(L);
-    case 128: return pre ? launch_cfg<KCfg<128, 1, 64, MODE_PRE>>(L) : launch_cfg<KCfg<128, 1, 64, 0>>(L);
-    case 256: return pre ? launch_cfg<KCfg<256, 1, 64, MODE_PRE>>(L) : launch_cfg<KCfg<256, 1, 64, 0>>(L);
+  switch (L.bn) {
+    case 64:  return by_mode<64>(L, pre);
+    case 128: return by_mode<128>(L, pre);
+    case 256: return by_mode<256>(L, pre);
     default: break;
   }
-  set_error("internal: no plain-GEMM kernel with tile width %d", L.bn_sub);
+  set_error("internal: no plain-GEMM kernel with tile width %d", L.bn);
   return FNORM_ERR_UNSUPPORTED;
 }
 

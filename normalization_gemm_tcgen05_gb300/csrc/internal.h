@@ -27,6 +27,9 @@ fnorm_status_t current_device(DeviceInfo* out);
 
 uint64_t wait_limit_ns();
 int forced_postnorm_cluster();
+// programmatic dependent launch for every kernel of the library (environment
+// variable FNORM_PDL=0 turns it off)
+bool pdl_enabled();
 
 // 2-D row-major bf16 tensor map: `inner` elements per row (contiguous),
 // `outer` rows, `pitch_bytes` between rows; box of box_inner x box_outer.
@@ -39,9 +42,11 @@ struct FusedLaunch {
   const void* B;
   void* C;
   int M, N, K;
-  int mode;     // MODE_* bits of fused_gemm.cuh (cluster bits are set by the planner)
-  int bn_sub;   // UMMA N of one accumulator subtile (64..256, multiple of 64)
-  int nsub;     // accumulator subtiles per CTA tile (1 or 2)
+  int mode;     // MODE_* bits of fused_gemm.cuh (cluster/spill/resident-B bits are set by the launcher)
+  int bn;       // UMMA N of one accumulator tile (64..256, multiple of 64)
+  int slices;   // spill layout: BN-column slices per CTA and row block, else 1
+  bool spill;   // post-norm spill layout (rows wider than the cluster's tensor memory)
+  bool bres;    // all of B resident in shared memory (N <= bn, K <= 128 KB / (bn * 2), many row blocks)
   int cluster;  // CTAs per cluster along N (post-norm), else 1
   float eps, pre_eps;
   const void* gamma;

@@ -166,6 +166,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// order this thread's completed async-proxy (TMA store) global writes with
+// its later generic-proxy accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// 16-byte global load cached in L2 only (data written earlier by this kernel)
+__device__ __forceinline__ uint4 ld_global_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // --------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor core
 // --------------------------------------------------------------------------
@@ -263,6 +284,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// --------------------------------------------------------------------------
+// programmatic dependent launch
+// --------------------------------------------------------------------------
+// Block until the grids this one depends on (earlier launches in the stream)
+// have completed and their memory is visible.  Every global access of a
+// kernel launched with programmatic serialisation comes after this.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled (its own wait still
+// orders its memory accesses after this grid's completion).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // --------------------------------------------------------------------------

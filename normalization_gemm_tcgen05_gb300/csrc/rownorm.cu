@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ mean_out,
                                                        float* __restrict__ rstd_out) {
   __shared__ float red[32];
+  grid_dependency_wait();  // launched with programmatic serialisation: inputs are ready after this
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int rpb = blockDim.x / tpr;
   const int row = blockIdx.x * rpb + static_cast<int>(threadIdx.x) / tpr;
   const int t = static_cast<int>(threadIdx.x) % tpr;
@@ -149,17 +151,25 @@ fnorm_status_t launch_rownorm(const void* X, void* Y, int M, int N, bool layerno
   const int block = tpr > 256 ? tpr : 256;
   const int rpb = block / tpr;
   const int grid = (M + rpb - 1) / rpb;
-  if (layernorm)
-    rownorm_kernel<true><<<grid, block, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Y), M, N, tpr,
-        static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(beta), eps, mean_out,
-        rstd_out);
-  else
-    rownorm_kernel<false><<<grid, block, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Y), M, N, tpr,
-        static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(beta), eps, mean_out,
-        rstd_out);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  const auto* x = static_cast<const __nv_bfloat16*>(X);
+  auto* y = static_cast<__nv_bfloat16*>(Y);
+  const auto* g = static_cast<const __nv_bfloat16*>(gamma);
+  const auto* b = static_cast<const __nv_bfloat16*>(beta);
+  const cudaError_t e =
+      layernorm ? cudaLaunchKernelEx(&cfg, rownorm_kernel<true>, x, y, M, N, tpr, g, b, eps, mean_out, rstd_out)
+                : cudaLaunchKernelEx(&cfg, rownorm_kernel<false>, x, y, M, N, tpr, g, b, eps, mean_out, rstd_out);
   if (e != cudaSuccess) return cuda_fail(e, "row norm launch");
   return FNORM_OK;
 }

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -90,6 +91,14 @@ fnorm_status_t current_device(DeviceInfo* out) {
 
 uint64_t wait_limit_ns() { return g_wait_limit.load(std::memory_order_relaxed); }
 void set_wait_limit(uint64_t ns) { g_wait_limit.store(ns, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("FNORM_PDL");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
 
 // --------------------------------------------------------------------------
 // tensor maps

@@ -77,8 +77,9 @@ def test_postnorm_argument_rules(L):
     # pre_rmsnorm flag out of range and a bad pre_eps
     assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, 2, 1e-6, None, None, None, None) == 1
     assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, 1, 0.0, None, None, None, None) == 1
-    # rows wider than any plan
-    assert f(FAKE, FAKE, FAKE, 128, 16384, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None, None) == 2
+    # misaligned gamma
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, ctypes.c_void_p(0x10002), None, 1e-5, 0, 1e-6, None, None, None,
+             None) == 1
 
 
 def test_norm_rejects_bad_sizes(L):
@@ -88,8 +89,9 @@ def test_norm_rejects_bad_sizes(L):
 
 
 @pytest.mark.parametrize("N,cluster,cols", [(8, 1, 64), (64, 1, 64), (128, 1, 128), (200, 1, 256), (256, 1, 256),
-                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (2048, 8, 256),
-                                            (3000, 8, 512), (4096, 8, 512), (8192, 16, 512)])
+                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (1032, 4, 512),
+                                            (2048, 4, 512), (2056, 4, 768), (3000, 4, 768), (4096, 4, 1024),
+                                            (8192, 4, 2048), (16384, 4, 4096)])
 def test_postnorm_plan(L, N, cluster, cols):
     import normalization_gemm_tcgen05_gb300 as fn
     assert fn.postnorm_plan(N) == (cluster, cols)
@@ -100,13 +102,16 @@ def test_forced_cluster(L):
     try:
         fn.set_postnorm_cluster(8)
         assert fn.postnorm_plan(1024) == (8, 128)
-        fn.set_postnorm_cluster(16)
-        assert fn.postnorm_plan(1024) == (16, 512)
+        with pytest.raises(fn.FnormError):             # 8 CTAs hold at most 128 columns each
+            fn.postnorm_plan(2048)
+        fn.set_postnorm_cluster(2)
+        assert fn.postnorm_plan(1024) == (2, 512)      # spill: two 256-column slices per CTA
         fn.set_postnorm_cluster(1)
-        with pytest.raises(fn.FnormError):
-            fn.postnorm_plan(1024)
-        with pytest.raises(fn.FnormError):
-            fn.set_postnorm_cluster(3)
+        assert fn.postnorm_plan(1024) == (1, 1024)
+        assert fn.postnorm_plan(256) == (1, 256)       # resident, one CTA
+        for bad in (3, 16, -1):
+            with pytest.raises(fn.FnormError):
+                fn.set_postnorm_cluster(bad)
     finally:
         fn.set_postnorm_cluster(0)
     assert fn.postnorm_plan(1024) == (4, 256)

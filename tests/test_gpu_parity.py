@@ -151,7 +151,8 @@ def test_pre_and_post_in_one_kernel(norm):
 # ----------------------------------------------------------------------------
 # GEMM + post-norm over a cluster along N (DSMEM row-statistics exchange)
 # ----------------------------------------------------------------------------
-CLUSTER_N = [320, 512, 1024, 2048, 3000, 4096, 8192]
+CLUSTER_N = [320, 512, 640, 1024]                  # resident slices, 2 or 4 CTAs
+SPILL_N = [1032, 2048, 3000, 4096, 8192, 12288]    # spill layout, 4 CTAs, 2..12 slices each
 
 
 @pytest.mark.parametrize("N", CLUSTER_N)
@@ -159,30 +160,53 @@ CLUSTER_N = [320, 512, 1024, 2048, 3000, 4096, 8192]
 def test_postnorm_cluster(norm, N):
     w, d = _case("cfg4_n1024_ln", N + (norm == "rmsnorm"), M=300, N=N, K=256)
     c, cols = fn.postnorm_plan(N)
-    assert c > 1 and c * cols >= N
+    assert c > 1 and c * cols >= N and cols <= 256
+    _post(w, d, norm)
+
+
+@pytest.mark.parametrize("N", SPILL_N)
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_postnorm_spill(norm, N):
+    w, d = _case("cfg4_n4096_ln", N + 7 * (norm == "rmsnorm"), M=520, N=N, K=192)
+    c, cols = fn.postnorm_plan(N)
+    assert cols > 256
     _post(w, d, norm)
 
 
 def test_postnorm_cluster_with_pre():
-    w, d = _case("cfg5", 13, M=400, N=2048, K=256)
+    w, d = _case("cfg5", 13, M=400, N=1024, K=256)
     _post(w, d, "layernorm", pre=True)
+
+
+def test_postnorm_spill_with_pre_and_no_affine():
+    w, d = _case("cfg5", 14, M=300, N=4096, K=256)
+    _post(w, d, "layernorm", pre=True)
+    _post(w, d, "rmsnorm", pre=True, affine=False)
+
+
+def test_postnorm_spill_many_row_blocks():
+    # more row blocks than co-resident clusters: every CTA carries a pending
+    # normalisation across row blocks
+    w, d = _case("cfg4_n4096_ln", 15, M=128 * 160 + 37, N=3072, K=64)
+    _post(w, d, "layernorm")
 
 
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
 def test_cluster_sizes_agree(norm):
-    # the statistics split into per-CTA partials: cluster sizes 4, 8 and 16 must
-    # give the same row statistics up to fp32 summation order
+    # the statistics split into per-CTA partials: cluster sizes 1 and 2 (spill
+    # layout) and 4 and 8 (resident) must give the same row statistics up to
+    # fp32 summation order
     w, d = _case("cfg4_n1024_ln", 21, M=256, N=1024, K=512)
     outs = {}
     try:
-        for c in (4, 8, 16):
+        for c in (1, 2, 4, 8):
             fn.set_postnorm_cluster(c)
             assert fn.postnorm_plan(1024)[0] == c
             outs[c] = _post(w, d, norm)
     finally:
         fn.set_postnorm_cluster(0)
     r4 = np64(outs[4][1]["rstd"])
-    for c in (8, 16):
+    for c in (1, 2, 8):
         rc = np64(outs[c][1]["rstd"])
         assert np.max(np.abs(rc - r4) / r4) < 1e-5, f"cluster {c} rstd differs from cluster 4"
 
@@ -245,10 +269,18 @@ def test_invalid_arguments_launch_nothing():
     with pytest.raises(fn.FnormError) as e:
         fn.lazy_prenorm_gemm(A, B, eps=0.0)
     assert e.value.status == fn.INVALID_ARG
-    Bw = torch.randn(64, 16384, device=DEV).to(torch.bfloat16)
+    g = torch.ones(80, dtype=torch.bfloat16, device=DEV)[1:65]  # gamma 2 bytes off a 16-byte boundary
     with pytest.raises(fn.FnormError) as e:
-        fn.gemm_postnorm(A, Bw, "layernorm")
-    assert e.value.status == fn.UNSUPPORTED
+        fn.gemm_postnorm(A, B, "layernorm", g)
+    assert e.value.status == fn.INVALID_ARG
+    try:
+        fn.set_postnorm_cluster(8)
+        Bw = torch.randn(64, 2048, device=DEV).to(torch.bfloat16)
+        with pytest.raises(fn.FnormError) as e:
+            fn.gemm_postnorm(A, Bw, "layernorm")
+        assert e.value.status == fn.UNSUPPORTED
+    finally:
+        fn.set_postnorm_cluster(0)
     fn.check_status(DEV)
 
 
@@ -281,3 +313,57 @@ def test_stream_and_graph_capture():
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ----------------------------------------------------------------------------
+# B resident in shared memory (N <= tile width, short K, more row blocks than SMs)
+# ----------------------------------------------------------------------------
+BRES_CASES = [("gemm", 64, 1024), ("gemm", 128, 512), ("gemm", 256, 256), ("prenorm", 256, 256),
+              ("layernorm", 256, 256), ("rmsnorm", 128, 512), ("layernorm", 64, 1000), ("pre+layernorm", 256, 256)]
+
+
+@pytest.mark.parametrize("kind,N,K", BRES_CASES, ids=lambda v: str(v))
+def test_resident_B(kind, N, K):
+    M = 128 * 170 + 45  # more row blocks than the 152 SMs, ragged tail
+    w, d = _case("cfg5", 40 + N + K, M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    A, B = _dev(d["A"]), _dev(d["B"])
+    if kind == "gemm":
+        assert_out_close(fn.gemm(A, B), oracle.gemm(to_f64(d["A"]), to_f64(d["B"])))
+    elif kind == "prenorm":
+        C, r = fn.lazy_prenorm_gemm(A, B, 1e-6, return_rstd=True)
+        Cr, rr = oracle.lazy_prenorm_gemm(to_f64(d["A"]), to_f64(d["B"]), 1e-6)
+        assert_out_close(C, Cr)
+        assert_rstd_close(r, rr)
+    elif kind == "pre+layernorm":
+        _post(w, d, "layernorm", pre=True)
+    else:
+        _post(w, d, kind)
+    fn.check_status(DEV)
+
+
+def test_without_programmatic_dependent_launch():
+    # the same kernels launched without programmatic serialisation
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path.insert(0, %r); sys.path.insert(0, %r)\n"
+        "import torch\n"
+        "import normalization_gemm_tcgen05_gb300 as fn, oracle\n"
+        "from workloads import WORKLOADS, make_inputs, to_f64\n"
+        "from gpu_util import assert_out_close\n"
+        "w = WORKLOADS['cfg4_n4096_ln'].scaled(M=300, K=128)\n"
+        "d = make_inputs(w, 3)\n"
+        "dev = torch.device('cuda', 0)\n"
+        "C = fn.gemm_postnorm(d['A'].to(dev), d['B'].to(dev), 'layernorm', d['gamma'].to(dev), d['beta'].to(dev), w.eps)\n"
+        "ref = oracle.gemm_postnorm(to_f64(d['A']), to_f64(d['B']), 'layernorm', to_f64(d['gamma']), to_f64(d['beta']), w.eps)\n"
+        "assert_out_close(C, ref['C'])\n"
+        "Y = fn.layernorm(C, None, None, 1e-5)\n"
+        "assert_out_close(Y, oracle.layernorm(to_f64(C.cpu()), None, None, 1e-5)[0])\n"
+        "fn.check_status(dev)\n"
+        "print('ok')\n"
+    ) % (os.path.dirname(here), here)
+    env = dict(os.environ, FNORM_PDL="0")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
