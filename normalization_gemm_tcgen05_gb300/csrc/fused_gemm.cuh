@@ -130,6 +130,11 @@ struct KCfg {
   static constexpr bool AUXW = PRE || NORMW;  // warps 10-13 present
   static constexpr int HALF = BN / 2;          // columns per epilogue half
   static constexpr int NCH = HALF / 32;        // 32-column subtiles per half
+  // 32-column subtiles loaded from TMEM per wait: the whole half when the
+  // register budget allows (320 threads: 168 registers), else two (448
+  // threads: 128 registers; cluster exchange code needs the room too)
+  static constexpr int LDB = (AUXW || (CLUSTER && NCH > 2)) ? (NCH < 2 ? NCH : 2) : NCH;
+  static constexpr bool KEEP = (LDB == NCH);  // one TMEM read serves statistics and output
   static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
   static constexpr int GB = (POST && !SPILL) ? BN : 1;  // gamma/beta kept in shared memory
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
@@ -213,6 +218,17 @@ __device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, in
   }
 }
 
+// Load NB consecutive 32-column subtiles of this warp's TMEM lanes with a
+// single wait (one round trip instead of NB).
+template <int NB>
+__device__ __forceinline__ void tmem_load_batch(uint32_t taddr, uint32_t (&r)[NB][32]) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) tmem_ld_32x32b_x32(taddr + b * 32, r[b]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int b = 0; b < NB; ++b) reg_fence(r[b]);
+}
+
 // Parallel-variance combination: fold (mean_b, m2_b) over nb values into
 // (mean, m2) over n values.
 __device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n, float mean_b, float m2_b,
@@ -271,12 +287,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&aux->acc_full[b]), 1);
       mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps);
-      mbar_init(smem_u32(&aux->ss_full[b]), 128);
-      mbar_init(smem_u32(&aux->ss_empty[b]), 32 * kEpiWarps);
+      // handoffs between warp groups: one arrival per warp, after __syncwarp
+      mbar_init(smem_u32(&aux->ss_full[b]), 4);
+      mbar_init(smem_u32(&aux->ss_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->xbar[b]), 1);
-      mbar_init(smem_u32(&aux->nstat_full[b]), 32 * kEpiWarps);
-      mbar_init(smem_u32(&aux->nstat_empty[b]), 128);
-      mbar_init(smem_u32(&aux->ebar[b]), 32 * kEpiWarps);
+      mbar_init(smem_u32(&aux->nstat_full[b]), kEpiWarps);
+      mbar_init(smem_u32(&aux->nstat_empty[b]), 4);
+      mbar_init(smem_u32(&aux->ebar[b]), kEpiWarps);
     }
     mbar_init(smem_u32(&aux->teardown), 1);
     mbar_init(smem_u32(&aux->bres_full), 1);
@@ -451,7 +468,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     int esn = 0;
     auto esync = [&]() -> bool {
       const int b = esn & 1;
-      mbar_arrive(smem_u32(&aux->ebar[b]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&aux->ebar[b]));
       const bool r =
           mbar_wait_warp(wc, smem_u32(&aux->ebar[b]), static_cast<uint32_t>(esn >> 1) & 1u, kSiteEpilogue);
       ++esn;
@@ -538,7 +556,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             break;
           }
           const float ss = aux->ss[sb][row];
-          mbar_arrive(smem_u32(&aux->ss_empty[sb]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&aux->ss_empty[sb]));
           pre = rsqrtf(ss / static_cast<float>(K) + p.pre_eps);
         }
         const int nvh = min(max(N - c0h, 0), HALF);  // valid columns of this half
@@ -546,27 +565,30 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (SPILL) {
           // ---- pass 1: statistics + un-normalised (pre-scaled) bf16 slice to C ----
           if (s == 0) sum1 = sum2 = 0.0f;
-          for (int c = 0; c < NCH; ++c) {
-            if (c * 32 >= nvh) break;
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tb + c * 32, r);
-            tmem_ld_wait();
-            reg_fence(r);
-            if (LN && s == 0 && c == 0) k0 = __uint_as_float(r[0]) * pre;
-            uint32_t w[16];
-            float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
-            const int lim = nvh - c * 32;
+          for (int cb = 0; cb < NCH / Cfg::LDB; ++cb) {
+            if (cb * Cfg::LDB * 32 >= nvh) break;
+            uint32_t r[Cfg::LDB][32];
+            tmem_load_batch<Cfg::LDB>(tb + cb * Cfg::LDB * 32, r);
+            if (LN && s == 0 && cb == 0) k0 = __uint_as_float(r[0][0]) * pre;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float v0 = __uint_as_float(r[j]) * pre, v1 = __uint_as_float(r[j + 1]) * pre;
-              const float d0 = LN ? v0 - k0 : v0, d1 = LN ? v1 - k0 : v1;
-              if (j < lim) { a1[0] += d0; a2[0] = fmaf(d0, d0, a2[0]); }
-              if (j + 1 < lim) { a1[1] += d1; a2[1] = fmaf(d1, d1, a2[1]); }
-              w[j >> 1] = pack_bf16x2(v0, v1);
+            for (int b = 0; b < Cfg::LDB; ++b) {
+              const int c = cb * Cfg::LDB + b;
+              if (c * 32 >= nvh) break;
+              uint32_t w[16];
+              float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
+              const int lim = nvh - c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float v0 = __uint_as_float(r[b][j]) * pre, v1 = __uint_as_float(r[b][j + 1]) * pre;
+                const float d0 = LN ? v0 - k0 : v0, d1 = LN ? v1 - k0 : v1;
+                if (j < lim) { a1[0] += d0; a2[0] = fmaf(d0, d0, a2[0]); }
+                if (j + 1 < lim) { a1[1] += d1; a2[1] = fmaf(d1, d1, a2[1]); }
+                w[j >> 1] = pack_bf16x2(v0, v1);
+              }
+              sum1 += a1[0] + a1[1];
+              sum2 += a2[0] + a2[1];
+              store_box(w, c0h + c * 32, m0);
             }
-            sum1 += a1[0] + a1[1];
-            sum2 += a2[0] + a2[1];
-            store_box(w, c0h + c * 32, m0);
           }
           tc_fence_before();
           __syncwarp();
@@ -628,7 +650,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 aux->nstat_m0[b] = m0;
                 aux->nstat_c0[b] = cbase;
               }
-              mbar_arrive(smem_u32(&aux->nstat_full[b]));
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&aux->nstat_full[b]));
             } else {
               while (pend) {  // (only when S == 1 would anything remain)
                 normalize_slice<LN>(p, pm0 + q * 32 + 16 * h, 16, 16 * h, pc0 + pnext * BN, pmean, prstd, lane);
@@ -656,25 +679,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
 
         // ---- resident layouts: statistics straight from tensor memory ----
+        constexpr int LDB = Cfg::LDB, NBATCH = NCH / LDB;
+        uint32_t r[LDB][32];
+        if (Cfg::KEEP) tmem_load_batch<LDB>(tb, r);  // the whole half, once
         float mean = 0.0f, rstd = 1.0f;
         if (POST) {
           float kk = 0.0f;
           float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
-          for (int c = 0; c < NCH; ++c) {
-            if (c * 32 >= nvh) break;
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tb + c * 32, r);
-            tmem_ld_wait();
-            reg_fence(r);
-            if (LN && c == 0) kk = __uint_as_float(r[0]) * pre;
-            const int lim = nvh - c * 32;
+          for (int cb = 0; cb < NBATCH; ++cb) {
+            if (cb * LDB * 32 >= nvh) break;
+            if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
+            if (LN && cb == 0) kk = __uint_as_float(r[0][0]) * pre;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float v = __uint_as_float(r[j]) * pre;
-              const float d = LN ? v - kk : v;
-              if (j < lim) {
-                a1[j & 1] += d;
-                a2[j & 1] = fmaf(d, d, a2[j & 1]);
+            for (int b = 0; b < LDB; ++b) {
+              const int lim = nvh - (cb * LDB + b) * 32;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float v = __uint_as_float(r[b][j]) * pre;
+                const float d = LN ? v - kk : v;
+                if (j < lim) {
+                  a1[j & 1] += d;
+                  a2[j & 1] = fmaf(d, d, a2[j & 1]);
+                }
               }
             }
           }
@@ -710,25 +736,27 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
 
         // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
-        for (int c = 0; c < NCH; ++c) {
-          const int col0 = c0h + c * 32;
-          if (col0 >= N) break;
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tb + c * 32, r);
-          tmem_ld_wait();
-          reg_fence(r);
-          uint32_t w[16];
+        for (int cb = 0; cb < NBATCH; ++cb) {
+          if (c0h + cb * LDB * 32 >= N) break;
+          if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float y0 = __uint_as_float(r[j]) * pre, y1 = __uint_as_float(r[j + 1]) * pre;
-            if (POST) {
-              const int cj = h * HALF + c * 32 + j;
-              y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
-              y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
+          for (int b = 0; b < LDB; ++b) {
+            const int c = cb * LDB + b;
+            const int col0 = c0h + c * 32;
+            if (col0 >= N) break;
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float y0 = __uint_as_float(r[b][j]) * pre, y1 = __uint_as_float(r[b][j + 1]) * pre;
+              if (POST) {
+                const int cj = h * HALF + c * 32 + j;
+                y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
+                y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
+              }
+              w[j >> 1] = pack_bf16x2(y0, y1);
             }
-            w[j >> 1] = pack_bf16x2(y0, y1);
+            store_box(w, col0, m0);
           }
-          store_box(w, col0, m0);
         }
         tc_fence_before();
         __syncwarp();
@@ -767,7 +795,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       const float2 st = aux->nstat[b][k * 32 + lane];
       const int m0 = aux->nstat_m0[b];
       const int c0 = aux->nstat_c0[b];
-      mbar_arrive(smem_u32(&aux->nstat_empty[b]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&aux->nstat_empty[b]));
       for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
     }
   } else if (PRE) {
@@ -819,7 +848,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           break;
         }
         aux->ss[sb][row] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        mbar_arrive(smem_u32(&aux->ss_full[sb]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&aux->ss_full[sb]));
       }
     }
   }
