@@ -105,8 +105,8 @@ struct Aux {
   float ss[2][128];
   float2 nstat[2][128];
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
-  float gam[GB];
-  float bet[GB];
+  alignas(16) float gam[GB];
+  alignas(16) float bet[GB];
   float2 xstat[2][CLMAX > 0 ? CLMAX : 1][128];
 };
 
@@ -227,6 +227,59 @@ __device__ __forceinline__ void tmem_load_batch(uint32_t taddr, uint32_t (&r)[NB
   tmem_ld_wait();
 #pragma unroll
   for (int b = 0; b < NB; ++b) reg_fence(r[b]);
+}
+
+// Accumulate one 32-column subtile of raw accumulator values into row sums:
+// LayerNorm s1 += u - k, s2 += (u - k)^2 (k: the shift); RMSNorm s2 += u^2.
+// Columns j >= lim are ignored; full subtiles take the unpredicated loop.
+template <bool LN>
+__device__ __forceinline__ void accum_stats(const uint32_t (&r)[32], int lim, float k, float (&s1)[2],
+                                            float (&s2)[2]) {
+  if (lim >= 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float d = LN ? __uint_as_float(r[j]) - k : __uint_as_float(r[j]);
+      if (LN) s1[j & 1] += d;
+      s2[j & 1] = fmaf(d, d, s2[j & 1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < lim) {
+        const float d = LN ? __uint_as_float(r[j]) - k : __uint_as_float(r[j]);
+        if (LN) s1[j & 1] += d;
+        s2[j & 1] = fmaf(d, d, s2[j & 1]);
+      }
+    }
+  }
+}
+
+// y = (u * a + b) * gamma_j + beta_j for one 32-column subtile, packed to
+// bf16 pairs (two FMAs per element; gamma/beta read as float4 broadcasts)
+__device__ __forceinline__ void affine_pack(const uint32_t (&r)[32], float a, float b, const float* gam,
+                                            const float* bet, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 g = *reinterpret_cast<const float4*>(gam + j);
+    const float4 be = *reinterpret_cast<const float4*>(bet + j);
+    const float y0 = fmaf(fmaf(__uint_as_float(r[j]), a, b), g.x, be.x);
+    const float y1 = fmaf(fmaf(__uint_as_float(r[j + 1]), a, b), g.y, be.y);
+    const float y2 = fmaf(fmaf(__uint_as_float(r[j + 2]), a, b), g.z, be.z);
+    const float y3 = fmaf(fmaf(__uint_as_float(r[j + 3]), a, b), g.w, be.w);
+    w[j >> 1] = pack_bf16x2(y0, y1);
+    w[(j >> 1) + 1] = pack_bf16x2(y2, y3);
+  }
+}
+
+// y = u * a (a = 1 for the plain GEMM), packed to bf16 pairs
+template <bool SCALE>
+__device__ __forceinline__ void scale_pack(const uint32_t (&r)[32], float a, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float y0 = SCALE ? __uint_as_float(r[j]) * a : __uint_as_float(r[j]);
+    const float y1 = SCALE ? __uint_as_float(r[j + 1]) * a : __uint_as_float(r[j + 1]);
+    w[j >> 1] = pack_bf16x2(y0, y1);
+  }
 }
 
 // Parallel-variance combination: fold (mean_b, m2_b) over nb values into
@@ -569,24 +622,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (cb * Cfg::LDB * 32 >= nvh) break;
             uint32_t r[Cfg::LDB][32];
             tmem_load_batch<Cfg::LDB>(tb + cb * Cfg::LDB * 32, r);
-            if (LN && s == 0 && cb == 0) k0 = __uint_as_float(r[0][0]) * pre;
+            if (LN && s == 0 && cb == 0) k0 = __uint_as_float(r[0][0]);
 #pragma unroll
             for (int b = 0; b < Cfg::LDB; ++b) {
               const int c = cb * Cfg::LDB + b;
               if (c * 32 >= nvh) break;
-              uint32_t w[16];
               float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
-              const int lim = nvh - c * 32;
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                const float v0 = __uint_as_float(r[b][j]) * pre, v1 = __uint_as_float(r[b][j + 1]) * pre;
-                const float d0 = LN ? v0 - k0 : v0, d1 = LN ? v1 - k0 : v1;
-                if (j < lim) { a1[0] += d0; a2[0] = fmaf(d0, d0, a2[0]); }
-                if (j + 1 < lim) { a1[1] += d1; a2[1] = fmaf(d1, d1, a2[1]); }
-                w[j >> 1] = pack_bf16x2(v0, v1);
-              }
+              accum_stats<LN>(r[b], nvh - c * 32, k0, a1, a2);
               sum1 += a1[0] + a1[1];
               sum2 += a2[0] + a2[1];
+              uint32_t w[16];
+              scale_pack<PRE>(r[b], pre, w);  // the (pre-scaled) value before the norm
               store_box(w, c0h + c * 32, m0);
             }
           }
@@ -608,12 +654,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               for (int hh = 0; hh < 2; ++hh)
                 nh[hh] += static_cast<float>(min(max(N - (cbase + s2 * BN + hh * HALF), 0), HALF));
             const float nmine = nh[h];
-            float part0, part1;
+            float part0, part1;  // statistics of the pre-scaled values v = pre * u
             if (LN) {
-              part0 = nmine > 0.0f ? k0 + sum1 / nmine : 0.0f;
-              part1 = nmine > 0.0f ? fmaxf(sum2 - sum1 * sum1 / nmine, 0.0f) : 0.0f;
+              part0 = nmine > 0.0f ? pre * (k0 + sum1 / nmine) : 0.0f;
+              part1 = nmine > 0.0f ? pre * pre * fmaxf(sum2 - sum1 * sum1 / nmine, 0.0f) : 0.0f;
             } else {
-              part0 = sum2;
+              part0 = pre * pre * sum2;
               part1 = 0.0f;
             }
             if (!combine_halves(part0, part1, nh[0], nh[1]) || !exchange(part0, part1, g, xit)) {
@@ -689,29 +735,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           for (int cb = 0; cb < NBATCH; ++cb) {
             if (cb * LDB * 32 >= nvh) break;
             if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
-            if (LN && cb == 0) kk = __uint_as_float(r[0][0]) * pre;
+            if (LN && cb == 0) kk = __uint_as_float(r[0][0]);
 #pragma unroll
             for (int b = 0; b < LDB; ++b) {
               const int lim = nvh - (cb * LDB + b) * 32;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float v = __uint_as_float(r[b][j]) * pre;
-                const float d = LN ? v - kk : v;
-                if (j < lim) {
-                  a1[j & 1] += d;
-                  a2[j & 1] = fmaf(d, d, a2[j & 1]);
-                }
-              }
+              if (lim > 0) accum_stats<LN>(r[b], lim, kk, a1, a2);
             }
           }
           const float s1 = a1[0] + a1[1], s2 = a2[0] + a2[1];
           const float nf = static_cast<float>(nvh);
-          float part0, part1;
+          float part0, part1;  // statistics of the pre-scaled values v = pre * u
           if (LN) {
-            part0 = nvh > 0 ? kk + s1 / nf : 0.0f;
-            part1 = nvh > 0 ? fmaxf(s2 - s1 * s1 / nf, 0.0f) : 0.0f;
+            part0 = nvh > 0 ? pre * (kk + s1 / nf) : 0.0f;
+            part1 = nvh > 0 ? pre * pre * fmaxf(s2 - s1 * s1 / nf, 0.0f) : 0.0f;
           } else {
-            part0 = s2;
+            part0 = pre * pre * s2;
             part1 = 0.0f;
           }
           const float n_h0 = static_cast<float>(min(max(N - n0, 0), HALF));
@@ -745,15 +783,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int col0 = c0h + c * 32;
             if (col0 >= N) break;
             uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float y0 = __uint_as_float(r[b][j]) * pre, y1 = __uint_as_float(r[b][j + 1]) * pre;
-              if (POST) {
-                const int cj = h * HALF + c * 32 + j;
-                y0 = (LN ? (y0 - mean) : y0) * rstd * aux->gam[cj] + aux->bet[cj];
-                y1 = (LN ? (y1 - mean) : y1) * rstd * aux->gam[cj + 1] + aux->bet[cj + 1];
-              }
-              w[j >> 1] = pack_bf16x2(y0, y1);
+            if (POST) {
+              // y = (pre*u - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta
+              affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f, &aux->gam[h * HALF + c * 32],
+                          &aux->bet[h * HALF + c * 32], w);
+            } else {
+              scale_pack<PRE>(r[b], pre, w);
             }
             store_box(w, col0, m0);
           }
