@@ -29,4 +29,6 @@ from .fnorm_oracle import (  # noqa: F401
     layernorm,
     lazy_prenorm_gemm,
     gemm_postnorm,
+    prenorm_affine_gemm,
+    gemm_add_postnorm,
 )

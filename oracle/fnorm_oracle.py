@@ -22,7 +22,8 @@ from typing import Optional
 
 import numpy as np
 
-__all__ = ["gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm", "gemm_postnorm"]
+__all__ = ["gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm", "gemm_postnorm", "prenorm_affine_gemm",
+           "gemm_add_postnorm"]
 
 
 def _f64(x) -> np.ndarray:
@@ -124,3 +125,41 @@ def gemm_postnorm(A, B, norm: str, gamma=None, beta=None, eps: float = 1e-5,
     else:
         raise ValueError(f"unknown norm {norm!r}")
     return {"C": C, "mean": mean, "rstd": rstd, "pre_rstd": pre_rstd}
+
+
+def prenorm_affine_gemm(A, B, norm: str, gamma=None, beta=None, eps: float = 1e-6):
+    """C = (norm(A) * gamma + beta) @ B, the pre-norm with its elementwise affine.
+
+    [FNF-ru] "Lazy Pre-Norm" (the pre-norm feeding a GEMM) and its limits
+    section (the affine and the LayerNorm mean do not commute with the row
+    scale); [ATB] 1.1 / 1.2 for the norms.  The oracle materialises the
+    normalised, affine-transformed A in float64 and multiplies it by B.
+    Returns (C, mean or None, rstd) of the rows of A.
+    """
+    if norm == "layernorm":
+        Y, mean, rstd = layernorm(A, gamma, beta, eps)
+    elif norm == "rmsnorm":
+        Y, rstd = rmsnorm(A, gamma, beta, eps)
+        mean = None
+    else:
+        raise ValueError(f"unknown norm {norm!r}")
+    return gemm(Y, B), mean, rstd
+
+
+def gemm_add_postnorm(A, B, R, norm: str, gamma=None, beta=None, eps: float = 1e-5) -> dict:
+    """C = norm(A @ B + R) * gamma + beta: a residual added before the post-norm.
+
+    [FNF-ru] "FlashNormAttention" (a residual connection followed by a
+    post-RMSNorm, the residual added through the accumulator); [ATB] 1.1 / 1.2.
+    The oracle materialises H = A @ B + R in float64 and normalises its rows.
+    Returns a dict with "C", "H", "rstd" and "mean" (LayerNorm only).
+    """
+    H = gemm(A, B) + _f64(R)
+    if norm == "layernorm":
+        C, mean, rstd = layernorm(H, gamma, beta, eps)
+    elif norm == "rmsnorm":
+        C, rstd = rmsnorm(H, gamma, beta, eps)
+        mean = None
+    else:
+        raise ValueError(f"unknown norm {norm!r}")
+    return {"C": C, "H": H, "mean": mean, "rstd": rstd}

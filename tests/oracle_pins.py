@@ -300,6 +300,70 @@ def check_pre_and_post(o):
     _close(d["pre_rstd"], (Ah[:, 0] / _t(A)[:, 0]).numpy(), 1e-12, 0, "pre rstd")
 
 
+# --------------------------------------------------------------------------
+# pre-norm with affine feeding a GEMM; residual added before the post-norm
+# --------------------------------------------------------------------------
+def check_prenorm_affine_golden(o):
+    g = load_golden("prenorm_affine_gemm.txt")
+    C, mu, r = o.prenorm_affine_gemm(g["A"][None, :], g["B"], "layernorm", g["gamma"], g["beta"], g["eps"])
+    _close(C, g["C"][None, :], what="pre-LN affine golden C")
+    _close(mu, [g["mean"]], what="pre-LN affine golden mean")
+    _close(r, [g["rstd"]], what="pre-LN affine golden rstd")
+
+
+def check_prenorm_affine_torch(o):
+    rng = _rng(13)
+    A = rng.standard_normal((7, 40)) * 2 + 0.7
+    B = rng.standard_normal((40, 12)) / np.sqrt(40)
+    gam = 1 + 0.1 * rng.standard_normal(40)
+    bet = 0.1 * rng.standard_normal(40)
+    C, _, _ = o.prenorm_affine_gemm(A, B, "layernorm", gam, bet, 1e-5)
+    ref = (F.layer_norm(_t(A), (40,), _t(gam), _t(bet), 1e-5) @ _t(B)).numpy()
+    _close(C, ref, 1e-12, 1e-12, "pre-LN affine vs torch")
+    C, _, _ = o.prenorm_affine_gemm(A, B, "rmsnorm", gam, None, 1e-6)
+    ref = (F.rms_norm(_t(A), (40,), _t(gam), 1e-6) @ _t(B)).numpy()
+    _close(C, ref, 1e-12, 1e-12, "pre-RMS affine vs torch")
+
+
+def check_prenorm_affine_lazy_identity(o):
+    # the lazy form: gamma folds into B, beta into a bias, the LayerNorm mean
+    # into a rank-one correction with the column sums of the folded B
+    rng = _rng(14)
+    A = rng.standard_normal((9, 24)) * 3 + 1.5
+    B = rng.standard_normal((24, 10))
+    gam = 1 + 0.2 * rng.standard_normal(24)
+    bet = 0.3 * rng.standard_normal(24)
+    C, mu, r = o.prenorm_affine_gemm(A, B, "layernorm", gam, bet, 0.01)
+    Bg = gam[:, None] * B
+    lazy = r[:, None] * (A @ Bg - mu[:, None] * Bg.sum(axis=0)[None, :]) + (bet @ B)[None, :]
+    _close(C, lazy, 1e-11, 1e-11, "lazy pre-LN identity")
+
+
+def check_add_postnorm_torch(o):
+    rng = _rng(15)
+    A = rng.standard_normal((6, 16))
+    B = rng.standard_normal((16, 20)) / 4
+    R = rng.standard_normal((6, 20)) * 2
+    gam = 1 + 0.1 * rng.standard_normal(20)
+    bet = 0.1 * rng.standard_normal(20)
+    d = o.gemm_add_postnorm(A, B, R, "layernorm", gam, bet, 1e-5)
+    H = _t(A) @ _t(B) + _t(R)
+    _close(d["C"], F.layer_norm(H, (20,), _t(gam), _t(bet), 1e-5).numpy(), 1e-12, 1e-12, "add post-LN vs torch")
+    _close(d["H"], H.numpy(), 1e-13, 1e-13, "add post-LN H")
+    d = o.gemm_add_postnorm(A, B, R, "rmsnorm", gam, None, 1e-5)
+    _close(d["C"], F.rms_norm(H, (20,), _t(gam), 1e-5).numpy(), 1e-12, 1e-12, "add post-RMS vs torch")
+
+
+def check_add_postnorm_cancel(o):
+    # R = -A@B cancels the product: a zero row before the norm
+    A = np.arange(12, dtype=np.float64).reshape(3, 4) - 5
+    B = np.arange(8, dtype=np.float64).reshape(4, 2) / 3
+    bet = np.array([0.25, -0.5])
+    d = o.gemm_add_postnorm(A, B, -(A @ B), "layernorm", None, bet, 0.04)
+    _close(d["C"], np.tile(bet, (3, 1)), what="cancelled residual gives beta")
+    _close(d["rstd"], [5.0, 5.0, 5.0], what="cancelled residual rstd = 1/sqrt(eps)")
+
+
 ALL_CHECKS = [
     check_gemm_bruteforce, check_gemm_torch,
     check_rmsnorm_golden, check_rmsnorm_torch, check_rmsnorm_unit_rms,
@@ -310,4 +374,6 @@ ALL_CHECKS = [
     check_prenorm_const_row,
     check_postnorm_golden, check_postnorm_torch, check_postnorm_identity_B,
     check_postnorm_split_stats, check_pre_and_post,
+    check_prenorm_affine_golden, check_prenorm_affine_torch, check_prenorm_affine_lazy_identity,
+    check_add_postnorm_torch, check_add_postnorm_cancel,
 ]

@@ -10,7 +10,7 @@ import oracle.fnorm_oracle as O
 from oracle_pins import ALL_CHECKS
 
 _real = {name: getattr(O, name) for name in ("gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm",
-                                             "gemm_postnorm")}
+                                             "gemm_postnorm", "prenorm_affine_gemm", "gemm_add_postnorm")}
 
 
 def _gemm_transposed(A, B):          # transposed operand
@@ -88,6 +88,26 @@ def _postnorm_skip_pre(A, B, norm, gamma=None, beta=None, eps=1e-5, pre_rmsnorm=
     return d
 
 
+def _prenorm_affine_after_gemm(A, B, norm, gamma=None, beta=None, eps=1e-6):
+    # the affine applied to the GEMM output instead of to the normalised A
+    if norm == "layernorm":
+        Y, mu, r = _real["layernorm"](A, None, None, eps)
+    else:
+        (Y, r), mu = _real["rmsnorm"](A, None, None, eps), None
+    C = _real["gemm"](Y, B)
+    if gamma is not None:
+        C = C * np.mean(gamma)
+    if beta is not None:
+        C = C + np.mean(beta)
+    return C, mu, r
+
+
+def _add_postnorm_residual_dropped(A, B, R, norm, gamma=None, beta=None, eps=1e-5):
+    d = _real["gemm_postnorm"](A, B, norm, gamma, beta, eps)
+    d["H"] = _real["gemm"](A, B)
+    return d
+
+
 MUTANTS = {
     "gemm_transposed_B": ("gemm", _gemm_transposed),
     "gemm_dropped_k_term": ("gemm", _gemm_dropped_k),
@@ -101,6 +121,8 @@ MUTANTS = {
     "postnorm_norm_before_gemm": ("gemm_postnorm", _postnorm_before_gemm),
     "postnorm_rms_as_layernorm": ("gemm_postnorm", _postnorm_rms_centred),
     "postnorm_pre_stage_skipped": ("gemm_postnorm", _postnorm_skip_pre),
+    "prenorm_affine_after_gemm": ("prenorm_affine_gemm", _prenorm_affine_after_gemm),
+    "add_postnorm_residual_dropped": ("gemm_add_postnorm", _add_postnorm_residual_dropped),
 }
 
 
