@@ -3,6 +3,9 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload cfg2|cfg1|cfg3|cfg4|cfg5|all]
 
+Workload groups: cfg1..cfg5 (the five configurations), res (residual-add
+post-norm), preaff (pre-norm with its affine folded into B), all.
+
 Default workload (one JSON line on stdout): GEMM + post-LayerNorm with affine,
 A[16384,1024] @ B[1024,N] for N = 64 and N = 128 (both launches make one step).
 Metric: fused norm-GEMM TFLOP/s (2*M*N*K per launch), with the roofline of the
@@ -53,6 +56,8 @@ GROUPS = {
     "cfg4": ["cfg4_n1024_ln", "cfg4_n1024_rms", "cfg4_n4096_ln", "cfg4_n4096_rms", "cfg4_n8192_ln",
              "cfg4_n8192_rms"],
     "cfg5": ["cfg5"],
+    "res": ["res_ln_n128", "res_rms_n1024"],
+    "preaff": ["preln_affine", "prerms_gamma"],
 }
 GROUP_TEXT = {
     "cfg1": "Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128], eps 1e-6",
@@ -61,6 +66,10 @@ GROUP_TEXT = {
     "cfg4": "GEMM + post-LayerNorm and post-RMSNorm over a CTA cluster, A[16384,2048] @ B[2048,N], "
             "N in {1024,4096,8192}",
     "cfg5": "pre-RMSNorm + GEMM + post-LayerNorm(affine) in one kernel, A[65536,256] @ B[256,256]",
+    "res": "GEMM + residual + post-norm: LayerNorm(affine) A[16384,1024] @ B[1024,128] + R, "
+           "RMSNorm(gamma) A[16384,2048] @ B[2048,1024] + R",
+    "preaff": "pre-norm with affine folded into B + GEMM, A[8192,4096] @ B[4096,4096]: LayerNorm(gamma, beta), "
+              "RMSNorm(gamma)",
 }
 KERNEL_SOURCES = ["fused_gemm.cuh", "ptx.cuh", "fused_launch.cuh", "rownorm.cu"]
 
@@ -206,6 +215,13 @@ class Case:
         self.B = [d["B"].to(device) for _ in range(self.R)]
         self.g = None if d["gamma"] is None else d["gamma"].to(device)
         self.b = None if d["beta"] is None else d["beta"].to(device)
+        # residual-add post-norm: R rotates with A
+        self.Rres = None if d["R"] is None else [d["R"].to(device) for _ in range(self.R)]
+        # pre-norm with affine: the weight is folded once per copy (a one-time
+        # preparation of a fixed weight, outside the timed step)
+        self.fold = None
+        if w.kind == "prenorm_affine":
+            self.fold = [fn.fold_prenorm_affine(Bj, self.g, self.b) for Bj in self.B]
         self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         self.Y = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         nst = 3
@@ -223,6 +239,11 @@ class Case:
         st = self.stats[j]
         if w.kind == "prenorm":
             fn.lazy_prenorm_gemm(self.A[j], self.B[j], w.eps, out=self.C[j])
+        elif w.kind == "prenorm_affine":
+            Bf, cs, bias = self.fold[j]
+            fn.prenorm_gemm(self.A[j], Bf, w.norm, cs, bias, w.eps, out=self.C[j])
+        elif w.residual:
+            fn.gemm_add_postnorm(self.A[j], self.B[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.C[j])
         elif w.kind == "postnorm":
             fn.gemm_postnorm(self.A[j], self.B[j], w.norm, self.g, self.b, w.eps, pre_rmsnorm=w.pre_rmsnorm,
                              pre_eps=w.pre_eps, out=self.C[j])
@@ -240,6 +261,12 @@ class Case:
         if w.kind == "prenorm":
             k = i % self.R
             fn.rmsnorm(self.A[k], None, w.eps, out=self._pre_out(k))
+        elif w.kind == "prenorm_affine":
+            k = i % self.R
+            self._pre_norm(k, self.A[k], self._pre_out(k))
+        elif w.residual:
+            k = i % self.R
+            fn.add_rownorm(self.Cn[j], self.Rres[k], w.norm, self.g, self.b, w.eps, out=self.Yn[j])
         else:
             if w.pre_rmsnorm:
                 k = i % self.R
@@ -255,6 +282,12 @@ class Case:
         if w.kind == "prenorm":
             fn.rmsnorm(self.A[j], None, w.eps, out=self._pre_out(j))
             fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+        elif w.kind == "prenorm_affine":
+            self._pre_norm(j, self.A[j], self._pre_out(j))
+            fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+        elif w.residual:
+            fn.gemm(self.A[j], self.B[j], out=self.C[j])
+            fn.add_rownorm(self.C[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.Y[j])
         else:
             if w.pre_rmsnorm:
                 fn.rmsnorm(self.A[j], None, w.pre_eps, out=self._pre_out(j))
@@ -265,6 +298,14 @@ class Case:
                 fn.layernorm(self.C[j], self.g, self.b, w.eps, out=self.Y[j])
             else:
                 fn.rmsnorm(self.C[j], self.g, w.eps, out=self.Y[j])
+
+    def _pre_norm(self, j, X, out):
+        """The standalone pre-norm with its affine over rows of length K."""
+        w, fn = self.w, self.fn
+        if w.norm == "layernorm":
+            fn.layernorm(X, self.g, self.b, w.eps, out=out)
+        else:
+            fn.rmsnorm(X, self.g, w.eps, out=out)
 
     _pre = None
 
@@ -408,13 +449,14 @@ def run_e2e(cases, K, W, world, device) -> dict:
         hB = c.host["B"].pin_memory()
         hg = None if c.host["gamma"] is None else c.host["gamma"].pin_memory()
         hb = None if c.host["beta"] is None else c.host["beta"].pin_memory()
+        hR = None if c.host["R"] is None else c.host["R"].pin_memory()
         hC = torch.empty((c.w.M, c.w.N), dtype=torch.bfloat16).pin_memory()
-        host.append((hA, hB, hg, hb, hC))
-    h2d = sum(t.numel() * t.element_size() for h in host for t in h[:4] if t is not None)
-    d2h = sum(h[4].numel() * h[4].element_size() for h in host)
+        host.append((hA, hB, hg, hb, hR, hC))
+    h2d = sum(t.numel() * t.element_size() for h in host for t in h[:5] if t is not None)
+    d2h = sum(h[5].numel() * h[5].element_size() for h in host)
 
     def step():
-        for c, (hA, hB, hg, hb, hC) in zip(cases, host):
+        for c, (hA, hB, hg, hb, hR, hC) in zip(cases, host):
             dA, dB = c.A[0], c.B[0]
             dA.copy_(hA, non_blocking=True)
             dB.copy_(hB, non_blocking=True)
@@ -422,9 +464,18 @@ def run_e2e(cases, K, W, world, device) -> dict:
                 c.g.copy_(hg, non_blocking=True)
             if hb is not None:
                 c.b.copy_(hb, non_blocking=True)
+            if hR is not None:
+                c.Rres[0].copy_(hR, non_blocking=True)
             w = c.w
             if w.kind == "prenorm":
                 fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
+            elif w.kind == "prenorm_affine":
+                # the weight arrives from the host every step: fold, then the fused GEMM
+                Bf, cs, bias = c.fold[0]
+                fn.fold_prenorm_affine(dB, c.g, c.b, out=Bf, colsum_out=cs, bias_out=bias)
+                fn.prenorm_gemm(dA, Bf, w.norm, cs if w.norm == "layernorm" else None, bias, w.eps, out=c.C[0])
+            elif w.residual:
+                fn.gemm_add_postnorm(dA, dB, c.Rres[0], w.norm, c.g, c.b, w.eps, out=c.C[0])
             else:
                 fn.gemm_postnorm(dA, dB, w.norm, c.g, c.b, w.eps, pre_rmsnorm=w.pre_rmsnorm, pre_eps=w.pre_eps,
                                  out=c.C[0])
@@ -457,6 +508,10 @@ def oracle_step(w: Workload, d: dict, rows: np.ndarray):
     A = d["A64"][rows]
     if w.kind == "prenorm":
         oracle.lazy_prenorm_gemm(A, d["B64"], w.eps)
+    elif w.kind == "prenorm_affine":
+        oracle.prenorm_affine_gemm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps)
+    elif w.residual:
+        oracle.gemm_add_postnorm(A, d["B64"], d["R64"][rows], w.norm, d["g64"], d["b64"], w.eps)
     elif w.kind == "postnorm":
         oracle.gemm_postnorm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps, pre_rmsnorm=w.pre_rmsnorm,
                              pre_eps=w.pre_eps)
@@ -471,7 +526,7 @@ def _oracle_inputs(names):
         w = WORKLOADS[n]
         d = make_inputs(w, 0)
         out.append((w, {"A64": to_f64(d["A"]), "B64": to_f64(d["B"]), "g64": to_f64(d["gamma"]),
-                        "b64": to_f64(d["beta"])}))
+                        "b64": to_f64(d["beta"]), "R64": to_f64(d["R"])}))
     return out
 
 

@@ -124,6 +124,78 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
                                    void* stream);
 
 /*
+ * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual
+ * added to the fp32 accumulator in the epilogue, before the post-norm's row
+ * statistics.
+ *   [FNF-ru] "FlashNormAttention" (a residual connection followed by a
+ *   post-RMSNorm, with the tensor-core accumulator used for the addition);
+ *   [ATB] 1.1 and 1.2 for the norms.  The row split over a cluster and the
+ *   spill layout for wide rows are those of fnorm_gemm_postnorm; in the spill
+ *   layout the bf16 values written before normalisation are A @ B + R.
+ *   R:           [M,N] bf16 residual, 16-byte aligned; must not overlap C.
+ *   Other arguments as fnorm_gemm_postnorm (this form has no pre-norm).
+ */
+fnorm_status_t fnorm_gemm_add_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* R,
+                                       fnorm_bf16* C, int64_t M, int64_t N, int64_t K, fnorm_norm_t norm,
+                                       const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                       float* mean_out, float* rstd_out, void* stream);
+
+/*
+ * fnorm_fold_prenorm_affine — fold the fixed elementwise affine of a pre-norm
+ * into the weight of the GEMM that the normalised rows feed:
+ *   B_folded[k,n] = bf16(gamma[k] * B[k,n])   (round to nearest even)
+ *   colsum[n]     = sum_k B_folded[k,n]       (fp32, over the rounded values)
+ *   bias[n]       = sum_k beta[k] * B[k,n]    (fp32)
+ *   [ATB] 6.4 (with gamma fixed, as at inference, it can be folded into the
+ *   weights of the following matmul; a training step, whose gamma changes,
+ *   folds again); [FNF-ru] "Lazy Pre-Norm" limits (the per-column affine does
+ *   not commute with the GEMM, so it cannot stay in the prologue).
+ *   B:        [K,N] bf16.
+ *   gamma:    [K] bf16, or NULL (B_folded is then a copy of B).
+ *   beta:     [K] bf16, or NULL; bias must be non-NULL exactly when beta is.
+ *   B_folded: [K,N] bf16 output; may be B itself (in place), no other overlap.
+ *   colsum:   [N] fp32 output (16-byte aligned), or NULL.  Needed by
+ *             fnorm_prenorm_gemm for LayerNorm.
+ *   bias:     [N] fp32 output (16-byte aligned), or NULL.
+ *   Reductions run in a fixed order: the outputs are deterministic.
+ *   (M is absent: there is no A; K and N follow the shared size rules.)
+ */
+fnorm_status_t fnorm_fold_prenorm_affine(const fnorm_bf16* B, int64_t K, int64_t N, const fnorm_bf16* gamma,
+                                         const fnorm_bf16* beta, fnorm_bf16* B_folded, float* colsum,
+                                         float* bias, void* stream);
+
+/*
+ * fnorm_prenorm_gemm — C = (norm(A) * gamma + beta) @ B, a pre-norm with
+ * elementwise affine feeding a GEMM, in one lazy kernel on the weight folded
+ * by fnorm_fold_prenorm_affine:
+ *   RMSNorm:   C = rstd * (A @ B_folded) + bias
+ *   LayerNorm: C = rstd * (A @ B_folded - mean * colsum) + bias
+ *   mean and rstd are the row statistics of A (rstd = 1/sqrt(var + eps) with
+ *   the biased variance for LayerNorm, 1/sqrt(mean(a^2) + eps) for RMSNorm),
+ *   summed in fp32 from the A tiles in shared memory by a dedicated norm warp
+ *   group while the tensor cores run (LayerNorm: sums shifted by the row's
+ *   first element), and applied to the fp32 accumulator before the bf16
+ *   rounding of C.
+ *   [FNF-ru] "Lazy Pre-Norm" (the row scale applied after the k-loop) and
+ *   "FlashNormAttention" (a pre-LayerNorm computed by its own warp group);
+ *   [ATB] 1.1, 1.2.  Removing the mean after the GEMM is exact in real
+ *   arithmetic: sum_k (a_k - mean) * B'[k,n] = (A @ B')[m,n] - mean * colsum[n];
+ *   colsum sums the same rounded B' the tensor cores multiply.
+ *   B_folded: [K,N] bf16 (fnorm_fold_prenorm_affine; with gamma = NULL it is B).
+ *   colsum:   [N] fp32, 16-byte aligned; required for LayerNorm, unused (may
+ *             be NULL) for RMSNorm.
+ *   bias:     [N] fp32, 16-byte aligned, or NULL (beta = 0).
+ *   eps:      epsilon of the pre-norm, inside the square root.
+ *   mean_out: [M] fp32 (LayerNorm only, else must be NULL), or NULL.
+ *   rstd_out: [M] fp32, or NULL.
+ *   With RMSNorm and bias == NULL this is fnorm_lazy_prenorm_gemm on B_folded.
+ */
+fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folded, fnorm_bf16* C,
+                                  int64_t M, int64_t N, int64_t K, fnorm_norm_t norm, const float* colsum,
+                                  const float* bias, float eps, float* mean_out, float* rstd_out,
+                                  void* stream);
+
+/*
  * fnorm_rmsnorm — standalone row RMSNorm, Y = X / sqrt(mean(X^2) + eps) * gamma.
  *   [ATB] 1.2.  The unfused comparison kernel ([FNF-ru] FAQ: a standalone norm
  *   stays memory-bound however well it is written).  gamma: [N] or NULL.
@@ -140,6 +212,20 @@ fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int6
 fnorm_status_t fnorm_layernorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N,
                                const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
                                float* mean_out, float* rstd_out, void* stream);
+
+/*
+ * fnorm_add_rownorm — standalone residual-add row norm,
+ *   Y = norm(X + R) * gamma + beta, the sum X + R taken in fp32 per element.
+ *   The unfused comparison of fnorm_gemm_add_postnorm (its norm half after a
+ *   plain fnorm_gemm); [FNF-ru] "FlashNormAttention" (residual connection and
+ *   post-RMSNorm); [ATB] 1.1, 1.2.
+ *   X, R, Y: [M,N] bf16; R must not overlap Y.  norm: FNORM_LAYERNORM or
+ *   FNORM_RMSNORM.  gamma, beta: [N] or NULL.  mean_out (LayerNorm only),
+ *   rstd_out: [M] fp32 or NULL.  N <= 32768.
+ */
+fnorm_status_t fnorm_add_rownorm(const fnorm_bf16* X, const fnorm_bf16* R, fnorm_bf16* Y, int64_t M, int64_t N,
+                                 fnorm_norm_t norm, const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                 float* mean_out, float* rstd_out, void* stream);
 
 /*
  * fnorm_check_status — synchronise `stream`, then read and clear the device

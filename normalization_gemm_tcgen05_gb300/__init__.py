@@ -13,7 +13,12 @@ Forms (see the header for the full contract):
 * ``lazy_prenorm_gemm(A, B, eps)``    C = rmsnorm(A) @ B = (A @ B) * rstd(A)
 * ``gemm_postnorm(A, B, norm, ...)``  C = norm(A @ B) * gamma + beta, optionally
   norm(rmsnorm(A) @ B); rows wider than one CTA tile are split over a cluster
-* ``rmsnorm(X)`` / ``layernorm(X)``   standalone row norms (unfused comparison)
+* ``gemm_add_postnorm(A, B, R, norm, ...)``  C = norm(A @ B + R) * gamma + beta
+* ``fold_prenorm_affine(B, gamma, beta)``  B' = bf16(diag(gamma) B), colsum(B'), beta @ B
+* ``prenorm_gemm(A, B', norm, colsum, bias)``  C = (norm(A) * gamma + beta) @ B,
+  LayerNorm or RMSNorm, lazily on the folded weight
+* ``rmsnorm(X)`` / ``layernorm(X)`` / ``add_rownorm(X, R, norm)``  standalone
+  row norms (the unfused comparison)
 
 ``lib()`` returns the ctypes handle with every entry point declared, for
 callers that want the raw C ABI.
@@ -27,7 +32,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "gemm_postnorm", "rmsnorm",
+    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "gemm_postnorm", "gemm_add_postnorm",
+    "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
     "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
 ]
@@ -63,8 +69,13 @@ _SIGNATURES = {
     "fnorm_lazy_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _f32, _p, _p]),
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
+    "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
+                                            _p, _p, _p]),
+    "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
+    "fnorm_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32, _p, _p, _p]),
     "fnorm_rmsnorm": (_c_status, [_p, _p, _i64, _i64, _p, _f32, _p, _p]),
     "fnorm_layernorm": (_c_status, [_p, _p, _i64, _i64, _p, _p, _f32, _p, _p, _p]),
+    "fnorm_add_rownorm": (_c_status, [_p, _p, _p, _i64, _i64, ctypes.c_int, _p, _p, _f32, _p, _p, _p]),
     "fnorm_check_status": (_c_status, [_p]),
     "fnorm_last_error": (ctypes.c_char_p, []),
     "fnorm_set_wait_limit_ns": (_c_status, [ctypes.c_uint64]),
@@ -130,6 +141,16 @@ def _vec(t: Optional[torch.Tensor], n: int, name: str, device) -> Optional[torch
         return None
     if t.dtype != torch.bfloat16 or t.dim() != 1 or t.numel() != n:
         raise ValueError(f"{name} must be a bfloat16 vector of length {n}")
+    if not t.is_cuda or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor on {device}")
+    return t
+
+
+def _fvec(t: Optional[torch.Tensor], n: int, name: str, device) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or t.dim() != 1 or t.numel() != n:
+        raise ValueError(f"{name} must be a float32 vector of length {n}")
     if not t.is_cuda or t.device != device or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor on {device}")
     return t
@@ -222,6 +243,87 @@ def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Opt
     return (C, stats) if return_stats else C
 
 
+def gemm_add_postnorm(A: torch.Tensor, B: torch.Tensor, R: torch.Tensor, norm="rmsnorm",
+                      gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None, eps: float = 1e-5,
+                      out: Optional[torch.Tensor] = None, return_stats: bool = False):
+    """C = norm(A @ B + R) * gamma + beta: the residual R [M, N] is added to the
+    fp32 accumulator before the post-norm.  With ``return_stats`` also returns
+    {"rstd", "mean" (LayerNorm)} of the rows of A @ B + R."""
+    M, N, K = _ab(A, B)
+    _mat(R, "R")
+    if tuple(R.shape) != (M, N) or R.device != A.device:
+        raise ValueError(f"R must have shape {(M, N)} on {A.device}")
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    nid = _NORMS[norm]
+    gamma = _vec(gamma, N, "gamma", A.device)
+    beta = _vec(beta, N, "beta", A.device)
+    C = _out(out, (M, N), A.device)
+    stats = {}
+    if return_stats:
+        stats["rstd"] = _stat(M, A.device)
+        stats["mean"] = _stat(M, A.device) if nid == LAYERNORM else None
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_gemm_add_postnorm(
+            _ptr(A), _ptr(B), _ptr(R), _ptr(C), M, N, K, nid, _ptr(gamma), _ptr(beta), float(eps),
+            _ptr(stats.get("mean")), _ptr(stats.get("rstd")), _stream(A.device)))
+    return (C, stats) if return_stats else C
+
+
+def fold_prenorm_affine(B: torch.Tensor, gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, colsum_out: Optional[torch.Tensor] = None,
+                        bias_out: Optional[torch.Tensor] = None):
+    """Fold a pre-norm's fixed affine into the weight B [K, N] it feeds.
+
+    Returns (B_folded, colsum, bias): B_folded = bf16(diag(gamma) B) [K, N],
+    colsum = column sums of B_folded (fp32 [N]) and bias = beta @ B (fp32 [N],
+    None without beta).  ``out`` may be B itself (fold in place);
+    ``colsum_out`` / ``bias_out`` receive the sums when given.
+    """
+    _mat(B, "B")
+    K, N = B.shape
+    gamma = _vec(gamma, K, "gamma", B.device)
+    beta = _vec(beta, K, "beta", B.device)
+    Bf = _out(out, (K, N), B.device, "out")
+    colsum = _fvec(colsum_out, N, "colsum_out", B.device)
+    if colsum is None:
+        colsum = torch.empty(N, dtype=torch.float32, device=B.device)
+    bias = None
+    if beta is not None:
+        bias = _fvec(bias_out, N, "bias_out", B.device)
+        if bias is None:
+            bias = torch.empty(N, dtype=torch.float32, device=B.device)
+    with torch.cuda.device(B.device):
+        _check(lib().fnorm_fold_prenorm_affine(_ptr(B), K, N, _ptr(gamma), _ptr(beta), _ptr(Bf), _ptr(colsum),
+                                               _ptr(bias), _stream(B.device)))
+    return Bf, colsum, bias
+
+
+def prenorm_gemm(A: torch.Tensor, B_folded: torch.Tensor, norm="layernorm", colsum: Optional[torch.Tensor] = None,
+                 bias: Optional[torch.Tensor] = None, eps: float = 1e-5, out: Optional[torch.Tensor] = None,
+                 return_stats: bool = False):
+    """C = (norm(A) * gamma + beta) @ B on the weight folded by
+    ``fold_prenorm_affine``: rstd * (A @ B' - mean * colsum) + bias for
+    LayerNorm, rstd * (A @ B') + bias for RMSNorm.  With ``return_stats`` also
+    returns {"rstd", "mean" (LayerNorm)} of the rows of A."""
+    M, N, K = _ab(A, B_folded)
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    nid = _NORMS[norm]
+    colsum = _fvec(colsum, N, "colsum", A.device)
+    bias = _fvec(bias, N, "bias", A.device)
+    C = _out(out, (M, N), A.device)
+    stats = {}
+    if return_stats:
+        stats["rstd"] = _stat(M, A.device)
+        stats["mean"] = _stat(M, A.device) if nid == LAYERNORM else None
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_prenorm_gemm(
+            _ptr(A), _ptr(B_folded), _ptr(C), M, N, K, nid, _ptr(colsum), _ptr(bias), float(eps),
+            _ptr(stats.get("mean")), _ptr(stats.get("rstd")), _stream(A.device)))
+    return (C, stats) if return_stats else C
+
+
 def rmsnorm(X: torch.Tensor, gamma: Optional[torch.Tensor] = None, eps: float = 1e-6,
             out: Optional[torch.Tensor] = None, return_rstd: bool = False):
     """Standalone row RMSNorm (the unfused comparison kernel)."""
@@ -250,6 +352,31 @@ def layernorm(X: torch.Tensor, gamma: Optional[torch.Tensor] = None, beta: Optio
         _check(lib().fnorm_layernorm(_ptr(X), _ptr(Y), M, N, _ptr(gamma), _ptr(beta), float(eps), _ptr(mean),
                                      _ptr(rstd), _stream(X.device)))
     return (Y, {"mean": mean, "rstd": rstd}) if return_stats else Y
+
+
+def add_rownorm(X: torch.Tensor, R: torch.Tensor, norm="rmsnorm", gamma: Optional[torch.Tensor] = None,
+                beta: Optional[torch.Tensor] = None, eps: float = 1e-5, out: Optional[torch.Tensor] = None,
+                return_stats: bool = False):
+    """Standalone norm(X + R) * gamma + beta (the unfused residual-add norm)."""
+    _mat(X, "X")
+    _mat(R, "R")
+    M, N = X.shape
+    if tuple(R.shape) != (M, N) or R.device != X.device:
+        raise ValueError(f"R must have shape {(M, N)} on {X.device}")
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    nid = _NORMS[norm]
+    gamma = _vec(gamma, N, "gamma", X.device)
+    beta = _vec(beta, N, "beta", X.device)
+    Y = _out(out, (M, N), X.device)
+    stats = {}
+    if return_stats:
+        stats["rstd"] = _stat(M, X.device)
+        stats["mean"] = _stat(M, X.device) if nid == LAYERNORM else None
+    with torch.cuda.device(X.device):
+        _check(lib().fnorm_add_rownorm(_ptr(X), _ptr(R), _ptr(Y), M, N, nid, _ptr(gamma), _ptr(beta), float(eps),
+                                       _ptr(stats.get("mean")), _ptr(stats.get("rstd")), _stream(X.device)))
+    return (Y, stats) if return_stats else Y
 
 
 def check_status(device=None) -> None:

@@ -220,6 +220,104 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
 }
 
+fnorm_status_t fnorm_fold_prenorm_affine(const fnorm_bf16* B, int64_t K, int64_t N, const fnorm_bf16* gamma,
+                                         const fnorm_bf16* beta, fnorm_bf16* B_folded, float* colsum, float* bias,
+                                         void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(0, N, K));
+  if ((beta == nullptr) != (bias == nullptr)) return bad("bias must be given exactly when beta is");
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(B_folded, "B_folded", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 2, true));
+  FN_TRY(check_ptr(beta, "beta", 2, true));
+  FN_TRY(check_ptr(colsum, "colsum", 16, true));
+  FN_TRY(check_ptr(bias, "bias", 16, true));
+  {
+    // B_folded may be B itself (in place) but no other overlap
+    const auto b0 = reinterpret_cast<uintptr_t>(B), f0 = reinterpret_cast<uintptr_t>(B_folded);
+    const uintptr_t bytes = static_cast<uintptr_t>(K) * static_cast<uintptr_t>(N) * 2u;
+    if (b0 != f0 && b0 < f0 + bytes && f0 < b0 + bytes) return bad("B_folded overlaps B without being B");
+  }
+  return launch_fold_prenorm_affine(B, static_cast<int>(K), static_cast<int>(N), gamma, beta, B_folded, colsum,
+                                    bias, static_cast<cudaStream_t>(stream));
+}
+
+fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folded, fnorm_bf16* C, int64_t M,
+                                  int64_t N, int64_t K, fnorm_norm_t norm, const float* colsum, const float* bias,
+                                  float eps, float* mean_out, float* rstd_out, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  FN_TRY(check_eps(eps, "eps"));
+  const bool ln = norm == FNORM_LAYERNORM;
+  if (!ln && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
+  if (ln && colsum == nullptr) return bad("LayerNorm needs the column sums of the folded B (colsum)");
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B_folded, "B_folded", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(colsum, "colsum", 16, true));
+  FN_TRY(check_ptr(bias, "bias", 16, true));
+  FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  FusedLaunch L = base_launch(A, B_folded, C, M, N, K, stream);
+  L.bn = gemm_tile_n(N);
+  L.bres = want_resident_b(M, N, K, L.bn);
+  L.pre_eps = eps;
+  L.rstd_out = rstd_out;
+  if (!ln && bias == nullptr) {
+    // RMSNorm with gamma only: the folded B makes it the plain lazy pre-norm
+    L.mode = MODE_PRE;
+    return launch_fused_plain(L);
+  }
+  L.mode = MODE_PRE | MODE_AFF | (ln ? MODE_PRE_LN : 0);
+  L.colsum = ln ? colsum : nullptr;
+  L.bias = bias;
+  L.mean_out = ln ? mean_out : nullptr;
+  return launch_fused_prenorm_affine(L);
+}
+
+fnorm_status_t fnorm_gemm_add_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* R, fnorm_bf16* C,
+                                       int64_t M, int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                       const fnorm_bf16* beta, float eps, float* mean_out, float* rstd_out,
+                                       void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  FN_TRY(check_eps(eps, "eps"));
+  if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
+  PostPlan plan{};
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(R, "R", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
+  FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  {
+    const auto r0 = reinterpret_cast<uintptr_t>(R), c0 = reinterpret_cast<uintptr_t>(C);
+    const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(N) * 2u;
+    if (r0 < c0 + bytes && c0 < r0 + bytes) return bad("R must not overlap C");
+  }
+  FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  L.mode = MODE_POST | MODE_RES | (norm == FNORM_LAYERNORM ? MODE_LN : 0);
+  L.bn = plan.bn;
+  L.slices = plan.slices;
+  L.spill = plan.spill;
+  L.cluster = plan.cluster;
+  L.bres = (plan.cluster == 1 && !plan.spill) && want_resident_b(M, N, K, plan.bn);
+  L.eps = eps;
+  L.gamma = gamma;
+  L.beta = beta;
+  L.mean_out = mean_out;
+  L.rstd_out = rstd_out;
+  L.R = R;
+  return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_residual(L) : launch_fused_post_residual_cluster(L);
+}
+
 fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
                              float eps, float* rstd_out, void* stream) {
   clear_error();
@@ -231,7 +329,7 @@ fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int6
   FN_TRY(check_ptr(Y, "Y", 16, false));
   FN_TRY(check_ptr(gamma, "gamma", 16, true));
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
-  return launch_rownorm(X, Y, static_cast<int>(M), static_cast<int>(N), false, gamma, nullptr, eps, nullptr,
+  return launch_rownorm(X, nullptr, Y, static_cast<int>(M), static_cast<int>(N), false, gamma, nullptr, eps, nullptr,
                         rstd_out, static_cast<cudaStream_t>(stream));
 }
 
@@ -249,8 +347,29 @@ fnorm_status_t fnorm_layernorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, in
   FN_TRY(check_ptr(beta, "beta", 16, true));
   FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
-  return launch_rownorm(X, Y, static_cast<int>(M), static_cast<int>(N), true, gamma, beta, eps, mean_out,
+  return launch_rownorm(X, nullptr, Y, static_cast<int>(M), static_cast<int>(N), true, gamma, beta, eps, mean_out,
                         rstd_out, static_cast<cudaStream_t>(stream));
+}
+
+fnorm_status_t fnorm_add_rownorm(const fnorm_bf16* X, const fnorm_bf16* R, fnorm_bf16* Y, int64_t M, int64_t N,
+                                 fnorm_norm_t norm, const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                 float* mean_out, float* rstd_out, void* stream) {
+  clear_error();
+  if (M < 0 || M > kMaxDim) return bad("M must be in [0, 2^31)");
+  if (N < 8 || N % 8 != 0 || N > 32768) return bad("N must be a multiple of 8 in [8, 32768]");
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  FN_TRY(check_eps(eps, "eps"));
+  if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(X, "X", 16, false));
+  FN_TRY(check_ptr(R, "R", 16, false));
+  FN_TRY(check_ptr(Y, "Y", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
+  FN_TRY(check_ptr(mean_out, "mean_out", 4, true));
+  FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
+  return launch_rownorm(X, R, Y, static_cast<int>(M), static_cast<int>(N), norm == FNORM_LAYERNORM, gamma, beta,
+                        eps, mean_out, rstd_out, static_cast<cudaStream_t>(stream));
 }
 
 fnorm_status_t fnorm_check_status(void* stream) {

@@ -61,6 +61,9 @@ enum : int {
   MODE_CLUSTER = 8,   // rows split over a cluster of CTAs along N
   MODE_SPILL = 16,    // spill layout: S slices per CTA, normalised from L2
   MODE_BRES = 32,     // all of B (K x BN, <= 128 KB) resident in shared memory
+  MODE_PRE_LN = 64,   // the lazy pre-norm is LayerNorm (mean removed by a column-sum correction)
+  MODE_AFF = 128,     // lazy pre-norm affine folded into B: column sums and a bias per column
+  MODE_RES = 256,     // residual R added to the accumulator before the post-norm
 };
 
 struct FusedParams {
@@ -74,6 +77,9 @@ struct FusedParams {
   float* mean_out;
   float* rstd_out;
   float* pre_rstd_out;
+  const float* colsum;        // [N] column sums of the (gamma-folded) B (MODE_PRE_LN)
+  const float* bias;          // [N] beta @ B, or NULL (MODE_AFF)
+  const __nv_bfloat16* R;     // [M, N] residual (MODE_RES)
   uint32_t* status;
   unsigned long long wait_limit_ns;
 };
@@ -95,7 +101,7 @@ struct Aux {
   uint64_t xbar[2];
   uint64_t nstat_full[2];
   uint64_t nstat_empty[2];
-  uint64_t ebar[2];  // bounded group barrier of the eight epilogue warps
+  uint64_t ebar[4][2];  // bounded barrier of the two epilogue warps of each TMEM lane quarter
   uint64_t teardown;
   uint64_t bres_full;
   uint32_t tmem_base;
@@ -103,6 +109,8 @@ struct Aux {
   int nstat_m0[2];
   int nstat_c0[2];
   float ss[2][128];
+  float ss1[2][128];  // pre-LayerNorm: shifted sums of the A rows and the shift
+  float ssk[2][128];
   float2 nstat[2][128];
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
   alignas(16) float gam[GB];
@@ -124,6 +132,9 @@ struct KCfg {
   static constexpr bool CLUSTER = (MODE & MODE_CLUSTER) != 0;
   static constexpr bool SPILL = (MODE & MODE_SPILL) != 0;
   static constexpr bool BRES = (MODE & MODE_BRES) != 0;
+  static constexpr bool PRE_LN = (MODE & MODE_PRE_LN) != 0;
+  static constexpr bool AFF = (MODE & MODE_AFF) != 0;
+  static constexpr bool RES = (MODE & MODE_RES) != 0;
   // the spill layout's in-place normalisation runs in its own warps (10-13)
   // unless those warps compute the Lazy Pre-Norm sums of squares
   static constexpr bool NORMW = SPILL && !PRE;
@@ -162,6 +173,9 @@ struct KCfg {
   static_assert(!SPILL || (BN == 256 && POST && CLUSTER), "spill layout: 256-column slices, post-norm, cluster");
   static_assert(!CLUSTER || (POST && CLMAX_ >= 1 && CLMAX_ <= 8), "clusters serve the post-norm, up to 8 CTAs");
   static_assert(!BRES || !CLUSTER, "resident B serves one CTA per row block");
+  static_assert(!(PRE_LN || AFF) || (PRE && !POST), "the folded-affine pre-norm serves the pre-norm GEMM alone");
+  static_assert(!PRE_LN || AFF, "the pre-LayerNorm needs its column sums");
+  static_assert(!RES || (POST && !PRE), "the residual serves the post-norm");
 };
 
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
@@ -188,6 +202,12 @@ __device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, in
     bv[0] = bf16_lo(u.x); bv[1] = bf16_hi(u.x); bv[2] = bf16_lo(u.y); bv[3] = bf16_hi(u.y);
     bv[4] = bf16_lo(u.z); bv[5] = bf16_hi(u.z); bv[6] = bf16_lo(u.w); bv[7] = bf16_hi(u.w);
   }
+  uint64_t g2[4], b2[4];  // gamma, beta as packed pairs
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    g2[h] = f2(gv[2 * h], gv[2 * h + 1]);
+    b2[h] = f2(bv[2 * h], bv[2 * h + 1]);
+  }
 #pragma unroll 1
   for (int rr = 0; rr < nrows; rr += 8) {
     uint4 v[8];  // eight rows of loads in flight per lane
@@ -204,13 +224,13 @@ __device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, in
       const int m = r0 + rr + u;
       if (colok && rr + u < nrows && m < p.M) {
         const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const uint64_t mu2 = f2(mu, mu), rs2 = f2(rs, rs);
         uint32_t o[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float x0 = bf16_lo(in[h]), x1 = bf16_hi(in[h]);
-          const float y0 = (LN ? (x0 - mu) : x0) * rs * gv[2 * h] + bv[2 * h];
-          const float y1 = (LN ? (x1 - mu) : x1) * rs * gv[2 * h + 1] + bv[2 * h + 1];
-          o[h] = pack_bf16x2(y0, y1);
+          // y = (x - mean) * rstd * gamma + beta
+          const uint64_t x = f2(bf16_lo(in[h]), bf16_hi(in[h]));
+          o[h] = pack_bf16x2_f2(f2_fma(f2_mul(LN ? f2_sub(x, mu2) : x, rs2), g2[h], b2[h]));
         }
         st_global_v4(p.C + static_cast<size_t>(m) * p.N + col, make_uint4(o[0], o[1], o[2], o[3]));
       }
@@ -231,17 +251,27 @@ __device__ __forceinline__ void tmem_load_batch(uint32_t taddr, uint32_t (&r)[NB
 
 // Accumulate one 32-column subtile of raw accumulator values into row sums:
 // LayerNorm s1 += u - k, s2 += (u - k)^2 (k: the shift); RMSNorm s2 += u^2.
-// Columns j >= lim are ignored; full subtiles take the unpredicated loop.
+// Even and odd columns go to separate sums ([0], [1]); a full subtile runs
+// them as packed pairs.  Columns j >= lim are ignored.
 template <bool LN>
 __device__ __forceinline__ void accum_stats(const uint32_t (&r)[32], int lim, float k, float (&s1)[2],
                                             float (&s2)[2]) {
   if (lim >= 32) {
+    const uint64_t kk = f2(k, k);
+    uint64_t a1 = f2(s1[0], s1[1]), a2 = f2(s2[0], s2[1]);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float d = LN ? __uint_as_float(r[j]) - k : __uint_as_float(r[j]);
-      if (LN) s1[j & 1] += d;
-      s2[j & 1] = fmaf(d, d, s2[j & 1]);
+    for (int j = 0; j < 32; j += 2) {
+      const uint64_t u = f2u(r[j], r[j + 1]);
+      const uint64_t d = LN ? f2_sub(u, kk) : u;
+      if (LN) a1 = f2_add(a1, d);
+      a2 = f2_fma(d, d, a2);
     }
+    if (LN) {
+      s1[0] = f2_lo(a1);
+      s1[1] = f2_hi(a1);
+    }
+    s2[0] = f2_lo(a2);
+    s2[1] = f2_hi(a2);
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -258,28 +288,78 @@ __device__ __forceinline__ void accum_stats(const uint32_t (&r)[32], int lim, fl
 // bf16 pairs (two FMAs per element; gamma/beta read as float4 broadcasts)
 __device__ __forceinline__ void affine_pack(const uint32_t (&r)[32], float a, float b, const float* gam,
                                             const float* bet, uint32_t (&w)[16]) {
+  const uint64_t aa = f2(a, a), bb = f2(b, b);
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
     const float4 g = *reinterpret_cast<const float4*>(gam + j);
     const float4 be = *reinterpret_cast<const float4*>(bet + j);
-    const float y0 = fmaf(fmaf(__uint_as_float(r[j]), a, b), g.x, be.x);
-    const float y1 = fmaf(fmaf(__uint_as_float(r[j + 1]), a, b), g.y, be.y);
-    const float y2 = fmaf(fmaf(__uint_as_float(r[j + 2]), a, b), g.z, be.z);
-    const float y3 = fmaf(fmaf(__uint_as_float(r[j + 3]), a, b), g.w, be.w);
-    w[j >> 1] = pack_bf16x2(y0, y1);
-    w[(j >> 1) + 1] = pack_bf16x2(y2, y3);
+    const uint64_t y01 = f2_fma(f2_fma(f2u(r[j], r[j + 1]), aa, bb), f2(g.x, g.y), f2(be.x, be.y));
+    const uint64_t y23 = f2_fma(f2_fma(f2u(r[j + 2], r[j + 3]), aa, bb), f2(g.z, g.w), f2(be.z, be.w));
+    w[j >> 1] = pack_bf16x2_f2(y01);
+    w[(j >> 1) + 1] = pack_bf16x2_f2(y23);
   }
 }
 
 // y = u * a (a = 1 for the plain GEMM), packed to bf16 pairs
 template <bool SCALE>
 __device__ __forceinline__ void scale_pack(const uint32_t (&r)[32], float a, uint32_t (&w)[16]) {
+  const uint64_t aa = f2(a, a);
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const float y0 = SCALE ? __uint_as_float(r[j]) * a : __uint_as_float(r[j]);
-    const float y1 = SCALE ? __uint_as_float(r[j + 1]) * a : __uint_as_float(r[j + 1]);
-    w[j >> 1] = pack_bf16x2(y0, y1);
+    const uint64_t u = f2u(r[j], r[j + 1]);
+    w[j >> 1] = pack_bf16x2_f2(SCALE ? f2_mul(u, aa) : u);
   }
+}
+
+// Lazy pre-norm with folded affine: y = u * a + (colsum_n * c + bias_n) for
+// one 32-column subtile of which `nvalid` columns lie inside the row
+// (c = -mean * rstd for LayerNorm, 0 for RMSNorm).  colsum/bias are fp32,
+// 16-byte aligned, read as float4 broadcasts (every lane reads the same
+// columns); N is a multiple of 8, so a group of 4 is wholly in or out.
+template <bool HAS_CS>
+__device__ __forceinline__ void prenorm_pack(const uint32_t (&r)[32], float a, float c, const float* cs,
+                                             const float* bias, int nvalid, uint32_t (&w)[16]) {
+  const uint64_t aa = f2(a, a), cc = f2(c, c);
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bb = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < nvalid) {
+      if (HAS_CS) sc = __ldg(reinterpret_cast<const float4*>(cs + j));
+      if (bias != nullptr) bb = __ldg(reinterpret_cast<const float4*>(bias + j));
+    }
+    const uint64_t y01 = f2_fma(f2u(r[j], r[j + 1]), aa, f2_fma(f2(sc.x, sc.y), cc, f2(bb.x, bb.y)));
+    const uint64_t y23 = f2_fma(f2u(r[j + 2], r[j + 3]), aa, f2_fma(f2(sc.z, sc.w), cc, f2(bb.z, bb.w)));
+    w[j >> 1] = pack_bf16x2_f2(y01);
+    w[(j >> 1) + 1] = pack_bf16x2_f2(y23);
+  }
+}
+
+// Residual through the accumulator: write R[m, col0 .. col0 + 32*NC) (bf16,
+// widened exactly to fp32) into this warp's TMEM lanes of an accumulator
+// buffer, which the MMAs of the next tile in that buffer then accumulate onto
+// (D = A @ B + R).  Rows past M and columns past N are written as zero (N is
+// a multiple of 8, so 8-column groups are whole).  Returns after the stores
+// have completed.
+template <int NC>
+__device__ __forceinline__ void preload_residual(const FusedParams& p, uint32_t taddr, int m, int col0) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    uint32_t v[32];
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const int col = col0 + c * 32 + g8 * 8;
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (m < p.M && col < p.N) x = __ldg(reinterpret_cast<const uint4*>(p.R + static_cast<size_t>(m) * p.N + col));
+      const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        v[g8 * 8 + 2 * hh] = __float_as_uint(bf16_lo(in[hh]));
+        v[g8 * 8 + 2 * hh + 1] = __float_as_uint(bf16_hi(in[hh]));
+      }
+    }
+    tmem_st_32x32b_x32(taddr + c * 32, v);
+  }
+  tmem_st_wait();
 }
 
 // Parallel-variance combination: fold (mean_b, m2_b) over nb values into
@@ -302,6 +382,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr int BK = Cfg::BK, BN = Cfg::BN, STAGES = Cfg::STAGES, HALF = Cfg::HALF, NCH = Cfg::NCH;
   constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER, SPILL = Cfg::SPILL;
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
+  constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX>;
 
@@ -346,7 +427,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->xbar[b]), 1);
       mbar_init(smem_u32(&aux->nstat_full[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->nstat_empty[b]), 4);
-      mbar_init(smem_u32(&aux->ebar[b]), kEpiWarps);
+      for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&aux->ebar[qq][b]), kEpiWarps / 4);
     }
     mbar_init(smem_u32(&aux->teardown), 1);
     mbar_init(smem_u32(&aux->bres_full), 1);
@@ -430,7 +511,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         for (int s = 0; s < S && ok; ++s, ++it) {
           const int buf = it & 1;
           const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-          if (!mbar_wait(wc, smem_u32(&aux->acc_empty[buf]), aph ^ 1u, kSiteMma)) {
+          // with the residual, the epilogue releases each buffer once more
+          // up front, after writing the first tile's R into it
+          if (!mbar_wait(wc, smem_u32(&aux->acc_empty[buf]), RES ? aph : aph ^ 1u, kSiteMma)) {
             ok = false;
             break;
           }
@@ -453,7 +536,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               // stride along N, SBO = 8-row group stride along K; a K step of 16
               // rows is 2048 bytes.
               const uint64_t db = make_smem_desc(sb + ks * (16 * 128), BK * 128, 1024, kSwizzle128B);
-              umma_bf16(d0, da, db, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+              umma_bf16(d0, da, db, Cfg::IDESC, (RES || (kb | ks) != 0) ? 1u : 0u);
             }
             umma_commit(smem_u32(&aux->empty[stage]));
             if (++stage == STAGES) {
@@ -516,15 +599,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       if (Cfg::STG_BUFS == 2) sbuf ^= 1u;
     };
 
-    // barrier of the eight epilogue warps on an mbarrier, so that it is
+    // barrier of the two epilogue warps that share this TMEM lane quarter
+    // (the same 32 rows, one column half each) on an mbarrier, so that it is
     // bounded like every other wait (returns false if it gave up)
     int esn = 0;
     auto esync = [&]() -> bool {
       const int b = esn & 1;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&aux->ebar[b]));
+      if (lane == 0) mbar_arrive(smem_u32(&aux->ebar[q][b]));
       const bool r =
-          mbar_wait_warp(wc, smem_u32(&aux->ebar[b]), static_cast<uint32_t>(esn >> 1) & 1u, kSiteEpilogue);
+          mbar_wait_warp(wc, smem_u32(&aux->ebar[q][b]), static_cast<uint32_t>(esn >> 1) & 1u, kSiteEpilogue);
       ++esn;
       return r;
     };
@@ -574,6 +658,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       return true;
     };
 
+    // residual: write R of iteration it2's tile into its accumulator buffer
+    // (this warp's lanes and column half); false if there is no such tile
+    auto preload_iter = [&](int it2) -> bool {
+      const int t2 = cid + (it2 / S) * ncl;
+      if (t2 >= total) return false;
+      const int g2 = t2 % ngroups;
+      const int n0b = (g2 * C + rank) * cta_cols + (it2 % S) * BN;
+      const uint32_t tb2 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>((it2 & 1) * BN + h * HALF);
+      preload_residual<NCH>(p, tb2, (t2 / ngroups) * Cfg::BM + row, n0b + h * HALF);
+      return true;
+    };
+    if (RES) {
+      // the first two tiles' buffers start out holding their residual
+      for (int i2 = 0; i2 < 2; ++i2) {
+        if (!preload_iter(i2)) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[i2]));
+      }
+    }
+
     // spill-layout state: running shifted sums of this half over the current
     // row block, and (inline normalisation only) the pending row block
     float k0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f;
@@ -599,8 +705,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                             static_cast<uint32_t>(buf * BN + h * HALF);
 
-        // ---- lazy pre-norm scale: rstd of the A row ----
-        float pre = 1.0f;
+        // ---- lazy pre-norm scale: rstd (and, for LayerNorm, mean) of the A row ----
+        float pre = 1.0f, pre_mean = 0.0f;
         if (PRE) {
           const int sb = it & 1;
           if (!mbar_wait_warp(wc, smem_u32(&aux->ss_full[sb]), static_cast<uint32_t>(it >> 1) & 1u,
@@ -609,9 +715,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             break;
           }
           const float ss = aux->ss[sb][row];
+          const float kf = static_cast<float>(K);
+          if (PRE_LN) {
+            // LayerNorm of the A row from its shifted sums (shift: ssk)
+            const float s1 = aux->ss1[sb][row];
+            pre_mean = aux->ssk[sb][row] + s1 / kf;
+            const float var = fmaxf(ss / kf - (s1 / kf) * (s1 / kf), 0.0f);
+            pre = rsqrtf(var + p.pre_eps);
+          } else {
+            pre = rsqrtf(ss / kf + p.pre_eps);
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&aux->ss_empty[sb]));
-          pre = rsqrtf(ss / static_cast<float>(K) + p.pre_eps);
         }
         const int nvh = min(max(N - c0h, 0), HALF);  // valid columns of this half
 
@@ -636,6 +751,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               store_box(w, c0h + c * 32, m0);
             }
           }
+          if (RES) preload_iter(it + 2);  // this buffer's next tile starts from its residual
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
@@ -784,15 +900,20 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (col0 >= N) break;
             uint32_t w[16];
             if (POST) {
-              // y = (pre*u - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta
+              // y = (v - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta, v = pre * u
               affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f, &aux->gam[h * HALF + c * 32],
                           &aux->bet[h * HALF + c * 32], w);
+            } else if (AFF) {
+              // lazy pre-norm with folded affine: y = rstd * (u - mean * colsum_n) + bias_n
+              prenorm_pack<PRE_LN>(r[b], pre, -pre_mean * pre, p.colsum + col0,
+                                   p.bias == nullptr ? nullptr : p.bias + col0, N - col0, w);
             } else {
               scale_pack<PRE>(r[b], pre, w);
             }
             store_box(w, col0, m0);
           }
         }
+        if (RES) preload_iter(it + 2);  // this buffer's next tile starts from its residual
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
@@ -808,6 +929,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             }
           } else if (PRE) {
             if (g == 0 && p.rstd_out != nullptr) p.rstd_out[m] = pre;
+            if (PRE_LN && g == 0 && p.mean_out != nullptr) p.mean_out[m] = pre_mean;
           }
         }
       }
@@ -847,6 +969,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     for (int t = cid; t < total && ok; t += ncl) {
       for (int s = 0; s < S && ok; ++s, ++it) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float lsum[4] = {0.f, 0.f, 0.f, 0.f};  // pre-LayerNorm: sums of (a - shift)
+        float shift = 0.0f;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_warp(wc, smem_u32(&aux->full[stage]), phase, kSiteNorm)) {
             ok = false;
@@ -858,15 +982,29 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             // visit the row's physical chunks in a bank-conflict-free order;
             // the sum does not depend on the order
             const uint4 v = *reinterpret_cast<const uint4*>(arow + ((ch ^ swz) << 4));
-            float x;
-            x = bf16_lo(v.x); acc[0] = fmaf(x, x, acc[0]);
-            x = bf16_hi(v.x); acc[1] = fmaf(x, x, acc[1]);
-            x = bf16_lo(v.y); acc[2] = fmaf(x, x, acc[2]);
-            x = bf16_hi(v.y); acc[3] = fmaf(x, x, acc[3]);
-            x = bf16_lo(v.z); acc[0] = fmaf(x, x, acc[0]);
-            x = bf16_hi(v.z); acc[1] = fmaf(x, x, acc[1]);
-            x = bf16_lo(v.w); acc[2] = fmaf(x, x, acc[2]);
-            x = bf16_hi(v.w); acc[3] = fmaf(x, x, acc[3]);
+            if (PRE_LN) {
+              // the first value this thread reads (a[row][0]) is the shift
+              if (kb == 0 && ch == 0) shift = bf16_lo(v.x);
+              const float xs[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                   bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                // zero-filled K tail: a = 0 contributes (0 - shift), removed below
+                const float d = xs[e] - shift;
+                lsum[e & 3] += d;
+                acc[e & 3] = fmaf(d, d, acc[e & 3]);
+              }
+            } else {
+              float x;
+              x = bf16_lo(v.x); acc[0] = fmaf(x, x, acc[0]);
+              x = bf16_hi(v.x); acc[1] = fmaf(x, x, acc[1]);
+              x = bf16_lo(v.y); acc[2] = fmaf(x, x, acc[2]);
+              x = bf16_hi(v.y); acc[3] = fmaf(x, x, acc[3]);
+              x = bf16_lo(v.z); acc[0] = fmaf(x, x, acc[0]);
+              x = bf16_hi(v.z); acc[1] = fmaf(x, x, acc[1]);
+              x = bf16_lo(v.w); acc[2] = fmaf(x, x, acc[2]);
+              x = bf16_hi(v.w); acc[3] = fmaf(x, x, acc[3]);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&aux->empty[stage]));
@@ -882,7 +1020,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           ok = false;
           break;
         }
-        aux->ss[sb][row] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        float s2t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        if (PRE_LN) {
+          float s1t = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+          // the zero-filled tail of the last k-block added (0 - shift) per element
+          const float pad = static_cast<float>(num_kb * BK - K);
+          s1t += pad * shift;
+          s2t -= pad * shift * shift;
+          aux->ss1[sb][row] = s1t;
+          aux->ssk[sb][row] = shift;
+        }
+        aux->ss[sb][row] = s2t;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&aux->ss_full[sb]));
       }

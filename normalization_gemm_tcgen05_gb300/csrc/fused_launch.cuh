@@ -55,6 +55,9 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.mean_out = L.mean_out;
   p.rstd_out = L.rstd_out;
   p.pre_rstd_out = L.pre_rstd_out;
+  p.colsum = L.colsum;
+  p.bias = L.bias;
+  p.R = static_cast<const __nv_bfloat16*>(L.R);
   p.status = dev.status;
   p.wait_limit_ns = wait_limit_ns();
 

@@ -54,6 +54,9 @@ struct FusedLaunch {
   float* mean_out;
   float* rstd_out;
   float* pre_rstd_out;
+  const float* colsum;  // pre-norm with folded affine: column sums of the folded B (LayerNorm)
+  const float* bias;    // pre-norm with folded affine: beta @ B, or NULL
+  const void* R;        // residual [M, N] added before the post-norm, or NULL
   cudaStream_t stream;
 };
 
@@ -61,8 +64,16 @@ struct FusedLaunch {
 fnorm_status_t launch_fused_plain(const FusedLaunch& L);          // GEMM, Lazy Pre-Norm
 fnorm_status_t launch_fused_post_single(const FusedLaunch& L);    // post-norm, one CTA per row block
 fnorm_status_t launch_fused_post_cluster(const FusedLaunch& L);   // post-norm over a cluster
+fnorm_status_t launch_fused_prenorm_affine(const FusedLaunch& L); // lazy pre-norm, affine folded into B
+fnorm_status_t launch_fused_post_residual(const FusedLaunch& L);  // residual + post-norm, one CTA per row block
+fnorm_status_t launch_fused_post_residual_cluster(const FusedLaunch& L);  // residual + post-norm over a cluster
 
-fnorm_status_t launch_rownorm(const void* X, void* Y, int M, int N, bool layernorm, const void* gamma,
+// B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
+fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,
+                                          void* B_folded, float* colsum, float* bias, cudaStream_t stream);
+
+// R (optional, [M, N]) is added to X before the norm
+fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int N, bool layernorm, const void* gamma,
                               const void* beta, float eps, float* mean_out, float* rstd_out,
                               cudaStream_t stream);
 

@@ -1,6 +1,7 @@
-// rownorm.cu — standalone row RMSNorm / LayerNorm (the unfused comparison
-// kernels).  [ATB] sections 1.1 (LayerNorm) and 1.2 (RMSNorm); [FNF-ru] FAQ:
-// a standalone norm reads and writes the whole tensor and stays memory-bound.
+// rownorm.cu — standalone row RMSNorm / LayerNorm, optionally of X + R (the
+// unfused comparison kernels).  [ATB] sections 1.1 (LayerNorm) and 1.2
+// (RMSNorm); [FNF-ru] FAQ: a standalone norm reads and writes the whole tensor
+// and stays memory-bound; [FNF-ru] "FlashNormAttention" for the residual add.
 //
 // Memory-bound single pass from registers: a group of `tpr` threads (a power
 // of two) owns one row; each thread loads up to VPT 16-byte vectors of it,
@@ -42,8 +43,9 @@ __device__ __forceinline__ float group_sum(float v, int tpr, float* red) {
   return s;
 }
 
-template <bool LN>
+template <bool LN, bool RESID>
 __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __restrict__ X,
+                                                       const __nv_bfloat16* __restrict__ R,
                                                        __nv_bfloat16* __restrict__ Y, int M, int N, int tpr,
                                                        const __nv_bfloat16* __restrict__ gamma,
                                                        const __nv_bfloat16* __restrict__ beta, float eps,
@@ -58,6 +60,7 @@ __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __re
   const int nvec = N >> 3;
   const bool row_ok = row < M;
   const __nv_bfloat16* xr = X + static_cast<size_t>(row_ok ? row : 0) * N;
+  const __nv_bfloat16* rr = RESID ? R + static_cast<size_t>(row_ok ? row : 0) * N : nullptr;
 
   float x[kVPT * 8];
 #pragma unroll
@@ -69,6 +72,14 @@ __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __re
     x[i * 8 + 2] = bf16_lo(v.y); x[i * 8 + 3] = bf16_hi(v.y);
     x[i * 8 + 4] = bf16_lo(v.z); x[i * 8 + 5] = bf16_hi(v.z);
     x[i * 8 + 6] = bf16_lo(v.w); x[i * 8 + 7] = bf16_hi(v.w);
+    if (RESID) {  // residual: the row normalised is x + r, summed in fp32
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (row_ok && vi < nvec) u = ld_stream(rr + vi * 8);
+      x[i * 8 + 0] += bf16_lo(u.x); x[i * 8 + 1] += bf16_hi(u.x);
+      x[i * 8 + 2] += bf16_lo(u.y); x[i * 8 + 3] += bf16_hi(u.y);
+      x[i * 8 + 4] += bf16_lo(u.z); x[i * 8 + 5] += bf16_hi(u.z);
+      x[i * 8 + 6] += bf16_lo(u.w); x[i * 8 + 7] += bf16_hi(u.w);
+    }
   }
   const float inv_n = 1.0f / static_cast<float>(N);
   float mean = 0.0f, rstd;
@@ -134,7 +145,7 @@ __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __re
 
 }  // namespace
 
-fnorm_status_t launch_rownorm(const void* X, void* Y, int M, int N, bool layernorm, const void* gamma,
+fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int N, bool layernorm, const void* gamma,
                               const void* beta, float eps, float* mean_out, float* rstd_out,
                               cudaStream_t stream) {
   DeviceInfo dev;
@@ -164,12 +175,13 @@ fnorm_status_t launch_rownorm(const void* X, void* Y, int M, int N, bool layerno
     cfg.numAttrs = 1;
   }
   const auto* x = static_cast<const __nv_bfloat16*>(X);
+  const auto* r = static_cast<const __nv_bfloat16*>(R);
   auto* y = static_cast<__nv_bfloat16*>(Y);
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
-  const cudaError_t e =
-      layernorm ? cudaLaunchKernelEx(&cfg, rownorm_kernel<true>, x, y, M, N, tpr, g, b, eps, mean_out, rstd_out)
-                : cudaLaunchKernelEx(&cfg, rownorm_kernel<false>, x, y, M, N, tpr, g, b, eps, mean_out, rstd_out);
+  auto kern = layernorm ? (r != nullptr ? rownorm_kernel<true, true> : rownorm_kernel<true, false>)
+                        : (r != nullptr ? rownorm_kernel<false, true> : rownorm_kernel<false, false>);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, r, y, M, N, tpr, g, b, eps, mean_out, rstd_out);
   if (e != cudaSuccess) return cuda_fail(e, "row norm launch");
   return FNORM_OK;
 }

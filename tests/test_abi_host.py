@@ -31,7 +31,8 @@ def _header_functions():
 def test_header_declares_the_boundary():
     names = _header_functions()
     for required in ("fnorm_gemm", "fnorm_lazy_prenorm_gemm", "fnorm_gemm_postnorm", "fnorm_rmsnorm",
-                     "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error"):
+                     "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
+                     "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm"):
         assert required in names
 
 
@@ -82,7 +83,58 @@ def test_postnorm_argument_rules(L):
              None) == 1
 
 
+def test_add_postnorm_argument_rules(L):
+    f = L.fnorm_gemm_add_postnorm
+    ok = (FAKE, FAKE, ctypes.c_void_p(0x200000), ctypes.c_void_p(0x400000))  # A, B, R, C: R and C disjoint
+    # unknown norm, mean_out with RMSNorm, bad eps
+    assert f(*ok, 128, 64, 64, 7, None, None, 1e-5, None, None, None) == 1
+    assert f(*ok, 128, 64, 64, 0, None, None, 1e-5, FAKE, None, None) == 1
+    assert f(*ok, 128, 64, 64, 0, None, None, 0.0, None, None, None) == 1
+    # R missing, misaligned, or overlapping C
+    assert f(FAKE, FAKE, None, ok[3], 128, 64, 64, 0, None, None, 1e-5, None, None, None) == 1
+    assert b"R" in L.fnorm_last_error()
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x200008), ok[3], 128, 64, 64, 0, None, None, 1e-5, None, None, None) == 1
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x400000 + 128 * 64), ok[3], 128, 64, 64, 0, None, None, 1e-5, None, None,
+             None) == 1
+    assert b"overlap" in L.fnorm_last_error()
+
+
+def test_fold_argument_rules(L):
+    f = L.fnorm_fold_prenorm_affine
+    out = ctypes.c_void_p(0x400000)
+    # sizes: K and N multiples of 8
+    assert f(FAKE, 60, 64, None, None, out, None, None, None) == 1
+    assert f(FAKE, 64, 12, None, None, out, None, None, None) == 1
+    # bias exactly when beta
+    assert f(FAKE, 64, 64, None, FAKE, out, None, None, None) == 1
+    assert f(FAKE, 64, 64, None, None, out, None, FAKE, None) == 1
+    # colsum / bias must be 16-byte aligned
+    assert f(FAKE, 64, 64, None, None, out, ctypes.c_void_p(0x10004), None, None) == 1
+    # partial overlap of B_folded with B (in place, B_folded == B, is allowed)
+    assert f(FAKE, 64, 64, None, None, ctypes.c_void_p(0x10000 + 64), None, None, None) == 1
+    assert b"overlap" in L.fnorm_last_error()
+
+
+def test_prenorm_gemm_argument_rules(L):
+    f = L.fnorm_prenorm_gemm
+    # LayerNorm needs the column sums
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, None, None, 1e-5, None, None, None) == 1
+    assert b"colsum" in L.fnorm_last_error()
+    # mean_out only for LayerNorm; unknown norm; bad eps
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 0, None, None, 1e-5, FAKE, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 3, FAKE, None, 1e-5, None, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, FAKE, None, -1.0, None, None, None) == 1
+    # misaligned colsum / bias
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 1, ctypes.c_void_p(0x10004), None, 1e-5, None, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 128, 64, 64, 0, None, ctypes.c_void_p(0x10008), 1e-5, None, None, None) == 1
+    # M == 0 is an empty call that touches nothing
+    assert f(None, None, None, 0, 64, 64, 1, FAKE, None, 1e-5, None, None, None) == 0
+
+
 def test_norm_rejects_bad_sizes(L):
+    assert L.fnorm_add_rownorm(FAKE, None, FAKE, 16, 64, 0, None, None, 1e-5, None, None, None) == 1
+    assert L.fnorm_add_rownorm(FAKE, FAKE, FAKE, 16, 64, 0, None, None, 1e-5, FAKE, None, None) == 1
+    assert L.fnorm_add_rownorm(FAKE, FAKE, FAKE, 16, 64, 5, None, None, 1e-5, None, None, None) == 1
     assert L.fnorm_rmsnorm(FAKE, FAKE, 16, 12, None, 1e-6, None, None) == 1
     assert L.fnorm_layernorm(FAKE, FAKE, 16, 65536, None, None, 1e-5, None, None, None) == 1
     assert L.fnorm_layernorm(FAKE, FAKE, 16, 64, ctypes.c_void_p(0x10002), None, 1e-5, None, None, None) == 1

@@ -3,8 +3,8 @@
 The fused kernel runs over the whole workload; the fp64 oracle recomputes a
 sample of rows one by one (first and last rows, tile boundaries, seeded random
 rows and, for the outlier workload, outlier rows), all N columns each, since
-rows of the path are independent.  The Lazy Pre-Norm rstd is compared on every
-row (it depends on A alone).
+rows of the path are independent.  The pre-norm statistics (rstd, and the
+mean of a pre-LayerNorm) are compared on every row (they depend on A alone).
 """
 import numpy as np
 import pytest
@@ -44,6 +44,31 @@ def test_full_size(name):
         assert_out_close(C[torch.from_numpy(rows).to(DEV)], Cr, f"{name} sampled rows")
         _, r_all = oracle.rmsnorm(A64, None, None, w.eps)
         assert_rstd_close(rstd, r_all, f"{name} rstd (all rows)")
+    elif w.kind == "prenorm_affine":
+        g = None if d["gamma"] is None else d["gamma"].to(DEV)
+        be = None if d["beta"] is None else d["beta"].to(DEV)
+        Bf, colsum, bias = fn.fold_prenorm_affine(B, g, be)
+        C, st = fn.prenorm_gemm(A, Bf, w.norm, colsum, bias, w.eps, return_stats=True)
+        Cr, _, _ = oracle.prenorm_affine_gemm(A64[rows], to_f64(d["B"]), w.norm, to_f64(d["gamma"]),
+                                              to_f64(d["beta"]), w.eps)
+        assert_out_close(C[torch.from_numpy(rows).to(DEV)], Cr, f"{name} sampled rows")
+        if w.norm == "layernorm":
+            _, m_all, r_all = oracle.layernorm(A64, None, None, w.eps)
+            assert_mean_close(st["mean"], m_all, r_all, f"{name} mean (all rows)")
+        else:
+            _, r_all = oracle.rmsnorm(A64, None, None, w.eps)
+        assert_rstd_close(st["rstd"], r_all, f"{name} rstd (all rows)")
+    elif w.residual:
+        g = None if d["gamma"] is None else d["gamma"].to(DEV)
+        b = None if d["beta"] is None else d["beta"].to(DEV)
+        C, st = fn.gemm_add_postnorm(A, B, d["R"].to(DEV), w.norm, g, b, w.eps, return_stats=True)
+        ref = oracle.gemm_add_postnorm(A64[rows], to_f64(d["B"]), to_f64(d["R"])[rows], w.norm,
+                                       to_f64(d["gamma"]), to_f64(d["beta"]), w.eps)
+        idx = torch.from_numpy(rows).to(DEV)
+        assert_out_close(C[idx], ref["C"], f"{name} sampled rows")
+        assert_rstd_close(st["rstd"][idx], ref["rstd"], f"{name} rstd")
+        if w.norm == "layernorm":
+            assert_mean_close(st["mean"][idx], ref["mean"], ref["rstd"], f"{name} mean")
     else:
         g = None if d["gamma"] is None else d["gamma"].to(DEV)
         b = None if d["beta"] is None else d["beta"].to(DEV)

@@ -21,9 +21,25 @@ Workloads (all bf16, row-major; "N(0, s)" means standard deviation s):
   eps 1e-5) in one kernel: A[65536,256] N(0,1) with 1% of rows (655 rows,
   drawn without replacement) scaled by 100; B[256,256] N(0,1/16).
 
+Forms beyond the five configurations (same distributions where they apply):
+
+* ``res_ln_n128``  residual-add post-LayerNorm: cfg2_n128 plus R[16384,128]
+  N(0,1).
+* ``res_rms_n1024``  residual-add post-RMSNorm (gamma only) over a cluster:
+  cfg4_n1024_rms plus R[16384,1024] N(0,1).
+* ``preln_affine``  pre-LayerNorm with affine feeding a GEMM:
+  A[8192,4096] = (N(0,1) + o_m) * s_m with a per-row offset o_m ~ N(0,1) (a
+  row mean of the order of the row's spread) and the log-uniform row scale
+  s_m; gamma[4096] 1+N(0,0.1), beta[4096] N(0,0.1); B[4096,4096] N(0,1/64);
+  eps 1e-5.
+* ``prerms_gamma``  Lazy Pre-RMSNorm with gamma folded into B: cfg3's A and B,
+  gamma[4096] 1+N(0,0.1), no beta, eps 1e-6.
+
 Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
-float32 in the order A, row scale, outlier rows, B, gamma, beta, then rounded
-once to bf16 (round to nearest even) by ``torch.Tensor.to(torch.bfloat16)``.
+float32 in the order A, row scale, outlier rows, row offset, B, gamma, beta, R
+(each only where the workload has it), then rounded once to bf16 (round to
+nearest even) by ``torch.Tensor.to(torch.bfloat16)``.  gamma and beta have
+length N for a post-norm and K for a pre-norm with affine.
 """
 from __future__ import annotations
 
@@ -38,19 +54,21 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "prenorm" | "postnorm" | "gemm"
+    kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "gemm"
     M: int
     K: int
     N: int
     b_std: float
     eps: float = 1e-5
-    norm: Optional[str] = None        # "layernorm" | "rmsnorm" (postnorm only)
+    norm: Optional[str] = None        # "layernorm" | "rmsnorm" (postnorm, prenorm_affine)
     gamma: bool = False
     beta: bool = False
     pre_rmsnorm: bool = False         # cfg5: pre-RMSNorm scale before the post-norm
     pre_eps: float = 1e-6
     a_row_scale: bool = False         # log-uniform [0.1, 10] per-row scale on A
     a_outlier_frac: float = 0.0       # fraction of rows of A multiplied by 100
+    a_row_offset: float = 0.0         # std of a per-row offset added to A before the row scale
+    residual: bool = False            # residual R[M,N] N(0,1) added before the post-norm
     description: str = ""
 
     def scaled(self, **kw) -> "Workload":
@@ -62,16 +80,33 @@ class Workload:
         return 2.0 * self.M * self.N * self.K
 
     @property
+    def affine_len(self) -> int:
+        """Length of gamma/beta: K for a pre-norm with affine, else N."""
+        return self.K if self.kind == "prenorm_affine" else self.N
+
+    @property
     def algorithmic_bytes(self) -> float:
-        """A + B + C in bf16, plus gamma/beta and the fp32 row statistics."""
+        """Bytes one fused launch must move: A + B + C in bf16 (+ R), gamma/beta
+        (post-norm) or the folded weight's fp32 column sums and bias row
+        (pre-norm with affine), and the fp32 row statistics."""
         b = 2.0 * (self.M * self.K + self.K * self.N + self.M * self.N)
-        if self.gamma:
-            b += 2.0 * self.N
-        if self.beta:
-            b += 2.0 * self.N
+        if self.residual:
+            b += 2.0 * self.M * self.N
+        if self.kind == "prenorm_affine":
+            if self.norm == "layernorm":
+                b += 4.0 * self.N
+            if self.beta:
+                b += 4.0 * self.N
+        else:
+            if self.gamma:
+                b += 2.0 * self.N
+            if self.beta:
+                b += 2.0 * self.N
         nstats = 0
         if self.kind == "prenorm":
             nstats = 1
+        elif self.kind == "prenorm_affine":
+            nstats = 2 if self.norm == "layernorm" else 1
         elif self.kind == "postnorm":
             nstats = 2 if self.norm == "layernorm" else 1
             if self.pre_rmsnorm:
@@ -109,6 +144,19 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
              a_outlier_frac=0.01,
              description="pre-RMSNorm + GEMM + post-LayerNorm(affine) in one kernel, "
                          "A[65536,256] @ B[256,256]"),
+    Workload("res_ln_n128", "postnorm", M=16384, K=1024, N=128, b_std=1.0 / 32.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True, residual=True,
+             description="GEMM + residual + post-LayerNorm(affine), A[16384,1024] @ B[1024,128] + R"),
+    Workload("res_rms_n1024", "postnorm", M=16384, K=2048, N=1024, b_std=1.0 / 45.0, eps=1e-5,
+             norm="rmsnorm", gamma=True, beta=False, residual=True,
+             description="GEMM + residual + post-RMSNorm(gamma) over a CTA cluster, "
+                         "A[16384,2048] @ B[2048,1024] + R"),
+    Workload("preln_affine", "prenorm_affine", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True, a_row_scale=True, a_row_offset=1.0,
+             description="pre-LayerNorm(affine, folded into B) + GEMM, A[8192,4096] @ B[4096,4096]"),
+    Workload("prerms_gamma", "prenorm_affine", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-6,
+             norm="rmsnorm", gamma=True, beta=False, a_row_scale=True,
+             description="Lazy Pre-RMSNorm with gamma folded into B, A[8192,4096] @ B[4096,4096]"),
 ]}
 
 
@@ -132,28 +180,39 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     if w.a_row_scale:
         lo, hi = math.log(0.1), math.log(10.0)
         row_scale = np.exp(rng.uniform(lo, hi, size=w.M)).astype(np.float32)
-        a *= row_scale[:, None]
     outl = outlier_rows(w.M, w.a_outlier_frac, rng)
+    row_offset = None
+    if w.a_row_offset > 0.0:
+        row_offset = rng.standard_normal(w.M, dtype=np.float32) * np.float32(w.a_row_offset)
+        a += row_offset[:, None]
+    if row_scale is not None:
+        a *= row_scale[:, None]
     if outl.size:
         a[outl] *= np.float32(100.0)
     b = rng.standard_normal((w.K, w.N), dtype=np.float32) * np.float32(w.b_std)
-    gamma = beta = None
+    gamma = beta = r = None
+    n_aff = w.affine_len
     if w.gamma:
-        gamma = np.float32(1.0) + np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32)
+        gamma = np.float32(1.0) + np.float32(0.1) * rng.standard_normal(n_aff, dtype=np.float32)
     if w.beta:
-        beta = np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32)
+        beta = np.float32(0.1) * rng.standard_normal(n_aff, dtype=np.float32)
+    if w.residual:
+        r = rng.standard_normal((w.M, w.N), dtype=np.float32)
 
     def bf16(x):
         return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
 
-    return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta),
-            "row_scale": row_scale, "outliers": outl}
+    return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta), "R": bf16(r),
+            "row_scale": row_scale, "outliers": outl, "row_offset": row_offset}
 
 
 def make_rows_inputs(w: Workload, rows: np.ndarray, seed: int = 0) -> dict:
     """The full-size inputs restricted to ``rows`` of A (for sampled checks)."""
     d = make_inputs(w, seed)
-    d["A"] = d["A"][torch.from_numpy(np.asarray(rows, dtype=np.int64))].contiguous()
+    idx = torch.from_numpy(np.asarray(rows, dtype=np.int64))
+    d["A"] = d["A"][idx].contiguous()
+    if d["R"] is not None:
+        d["R"] = d["R"][idx].contiguous()
     return d
 
 
