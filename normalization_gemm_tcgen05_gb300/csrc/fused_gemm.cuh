@@ -90,7 +90,10 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
   return p;
 }
 
-template <int STAGES_, int GB, int CLMAX>
+// Shared-memory control block.  Arrays a mode does not use shrink to one
+// element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
+// spill-layout handoff), so each kernel carries only what it needs.
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -108,10 +111,10 @@ struct Aux {
   int abort_flag;
   int nstat_m0[2];
   int nstat_c0[2];
-  float ss[2][128];
-  float ss1[2][128];  // pre-LayerNorm: shifted sums of the A rows and the shift
-  float ssk[2][128];
-  float2 nstat[2][128];
+  float ss[2][SSN];
+  float ss1[2][SS1N];  // pre-LayerNorm: shifted sums of the A rows and the shift
+  float ssk[2][SS1N];
+  float2 nstat[2][NSN];
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
   alignas(16) float gam[GB];
   alignas(16) float bet[GB];
@@ -155,7 +158,8 @@ struct KCfg {
   static constexpr int KB_MAX = BRES ? (int)(131072u / B_BYTES) : 0;
   static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES);
-  static constexpr uint32_t AUX_BYTES = (sizeof(Aux<kMaxStages, GB, CLMAX>) + 15) / 16 * 16;
+  static constexpr int SSN = PRE ? 128 : 1, SS1N = PRE_LN ? 128 : 1, NSN = SPILL ? 128 : 1;
+  static constexpr uint32_t AUX_BYTES = (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
   // that buys a pipeline stage below 4
   static constexpr int stages_with(int bufs) {
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);

@@ -11,6 +11,11 @@
 
 namespace fnorm {
 
+// Pipeline depth the compute-bound cluster kernels are tuned for: a 4-stage
+// ring of 48 KB stages (one staging box per epilogue warp makes room for it).
+static_assert(KCfg<256, MODE_POST | MODE_LN | MODE_CLUSTER, 4>::STAGES >= 4, "resident cluster ring");
+static_assert(KCfg<256, MODE_POST | MODE_LN | MODE_CLUSTER | MODE_SPILL, 4>::STAGES >= 4, "spill ring");
+
 namespace {
 template <int BN, int EXTRA, int CLMAX>
 fnorm_status_t by_mode(const FusedLaunch& L) {

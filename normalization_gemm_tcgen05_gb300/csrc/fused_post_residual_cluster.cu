@@ -5,6 +5,9 @@
 
 namespace fnorm {
 
+static_assert(KCfg<256, MODE_POST | MODE_CLUSTER | MODE_RES, 4>::STAGES >= 4, "resident cluster ring");
+static_assert(KCfg<256, MODE_POST | MODE_LN | MODE_CLUSTER | MODE_SPILL | MODE_RES, 4>::STAGES >= 4, "spill ring");
+
 namespace {
 template <int BN, int EXTRA, int CLMAX>
 fnorm_status_t by_mode(const FusedLaunch& L) {

@@ -5,6 +5,10 @@
 
 namespace fnorm {
 
+static_assert(KCfg<128, MODE_POST | MODE_LN>::STAGES >= 5 && KCfg<64, MODE_POST | MODE_LN>::STAGES >= 7,
+              "post-norm, narrow tiles");
+static_assert(KCfg<256, MODE_POST | MODE_LN | MODE_PRE | MODE_BRES>::STAGES >= 4, "pre + post-norm, resident B");
+
 namespace {
 template <int BN, int X>
 fnorm_status_t by_mode_x(const FusedLaunch& L) {

@@ -6,6 +6,8 @@
 
 namespace fnorm {
 
+static_assert(KCfg<256, MODE_PRE | MODE_PRE_LN | MODE_AFF>::STAGES >= 4, "pre-LayerNorm, 256-column tiles");
+
 namespace {
 template <int BN, int X>
 fnorm_status_t by_mode_x(const FusedLaunch& L) {
