@@ -93,7 +93,7 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // Shared-memory control block.  Arrays a mode does not use shrink to one
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff), so each kernel carries only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -111,8 +111,8 @@ struct Aux {
   int abort_flag;
   int nstat_m0[2];
   int nstat_c0[2];
-  float ss[2][SSN];
-  float ss1[2][SS1N];  // pre-LayerNorm: shifted sums of the A rows and the shift
+  float ss[2][NPART][SSN];    // pre-norm row sums, one slot per norm-warp part
+  float ss1[2][NPART][SS1N];  // pre-LayerNorm: shifted sums of the A rows and the shift
   float ssk[2][SS1N];
   float2 nstat[2][NSN];
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
@@ -159,7 +159,13 @@ struct KCfg {
   static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES);
   static constexpr int SSN = PRE ? 128 : 1, SS1N = PRE_LN ? 128 : 1, NSN = SPILL ? 128 : 1;
-  static constexpr uint32_t AUX_BYTES = (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN>) + 15) / 16 * 16;
+  // norm warps: 4 (one row per thread), or 8 for the pre-LayerNorm, whose
+  // shifted sums cost more per element: two parts take half of each row's
+  // 16-byte chunks each
+  static constexpr int NPART = PRE_LN ? 2 : 1;
+  static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
+  static constexpr uint32_t AUX_BYTES =
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
   // that buys a pipeline stage below 4
   static constexpr int stages_with(int bufs) {
@@ -169,7 +175,7 @@ struct KCfg {
   static constexpr uint32_t STG_BYTES = kEpiWarps * STG_BUFS * kBoxBytes;
   static constexpr int STAGES = stages_with(STG_BUFS) < kMaxStages ? stages_with(STG_BUFS) : kMaxStages;
   static constexpr uint32_t SMEM_BYTES = 1024 + BRES_BYTES + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;
-  static constexpr int NUM_THREADS = 32 * (2 + kEpiWarps + (AUXW ? 4 : 0));
+  static constexpr int NUM_THREADS = 32 * (2 + kEpiWarps + AUX_WARPS);
   static constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, true);
 
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -420,13 +426,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&aux->full[s]), 1);
-      mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 : 0));
+      mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 * Cfg::NPART : 0));
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&aux->acc_full[b]), 1);
       mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps);
       // handoffs between warp groups: one arrival per warp, after __syncwarp
-      mbar_init(smem_u32(&aux->ss_full[b]), 4);
+      mbar_init(smem_u32(&aux->ss_full[b]), 4 * Cfg::NPART);
       mbar_init(smem_u32(&aux->ss_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->xbar[b]), 1);
       mbar_init(smem_u32(&aux->nstat_full[b]), kEpiWarps);
@@ -718,11 +724,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const float ss = aux->ss[sb][row];
+          const float ss = Cfg::NPART == 2 ? aux->ss[sb][0][row] + aux->ss[sb][Cfg::NPART - 1][row]
+                                           : aux->ss[sb][0][row];
           const float kf = static_cast<float>(K);
           if (PRE_LN) {
             // LayerNorm of the A row from its shifted sums (shift: ssk)
-            const float s1 = aux->ss1[sb][row];
+            const float s1 = Cfg::NPART == 2 ? aux->ss1[sb][0][row] + aux->ss1[sb][Cfg::NPART - 1][row]
+                                             : aux->ss1[sb][0][row];
             pre_mean = aux->ssk[sb][row] + s1 / kf;
             const float var = fmaxf(ss / kf - (s1 / kf) * (s1 / kf), 0.0f);
             pre = rsqrtf(var + p.pre_eps);
@@ -962,9 +970,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     }
   } else if (PRE) {
     // ======================= norm warps (Lazy Pre-Norm) =======================
-    const int row = (warp - (2 + kEpiWarps)) * 32 + lane;
+    // 4 x NPART warps: warp nw takes row (nw % 4) * 32 + lane and part nw / 4
+    // of each staged row's 16-byte chunks
+    const int nw = warp - (2 + kEpiWarps);
+    const int row = (nw & 3) * 32 + lane;
+    const int part = nw >> 2;
     constexpr int ROW_BYTES = BK * 2;
     constexpr int CHUNKS = ROW_BYTES / 16;
+    constexpr int CPP = CHUNKS / Cfg::NPART;  // chunks per part
     // swizzle phase of this row: chunk index XOR (row address bits 7..9)
     const int swz = ((row * ROW_BYTES) >> 7) & (CHUNKS - 1);
     uint32_t stage = 0, phase = 0;
@@ -972,42 +985,42 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
       for (int s = 0; s < S && ok; ++s, ++it) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        float lsum[4] = {0.f, 0.f, 0.f, 0.f};  // pre-LayerNorm: sums of (a - shift)
+        // packed pairs of partial sums: acc = sum of squares (of a - shift for
+        // the pre-LayerNorm), lsum = sum of (a - shift)
+        uint64_t acc[2] = {0ull, 0ull}, lsum[2] = {0ull, 0ull};
         float shift = 0.0f;
+        uint64_t sh2 = 0ull;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_warp(wc, smem_u32(&aux->full[stage]), phase, kSiteNorm)) {
             ok = false;
             break;
           }
           const uint8_t* arow = smem + stage * STAGE_BYTES + row * ROW_BYTES;
+          if (PRE_LN && kb == 0) {
+            // the shift is the row's first element, a[row][0] (logical chunk 0),
+            // the same for both parts
+            shift = bf16_lo(*reinterpret_cast<const uint32_t*>(arow + (swz << 4)));
+            sh2 = f2(shift, shift);
+          }
 #pragma unroll
-          for (int ch = 0; ch < CHUNKS; ++ch) {
-            // visit the row's physical chunks in a bank-conflict-free order;
-            // the sum does not depend on the order
+          for (int c = 0; c < CPP; ++c) {
+            // visit the part's chunks in a bank-conflict-free order (the
+            // lanes' rows have distinct swizzle phases); sums do not depend
+            // on the order
+            const int ch = part * CPP + c;
             const uint4 v = *reinterpret_cast<const uint4*>(arow + ((ch ^ swz) << 4));
-            if (PRE_LN) {
-              // the first value this thread reads (a[row][0]) is the shift
-              if (kb == 0 && ch == 0) shift = bf16_lo(v.x);
-              const float xs[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                                   bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < 4; ++e) {
+              const uint64_t x = f2(bf16_lo(wv[e]), bf16_hi(wv[e]));
+              if (PRE_LN) {
                 // zero-filled K tail: a = 0 contributes (0 - shift), removed below
-                const float d = xs[e] - shift;
-                lsum[e & 3] += d;
-                acc[e & 3] = fmaf(d, d, acc[e & 3]);
+                const uint64_t d = f2_sub(x, sh2);
+                lsum[e & 1] = f2_add(lsum[e & 1], d);
+                acc[e & 1] = f2_fma(d, d, acc[e & 1]);
+              } else {
+                acc[e & 1] = f2_fma(x, x, acc[e & 1]);
               }
-            } else {
-              float x;
-              x = bf16_lo(v.x); acc[0] = fmaf(x, x, acc[0]);
-              x = bf16_hi(v.x); acc[1] = fmaf(x, x, acc[1]);
-              x = bf16_lo(v.y); acc[2] = fmaf(x, x, acc[2]);
-              x = bf16_hi(v.y); acc[3] = fmaf(x, x, acc[3]);
-              x = bf16_lo(v.z); acc[0] = fmaf(x, x, acc[0]);
-              x = bf16_hi(v.z); acc[1] = fmaf(x, x, acc[1]);
-              x = bf16_lo(v.w); acc[2] = fmaf(x, x, acc[2]);
-              x = bf16_hi(v.w); acc[3] = fmaf(x, x, acc[3]);
             }
           }
           __syncwarp();
@@ -1024,17 +1037,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           ok = false;
           break;
         }
-        float s2t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        float s2t = (f2_lo(acc[0]) + f2_hi(acc[0])) + (f2_lo(acc[1]) + f2_hi(acc[1]));
         if (PRE_LN) {
-          float s1t = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-          // the zero-filled tail of the last k-block added (0 - shift) per element
-          const float pad = static_cast<float>(num_kb * BK - K);
-          s1t += pad * shift;
-          s2t -= pad * shift * shift;
-          aux->ss1[sb][row] = s1t;
-          aux->ssk[sb][row] = shift;
+          float s1t = (f2_lo(lsum[0]) + f2_hi(lsum[0])) + (f2_lo(lsum[1]) + f2_hi(lsum[1]));
+          if (part == 0) {
+            // the zero-filled tail of the last k-block added (0 - shift) per
+            // element to one part or the other; both share the shift, so part
+            // 0 removes all of it from the total
+            const float pad = static_cast<float>(num_kb * BK - K);
+            s1t += pad * shift;
+            s2t -= pad * shift * shift;
+            aux->ssk[sb][row] = shift;
+          }
+          aux->ss1[sb][part][row] = s1t;
         }
-        aux->ss[sb][row] = s2t;
+        aux->ss[sb][part][row] = s2t;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&aux->ss_full[sb]));
       }
