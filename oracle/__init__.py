@@ -31,4 +31,6 @@ from .fnorm_oracle import (  # noqa: F401
     gemm_postnorm,
     prenorm_affine_gemm,
     gemm_add_postnorm,
+    lazy_prenorm_gemm_backward,
+    gemm_postnorm_backward,
 )

@@ -23,7 +23,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm", "gemm_postnorm", "prenorm_affine_gemm",
-           "gemm_add_postnorm"]
+           "gemm_add_postnorm", "lazy_prenorm_gemm_backward", "gemm_postnorm_backward"]
 
 
 def _f64(x) -> np.ndarray:
@@ -163,3 +163,71 @@ def gemm_add_postnorm(A, B, R, norm: str, gamma=None, beta=None, eps: float = 1e
     else:
         raise ValueError(f"unknown norm {norm!r}")
     return {"C": C, "H": H, "mean": mean, "rstd": rstd}
+
+
+def lazy_prenorm_gemm_backward(A, B, dC, eps: float = 1e-6):
+    """Gradients of C = rmsnorm(A) @ B (RMSNorm without affine) w.r.t. A and B.
+
+    [FNF-ru] "Lazy Pre-Norm" limits (the forward never materialises the
+    normalised A, so its backward has to rebuild it) and [TFN] (the backward's
+    norm work rides on a GEMM too).  The oracle materialises the forward and
+    applies the chain rule step by step:
+
+        A_hat  = A * r,  r = 1 / sqrt(mean_k(A^2) + eps)   (per row)
+        dA_hat = dC @ B^T
+        dB     = A_hat^T @ dC
+        dA     = r * dA_hat - r^3 * A * (sum_k dA_hat * A) / K   (RMSNorm backward)
+
+    Returns (dA, dB, r).
+    """
+    A = _f64(A)
+    B = _f64(B)
+    dC = _f64(dC)
+    K = A.shape[1]
+    A_hat, r = rmsnorm(A, None, None, eps)
+    dA_hat = gemm(dC, B.T)
+    dB = gemm(A_hat.T, dC)
+    dot = np.sum(dA_hat * A, axis=1)
+    dA = r[:, None] * dA_hat - (r ** 3 * dot / K)[:, None] * A
+    return dA, dB, r
+
+
+def gemm_postnorm_backward(A, B, dC, norm: str, gamma=None, beta=None, eps: float = 1e-5) -> dict:
+    """Gradients of C = norm(A @ B) * gamma + beta w.r.t. A, B, gamma, beta.
+
+    [TFN] ("fusion regrouping": the post-norm's backward is fused with a GEMM
+    other than its forward's); the norm derivatives are those of [ATB] 1.1 /
+    1.2's definitions.  The oracle materialises H = A @ B and its normalised
+    rows h_hat, then:
+
+        dgamma = sum_m dC * h_hat,   dbeta = sum_m dC,   dh = dC * gamma
+        LayerNorm: dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+        RMSNorm:   dH = rstd * (dh - h_hat * mean_n(dh * h_hat))
+        dA = dH @ B^T,   dB = A^T @ dH
+
+    Returns a dict with "dA", "dB", "dH", "dgamma", "dbeta", "mean" (LayerNorm,
+    else None) and "rstd".
+    """
+    A = _f64(A)
+    B = _f64(B)
+    dC = _f64(dC)
+    H = gemm(A, B)
+    N = H.shape[1]
+    g = np.ones(N) if gamma is None else np.asarray(gamma, dtype=np.float64)
+    if norm == "layernorm":
+        h_hat, mean, rstd = layernorm(H, None, None, eps)
+    elif norm == "rmsnorm":
+        h_hat, rstd = rmsnorm(H, None, None, eps)
+        mean = None
+    else:
+        raise ValueError(f"unknown norm {norm!r}")
+    dgamma = np.sum(dC * h_hat, axis=0)
+    dbeta = np.sum(dC, axis=0)
+    dh = dC * g[None, :]
+    proj = np.sum(dh * h_hat, axis=1) / N
+    if norm == "layernorm":
+        dH = rstd[:, None] * (dh - (np.sum(dh, axis=1) / N)[:, None] - h_hat * proj[:, None])
+    else:
+        dH = rstd[:, None] * (dh - h_hat * proj[:, None])
+    return {"dA": gemm(dH, B.T), "dB": gemm(A.T, dH), "dH": dH, "dgamma": dgamma, "dbeta": dbeta,
+            "mean": mean, "rstd": rstd}

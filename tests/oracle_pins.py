@@ -364,6 +364,91 @@ def check_add_postnorm_cancel(o):
     _close(d["rstd"], [5.0, 5.0, 5.0], what="cancelled residual rstd = 1/sqrt(eps)")
 
 
+# --------------------------------------------------------------------------
+# backward of the fused forms
+# --------------------------------------------------------------------------
+def check_prenorm_backward_autograd(o):
+    rng = _rng(16)
+    A = rng.standard_normal((6, 24)) * rng.uniform(0.2, 3.0, (6, 1))
+    B = rng.standard_normal((24, 10)) / 5
+    dC = rng.standard_normal((6, 10))
+    dA, dB, r = o.lazy_prenorm_gemm_backward(A, B, dC, 1e-3)
+    At = _t(A).requires_grad_(True)
+    Bt = _t(B).requires_grad_(True)
+    C = F.rms_norm(At, (24,), None, 1e-3) @ Bt
+    C.backward(_t(dC))
+    _close(dA, At.grad.numpy(), 1e-11, 1e-12, "prenorm dA vs autograd")
+    _close(dB, Bt.grad.numpy(), 1e-11, 1e-12, "prenorm dB vs autograd")
+
+
+def check_prenorm_backward_finite_diff(o):
+    # central differences of L = sum(dC * C(A, B)) through the oracle's forward
+    rng = _rng(17)
+    A = rng.standard_normal((2, 5))
+    B = rng.standard_normal((5, 3))
+    dC = rng.standard_normal((2, 3))
+    eps, h = 0.05, 1e-5
+    dA, dB, _ = o.lazy_prenorm_gemm_backward(A, B, dC, eps)
+
+    def loss(A_, B_):
+        return float(np.sum(dC * o.lazy_prenorm_gemm(A_, B_, eps)[0]))
+
+    for (i, j) in [(0, 0), (0, 4), (1, 2)]:
+        E = np.zeros_like(A)
+        E[i, j] = h
+        fd = (loss(A + E, B) - loss(A - E, B)) / (2 * h)
+        _close([dA[i, j]], [fd], 1e-6, 1e-8, f"prenorm dA[{i},{j}] vs finite differences")
+    for (i, j) in [(0, 0), (4, 2)]:
+        E = np.zeros_like(B)
+        E[i, j] = h
+        fd = (loss(A, B + E) - loss(A, B - E)) / (2 * h)
+        _close([dB[i, j]], [fd], 1e-6, 1e-8, f"prenorm dB[{i},{j}] vs finite differences")
+
+
+def check_prenorm_backward_scale_invariance(o):
+    # rmsnorm(c * a) = rmsnorm(a) up to eps, so dA . A = eps r^3 (dA_hat . A) per row
+    rng = _rng(18)
+    A = rng.standard_normal((5, 16)) * 2
+    B = rng.standard_normal((16, 7))
+    dC = rng.standard_normal((5, 7))
+    eps = 0.02
+    dA, _, r = o.lazy_prenorm_gemm_backward(A, B, dC, eps)
+    dA_hat = dC @ B.T
+    _close(np.sum(dA * A, axis=1), eps * r ** 3 * np.sum(dA_hat * A, axis=1), 1e-10, 1e-12,
+           "prenorm backward scale invariance")
+
+
+def check_postnorm_backward_autograd(o):
+    rng = _rng(19)
+    A = rng.standard_normal((5, 12))
+    B = rng.standard_normal((12, 20)) / 3
+    dC = rng.standard_normal((5, 20))
+    gam = 1 + 0.1 * rng.standard_normal(20)
+    bet = 0.1 * rng.standard_normal(20)
+    for norm in ("layernorm", "rmsnorm"):
+        d = o.gemm_postnorm_backward(A, B, dC, norm, gam, bet if norm == "layernorm" else None, 1e-4)
+        At, Bt = _t(A).requires_grad_(True), _t(B).requires_grad_(True)
+        gt, bt = _t(gam).requires_grad_(True), _t(bet).requires_grad_(True)
+        H = At @ Bt
+        C = F.layer_norm(H, (20,), gt, bt, 1e-4) if norm == "layernorm" else F.rms_norm(H, (20,), gt, 1e-4)
+        C.backward(_t(dC))
+        _close(d["dA"], At.grad.numpy(), 1e-10, 1e-12, f"post-{norm} dA vs autograd")
+        _close(d["dB"], Bt.grad.numpy(), 1e-10, 1e-12, f"post-{norm} dB vs autograd")
+        _close(d["dgamma"], gt.grad.numpy(), 1e-10, 1e-12, f"post-{norm} dgamma vs autograd")
+        if norm == "layernorm":
+            _close(d["dbeta"], bt.grad.numpy(), 1e-12, 1e-12, "post-LN dbeta vs autograd")
+
+
+def check_postnorm_backward_shift_invariance(o):
+    # LayerNorm ignores a constant added to a row, so each row of dH sums to 0
+    rng = _rng(20)
+    A = rng.standard_normal((4, 8))
+    B = rng.standard_normal((8, 16))
+    dC = rng.standard_normal((4, 16))
+    d = o.gemm_postnorm_backward(A, B, dC, "layernorm", 1 + rng.standard_normal(16) * 0.2, None, 1e-3)
+    _close(np.sum(d["dH"], axis=1), np.zeros(4), 0, 1e-12, "post-LN dH rows sum to zero")
+
+
 ALL_CHECKS = [
     check_gemm_bruteforce, check_gemm_torch,
     check_rmsnorm_golden, check_rmsnorm_torch, check_rmsnorm_unit_rms,
@@ -376,4 +461,6 @@ ALL_CHECKS = [
     check_postnorm_split_stats, check_pre_and_post,
     check_prenorm_affine_golden, check_prenorm_affine_torch, check_prenorm_affine_lazy_identity,
     check_add_postnorm_torch, check_add_postnorm_cancel,
+    check_prenorm_backward_autograd, check_prenorm_backward_finite_diff, check_prenorm_backward_scale_invariance,
+    check_postnorm_backward_autograd, check_postnorm_backward_shift_invariance,
 ]

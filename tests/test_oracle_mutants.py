@@ -10,7 +10,8 @@ import oracle.fnorm_oracle as O
 from oracle_pins import ALL_CHECKS
 
 _real = {name: getattr(O, name) for name in ("gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm",
-                                             "gemm_postnorm", "prenorm_affine_gemm", "gemm_add_postnorm")}
+                                             "gemm_postnorm", "prenorm_affine_gemm", "gemm_add_postnorm",
+                                             "lazy_prenorm_gemm_backward", "gemm_postnorm_backward")}
 
 
 def _gemm_transposed(A, B):          # transposed operand
@@ -108,6 +109,27 @@ def _add_postnorm_residual_dropped(A, B, R, norm, gamma=None, beta=None, eps=1e-
     return d
 
 
+def _prenorm_bwd_no_norm_term(A, B, dC, eps=1e-6):   # dA = r * dA_hat only
+    dA, dB, r = _real["lazy_prenorm_gemm_backward"](A, B, dC, eps)
+    return r[:, None] * (np.asarray(dC, np.float64) @ np.asarray(B, np.float64).T), dB, r
+
+
+def _prenorm_bwd_dB_unscaled(A, B, dC, eps=1e-6):    # dB from A instead of the rebuilt A_hat
+    dA, dB, r = _real["lazy_prenorm_gemm_backward"](A, B, dC, eps)
+    return dA, np.asarray(A, np.float64).T @ np.asarray(dC, np.float64), r
+
+
+def _postnorm_bwd_no_mean_term(A, B, dC, norm, gamma=None, beta=None, eps=1e-5):
+    d = _real["gemm_postnorm_backward"](A, B, dC, "rmsnorm" if norm == "layernorm" else norm, gamma, beta, eps)
+    if norm == "layernorm":  # LayerNorm backward without the mean removal
+        d["dbeta"] = np.sum(np.asarray(dC, np.float64), axis=0)
+    return d
+
+
+def _postnorm_bwd_gamma_ignored(A, B, dC, norm, gamma=None, beta=None, eps=1e-5):
+    return _real["gemm_postnorm_backward"](A, B, dC, norm, None, beta, eps)
+
+
 MUTANTS = {
     "gemm_transposed_B": ("gemm", _gemm_transposed),
     "gemm_dropped_k_term": ("gemm", _gemm_dropped_k),
@@ -123,6 +145,10 @@ MUTANTS = {
     "postnorm_pre_stage_skipped": ("gemm_postnorm", _postnorm_skip_pre),
     "prenorm_affine_after_gemm": ("prenorm_affine_gemm", _prenorm_affine_after_gemm),
     "add_postnorm_residual_dropped": ("gemm_add_postnorm", _add_postnorm_residual_dropped),
+    "prenorm_backward_norm_term_dropped": ("lazy_prenorm_gemm_backward", _prenorm_bwd_no_norm_term),
+    "prenorm_backward_dB_not_rebuilt": ("lazy_prenorm_gemm_backward", _prenorm_bwd_dB_unscaled),
+    "postnorm_backward_mean_term_dropped": ("gemm_postnorm_backward", _postnorm_bwd_no_mean_term),
+    "postnorm_backward_gamma_ignored": ("gemm_postnorm_backward", _postnorm_bwd_gamma_ignored),
 }
 
 
