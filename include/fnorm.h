@@ -124,6 +124,35 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
                                    void* stream);
 
 /*
+ * fnorm_lazy_prenorm_gemm_backward — gradients of C = rmsnorm(A) @ B
+ * (fnorm_lazy_prenorm_gemm) with respect to A and B, given dC = dL/dC:
+ *   dB = (A * rstd)^T @ dC                           [K,N]
+ *   dA = rstd * (dC @ B^T) - rstd^2 * (dC . C) / K * A   [M,K]
+ *   with rstd the forward's row rstd and (dC . C) the dot of row m of dC with
+ *   row m of the forward output C.  [FNF-ru] "Lazy Pre-Norm" limits (the
+ *   forward never materialises the normalised A, so the backward rebuilds it
+ *   on the fly) and [TFN] (fusion regrouping: the backward's norm work rides
+ *   on the GEMMs).  The second term of dA is the RMSNorm backward,
+ *   r^3 * A * sum_k(dA_hat * A) / K with dA_hat = dC @ B^T, rewritten through
+ *   sum_k dA_hat[m,k] A[m,k] = (dC . C)[m] / rstd[m], because C = (A @ B) * rstd.
+ *   Two kernels: the dgrad GEMM over N reads B^T straight from B, its norm
+ *   warps take the (dC . C) row dots from the staged tiles and its epilogue
+ *   forms dA; the wgrad GEMM over M reads A^T straight from A and its norm
+ *   warps scale each staged row of A by rstd (rounded to bf16, as the
+ *   materialised normalised A would be) before the tensor cores read it.
+ *   A:    [M,K] forward input.   B: [K,N] forward weight.
+ *   C:    [M,N] forward output (bf16, as fnorm_lazy_prenorm_gemm wrote it).
+ *   dC:   [M,N] gradient of the loss with respect to C.
+ *   rstd: [M] fp32 forward rstd (fnorm_lazy_prenorm_gemm's rstd_out).
+ *   dA:   [M,K] output, or NULL to skip it (then B and C may be NULL).
+ *   dB:   [K,N] output, or NULL to skip it.  With M == 0, dB is zeroed.
+ *   The sizes are the forward's.  eps is not needed: rstd carries it.
+ */
+fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
+                                                const fnorm_bf16* dC, const float* rstd, fnorm_bf16* dA,
+                                                fnorm_bf16* dB, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual
  * added to the fp32 accumulator in the epilogue, before the post-norm's row
  * statistics.

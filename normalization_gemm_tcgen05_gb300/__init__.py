@@ -11,6 +11,7 @@ Forms (see the header for the full contract):
 
 * ``gemm(A, B)``                      C = A @ B
 * ``lazy_prenorm_gemm(A, B, eps)``    C = rmsnorm(A) @ B = (A @ B) * rstd(A)
+* ``lazy_prenorm_gemm_backward(A, B, C, dC, rstd)``  its dA and dB
 * ``gemm_postnorm(A, B, norm, ...)``  C = norm(A @ B) * gamma + beta, optionally
   norm(rmsnorm(A) @ B); rows wider than one CTA tile are split over a cluster
 * ``gemm_add_postnorm(A, B, R, norm, ...)``  C = norm(A @ B + R) * gamma + beta
@@ -32,7 +33,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "gemm_postnorm", "gemm_add_postnorm",
+    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
     "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
@@ -69,6 +71,7 @@ _SIGNATURES = {
     "fnorm_lazy_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _f32, _p, _p]),
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
+    "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                             _p, _p, _p]),
     "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
@@ -212,6 +215,28 @@ def lazy_prenorm_gemm(A: torch.Tensor, B: torch.Tensor, eps: float = 1e-6, out: 
         _check(lib().fnorm_lazy_prenorm_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, float(eps), _ptr(rstd),
                                              _stream(A.device)))
     return (C, rstd) if return_rstd else C
+
+
+def lazy_prenorm_gemm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC: torch.Tensor,
+                               rstd: torch.Tensor, need_dA: bool = True, need_dB: bool = True,
+                               dA: Optional[torch.Tensor] = None, dB: Optional[torch.Tensor] = None):
+    """Gradients (dA, dB) of C = rmsnorm(A) @ B given dC; C and rstd are the
+    forward's output and row rstd (``lazy_prenorm_gemm(..., return_rstd=True)``).
+    A gradient not asked for is returned as None."""
+    M, N, K = _ab(A, B)
+    for t, name in ((C, "C"), (dC, "dC")):
+        _mat(t, name)
+        if tuple(t.shape) != (M, N) or t.device != A.device:
+            raise ValueError(f"{name} must have shape {(M, N)} on {A.device}")
+    if rstd.dtype != torch.float32 or rstd.dim() != 1 or rstd.numel() != M or not rstd.is_contiguous() \
+            or rstd.device != A.device:
+        raise ValueError(f"rstd must be a contiguous float32 vector of length {M} on {A.device}")
+    dA = _out(dA, (M, K), A.device, "dA") if need_dA else None
+    dB = _out(dB, (K, N), A.device, "dB") if need_dB else None
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_lazy_prenorm_gemm_backward(_ptr(A), _ptr(B), _ptr(C), _ptr(dC), _ptr(rstd), _ptr(dA),
+                                                      _ptr(dB), M, N, K, _stream(A.device)))
+    return dA, dB
 
 
 def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Optional[torch.Tensor] = None,

@@ -318,6 +318,49 @@ fnorm_status_t fnorm_gemm_add_postnorm(const fnorm_bf16* A, const fnorm_bf16* B,
   return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_residual(L) : launch_fused_post_residual_cluster(L);
 }
 
+fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
+                                                const fnorm_bf16* dC, const float* rstd, fnorm_bf16* dA,
+                                                fnorm_bf16* dB, int64_t M, int64_t N, int64_t K, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (dA == nullptr && dB == nullptr) return bad("at least one of dA, dB must be given");
+  FN_TRY(check_ptr(dA, "dA", 16, true));
+  FN_TRY(check_ptr(dB, "dB", 16, true));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    // an empty batch contributes nothing: dB = 0
+    if (dB != nullptr) {
+      cudaError_t e = cudaMemsetAsync(dB, 0, static_cast<size_t>(K) * static_cast<size_t>(N) * 2, st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dB)");
+    }
+    return FNORM_OK;
+  }
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, dA == nullptr));
+  FN_TRY(check_ptr(C, "C", 16, dA == nullptr));
+  FN_TRY(check_ptr(dC, "dC", 16, false));
+  FN_TRY(check_ptr(rstd, "rstd", 4, false));
+  if (dA != nullptr) {
+    // dA [M,K] = rstd * (dC @ B^T) - rstd^2 (dC . C) / K * A: a GEMM over N
+    FusedLaunch L = base_launch(dC, B, dA, M, K, N, stream);
+    L.mode = MODE_PRE | MODE_DGRAD | MODE_BT;
+    L.bn = gemm_tile_n(K);
+    L.Y = C;
+    L.X = A;
+    L.rowscale = rstd;
+    FN_TRY(launch_fused_backward(L));
+  }
+  if (dB != nullptr) {
+    // dB [K,N] = (A * rstd)^T @ dC: a GEMM over M with A^T read from A
+    FusedLaunch L = base_launch(A, dC, dB, K, N, M, stream);
+    L.mode = MODE_AT | MODE_ASCALE;
+    L.bn = gemm_tile_n(N);
+    L.rowscale = rstd;
+    FN_TRY(launch_fused_backward(L));
+  }
+  return FNORM_OK;
+}
+
 fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
                              float eps, float* rstd_out, void* stream) {
   clear_error();

@@ -57,6 +57,11 @@ struct FusedLaunch {
   const float* colsum;  // pre-norm with folded affine: column sums of the folded B (LayerNorm)
   const float* bias;    // pre-norm with folded affine: beta @ B, or NULL
   const void* R;        // residual [M, N] added before the post-norm, or NULL
+  // backward: A may be an A^T source ([K, M] row-major) and B a B^T source
+  // ([N, K] row-major), as the mode says
+  const void* Y;          // dgrad: [M, K] forward output, row-dotted with A (= dC)
+  const void* X;          // dgrad: [M, N] forward input combined in the epilogue
+  const float* rowscale;  // dgrad: forward rstd [M]; A-row scaling: [K] factors
   cudaStream_t stream;
 };
 
@@ -67,6 +72,7 @@ fnorm_status_t launch_fused_post_cluster(const FusedLaunch& L);   // post-norm o
 fnorm_status_t launch_fused_prenorm_affine(const FusedLaunch& L); // lazy pre-norm, affine folded into B
 fnorm_status_t launch_fused_post_residual(const FusedLaunch& L);  // residual + post-norm, one CTA per row block
 fnorm_status_t launch_fused_post_residual_cluster(const FusedLaunch& L);  // residual + post-norm over a cluster
+fnorm_status_t launch_fused_backward(const FusedLaunch& L);       // backward of the Lazy Pre-RMSNorm GEMM
 
 // B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
 fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,

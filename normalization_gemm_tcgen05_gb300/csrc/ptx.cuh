@@ -251,10 +251,11 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
 }
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// B bf16 (10-12 = 1), A major-ness at bit 15 (0 = K-major, 1 = MN-major), B
+// major-ness at bit 16 (same encoding), N >> 3 at bits 17-22, M >> 4 at bits
+// 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int m, int n, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

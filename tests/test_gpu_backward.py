@@ -1,0 +1,112 @@
+"""GPU parity of the backward of the Lazy Pre-RMSNorm GEMM against the fp64 oracle.
+
+The forward runs on the GPU (its bf16 output C and fp32 rstd are what a
+training step saves); the backward's dA and dB are compared with the oracle's
+chain rule on the same bf16 inputs.  Small cases span several tiles and ragged
+tails in M, N and K; the degenerate rows are a zero row and a constant row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normalization_gemm_tcgen05_gb300 as fn
+import oracle
+from gpu_util import assert_out_close, np64
+from workloads import WORKLOADS, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _case(M, N, K, seed):
+    w = WORKLOADS["prenorm_bwd"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    return w, make_inputs(w, seed)
+
+
+def _run(w, d, A=None):
+    A = d["A"] if A is None else A
+    Ad, Bd, dCd = A.to(DEV), d["B"].to(DEV), d["dC"].to(DEV)
+    C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+    dA, dB = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd)
+    fn.check_status(DEV)
+    rA, rB, _ = oracle.lazy_prenorm_gemm_backward(to_f64(A), to_f64(d["B"]), to_f64(d["dC"]), w.eps)
+    return dA, dB, rA, rB
+
+
+SHAPES = [(256, 128, 512), (200, 64, 72), (333, 256, 1000), (128, 520, 256), (1, 8, 8), (300, 192, 4096),
+          (1000, 1024, 128), (129, 4096, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES, ids=lambda v: str(v))
+def test_prenorm_backward(M, N, K):
+    w, d = _case(M, N, K, seed=M + 5 * N + K)
+    dA, dB, rA, rB = _run(w, d)
+    assert_out_close(dA, rA, f"dA {M}x{N}x{K}")
+    assert_out_close(dB, rB, f"dB {M}x{N}x{K}")
+
+
+def test_prenorm_backward_special_rows():
+    # a zero row has no gradient through the norm (dA row = rstd * dA_hat with
+    # rstd = 1/sqrt(eps)); a constant row and an outlier row stress the
+    # cancellation in the RMSNorm backward
+    w, d = _case(300, 128, 512, seed=3)
+    A = d["A"].clone()
+    A[4] = 0
+    A[5] = 1.5
+    A[6] *= 100
+    dA, dB, rA, rB = _run(w, d, A)
+    assert_out_close(dA, rA, "dA special rows")
+    assert_out_close(dB, rB, "dB special rows")
+    assert np.all(np64(dB).shape == (512, 128))
+
+
+def test_prenorm_backward_one_side():
+    w, d = _case(256, 256, 256, seed=4)
+    Ad, Bd, dCd = d["A"].to(DEV), d["B"].to(DEV), d["dC"].to(DEV)
+    C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+    dA, dB = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd, need_dB=False)
+    assert dB is None
+    dA2, dB2 = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd, need_dA=False)
+    assert dA2 is None
+    dA3, dB3 = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd)
+    assert torch.equal(dA, dA3) and torch.equal(dB2, dB3)
+
+
+def test_prenorm_backward_scale_invariance():
+    # rmsnorm(c a) = rmsnorm(a) up to eps: sum_k dA[m,k] A[m,k] = eps r^3 (dA_hat . a),
+    # tiny next to |dA| |a|, so each dA row is nearly orthogonal to its A row
+    w, d = _case(256, 256, 512, seed=5)
+    dA, _, _, _ = _run(w, d)
+    a = to_f64(d["A"])
+    g = np64(dA)
+    cos = np.abs(np.sum(g * a, axis=1)) / (np.linalg.norm(g, axis=1) * np.linalg.norm(a, axis=1) + 1e-30)
+    assert np.max(cos) < 2e-2, f"dA rows not orthogonal to A rows: max |cos| {np.max(cos):.3e}"
+
+
+def test_prenorm_backward_empty():
+    B = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    E = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    E2 = torch.empty(0, 128, dtype=torch.bfloat16, device=DEV)
+    dA, dB = fn.lazy_prenorm_gemm_backward(E, B, E2, E2, torch.empty(0, device=DEV))
+    assert dA.shape == (0, 64) and torch.all(dB == 0)
+
+
+def test_prenorm_backward_full_size():
+    # the bench's backward workload, in its launch configuration; sampled rows
+    # of dA and columns of dB recomputed by the oracle one at a time
+    w = WORKLOADS["prenorm_bwd"]
+    d = make_inputs(w, 0)
+    Ad, Bd, dCd = d["A"].to(DEV), d["B"].to(DEV), d["dC"].to(DEV)
+    C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+    dA, dB = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd)
+    fn.check_status(DEV)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1], rng.choice(w.M, 24, replace=False)]))
+    A64, B64, dC64 = to_f64(d["A"]), to_f64(d["B"]), to_f64(d["dC"])
+    rA, _, r = oracle.lazy_prenorm_gemm_backward(A64[rows], B64, dC64[rows], w.eps)
+    assert_out_close(dA[torch.from_numpy(rows).to(DEV)], rA, "dA sampled rows")
+    cols = np.unique(np.concatenate([[0, 255, 256, w.K - 1], rng.choice(w.K, 12, replace=False)]))
+    _, r_all = oracle.rmsnorm(A64, None, None, w.eps)
+    ref = (A64[:, cols] * r_all[:, None]).T @ dC64
+    assert_out_close(dB[torch.from_numpy(cols).to(DEV)], ref, "dB sampled rows")

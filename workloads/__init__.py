@@ -34,12 +34,15 @@ Forms beyond the five configurations (same distributions where they apply):
   eps 1e-5.
 * ``prerms_gamma``  Lazy Pre-RMSNorm with gamma folded into B: cfg3's A and B,
   gamma[4096] 1+N(0,0.1), no beta, eps 1e-6.
+* ``prenorm_bwd``  backward of the Lazy Pre-RMSNorm GEMM at cfg3's shape: cfg3's
+  A and B and an upstream gradient dC[8192,4096] N(0,1).
 
 Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
 float32 in the order A, row scale, outlier rows, row offset, B, gamma, beta, R
 (each only where the workload has it), then rounded once to bf16 (round to
 nearest even) by ``torch.Tensor.to(torch.bfloat16)``.  gamma and beta have
-length N for a post-norm and K for a pre-norm with affine.
+length N for a post-norm and K for a pre-norm with affine.  The backward's
+dC is drawn last.
 """
 from __future__ import annotations
 
@@ -54,7 +57,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "gemm"
+    kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "prenorm_backward" | "gemm"
     M: int
     K: int
     N: int
@@ -77,7 +80,8 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        return 2.0 * self.M * self.N * self.K
+        """2MNK per GEMM (the backward runs two: dA over N, dB over M)."""
+        return (4.0 if self.kind == "prenorm_backward" else 2.0) * self.M * self.N * self.K
 
     @property
     def affine_len(self) -> int:
@@ -89,6 +93,10 @@ class Workload:
         """Bytes one fused launch must move: A + B + C in bf16 (+ R), gamma/beta
         (post-norm) or the folded weight's fp32 column sums and bias row
         (pre-norm with affine), and the fp32 row statistics."""
+        if self.kind == "prenorm_backward":
+            # dgrad reads dC, B, C, A, rstd and writes dA; wgrad reads A, dC,
+            # rstd and writes dB
+            return 2.0 * (3 * self.M * self.N + 3 * self.M * self.K + 2 * self.K * self.N) + 8.0 * self.M
         b = 2.0 * (self.M * self.K + self.K * self.N + self.M * self.N)
         if self.residual:
             b += 2.0 * self.M * self.N
@@ -157,6 +165,9 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
     Workload("prerms_gamma", "prenorm_affine", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-6,
              norm="rmsnorm", gamma=True, beta=False, a_row_scale=True,
              description="Lazy Pre-RMSNorm with gamma folded into B, A[8192,4096] @ B[4096,4096]"),
+    Workload("prenorm_bwd", "prenorm_backward", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-6,
+             a_row_scale=True,
+             description="backward (dA, dB) of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096]"),
 ]}
 
 
@@ -198,11 +209,14 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         beta = np.float32(0.1) * rng.standard_normal(n_aff, dtype=np.float32)
     if w.residual:
         r = rng.standard_normal((w.M, w.N), dtype=np.float32)
+    dc = None
+    if w.kind == "prenorm_backward":
+        dc = rng.standard_normal((w.M, w.N), dtype=np.float32)
 
     def bf16(x):
         return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
 
-    return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta), "R": bf16(r),
+    return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta), "R": bf16(r), "dC": bf16(dc),
             "row_scale": row_scale, "outliers": outl, "row_offset": row_offset}
 
 
