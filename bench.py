@@ -4,7 +4,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload cfg2|cfg1|cfg3|cfg4|cfg5|all]
 
 Workload groups: cfg1..cfg5 (the five configurations), res (residual-add
-post-norm), preaff (pre-norm with its affine folded into B), all.
+post-norm), preaff (pre-norm with its affine folded into B), bwd (backward of
+the Lazy Pre-RMSNorm GEMM: 4MNK FLOPs a step), all.
 
 Default workload (one JSON line on stdout): GEMM + post-LayerNorm with affine,
 A[16384,1024] @ B[1024,N] for N = 64 and N = 128 (both launches make one step).
@@ -58,6 +59,7 @@ GROUPS = {
     "cfg5": ["cfg5"],
     "res": ["res_ln_n128", "res_rms_n1024"],
     "preaff": ["preln_affine", "prerms_gamma"],
+    "bwd": ["prenorm_bwd"],
 }
 GROUP_TEXT = {
     "cfg1": "Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128], eps 1e-6",
@@ -70,6 +72,7 @@ GROUP_TEXT = {
            "RMSNorm(gamma) A[16384,2048] @ B[2048,1024] + R",
     "preaff": "pre-norm with affine folded into B + GEMM, A[8192,4096] @ B[4096,4096]: LayerNorm(gamma, beta), "
               "RMSNorm(gamma)",
+    "bwd": "backward (dA, dB) of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], dC[8192,4096]",
 }
 KERNEL_SOURCES = ["fused_gemm.cuh", "ptx.cuh", "fused_launch.cuh", "rownorm.cu"]
 
@@ -222,6 +225,18 @@ class Case:
         self.fold = None
         if w.kind == "prenorm_affine":
             self.fold = [fn.fold_prenorm_affine(Bj, self.g, self.b) for Bj in self.B]
+        # backward: the forward's saved output and rstd per copy, the upstream
+        # gradient, and the gradients' buffers
+        if w.kind == "prenorm_backward":
+            fwd = [fn.lazy_prenorm_gemm(Aj, Bj, w.eps, return_rstd=True) for Aj, Bj in zip(self.A, self.B)]
+            self.Cf = [c for c, _ in fwd]
+            self.rstd = [r for _, r in fwd]
+            self.dC = [d["dC"].to(device) for _ in range(self.R)]
+            self.dA = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
+            self.dB = [torch.empty((w.K, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
+            self.G = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
+            self.work = [(torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device),
+                          torch.empty(w.M, dtype=torch.float32, device=device)) for _ in range(self.R)]
         self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         self.Y = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         nst = 3
@@ -242,6 +257,9 @@ class Case:
         elif w.kind == "prenorm_affine":
             Bf, cs, bias = self.fold[j]
             fn.prenorm_gemm(self.A[j], Bf, w.norm, cs, bias, w.eps, out=self.C[j])
+        elif w.kind == "prenorm_backward":
+            fn.lazy_prenorm_gemm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j],
+                                          dA=self.dA[j], dB=self.dB[j], work=self.work[j])
         elif w.residual:
             fn.gemm_add_postnorm(self.A[j], self.B[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.C[j])
         elif w.kind == "postnorm":
@@ -253,6 +271,10 @@ class Case:
 
     def gemm_only(self, i: int):
         j = i % self.R
+        if self.w.kind == "prenorm_backward":  # the two GEMMs of the backward: dC @ B^T, A^T @ dC
+            self.fn.gemm_ex(self.dC[j], self.B[j], trans_b=True, out=self.G[j])
+            self.fn.gemm_ex(self.A[j], self.dC[j], trans_a=True, out=self.dB[j])
+            return
         self.fn.gemm(self.A[j], self.B[j], out=self.C[j])
 
     def norm_only(self, i: int):
@@ -264,6 +286,11 @@ class Case:
         elif w.kind == "prenorm_affine":
             k = i % self.R
             self._pre_norm(k, self.A[k], self._pre_out(k))
+        elif w.kind == "prenorm_backward":
+            # the normalised A materialised for dB, and the RMSNorm backward for dA
+            k = i % self.R
+            fn.rmsnorm(self.A[k], None, w.eps, out=self._pre_out(k))
+            fn.rmsnorm_backward(self.G[k], self.A[k], self.rstd[k], out=self.dA[k])
         elif w.residual:
             k = i % self.R
             fn.add_rownorm(self.Cn[j], self.Rres[k], w.norm, self.g, self.b, w.eps, out=self.Yn[j])
@@ -285,6 +312,11 @@ class Case:
         elif w.kind == "prenorm_affine":
             self._pre_norm(j, self.A[j], self._pre_out(j))
             fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+        elif w.kind == "prenorm_backward":
+            fn.rmsnorm(self.A[j], None, w.eps, out=self._pre_out(j))
+            fn.gemm_ex(self.dC[j], self.B[j], trans_b=True, out=self.G[j])
+            fn.gemm_ex(self._pre_out(j), self.dC[j], trans_a=True, out=self.dB[j])
+            fn.rmsnorm_backward(self.G[j], self.A[j], self.rstd[j], out=self.dA[j])
         elif w.residual:
             fn.gemm(self.A[j], self.B[j], out=self.C[j])
             fn.add_rownorm(self.C[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.Y[j])
@@ -317,6 +349,8 @@ class Case:
 
     def launches_per_call(self, what: str) -> int:
         w = self.w
+        if w.kind == "prenorm_backward":
+            return {"fused": 3, "gemm": 2, "norm": 2}.get(what, 4)
         if what == "fused" or what == "gemm":
             return 1
         if what == "norm":
@@ -404,7 +438,8 @@ def run_ours(args, names, world, rank, local):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = load_traffic(dc.w.name)
-    roof["kernel"] = f"fused kernel, {dc.w.name}"
+    roof["kernel"] = (f"fused backward (row pass + dgrad + wgrad: one call, three launches), {dc.w.name}"
+                      if dc.w.kind == "prenorm_backward" else f"fused kernel, {dc.w.name}")
     roof["algorithmic_bytes"] = dc.w.algorithmic_bytes
     roof["peak_source"] = peaks["source"] + (" (burst)" if roof["bound"] == "tensor" else "")
 
@@ -431,7 +466,7 @@ def run_ours(args, names, world, rank, local):
         "roofline": roof,
         "latency_hidden": hidden,
         "e2e": e2e,
-        "gpu_launches": K * len(cases),
+        "gpu_launches": K * sum(c.launches_per_call("fused") for c in cases),
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -451,12 +486,21 @@ def run_e2e(cases, K, W, world, device) -> dict:
         hb = None if c.host["beta"] is None else c.host["beta"].pin_memory()
         hR = None if c.host["R"] is None else c.host["R"].pin_memory()
         hC = torch.empty((c.w.M, c.w.N), dtype=torch.bfloat16).pin_memory()
-        host.append((hA, hB, hg, hb, hR, hC))
+        bwd = None
+        if c.w.kind == "prenorm_backward":
+            # the backward's inputs (forward output, rstd, dC) in, dA and dB out
+            bwd = (c.Cf[0].cpu().pin_memory(), c.rstd[0].cpu().pin_memory(), c.host["dC"].pin_memory(),
+                   torch.empty((c.w.M, c.w.K), dtype=torch.bfloat16).pin_memory(),
+                   torch.empty((c.w.K, c.w.N), dtype=torch.bfloat16).pin_memory())
+            hC = None
+        host.append((hA, hB, hg, hb, hR, hC, bwd))
     h2d = sum(t.numel() * t.element_size() for h in host for t in h[:5] if t is not None)
-    d2h = sum(h[5].numel() * h[5].element_size() for h in host)
+    h2d += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][:3])
+    d2h = sum(h[5].numel() * h[5].element_size() for h in host if h[5] is not None)
+    d2h += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][3:])
 
     def step():
-        for c, (hA, hB, hg, hb, hR, hC) in zip(cases, host):
+        for c, (hA, hB, hg, hb, hR, hC, bwd) in zip(cases, host):
             dA, dB = c.A[0], c.B[0]
             dA.copy_(hA, non_blocking=True)
             dB.copy_(hB, non_blocking=True)
@@ -467,6 +511,16 @@ def run_e2e(cases, K, W, world, device) -> dict:
             if hR is not None:
                 c.Rres[0].copy_(hR, non_blocking=True)
             w = c.w
+            if bwd is not None:
+                hCf, hr, hdC, hdA, hdB = bwd
+                c.Cf[0].copy_(hCf, non_blocking=True)
+                c.rstd[0].copy_(hr, non_blocking=True)
+                c.dC[0].copy_(hdC, non_blocking=True)
+                fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
+                                              work=c.work[0])
+                hdA.copy_(c.dA[0], non_blocking=True)
+                hdB.copy_(c.dB[0], non_blocking=True)
+                continue
             if w.kind == "prenorm":
                 fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
             elif w.kind == "prenorm_affine":
@@ -508,6 +562,8 @@ def oracle_step(w: Workload, d: dict, rows: np.ndarray):
     A = d["A64"][rows]
     if w.kind == "prenorm":
         oracle.lazy_prenorm_gemm(A, d["B64"], w.eps)
+    elif w.kind == "prenorm_backward":
+        oracle.lazy_prenorm_gemm_backward(A, d["B64"], d["dC64"][rows], w.eps)
     elif w.kind == "prenorm_affine":
         oracle.prenorm_affine_gemm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps)
     elif w.residual:
@@ -526,7 +582,7 @@ def _oracle_inputs(names):
         w = WORKLOADS[n]
         d = make_inputs(w, 0)
         out.append((w, {"A64": to_f64(d["A"]), "B64": to_f64(d["B"]), "g64": to_f64(d["gamma"]),
-                        "b64": to_f64(d["beta"]), "R64": to_f64(d["R"])}))
+                        "b64": to_f64(d["beta"]), "R64": to_f64(d["R"]), "dC64": to_f64(d["dC"])}))
     return out
 
 
@@ -536,7 +592,7 @@ def _cores() -> int:
 
 
 def _sample_rows(w: Workload, budget_flops: float) -> np.ndarray:
-    per_row = 2.0 * w.N * w.K
+    per_row = w.flops / w.M
     n = int(max(1, min(w.M, budget_flops // per_row)))
     return np.linspace(0, w.M - 1, n).astype(np.int64)
 
@@ -557,7 +613,7 @@ def cpu_baseline(names, seconds: float) -> dict:
             if time.perf_counter() - t0 >= seconds / len(inputs):
                 break
         dt = time.perf_counter() - t0
-        flops += reps * 2.0 * len(rows) * w.N * w.K
+        flops += reps * len(rows) * w.flops / w.M
         t_total += dt
         samples.append(f"{w.name}: {reps} x {len(rows)} of {w.M} rows")
     return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
@@ -579,7 +635,7 @@ def run_reference(args, names, world, rank):
         for w, d, rows in sampled:
             oracle_step(w, d, rows)
     t = time.perf_counter() - t0
-    flops = args.steps * sum(2.0 * len(rows) * w.N * w.K for w, d, rows in sampled)
+    flops = args.steps * sum(len(rows) * w.flops / w.M for w, d, rows in sampled)
     value = flops / t / 1e12
     sample = "; ".join(f"{w.name}: {len(rows)} of {w.M} rows" for w, d, rows in sampled)
     return {

@@ -78,6 +78,18 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
                           int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * fnorm_gemm_ex — C = op(A) @ op(B), C [M,N], bf16 in and out, fp32 accumulate.
+ *   op(A) is A [M,K] (trans_a = 0) or the transpose of a [K,M] array
+ *   (trans_a = 1, read MN-major straight from its row-major layout; M must then
+ *   be a multiple of 8); op(B) is B [K,N] (trans_b = 0) or the transpose of an
+ *   [N,K] array (trans_b = 1, read K-major).  The same tcgen05 mainloop as
+ *   fnorm_gemm; the GEMM half of the backward's unfused comparison
+ *   (dC @ B^T, A_hat^T @ dC).
+ */
+fnorm_status_t fnorm_gemm_ex(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M, int64_t N,
+                             int64_t K, int trans_a, int trans_b, void* stream);
+
+/*
  * fnorm_lazy_prenorm_gemm — C = rmsnorm(A) @ B, RMSNorm without affine,
  * computed as (A @ B) * rstd(A).
  *   [FNF-ru] "Lazy Pre-Norm"; [FNF-es] "Lazy Pre-Norm: el truco matemático".
@@ -126,31 +138,37 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
 /*
  * fnorm_lazy_prenorm_gemm_backward — gradients of C = rmsnorm(A) @ B
  * (fnorm_lazy_prenorm_gemm) with respect to A and B, given dC = dL/dC:
- *   dB = (A * rstd)^T @ dC                           [K,N]
- *   dA = rstd * (dC @ B^T) - rstd^2 * (dC . C) / K * A   [M,K]
+ *   dB = (A * rstd)^T @ dC = A^T @ (rstd * dC)                      [K,N]
+ *   dA = rstd * (dC @ B^T) - rstd^2 * (dC . C) / K * A              [M,K]
  *   with rstd the forward's row rstd and (dC . C) the dot of row m of dC with
  *   row m of the forward output C.  [FNF-ru] "Lazy Pre-Norm" limits (the
- *   forward never materialises the normalised A, so the backward rebuilds it
- *   on the fly) and [TFN] (fusion regrouping: the backward's norm work rides
+ *   forward never materialises the normalised A, so the backward has to
+ *   rebuild it) and [TFN] (fusion regrouping: the backward's norm work rides
  *   on the GEMMs).  The second term of dA is the RMSNorm backward,
  *   r^3 * A * sum_k(dA_hat * A) / K with dA_hat = dC @ B^T, rewritten through
  *   sum_k dA_hat[m,k] A[m,k] = (dC . C)[m] / rstd[m], because C = (A @ B) * rstd.
- *   Two kernels: the dgrad GEMM over N reads B^T straight from B, its norm
- *   warps take the (dC . C) row dots from the staged tiles and its epilogue
- *   forms dA; the wgrad GEMM over M reads A^T straight from A and its norm
- *   warps scale each staged row of A by rstd (rounded to bf16, as the
- *   materialised normalised A would be) before the tensor cores read it.
+ *   The row scale moves to dC's side (A^T @ (rstd * dC)), so the normalised A
+ *   is never built; rstd * dC is rounded to bf16 once.  Three launches: one
+ *   memory-bound pass over the rows of dC and C writes dCs = rstd * dC and the
+ *   row coefficients; the dgrad GEMM over N reads B^T straight from B and its
+ *   epilogue adds coefficient * A to the accumulator; the wgrad GEMM over M
+ *   reads A^T straight from A.
  *   A:    [M,K] forward input.   B: [K,N] forward weight.
  *   C:    [M,N] forward output (bf16, as fnorm_lazy_prenorm_gemm wrote it).
  *   dC:   [M,N] gradient of the loss with respect to C.
  *   rstd: [M] fp32 forward rstd (fnorm_lazy_prenorm_gemm's rstd_out).
- *   dA:   [M,K] output, or NULL to skip it (then B and C may be NULL).
- *   dB:   [K,N] output, or NULL to skip it.  With M == 0, dB is zeroed.
+ *   dA:   [M,K] output, or NULL to skip it (then B may be NULL).
+ *   dB:   [K,N] output, or NULL to skip it (M must then be a multiple of 8).
+ *         With M == 0, dB is zeroed.
+ *   dCs:  [M,N] bf16 caller-owned workspace; receives rstd * dC.  Must not
+ *         overlap dC.
+ *   rowcoef: [M] fp32 caller-owned workspace; receives -rstd^2 (dC . C) / K.
  *   The sizes are the forward's.  eps is not needed: rstd carries it.
  */
 fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
                                                 const fnorm_bf16* dC, const float* rstd, fnorm_bf16* dA,
-                                                fnorm_bf16* dB, int64_t M, int64_t N, int64_t K, void* stream);
+                                                fnorm_bf16* dB, fnorm_bf16* dCs, float* rowcoef, int64_t M,
+                                                int64_t N, int64_t K, void* stream);
 
 /*
  * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual
@@ -255,6 +273,17 @@ fnorm_status_t fnorm_layernorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, in
 fnorm_status_t fnorm_add_rownorm(const fnorm_bf16* X, const fnorm_bf16* R, fnorm_bf16* Y, int64_t M, int64_t N,
                                  fnorm_norm_t norm, const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
                                  float* mean_out, float* rstd_out, void* stream);
+
+/*
+ * fnorm_rmsnorm_backward — standalone RMSNorm backward without affine: for
+ * Y = X * rstd (rstd = 1/sqrt(mean(X^2) + eps) per row, given),
+ *   dX = rstd * dY - rstd^3 * X * sum_n(dY * X) / N.
+ *   [ATB] 1.2 (the RMSNorm it differentiates); the unfused comparison of
+ *   fnorm_lazy_prenorm_gemm_backward's dA.  dY, X, dX: [M,N] bf16; rstd: [M]
+ *   fp32.  N <= 16384.
+ */
+fnorm_status_t fnorm_rmsnorm_backward(const fnorm_bf16* dY, const fnorm_bf16* X, const float* rstd, fnorm_bf16* dX,
+                                      int64_t M, int64_t N, void* stream);
 
 /*
  * fnorm_check_status — synchronise `stream`, then read and clear the device

@@ -10,6 +10,7 @@ raises ``FnormError``.
 Forms (see the header for the full contract):
 
 * ``gemm(A, B)``                      C = A @ B
+* ``gemm_ex(A, B, trans_a, trans_b)``  C = op(A) @ op(B), transposes read in place
 * ``lazy_prenorm_gemm(A, B, eps)``    C = rmsnorm(A) @ B = (A @ B) * rstd(A)
 * ``lazy_prenorm_gemm_backward(A, B, C, dC, rstd)``  its dA and dB
 * ``gemm_postnorm(A, B, norm, ...)``  C = norm(A @ B) * gamma + beta, optionally
@@ -33,7 +34,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "FnormError", "lib", "LIB_PATH", "gemm", "lazy_prenorm_gemm", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm", "lazy_prenorm_gemm_backward", "gemm_postnorm",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
@@ -68,10 +69,12 @@ _f32 = ctypes.c_float
 # name -> (restype, argtypes); the C ABI of include/fnorm.h
 _SIGNATURES = {
     "fnorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _p]),
+    "fnorm_gemm_ex": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _p]),
+    "fnorm_rmsnorm_backward": (_c_status, [_p, _p, _p, _p, _i64, _i64, _p]),
     "fnorm_lazy_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _f32, _p, _p]),
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
-    "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
+    "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                             _p, _p, _p]),
     "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
@@ -202,6 +205,41 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None) -
     return C
 
 
+def gemm_ex(A: torch.Tensor, B: torch.Tensor, trans_a: bool = False, trans_b: bool = False,
+            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """C = op(A) @ op(B): op(A) = A.T when ``trans_a`` (A given as [K, M]),
+    op(B) = B.T when ``trans_b`` (B given as [N, K]); no copy is made."""
+    _mat(A, "A")
+    _mat(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if trans_a else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if trans_b else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: op(A) is {M}x{K}, op(B) is {Kb}x{N}")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+    C = _out(out, (M, N), A.device)
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_gemm_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(trans_a), int(trans_b),
+                                   _stream(A.device)))
+    return C
+
+
+def rmsnorm_backward(dY: torch.Tensor, X: torch.Tensor, rstd: torch.Tensor,
+                     out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Standalone RMSNorm backward (no affine): dX from dY, X and the forward rstd."""
+    _mat(dY, "dY")
+    _mat(X, "X")
+    M, N = X.shape
+    if tuple(dY.shape) != (M, N) or dY.device != X.device:
+        raise ValueError(f"dY must have shape {(M, N)} on {X.device}")
+    if rstd.dtype != torch.float32 or rstd.numel() != M or not rstd.is_contiguous() or rstd.device != X.device:
+        raise ValueError(f"rstd must be a contiguous float32 vector of length {M} on {X.device}")
+    dX = _out(out, (M, N), X.device, "out")
+    with torch.cuda.device(X.device):
+        _check(lib().fnorm_rmsnorm_backward(_ptr(dY), _ptr(X), _ptr(rstd), _ptr(dX), M, N, _stream(X.device)))
+    return dX
+
+
 def lazy_prenorm_gemm(A: torch.Tensor, B: torch.Tensor, eps: float = 1e-6, out: Optional[torch.Tensor] = None,
                       return_rstd: bool = False):
     """C = rmsnorm(A) @ B (RMSNorm without affine) computed as (A @ B) * rstd(A).
@@ -219,10 +257,13 @@ def lazy_prenorm_gemm(A: torch.Tensor, B: torch.Tensor, eps: float = 1e-6, out: 
 
 def lazy_prenorm_gemm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC: torch.Tensor,
                                rstd: torch.Tensor, need_dA: bool = True, need_dB: bool = True,
-                               dA: Optional[torch.Tensor] = None, dB: Optional[torch.Tensor] = None):
+                               dA: Optional[torch.Tensor] = None, dB: Optional[torch.Tensor] = None,
+                               work: Optional[tuple] = None):
     """Gradients (dA, dB) of C = rmsnorm(A) @ B given dC; C and rstd are the
     forward's output and row rstd (``lazy_prenorm_gemm(..., return_rstd=True)``).
-    A gradient not asked for is returned as None."""
+    A gradient not asked for is returned as None.  ``work`` = (dCs [M, N]
+    bf16, rowcoef [M] fp32) are the library's workspaces, allocated when
+    absent; on return they hold rstd * dC and -rstd^2 (dC . C) / K."""
     M, N, K = _ab(A, B)
     for t, name in ((C, "C"), (dC, "dC")):
         _mat(t, name)
@@ -233,9 +274,15 @@ def lazy_prenorm_gemm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor
         raise ValueError(f"rstd must be a contiguous float32 vector of length {M} on {A.device}")
     dA = _out(dA, (M, K), A.device, "dA") if need_dA else None
     dB = _out(dB, (K, N), A.device, "dB") if need_dB else None
+    if work is None:
+        work = (torch.empty((M, N), dtype=torch.bfloat16, device=A.device), _stat(M, A.device))
+    dCs, coef = work
+    _out(dCs, (M, N), A.device, "dCs")
+    if coef.dtype != torch.float32 or coef.numel() != M or not coef.is_contiguous() or coef.device != A.device:
+        raise ValueError(f"rowcoef must be a contiguous float32 vector of length {M} on {A.device}")
     with torch.cuda.device(A.device):
         _check(lib().fnorm_lazy_prenorm_gemm_backward(_ptr(A), _ptr(B), _ptr(C), _ptr(dC), _ptr(rstd), _ptr(dA),
-                                                      _ptr(dB), M, N, K, _stream(A.device)))
+                                                      _ptr(dB), _ptr(dCs), _ptr(coef), M, N, K, _stream(A.device)))
     return dA, dB
 
 

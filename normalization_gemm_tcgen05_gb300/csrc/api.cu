@@ -161,6 +161,23 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
   return launch_fused_plain(L);
 }
 
+fnorm_status_t fnorm_gemm_ex(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M, int64_t N,
+                             int64_t K, int trans_a, int trans_b, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return bad("trans_a, trans_b must be 0 or 1");
+  if (trans_a && M % 8 != 0) return bad("with trans_a, M must be a multiple of 8 (the [K, M] row pitch)");
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(A, "A", 16, false));
+  FN_TRY(check_ptr(B, "B", 16, false));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  if (!trans_a && !trans_b) return fnorm_gemm(A, B, C, M, N, K, stream);
+  FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  L.mode = (trans_a ? MODE_AT : 0) | (trans_b ? MODE_BT : 0);
+  L.bn = gemm_tile_n(N);
+  return launch_fused_transposed(L);
+}
+
 fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
                                        int64_t N, int64_t K, float eps, float* rstd_out, void* stream) {
   clear_error();
@@ -320,7 +337,8 @@ fnorm_status_t fnorm_gemm_add_postnorm(const fnorm_bf16* A, const fnorm_bf16* B,
 
 fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
                                                 const fnorm_bf16* dC, const float* rstd, fnorm_bf16* dA,
-                                                fnorm_bf16* dB, int64_t M, int64_t N, int64_t K, void* stream) {
+                                                fnorm_bf16* dB, fnorm_bf16* dCs, float* rowcoef, int64_t M,
+                                                int64_t N, int64_t K, void* stream) {
   clear_error();
   FN_TRY(check_mnk(M, N, K));
   if (dA == nullptr && dB == nullptr) return bad("at least one of dA, dB must be given");
@@ -335,28 +353,38 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
     }
     return FNORM_OK;
   }
+  if (M % 8 != 0 && dB != nullptr) return bad("dB needs M to be a multiple of 8 (the [M, K] rows are read as A^T)");
   FN_TRY(check_ptr(A, "A", 16, false));
   FN_TRY(check_ptr(B, "B", 16, dA == nullptr));
-  FN_TRY(check_ptr(C, "C", 16, dA == nullptr));
+  FN_TRY(check_ptr(C, "C", 16, false));
   FN_TRY(check_ptr(dC, "dC", 16, false));
   FN_TRY(check_ptr(rstd, "rstd", 4, false));
+  FN_TRY(check_ptr(dCs, "dCs", 16, false));
+  FN_TRY(check_ptr(rowcoef, "rowcoef", 4, false));
+  {
+    const auto a0 = reinterpret_cast<uintptr_t>(dCs), b0 = reinterpret_cast<uintptr_t>(dC);
+    const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(N) * 2u;
+    if (a0 < b0 + bytes && b0 < a0 + bytes) return bad("dCs must not overlap dC");
+  }
+  // one pass over the rows: dCs = rstd * dC, rowcoef = -rstd^2 (dC . C) / K
+  FN_TRY(launch_backward_rows(dC, C, rstd, dCs, rowcoef, static_cast<int>(M), static_cast<int>(N),
+                              static_cast<int>(K), st));
   if (dA != nullptr) {
-    // dA [M,K] = rstd * (dC @ B^T) - rstd^2 (dC . C) / K * A: a GEMM over N
-    FusedLaunch L = base_launch(dC, B, dA, M, K, N, stream);
-    L.mode = MODE_PRE | MODE_DGRAD | MODE_BT;
+    // dA [M,K] = dCs @ B^T + rowcoef * A: a GEMM over N with the RMSNorm
+    // backward's row term in its epilogue
+    FusedLaunch L = base_launch(dCs, B, dA, M, K, N, stream);
+    L.mode = MODE_DGRAD | MODE_BT;
     L.bn = gemm_tile_n(K);
-    L.Y = C;
     L.X = A;
-    L.rowscale = rstd;
+    L.rowcoef = rowcoef;
     FN_TRY(launch_fused_backward(L));
   }
   if (dB != nullptr) {
-    // dB [K,N] = (A * rstd)^T @ dC: a GEMM over M with A^T read from A
-    FusedLaunch L = base_launch(A, dC, dB, K, N, M, stream);
-    L.mode = MODE_AT | MODE_ASCALE;
+    // dB [K,N] = A^T @ dCs: a GEMM over M reading A^T straight from A
+    FusedLaunch L = base_launch(A, dCs, dB, K, N, M, stream);
+    L.mode = MODE_AT;
     L.bn = gemm_tile_n(N);
-    L.rowscale = rstd;
-    FN_TRY(launch_fused_backward(L));
+    FN_TRY(launch_fused_transposed(L));
   }
   return FNORM_OK;
 }
@@ -413,6 +441,20 @@ fnorm_status_t fnorm_add_rownorm(const fnorm_bf16* X, const fnorm_bf16* R, fnorm
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
   return launch_rownorm(X, R, Y, static_cast<int>(M), static_cast<int>(N), norm == FNORM_LAYERNORM, gamma, beta,
                         eps, mean_out, rstd_out, static_cast<cudaStream_t>(stream));
+}
+
+fnorm_status_t fnorm_rmsnorm_backward(const fnorm_bf16* dY, const fnorm_bf16* X, const float* rstd, fnorm_bf16* dX,
+                                     int64_t M, int64_t N, void* stream) {
+  clear_error();
+  if (M < 0 || M > kMaxDim) return bad("M must be in [0, 2^31)");
+  if (N < 8 || N % 8 != 0 || N > 16384) return bad("N must be a multiple of 8 in [8, 16384]");
+  if (M == 0) return FNORM_OK;
+  FN_TRY(check_ptr(dY, "dY", 16, false));
+  FN_TRY(check_ptr(X, "X", 16, false));
+  FN_TRY(check_ptr(rstd, "rstd", 4, false));
+  FN_TRY(check_ptr(dX, "dX", 16, false));
+  return launch_rmsnorm_backward(dY, X, rstd, dX, static_cast<int>(M), static_cast<int>(N),
+                                 static_cast<cudaStream_t>(stream));
 }
 
 fnorm_status_t fnorm_check_status(void* stream) {

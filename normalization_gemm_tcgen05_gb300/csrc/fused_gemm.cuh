@@ -67,8 +67,7 @@ enum : int {
   // backward of the Lazy Pre-RMSNorm GEMM
   MODE_BT = 512,      // B operand K-major: read from a row-major [N, K] array (B^T of a [K, N] matrix)
   MODE_AT = 1024,     // A operand MN-major: read from a row-major [K, M] array (A^T of an [M, K] matrix)
-  MODE_ASCALE = 2048, // the norm warps scale each staged A row (a contraction index) by a factor
-  MODE_DGRAD = 4096,  // RMSNorm backward: norm warps take row dots of A with Y, epilogue combines with X
+  MODE_DGRAD = 4096,  // RMSNorm backward epilogue: y = u + c[m] * X[m, n]
 };
 
 struct FusedParams {
@@ -85,7 +84,7 @@ struct FusedParams {
   const float* colsum;        // [N] column sums of the (gamma-folded) B (MODE_PRE_LN)
   const float* bias;          // [N] beta @ B, or NULL (MODE_AFF)
   const __nv_bfloat16* R;     // [M, N] residual (MODE_RES)
-  const float* rowscale;      // MODE_DGRAD: rstd [M] of the forward rows; MODE_ASCALE: [K] factors
+  const float* rowcoef;       // MODE_DGRAD: [M] coefficients c of the forward rows
   const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows combined in the epilogue
   uint32_t* status;
   unsigned long long wait_limit_ns;
@@ -100,11 +99,10 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // Shared-memory control block.  Arrays a mode does not use shrink to one
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff), so each kernel carries only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int NRDY>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
-  uint64_t ready[NRDY];  // MODE_ASCALE: the staged A tile has been scaled
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t ss_full[2];
@@ -148,12 +146,11 @@ struct KCfg {
   static constexpr bool RES = (MODE & MODE_RES) != 0;
   static constexpr bool BT = (MODE & MODE_BT) != 0;
   static constexpr bool AT = (MODE & MODE_AT) != 0;
-  static constexpr bool ASCALE = (MODE & MODE_ASCALE) != 0;
   static constexpr bool DGRAD = (MODE & MODE_DGRAD) != 0;
   // the spill layout's in-place normalisation runs in its own warps (10-13)
   // unless those warps compute the Lazy Pre-Norm sums of squares
   static constexpr bool NORMW = SPILL && !PRE;
-  static constexpr bool AUXW = PRE || NORMW || ASCALE;  // warps 10-13 present
+  static constexpr bool AUXW = PRE || NORMW;  // warps 10-13 present
   static constexpr int HALF = BN / 2;          // columns per epilogue half
   static constexpr int NCH = HALF / 32;        // 32-column subtiles per half
   // 32-column subtiles loaded from TMEM per wait: the whole half when the
@@ -170,18 +167,15 @@ struct KCfg {
   // resident B: up to 128 KB, i.e. KB_MAX k-blocks of [64 x BN]
   static constexpr int KB_MAX = BRES ? (int)(131072u / B_BYTES) : 0;
   static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
-  // a stage: A tile, B tile, and for the backward's row dots a second
-  // [BM x BK] tile (Y) beside A
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES) + (DGRAD ? A_BYTES : 0u);
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES);
   static constexpr int SSN = PRE ? 128 : 1, SS1N = PRE_LN ? 128 : 1, NSN = SPILL ? 128 : 1;
   // norm warps: 4 (one row per thread), or 8 for the pre-LayerNorm, whose
-  // shifted sums cost more per element, and for the backward's row dots and
-  // A-row scaling: two parts take half of each row's 16-byte chunks each
-  static constexpr int NPART = (PRE_LN || ASCALE || DGRAD) ? 2 : 1;
+  // shifted sums cost more per element: two parts take half of each row's
+  // 16-byte chunks each
+  static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
-  static constexpr int NRDY = ASCALE ? kMaxStages : 1;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, NRDY>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
   // that buys a pipeline stage below 4
   static constexpr int stages_with(int bufs) {
@@ -202,10 +196,10 @@ struct KCfg {
   static_assert(!(PRE_LN || AFF) || (PRE && !POST), "the folded-affine pre-norm serves the pre-norm GEMM alone");
   static_assert(!PRE_LN || AFF, "the pre-LayerNorm needs its column sums");
   static_assert(!RES || (POST && !PRE), "the residual serves the post-norm");
-  static_assert(!(BT || AT || ASCALE || DGRAD) || (!POST && !BRES && !AFF && !RES),
+  static_assert(!(BT || AT || DGRAD) || (!POST && !BRES && !AFF && !RES),
                 "backward operand layouts serve the plain and lazy GEMMs");
-  static_assert(!DGRAD || (PRE && BT && !AT), "the dgrad: lazy row scalar, B^T operand");
-  static_assert(!ASCALE || (AT && !PRE), "the A-row scaling acts on an A^T operand");
+  static_assert(!DGRAD || (BT && !AT && !PRE), "the dgrad: B^T operand, per-row coefficients from memory");
+  static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
 };
 
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
@@ -408,15 +402,14 @@ __device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
-                      const FusedParams p) {
+                      const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
   constexpr int BK = Cfg::BK, BN = Cfg::BN, STAGES = Cfg::STAGES, HALF = Cfg::HALF, NCH = Cfg::NCH;
   constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER, SPILL = Cfg::SPILL;
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
-  constexpr bool BT = Cfg::BT, AT = Cfg::AT, ASCALE = Cfg::ASCALE, DGRAD = Cfg::DGRAD;
+  constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::NRDY>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -448,9 +441,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&aux->full[s]), 1);
-      if (ASCALE) mbar_init(smem_u32(&aux->ready[s]), 4 * Cfg::NPART);
-      // the MMA's commit, and for the lazy pre-norm the norm warps' reads;
-      // with the A-row scaling the MMA's commit alone (it ran after them)
+      // the MMA's commit, and for the lazy pre-norm the norm warps' reads
       mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 * Cfg::NPART : 0));
     }
     for (int b = 0; b < 2; ++b) {
@@ -473,7 +464,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    if (DGRAD) prefetch_tmap(&tmY);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&aux->tmem_base), Cfg::TMEM_COLS);
@@ -532,8 +522,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
               }
             }
-            // the backward's row dots: the Y tile matching A, beside B
-            if (DGRAD) tma_load_2d(sa + A_BYTES + Cfg::B_BYTES, &tmY, kb * BK, m0, full);
             filled |= 1u << stage;
             fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) {
@@ -569,9 +557,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * BN);
           for (int kb = 0; kb < num_kb; ++kb) {
-            // with the A-row scaling, the norm warps hand the stage over once
-            // they have scaled it
-            if (!mbar_wait(wc, smem_u32(ASCALE ? &aux->ready[stage] : &aux->full[stage]), phase, kSiteMma)) {
+            if (!mbar_wait(wc, smem_u32(&aux->full[stage]), phase, kSiteMma)) {
               ok = false;
               break;
             }
@@ -750,6 +736,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int c0h = n0 + h * HALF;                      // first column of this half
         const int buf = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        // dgrad: this half's X values, loaded while the tile's MMAs run
+        uint4 xv[DGRAD ? NCH : 1][4];
+        if (DGRAD) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              const int col = c0h + c * 32 + g8 * 8;
+              xv[c][g8] = make_uint4(0, 0, 0, 0);
+              if (m0 + row < M && col < N)
+                xv[c][g8] = __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(m0 + row) * N + col));
+            }
+        }
         if (!mbar_wait_warp(wc, smem_u32(&aux->acc_full[buf]), aph, kSiteEpilogue)) {
           ok = false;
           break;
@@ -777,17 +776,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             pre_mean = aux->ssk[sb][row] + s1 / kf;
             const float var = fmaxf(ss / kf - (s1 / kf) * (s1 / kf), 0.0f);
             pre = rsqrtf(var + p.pre_eps);
-          } else if (DGRAD) {
-            // RMSNorm backward: dA = rstd * (dC @ B^T) - rstd^2 * (dC . Y) / N * X,
-            // rstd of the forward row, (dC . Y) the norm warps' row dot
-            const int mr = m0 + row;
-            pre = mr < M ? __ldg(p.rowscale + mr) : 0.0f;
-            pre_mean = -pre * pre * ss / static_cast<float>(N);
           } else {
             pre = rsqrtf(ss / kf + p.pre_eps);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&aux->ss_empty[sb]));
+        }
+        if (DGRAD) {
+          // RMSNorm backward: dA = (rstd * dC) @ B^T + c * X, c = -rstd^2 (dC . C) / N
+          const int mr = m0 + row;
+          pre_mean = mr < M ? __ldg(p.rowcoef + mr) : 0.0f;
         }
         const int nvh = min(max(N - c0h, 0), HALF);  // valid columns of this half
 
@@ -953,19 +951,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
         for (int cb = 0; cb < NBATCH; ++cb) {
           if (c0h + cb * LDB * 32 >= N) break;
-          uint4 xv[DGRAD ? LDB : 1][4];
-          if (DGRAD) {
-            // this batch's X values, loaded while the accumulator is read
-#pragma unroll
-            for (int b = 0; b < LDB; ++b)
-#pragma unroll
-              for (int g8 = 0; g8 < 4; ++g8) {
-                const int col = c0h + (cb * LDB + b) * 32 + g8 * 8;
-                xv[b][g8] = make_uint4(0, 0, 0, 0);
-                if (m0 + row < M && col < N)
-                  xv[b][g8] = __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(m0 + row) * N + col));
-              }
-          }
           if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
 #pragma unroll
           for (int b = 0; b < LDB; ++b) {
@@ -978,16 +963,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f, &aux->gam[h * HALF + c * 32],
                           &aux->bet[h * HALF + c * 32], w);
             } else if (DGRAD) {
-              // y = u * rstd + c * x, c = -rstd^2 (dC . Y) / N
-              const uint64_t aa = f2(pre, pre), cc = f2(pre_mean, pre_mean);
+              // y = u + c * x
+              const uint64_t cc = f2(pre_mean, pre_mean);
 #pragma unroll
               for (int g8 = 0; g8 < 4; ++g8) {
-                const uint32_t xw[4] = {xv[b][g8].x, xv[b][g8].y, xv[b][g8].z, xv[b][g8].w};
+                const uint32_t xw[4] = {xv[c][g8].x, xv[c][g8].y, xv[c][g8].z, xv[c][g8].w};
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                   const int jj = g8 * 8 + 2 * hh;
-                  w[jj >> 1] = pack_bf16x2_f2(
-                      f2_fma(f2u(r[b][jj], r[b][jj + 1]), aa, f2_mul(f2(bf16_lo(xw[hh]), bf16_hi(xw[hh])), cc)));
+                  w[jj >> 1] = pack_bf16x2_f2(f2_fma(f2(bf16_lo(xw[hh]), bf16_hi(xw[hh])), cc, f2u(r[b][jj], r[b][jj + 1])));
                 }
               }
             } else if (AFF) {
@@ -1043,54 +1027,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&aux->nstat_empty[b]));
       for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
     }
-  } else if (ASCALE) {
-    // ============ norm warps: rebuild the normalised rows of an A^T tile ============
-    // Each stage holds two MN-major chunks of [64 contraction rows x 128 bytes]
-    // (128-byte swizzle).  Contraction row j is a row of the [K, M] source, so
-    // the whole 256-byte row j scales by rowscale[k0 + j]; the scaled values are
-    // rounded to bf16 in place, made visible to the tensor core, and the stage
-    // handed to the MMA through ready[stage].
-    constexpr int NT = 128 * Cfg::NPART;          // norm threads
-    constexpr int PIECES = 16;                     // 16-byte pieces per contraction row
-    constexpr int PPT = BK * PIECES / NT;          // pieces per thread and stage
-    const int t = static_cast<int>(threadIdx.x) - 32 * (2 + kEpiWarps);
-    const int j = t / (PIECES / PPT);              // contraction row of the stage
-    const int p0 = (t % (PIECES / PPT)) * PPT;     // first piece of this thread
-    uint32_t stage = 0, phase = 0;
-    bool ok = true;
-    for (int tt = cid; tt < total && ok; tt += ncl) {
-      for (int s2 = 0; s2 < S && ok; ++s2) {
-        for (int kb = 0; kb < num_kb; ++kb) {
-          const int kr = kb * BK + j;
-          const float f = kr < K ? __ldg(p.rowscale + kr) : 0.0f;  // issued before the wait
-          if (!mbar_wait_warp(wc, smem_u32(&aux->full[stage]), phase, kSiteNorm)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = smem + stage * STAGE_BYTES;
-          const uint64_t ff = f2(f, f);
-#pragma unroll
-          for (int q = 0; q < PPT; ++q) {
-            const int piece = p0 + q;
-            const int lp = piece & 7;  // logical 16-byte index inside the 128-byte row
-            uint4* ptr = reinterpret_cast<uint4*>(st + (piece >> 3) * (BK * 128) + j * 128 + ((lp ^ (j & 7)) << 4));
-            uint4 v = *ptr;
-            v.x = pack_bf16x2_f2(f2_mul(f2(bf16_lo(v.x), bf16_hi(v.x)), ff));
-            v.y = pack_bf16x2_f2(f2_mul(f2(bf16_lo(v.y), bf16_hi(v.y)), ff));
-            v.z = pack_bf16x2_f2(f2_mul(f2(bf16_lo(v.z), bf16_hi(v.z)), ff));
-            v.w = pack_bf16x2_f2(f2_mul(f2(bf16_lo(v.w), bf16_hi(v.w)), ff));
-            *ptr = v;
-          }
-          fence_proxy_async_smem();  // the generic-proxy writes, before the MMA reads them
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&aux->ready[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
   } else if (PRE) {
     // ======================= norm warps (Lazy Pre-Norm) =======================
     // 4 x NPART warps: warp nw takes row (nw % 4) * 32 + lane and part nw / 4
@@ -1133,17 +1069,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int ch = part * CPP + c;
             const uint4 v = *reinterpret_cast<const uint4*>(arow + ((ch ^ swz) << 4));
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint4 yv = make_uint4(0, 0, 0, 0);
-            if (DGRAD)  // the Y tile beside B has A's layout
-              yv = *reinterpret_cast<const uint4*>(arow + A_BYTES + Cfg::B_BYTES + ((ch ^ swz) << 4));
-            const uint32_t wy[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const uint64_t x = f2(bf16_lo(wv[e]), bf16_hi(wv[e]));
-              if (DGRAD) {
-                // row dot of the staged A (dC) with Y (the forward output)
-                acc[e & 1] = f2_fma(x, f2(bf16_lo(wy[e]), bf16_hi(wy[e])), acc[e & 1]);
-              } else if (PRE_LN) {
+              if (PRE_LN) {
                 // zero-filled K tail: a = 0 contributes (0 - shift), removed below
                 const uint64_t d = f2_sub(x, sh2);
                 lsum[e & 1] = f2_add(lsum[e & 1], d);

@@ -30,9 +30,8 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
 
   // A [M,K] in [128 x 64] boxes (A^T source [K,M]: [64 x 64] boxes); B [K,N]
   // in [64 x 64] boxes, MN-major for the MMA (B^T source [N,K]: [BN x 64]
-  // boxes, K-major); C [M,N] in [32 x 32] store boxes (64-byte rows); Y [M,K]
-  // like A
-  CUtensorMap ta, tb, tc, ty;
+  // boxes, K-major); C [M,N] in [32 x 32] store boxes (64-byte rows)
+  CUtensorMap ta, tb, tc;
   if (Cfg::AT)
     st = encode_tmap_bf16_2d(&ta, L.A, (uint64_t)L.M, (uint64_t)L.K, (uint64_t)L.M * 2, 64, Cfg::BK,
                              CU_TENSOR_MAP_SWIZZLE_128B);
@@ -47,13 +46,6 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     st = encode_tmap_bf16_2d(&tb, L.B, (uint64_t)L.N, (uint64_t)L.K, (uint64_t)L.N * 2, 64, Cfg::BK,
                              CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FNORM_OK) return st;
-  if (Cfg::DGRAD) {
-    st = encode_tmap_bf16_2d(&ty, L.Y, (uint64_t)L.K, (uint64_t)L.M, (uint64_t)L.K * 2, Cfg::BK, Cfg::BM,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != FNORM_OK) return st;
-  } else {
-    ty = ta;  // unused
-  }
   st = encode_tmap_bf16_2d(&tc, L.C, (uint64_t)L.N, (uint64_t)L.M, (uint64_t)L.N * 2, 32, 32,
                            CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != FNORM_OK) return st;
@@ -75,7 +67,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.colsum = L.colsum;
   p.bias = L.bias;
   p.R = static_cast<const __nv_bfloat16*>(L.R);
-  p.rowscale = L.rowscale;
+  p.rowcoef = L.rowcoef;
   p.X = static_cast<const __nv_bfloat16*>(L.X);
   p.status = dev.status;
   p.wait_limit_ns = wait_limit_ns();
@@ -133,7 +125,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     const long long grid = total < dev.num_sms ? total : dev.num_sms;
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, ty, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
   return FNORM_OK;
 }

@@ -59,9 +59,8 @@ struct FusedLaunch {
   const void* R;        // residual [M, N] added before the post-norm, or NULL
   // backward: A may be an A^T source ([K, M] row-major) and B a B^T source
   // ([N, K] row-major), as the mode says
-  const void* Y;          // dgrad: [M, K] forward output, row-dotted with A (= dC)
   const void* X;          // dgrad: [M, N] forward input combined in the epilogue
-  const float* rowscale;  // dgrad: forward rstd [M]; A-row scaling: [K] factors
+  const float* rowcoef;   // dgrad: [M] coefficients c = -rstd^2 (dC . C) / K
   cudaStream_t stream;
 };
 
@@ -82,6 +81,14 @@ fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const voi
 fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int N, bool layernorm, const void* gamma,
                               const void* beta, float eps, float* mean_out, float* rstd_out,
                               cudaStream_t stream);
+
+// backward row pass: dCs = bf16(rstd * dC) and coef[m] = -rstd^2 (dC . C)[m] / K
+fnorm_status_t launch_backward_rows(const void* dC, const void* C, const float* rstd, void* dCs, float* coef, int M,
+                                    int N, int K, cudaStream_t stream);
+// dX = rstd * dY - rstd^3 * X * sum(dY * X) / N per row (RMSNorm backward, no affine)
+fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const float* rstd, void* dX, int M, int N,
+                                       cudaStream_t stream);
+fnorm_status_t launch_fused_transposed(const FusedLaunch& L);   // plain GEMM with A^T and/or B^T operands
 
 fnorm_status_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 

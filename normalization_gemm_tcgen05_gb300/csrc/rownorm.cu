@@ -1,5 +1,6 @@
-// rownorm.cu — standalone row RMSNorm / LayerNorm, optionally of X + R (the
-// unfused comparison kernels).  [ATB] sections 1.1 (LayerNorm) and 1.2
+// rownorm.cu — standalone row RMSNorm / LayerNorm, optionally of X + R, and
+// the RMSNorm backward (the unfused comparison kernels); the fused backward's
+// row pass.  [ATB] sections 1.1 (LayerNorm) and 1.2
 // (RMSNorm); [FNF-ru] FAQ: a standalone norm reads and writes the whole tensor
 // and stays memory-bound; [FNF-ru] "FlashNormAttention" for the residual add.
 //
@@ -143,6 +144,99 @@ __global__ void __launch_bounds__(1024) rownorm_kernel(const __nv_bfloat16* __re
   }
 }
 
+// Standalone RMSNorm backward (no affine), the unfused comparison of the
+// fused backward: dX = rstd * dY - rstd^3 * X * sum_n(dY * X) / N per row, with
+// the forward's rstd given.  Same row layout as rownorm_kernel: a group of tpr
+// threads holds the row's dY and X in registers.
+__global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                           const __nv_bfloat16* __restrict__ X,
+                                                           const float* __restrict__ rstd_in,
+                                                           __nv_bfloat16* __restrict__ dX, int M, int N, int tpr) {
+  __shared__ float red[32];
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int rpb = blockDim.x / tpr;
+  const int row = blockIdx.x * rpb + static_cast<int>(threadIdx.x) / tpr;
+  const int t = static_cast<int>(threadIdx.x) % tpr;
+  const int nvec = N >> 3;
+  const bool row_ok = row < M;
+  const size_t off = static_cast<size_t>(row_ok ? row : 0) * N;
+  uint32_t g[kVPT * 4], x[kVPT * 4];  // bf16 pairs, widened when used
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int vi = t + i * tpr;
+    uint4 u = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
+    if (row_ok && vi < nvec) {
+      u = ld_stream(dY + off + vi * 8);
+      v = ld_stream(X + off + vi * 8);
+    }
+    g[i * 4] = u.x; g[i * 4 + 1] = u.y; g[i * 4 + 2] = u.z; g[i * 4 + 3] = u.w;
+    x[i * 4] = v.x; x[i * 4 + 1] = v.y; x[i * 4 + 2] = v.z; x[i * 4 + 3] = v.w;
+  }
+  float q = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kVPT * 4; ++j) {
+    q = fmaf(bf16_lo(g[j]), bf16_lo(x[j]), q);
+    q = fmaf(bf16_hi(g[j]), bf16_hi(x[j]), q);
+  }
+  const float dot = group_sum(q, tpr, red);
+  if (!row_ok) return;
+  const float r = rstd_in[row];
+  const float c = -r * r * r * dot / static_cast<float>(N);
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int vi = t + i * tpr;
+    if (vi >= nvec) break;
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t gg = g[i * 4 + h], xx = x[i * 4 + h];
+      w[h] = pack_bf16x2(fmaf(bf16_lo(gg), r, c * bf16_lo(xx)), fmaf(bf16_hi(gg), r, c * bf16_hi(xx)));
+    }
+    *reinterpret_cast<uint4*>(dX + off + vi * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// The backward's row pass over dC and the forward output C, one read of each:
+//   dCs[m,n] = bf16(rstd[m] * dC[m,n])       (the rebuilt scale, on dC's side)
+//   coef[m]  = -rstd[m]^2 * sum_n dC[m,n] C[m,n] / K
+// A group of tpr threads per row, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) backward_rows_kernel(const __nv_bfloat16* __restrict__ dC,
+                                                            const __nv_bfloat16* __restrict__ C,
+                                                            const float* __restrict__ rstd,
+                                                            __nv_bfloat16* __restrict__ dCs, float* __restrict__ coef,
+                                                            int M, int N, int K, int tpr) {
+  __shared__ float red[32];
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int rpb = blockDim.x / tpr;
+  const int row = blockIdx.x * rpb + static_cast<int>(threadIdx.x) / tpr;
+  const int t = static_cast<int>(threadIdx.x) % tpr;
+  const int nvec = N >> 3;
+  const bool row_ok = row < M;
+  const size_t off = static_cast<size_t>(row_ok ? row : 0) * N;
+  const float r = row_ok ? rstd[row] : 0.0f;
+  float q = 0.0f;
+  for (int vi = t; vi < nvec; vi += tpr) {
+    uint4 u = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
+    if (row_ok) {
+      u = ld_stream(dC + off + vi * 8);
+      v = ld_stream(C + off + vi * 8);
+    }
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w}, vw[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      q = fmaf(bf16_lo(uw[h]), bf16_lo(vw[h]), q);
+      q = fmaf(bf16_hi(uw[h]), bf16_hi(vw[h]), q);
+      o[h] = pack_bf16x2(bf16_lo(uw[h]) * r, bf16_hi(uw[h]) * r);
+    }
+    if (row_ok) *reinterpret_cast<uint4*>(dCs + off + vi * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  const float s = group_sum(q, tpr, red);
+  if (row_ok && t == 0) coef[row] = -r * r * s / static_cast<float>(K);
+}
+
 }  // namespace
 
 fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int N, bool layernorm, const void* gamma,
@@ -183,6 +277,70 @@ fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int 
                         : (r != nullptr ? rownorm_kernel<false, true> : rownorm_kernel<false, false>);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, r, y, M, N, tpr, g, b, eps, mean_out, rstd_out);
   if (e != cudaSuccess) return cuda_fail(e, "row norm launch");
+  return FNORM_OK;
+}
+
+fnorm_status_t launch_backward_rows(const void* dC, const void* C, const float* rstd, void* dCs, float* coef, int M,
+                                    int N, int K, cudaStream_t stream) {
+  DeviceInfo dev;
+  fnorm_status_t st = current_device(&dev);
+  if (st != FNORM_OK) return st;
+  // a group of up to 256 threads per row, about four 16-byte vectors each
+  const int nvec = N / 8;
+  int tpr = 1;
+  while (tpr < 256 && tpr * 4 < nvec) tpr <<= 1;
+  const int block = 256;
+  const int rpb = block / tpr;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)((M + rpb - 1) / rpb), 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, backward_rows_kernel, static_cast<const __nv_bfloat16*>(dC),
+                                           static_cast<const __nv_bfloat16*>(C), rstd,
+                                           static_cast<__nv_bfloat16*>(dCs), coef, M, N, K, tpr);
+  if (e != cudaSuccess) return cuda_fail(e, "backward row pass launch");
+  return FNORM_OK;
+}
+
+fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const float* rstd, void* dX, int M, int N,
+                                       cudaStream_t stream) {
+  DeviceInfo dev;
+  fnorm_status_t st = current_device(&dev);
+  if (st != FNORM_OK) return st;
+  const int nvec = N / 8;
+  const int need = (nvec + kVPT - 1) / kVPT;
+  int tpr = 1;
+  while (tpr < need) tpr <<= 1;
+  if (tpr > 512) {  // two row slices in registers: 512 threads a row at most
+    set_error("rows of %d elements exceed the RMSNorm backward kernel's %d", N, 512 * kVPT * 8);
+    return FNORM_ERR_UNSUPPORTED;
+  }
+  const int block = tpr > 256 ? tpr : 256;
+  const int rpb = block / tpr;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)((M + rpb - 1) / rpb), 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, rmsnorm_bwd_kernel, static_cast<const __nv_bfloat16*>(dY),
+                                           static_cast<const __nv_bfloat16*>(X), rstd,
+                                           static_cast<__nv_bfloat16*>(dX), M, N, tpr);
+  if (e != cudaSuccess) return cuda_fail(e, "RMSNorm backward launch");
   return FNORM_OK;
 }
 

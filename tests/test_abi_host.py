@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = _header_functions()
     for required in ("fnorm_gemm", "fnorm_lazy_prenorm_gemm", "fnorm_gemm_postnorm", "fnorm_rmsnorm",
                      "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
-                     "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm"):
+                     "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm", "fnorm_lazy_prenorm_gemm_backward",
+                     "fnorm_gemm_ex", "fnorm_rmsnorm_backward"):
         assert required in names
 
 
@@ -129,6 +130,28 @@ def test_prenorm_gemm_argument_rules(L):
     assert f(FAKE, FAKE, FAKE, 128, 64, 64, 0, None, ctypes.c_void_p(0x10008), 1e-5, None, None, None) == 1
     # M == 0 is an empty call that touches nothing
     assert f(None, None, None, 0, 64, 64, 1, FAKE, None, 1e-5, None, None, None) == 0
+
+
+def test_backward_argument_rules(L):
+    f = L.fnorm_lazy_prenorm_gemm_backward
+    W = ctypes.c_void_p(0x800000)  # workspace, disjoint from FAKE
+    # neither gradient asked for; workspaces missing; misaligned rstd; dCs over dC
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, W, W, 128, 64, 64, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, W, 128, 64, 64, None) == 1
+    assert b"dCs" in L.fnorm_last_error()
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, W, None, 128, 64, 64, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, ctypes.c_void_p(0x10002), None, FAKE, W, W, 128, 64, 64, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, W, 128, 64, 64, None) == 1
+    assert b"overlap" in L.fnorm_last_error()
+    # dB reads A^T: M must be a multiple of 8; bad sizes
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, W, W, 100, 64, 64, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, W, W, 128, 60, 64, None) == 1
+    g = L.fnorm_gemm_ex
+    assert g(FAKE, FAKE, FAKE, 100, 64, 64, 1, 0, None) == 1      # A^T needs M % 8 == 0
+    assert g(FAKE, FAKE, FAKE, 128, 64, 64, 2, 0, None) == 1
+    assert g(FAKE, FAKE, FAKE, 128, 64, 64, 0, -1, None) == 1
+    assert L.fnorm_rmsnorm_backward(FAKE, FAKE, FAKE, FAKE, 16, 32768, None) == 1
+    assert L.fnorm_rmsnorm_backward(FAKE, FAKE, None, FAKE, 16, 64, None) == 1
 
 
 def test_norm_rejects_bad_sizes(L):

@@ -34,8 +34,8 @@ def _run(w, d, A=None):
     return dA, dB, rA, rB
 
 
-SHAPES = [(256, 128, 512), (200, 64, 72), (333, 256, 1000), (128, 520, 256), (1, 8, 8), (300, 192, 4096),
-          (1000, 1024, 128), (129, 4096, 64)]
+SHAPES = [(256, 128, 512), (200, 64, 72), (336, 256, 1000), (128, 520, 256), (8, 8, 8), (304, 192, 4096),
+          (1000, 1024, 128), (136, 4096, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES, ids=lambda v: str(v))
@@ -50,7 +50,7 @@ def test_prenorm_backward_special_rows():
     # a zero row has no gradient through the norm (dA row = rstd * dA_hat with
     # rstd = 1/sqrt(eps)); a constant row and an outlier row stress the
     # cancellation in the RMSNorm backward
-    w, d = _case(300, 128, 512, seed=3)
+    w, d = _case(304, 128, 512, seed=3)
     A = d["A"].clone()
     A[4] = 0
     A[5] = 1.5
@@ -71,6 +71,17 @@ def test_prenorm_backward_one_side():
     assert dA2 is None
     dA3, dB3 = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd)
     assert torch.equal(dA, dA3) and torch.equal(dB2, dB3)
+
+
+def test_prenorm_backward_dA_any_M():
+    # dA alone has no M % 8 rule (only dB reads A^T); M = 333 and M = 1
+    for M in (333, 1):
+        w, d = _case(M, 128, 256, seed=M)
+        Ad, Bd, dCd = d["A"].to(DEV), d["B"].to(DEV), d["dC"].to(DEV)
+        C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+        dA, _ = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd, need_dB=False)
+        rA, _, _ = oracle.lazy_prenorm_gemm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(d["dC"]), w.eps)
+        assert_out_close(dA, rA, f"dA M={M}")
 
 
 def test_prenorm_backward_scale_invariance():
@@ -110,3 +121,45 @@ def test_prenorm_backward_full_size():
     _, r_all = oracle.rmsnorm(A64, None, None, w.eps)
     ref = (A64[:, cols] * r_all[:, None]).T @ dC64
     assert_out_close(dB[torch.from_numpy(cols).to(DEV)], ref, "dB sampled rows")
+
+
+# ----------------------------------------------------------------------------
+# the unfused comparison's pieces: transposed-operand GEMM, standalone RMSNorm backward
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(256, 128, 512), (200, 72, 136), (128, 520, 64), (1000, 256, 1000)],
+                         ids=lambda v: str(v))
+def test_gemm_transposed(M, N, K, ta, tb):
+    rng = np.random.default_rng(M + N + K + 2 * ta + tb)
+    A = torch.from_numpy(rng.standard_normal((K, M) if ta else (M, K), dtype=np.float32)).to(torch.bfloat16)
+    B = torch.from_numpy((rng.standard_normal((N, K) if tb else (K, N), dtype=np.float32)
+                          / np.float32(np.sqrt(K)))).to(torch.bfloat16)
+    C = fn.gemm_ex(A.to(DEV), B.to(DEV), trans_a=bool(ta), trans_b=bool(tb))
+    a64, b64 = to_f64(A), to_f64(B)
+    ref = oracle.gemm(a64.T if ta else a64, b64.T if tb else b64)
+    assert_out_close(C, ref, f"gemm_ex ta={ta} tb={tb} {M}x{N}x{K}")
+
+
+def test_gemm_transposed_identity_exact():
+    # op(A) @ I reproduces op(A) exactly (each product is exact in fp32)
+    A = torch.randn(192, 256, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    eye = torch.eye(192, dtype=torch.bfloat16)
+    C = fn.gemm_ex(A.to(DEV), eye.to(DEV), trans_a=True)
+    assert torch.equal(C.cpu(), A.t().contiguous())
+    # A @ (I given as its own transpose) = A
+    C2 = fn.gemm_ex(A.to(DEV), torch.eye(256, dtype=torch.bfloat16, device=DEV), trans_b=True)
+    assert torch.equal(C2.cpu(), A)
+
+
+@pytest.mark.parametrize("M,N", [(300, 64), (257, 1000), (64, 4096), (17, 8192)])
+def test_rmsnorm_backward_standalone(M, N):
+    rng = np.random.default_rng(M * N)
+    X = torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32) * 3).to(torch.bfloat16)
+    dY = torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32)).to(torch.bfloat16)
+    eps = 1e-6
+    _, r = oracle.rmsnorm(to_f64(X), None, None, eps)
+    rstd = torch.from_numpy(r.astype(np.float32)).to(DEV)
+    dX = fn.rmsnorm_backward(dY.to(DEV), X.to(DEV), rstd)
+    # the oracle's backward with B = I: dA_hat = dC, the RMSNorm backward itself
+    ref, _, _ = oracle.lazy_prenorm_gemm_backward(to_f64(X), np.eye(N), to_f64(dY), eps)
+    assert_out_close(dX, ref, f"rmsnorm_backward {M}x{N}")
