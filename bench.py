@@ -59,7 +59,7 @@ GROUPS = {
     "cfg5": ["cfg5"],
     "res": ["res_ln_n128", "res_rms_n1024"],
     "preaff": ["preln_affine", "prerms_gamma"],
-    "bwd": ["prenorm_bwd"],
+    "bwd": ["prenorm_bwd", "postnorm_bwd"],
 }
 GROUP_TEXT = {
     "cfg1": "Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128], eps 1e-6",
@@ -72,7 +72,8 @@ GROUP_TEXT = {
            "RMSNorm(gamma) A[16384,2048] @ B[2048,1024] + R",
     "preaff": "pre-norm with affine folded into B + GEMM, A[8192,4096] @ B[4096,4096]: LayerNorm(gamma, beta), "
               "RMSNorm(gamma)",
-    "bwd": "backward (dA, dB) of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], dC[8192,4096]",
+    "bwd": "backward of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], and of GEMM + post-LayerNorm, "
+           "A[16384,2048] @ B[2048,1024]",
 }
 KERNEL_SOURCES = ["fused_gemm.cuh", "ptx.cuh", "fused_launch.cuh", "rownorm.cu"]
 
@@ -237,6 +238,12 @@ class Case:
             self.G = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
             self.work = [(torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device),
                           torch.empty(w.M, dtype=torch.float32, device=device)) for _ in range(self.R)]
+        if w.kind == "postnorm_backward":
+            fwd = [fn.gemm_postnorm(Aj, Bj, w.norm, self.g, self.b, w.eps, return_stats=True)
+                   for Aj, Bj in zip(self.A, self.B)]
+            self.Cf = [c for c, _ in fwd]
+            self.rstd = [st["rstd"] for _, st in fwd]
+            self.dC = [d["dC"].to(device) for _ in range(self.R)]
         self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         self.Y = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         nst = 3
@@ -260,6 +267,9 @@ class Case:
         elif w.kind == "prenorm_backward":
             fn.lazy_prenorm_gemm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j],
                                           dA=self.dA[j], dB=self.dB[j], work=self.work[j])
+        elif w.kind == "postnorm_backward":
+            fn.gemm_postnorm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j], w.norm, self.g,
+                                      self.b)
         elif w.residual:
             fn.gemm_add_postnorm(self.A[j], self.B[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.C[j])
         elif w.kind == "postnorm":
@@ -271,6 +281,10 @@ class Case:
 
     def gemm_only(self, i: int):
         j = i % self.R
+        if self.w.kind == "postnorm_backward":  # the two GEMMs: dH @ B^T, A^T @ dH (dH: dC's shape)
+            self.fn.gemm_ex(self.dC[j], self.B[j], trans_b=True)
+            self.fn.gemm_ex(self.A[j], self.dC[j], trans_a=True)
+            return
         if self.w.kind == "prenorm_backward":  # the two GEMMs of the backward: dC @ B^T, A^T @ dC
             self.fn.gemm_ex(self.dC[j], self.B[j], trans_b=True, out=self.G[j])
             self.fn.gemm_ex(self.A[j], self.dC[j], trans_a=True, out=self.dB[j])
@@ -286,6 +300,11 @@ class Case:
         elif w.kind == "prenorm_affine":
             k = i % self.R
             self._pre_norm(k, self.A[k], self._pre_out(k))
+        elif w.kind == "postnorm_backward":
+            # the norm backward's passes alone (dgamma, dbeta and dH)
+            k = i % self.R
+            fn.gemm_postnorm_backward(self.A[k], self.B[k], self.Cf[k], self.dC[k], self.rstd[k], w.norm, self.g,
+                                      self.b, need=("dgamma", "dbeta"))
         elif w.kind == "prenorm_backward":
             # the normalised A materialised for dB, and the RMSNorm backward for dA
             k = i % self.R
@@ -312,6 +331,10 @@ class Case:
         elif w.kind == "prenorm_affine":
             self._pre_norm(j, self.A[j], self._pre_out(j))
             fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
+        elif w.kind == "postnorm_backward":
+            # the same decomposition: the norm backward's passes, then the GEMMs
+            fn.gemm_postnorm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j], w.norm, self.g,
+                                      self.b)
         elif w.kind == "prenorm_backward":
             fn.rmsnorm(self.A[j], None, w.eps, out=self._pre_out(j))
             fn.gemm_ex(self.dC[j], self.B[j], trans_b=True, out=self.G[j])
@@ -351,6 +374,8 @@ class Case:
         w = self.w
         if w.kind == "prenorm_backward":
             return {"fused": 3, "gemm": 2, "norm": 2}.get(what, 4)
+        if w.kind == "postnorm_backward":
+            return {"fused": 5, "gemm": 2, "norm": 2}.get(what, 5)
         if what == "fused" or what == "gemm":
             return 1
         if what == "norm":
@@ -487,7 +512,7 @@ def run_e2e(cases, K, W, world, device) -> dict:
         hR = None if c.host["R"] is None else c.host["R"].pin_memory()
         hC = torch.empty((c.w.M, c.w.N), dtype=torch.bfloat16).pin_memory()
         bwd = None
-        if c.w.kind == "prenorm_backward":
+        if c.w.kind.endswith("_backward"):
             # the backward's inputs (forward output, rstd, dC) in, dA and dB out
             bwd = (c.Cf[0].cpu().pin_memory(), c.rstd[0].cpu().pin_memory(), c.host["dC"].pin_memory(),
                    torch.empty((c.w.M, c.w.K), dtype=torch.bfloat16).pin_memory(),
@@ -516,10 +541,16 @@ def run_e2e(cases, K, W, world, device) -> dict:
                 c.Cf[0].copy_(hCf, non_blocking=True)
                 c.rstd[0].copy_(hr, non_blocking=True)
                 c.dC[0].copy_(hdC, non_blocking=True)
-                fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
-                                              work=c.work[0])
-                hdA.copy_(c.dA[0], non_blocking=True)
-                hdB.copy_(c.dB[0], non_blocking=True)
+                if w.kind == "prenorm_backward":
+                    fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
+                                                  work=c.work[0])
+                    hdA.copy_(c.dA[0], non_blocking=True)
+                    hdB.copy_(c.dB[0], non_blocking=True)
+                else:
+                    g = fn.gemm_postnorm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], w.norm, c.g, c.b,
+                                                  need=("dA", "dB"))
+                    hdA.copy_(g["dA"], non_blocking=True)
+                    hdB.copy_(g["dB"], non_blocking=True)
                 continue
             if w.kind == "prenorm":
                 fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
@@ -564,6 +595,8 @@ def oracle_step(w: Workload, d: dict, rows: np.ndarray):
         oracle.lazy_prenorm_gemm(A, d["B64"], w.eps)
     elif w.kind == "prenorm_backward":
         oracle.lazy_prenorm_gemm_backward(A, d["B64"], d["dC64"][rows], w.eps)
+    elif w.kind == "postnorm_backward":
+        oracle.gemm_postnorm_backward(A, d["B64"], d["dC64"][rows], w.norm, d["g64"], d["b64"], w.eps)
     elif w.kind == "prenorm_affine":
         oracle.prenorm_affine_gemm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps)
     elif w.residual:

@@ -171,6 +171,37 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
                                                 int64_t N, int64_t K, void* stream);
 
 /*
+ * fnorm_gemm_postnorm_backward — gradients of C = norm(A @ B) * gamma + beta
+ * (fnorm_gemm_postnorm without the pre-norm) given dC = dL/dC.  The forward
+ * never materialised H = A @ B; its normalised rows are rebuilt from the
+ * output, h_hat = (C - beta) / gamma (every gamma must be nonzero), then with
+ * dh = dC * gamma:
+ *   LayerNorm: dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+ *   RMSNorm:   dH = rstd * (dh - h_hat * mean_n(dh * h_hat))
+ *   dgamma = sum_m dC * h_hat;  dbeta = sum_m dC;
+ *   dA = dH @ B^T;  dB = A^T @ dH.
+ *   [TFN] (the backward of a post-norm fused with a GEMM through "fusion
+ *   regrouping"); [ATB] 1.1, 1.2 for the norms differentiated.  One row pass
+ *   (one warp per row) writes dH; a column pass and a fixed-order sum give
+ *   dgamma and dbeta (deterministic); the two GEMMs read dH in place, B^T and
+ *   dH^T through fnorm_gemm_ex.
+ *   A, B: forward inputs; C: [M,N] forward output; dC: [M,N].
+ *   gamma, beta: the forward's [N] bf16 (NULL: 1 and 0).
+ *   rstd: [M] fp32 forward rstd (rstd_out).  The mean is not needed.
+ *   dA [M,K], dB [K,N], dgamma [N] fp32, dbeta [N] fp32: outputs, each NULL
+ *   to skip (dB needs M to be a multiple of 8; with M == 0 dB, dgamma and
+ *   dbeta are zeroed).
+ *   dH: [M,N] bf16 workspace, needed with dA or dB; receives dH.
+ *   part: fp32 workspace of 2 * N * ceil(M / 64) values, needed with dgamma
+ *   or dbeta.
+ */
+fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
+                                           const fnorm_bf16* dC, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                           const fnorm_bf16* beta, const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
+                                           float* dgamma, float* dbeta, fnorm_bf16* dH, float* part, int64_t M,
+                                           int64_t N, int64_t K, void* stream);
+
+/*
  * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual
  * added to the fp32 accumulator in the epilogue, before the post-norm's row
  * statistics.

@@ -34,7 +34,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm",
+    "gemm_postnorm_backward", "lazy_prenorm_gemm_backward", "gemm_postnorm",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
@@ -75,6 +76,8 @@ _SIGNATURES = {
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
     "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
+    "fnorm_gemm_postnorm_backward": (_c_status, [_p, _p, _p, _p, ctypes.c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                                 _i64, _i64, _i64, _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                             _p, _p, _p]),
     "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
@@ -313,6 +316,38 @@ def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Opt
             1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
             _ptr(stats.get("pre_rstd")), _stream(A.device)))
     return (C, stats) if return_stats else C
+
+
+def gemm_postnorm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC: torch.Tensor, rstd: torch.Tensor,
+                           norm="layernorm", gamma: Optional[torch.Tensor] = None,
+                           beta: Optional[torch.Tensor] = None, need=("dA", "dB", "dgamma", "dbeta")) -> dict:
+    """Gradients of C = norm(A @ B) * gamma + beta given dC; C and rstd are the
+    forward's output and row rstd.  Returns a dict with the gradients named in
+    ``need`` (dA, dB bf16; dgamma, dbeta fp32) and "dH"."""
+    M, N, K = _ab(A, B)
+    for t, name in ((C, "C"), (dC, "dC")):
+        _mat(t, name)
+        if tuple(t.shape) != (M, N) or t.device != A.device:
+            raise ValueError(f"{name} must have shape {(M, N)} on {A.device}")
+    if rstd.dtype != torch.float32 or rstd.numel() != M or not rstd.is_contiguous() or rstd.device != A.device:
+        raise ValueError(f"rstd must be a contiguous float32 vector of length {M} on {A.device}")
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    gamma = _vec(gamma, N, "gamma", A.device)
+    beta = _vec(beta, N, "beta", A.device)
+    dev = A.device
+    out = {"dA": torch.empty((M, K), dtype=torch.bfloat16, device=dev) if "dA" in need else None,
+           "dB": torch.empty((K, N), dtype=torch.bfloat16, device=dev) if "dB" in need else None,
+           "dgamma": torch.empty(N, dtype=torch.float32, device=dev) if "dgamma" in need else None,
+           "dbeta": torch.empty(N, dtype=torch.float32, device=dev) if "dbeta" in need else None}
+    out["dH"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    part = torch.empty(2 * N * ((M + 63) // 64), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().fnorm_gemm_postnorm_backward(
+            _ptr(A), _ptr(B), _ptr(C), _ptr(dC), _NORMS[norm], _ptr(gamma), _ptr(beta), _ptr(rstd),
+            _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dgamma"]), _ptr(out["dbeta"]), _ptr(out["dH"]), _ptr(part),
+            M, N, K, _stream(dev)))
+    return out
 
 
 def gemm_add_postnorm(A: torch.Tensor, B: torch.Tensor, R: torch.Tensor, norm="rmsnorm",

@@ -389,6 +389,53 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
   return FNORM_OK;
 }
 
+fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf16* B, const fnorm_bf16* C,
+                                           const fnorm_bf16* dC, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                           const fnorm_bf16* beta, const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
+                                           float* dgamma, float* dbeta, fnorm_bf16* dH, float* part, int64_t M,
+                                           int64_t N, int64_t K, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  if (dA == nullptr && dB == nullptr && dgamma == nullptr && dbeta == nullptr) return bad("no gradient asked for");
+  FN_TRY(check_ptr(dA, "dA", 16, true));
+  FN_TRY(check_ptr(dB, "dB", 16, true));
+  FN_TRY(check_ptr(dgamma, "dgamma", 4, true));
+  FN_TRY(check_ptr(dbeta, "dbeta", 4, true));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool need_dh = dA != nullptr || dB != nullptr;
+  const bool need_cols = dgamma != nullptr || dbeta != nullptr;
+  if (M == 0) {
+    // an empty batch: zero dB, dgamma, dbeta
+    struct Z {
+      void* p;
+      size_t n;
+    } z[3] = {{dB, static_cast<size_t>(K) * N * 2}, {dgamma, static_cast<size_t>(N) * 4},
+              {dbeta, static_cast<size_t>(N) * 4}};
+    for (auto& e : z)
+      if (e.p != nullptr) {
+        cudaError_t err = cudaMemsetAsync(e.p, 0, e.n, st);
+        if (err != cudaSuccess) return cuda_fail(err, "cudaMemsetAsync");
+      }
+    return FNORM_OK;
+  }
+  if (dB != nullptr && M % 8 != 0) return bad("dB needs M to be a multiple of 8 (dH is read transposed)");
+  FN_TRY(check_ptr(A, "A", 16, dB == nullptr));
+  FN_TRY(check_ptr(B, "B", 16, dA == nullptr));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(dC, "dC", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
+  FN_TRY(check_ptr(rstd, "rstd", 4, !need_dh));
+  FN_TRY(check_ptr(dH, "dH", 16, !need_dh));
+  FN_TRY(check_ptr(part, "part", 16, !need_cols));
+  FN_TRY(launch_postnorm_backward_rows(dC, C, gamma, beta, rstd, norm == FNORM_LAYERNORM, need_dh ? dH : nullptr,
+                                       part, dgamma, dbeta, static_cast<int>(M), static_cast<int>(N), st));
+  if (dA != nullptr) FN_TRY(fnorm_gemm_ex(dH, B, dA, M, K, N, 0, 1, stream));   // dH @ B^T
+  if (dB != nullptr) FN_TRY(fnorm_gemm_ex(A, dH, dB, K, N, M, 1, 0, stream));   // A^T @ dH
+  return FNORM_OK;
+}
+
 fnorm_status_t fnorm_rmsnorm(const fnorm_bf16* X, fnorm_bf16* Y, int64_t M, int64_t N, const fnorm_bf16* gamma,
                              float eps, float* rstd_out, void* stream) {
   clear_error();

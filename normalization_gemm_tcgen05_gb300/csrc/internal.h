@@ -85,6 +85,12 @@ fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int 
 // backward row pass: dCs = bf16(rstd * dC) and coef[m] = -rstd^2 (dC . C)[m] / K
 fnorm_status_t launch_backward_rows(const void* dC, const void* C, const float* rstd, void* dCs, float* coef, int M,
                                     int N, int K, cudaStream_t stream);
+// post-norm backward: dH from dC and the forward output (h_hat = (C - beta) /
+// gamma), and dgamma/dbeta through per-64-row partials in part[groups][2][N]
+int postnorm_backward_groups(int M);
+fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, const void* gamma, const void* beta,
+                                             const float* rstd, bool layernorm, void* dH, float* part, float* dgamma,
+                                             float* dbeta, int M, int N, cudaStream_t stream);
 // dX = rstd * dY - rstd^3 * X * sum(dY * X) / N per row (RMSNorm backward, no affine)
 fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const float* rstd, void* dX, int M, int N,
                                        cudaStream_t stream);

@@ -237,6 +237,147 @@ __global__ void __launch_bounds__(256) backward_rows_kernel(const __nv_bfloat16*
   if (row_ok && t == 0) coef[row] = -r * r * s / static_cast<float>(K);
 }
 
+// Post-norm backward.  The forward's normalised rows are rebuilt from its
+// output: h_hat = (C - beta) / gamma (gamma != 0).  With dh = dC * gamma:
+//   LayerNorm: dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+//   RMSNorm:   dH = rstd * (dh - h_hat * mean_n(dh * h_hat))
+//   dgamma = sum_m dC * h_hat,   dbeta = sum_m dC.
+// Row pass: one warp per row, two sweeps over the row (sums, then dH; the
+// second sweep reads from L2), 16-byte loads, any N.
+constexpr int kRowsPerBlock = 8;
+
+__device__ __forceinline__ float bf16_at(const uint4& v, int e) {
+  const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
+  return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+template <bool LN>
+__global__ void __launch_bounds__(32 * kRowsPerBlock) postnorm_bwd_rows_kernel(
+    const __nv_bfloat16* __restrict__ dC, const __nv_bfloat16* __restrict__ C, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ beta, const float* __restrict__ rstd_in, __nv_bfloat16* __restrict__ dH, int M,
+    int N) {
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerBlock + warp;
+  if (row >= M) return;
+  const int nvec = N >> 3;
+  const size_t off = static_cast<size_t>(row) * N;
+  const float r = rstd_in[row];
+  float s1 = 0.0f, s2 = 0.0f;
+  for (int vi = lane; vi < nvec; vi += 32) {
+    const uint4 u = ld_stream(dC + off + vi * 8), v = *reinterpret_cast<const uint4*>(C + off + vi * 8);
+    uint4 g = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u), b = make_uint4(0, 0, 0, 0);
+    if (gamma != nullptr) g = *reinterpret_cast<const uint4*>(gamma + vi * 8);
+    if (beta != nullptr) b = *reinterpret_cast<const uint4*>(beta + vi * 8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float gm = bf16_at(g, e);
+      const float d = bf16_at(u, e) * gm;
+      s1 += d;
+      s2 = fmaf(d, (bf16_at(v, e) - bf16_at(b, e)) / gm, s2);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  }
+  const float inv_n = 1.0f / static_cast<float>(N);
+  const float m1 = LN ? s1 * inv_n : 0.0f, m2 = s2 * inv_n;
+  for (int vi = lane; vi < nvec; vi += 32) {
+    const uint4 u = *reinterpret_cast<const uint4*>(dC + off + vi * 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(C + off + vi * 8);
+    uint4 g = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u), b = make_uint4(0, 0, 0, 0);
+    if (gamma != nullptr) g = *reinterpret_cast<const uint4*>(gamma + vi * 8);
+    if (beta != nullptr) b = *reinterpret_cast<const uint4*>(beta + vi * 8);
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float y[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int e = 2 * h + q;
+        const float gm = bf16_at(g, e);
+        const float hat = (bf16_at(v, e) - bf16_at(b, e)) / gm;
+        y[q] = r * (bf16_at(u, e) * gm - m1 - hat * m2);
+      }
+      o[h] = pack_bf16x2(y[0], y[1]);
+    }
+    *reinterpret_cast<uint4*>(dH + off + vi * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Column pass: thread t owns 8 adjacent columns and walks kColRows rows,
+// accumulating dC * h_hat and dC; part[group][0][n], part[group][1][n].
+constexpr int kColRows = 64;
+
+__global__ void __launch_bounds__(256) postnorm_bwd_cols_kernel(const __nv_bfloat16* __restrict__ dC,
+                                                                const __nv_bfloat16* __restrict__ C,
+                                                                const __nv_bfloat16* __restrict__ gamma,
+                                                                const __nv_bfloat16* __restrict__ beta,
+                                                                float* __restrict__ part, int M, int N) {
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int vi = blockIdx.x * blockDim.x + threadIdx.x;  // 8-column group
+  const int grp = blockIdx.y;                            // 64-row group
+  if (vi >= (N >> 3)) return;
+  uint4 g = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u), b = make_uint4(0, 0, 0, 0);
+  if (gamma != nullptr) g = *reinterpret_cast<const uint4*>(gamma + vi * 8);
+  if (beta != nullptr) b = *reinterpret_cast<const uint4*>(beta + vi * 8);
+  float ig[8], bt[8], ag[8], ab[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ig[e] = 1.0f / bf16_at(g, e);
+    bt[e] = bf16_at(b, e);
+    ag[e] = ab[e] = 0.0f;
+  }
+  const int m_end = min(M, (grp + 1) * kColRows);
+  constexpr int kU = 8;  // rows of loads in flight
+  for (int m0 = grp * kColRows; m0 < m_end; m0 += kU) {
+    uint4 u[kU], v[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      u[k] = v[k] = make_uint4(0, 0, 0, 0);  // rows past M add zero
+      if (m0 + k < m_end) {
+        const size_t o = static_cast<size_t>(m0 + k) * N + vi * 8;
+        u[k] = ld_stream(dC + o);
+        v[k] = ld_stream(C + o);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kU; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float dc = bf16_at(u[k], e);
+        ag[e] = fmaf(dc, (bf16_at(v[k], e) - bt[e]) * ig[e], ag[e]);
+        ab[e] += dc;
+      }
+  }
+  float* pg = part + static_cast<size_t>(grp) * 2 * N + vi * 8;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    pg[e] = ag[e];
+    pg[N + e] = ab[e];
+  }
+}
+
+// dgamma[n] = sum_g part[g][0][n], dbeta[n] = sum_g part[g][1][n], in group order
+__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ part, int ngroups, int N,
+                                                         float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float a = 0.0f, b = 0.0f;
+  for (int k = 0; k < ngroups; ++k) {
+    a += part[static_cast<size_t>(k) * 2 * N + n];
+    b += part[static_cast<size_t>(k) * 2 * N + N + n];
+  }
+  if (dgamma != nullptr) dgamma[n] = a;
+  if (dbeta != nullptr) dbeta[n] = b;
+}
+
 }  // namespace
 
 fnorm_status_t launch_rownorm(const void* X, const void* R, void* Y, int M, int N, bool layernorm, const void* gamma,
@@ -307,6 +448,58 @@ fnorm_status_t launch_backward_rows(const void* dC, const void* C, const float* 
                                            static_cast<const __nv_bfloat16*>(C), rstd,
                                            static_cast<__nv_bfloat16*>(dCs), coef, M, N, K, tpr);
   if (e != cudaSuccess) return cuda_fail(e, "backward row pass launch");
+  return FNORM_OK;
+}
+
+namespace {
+cudaLaunchConfig_t small_cfg(dim3 grid, dim3 block, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  return cfg;
+}
+}  // namespace
+
+int postnorm_backward_groups(int M) { return (M + kColRows - 1) / kColRows; }
+
+fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, const void* gamma, const void* beta,
+                                             const float* rstd, bool layernorm, void* dH, float* part, float* dgamma,
+                                             float* dbeta, int M, int N, cudaStream_t stream) {
+  DeviceInfo dev;
+  fnorm_status_t st = current_device(&dev);
+  if (st != FNORM_OK) return st;
+  const auto* dc = static_cast<const __nv_bfloat16*>(dC);
+  const auto* c = static_cast<const __nv_bfloat16*>(C);
+  const auto* g = static_cast<const __nv_bfloat16*>(gamma);
+  const auto* b = static_cast<const __nv_bfloat16*>(beta);
+  cudaLaunchAttribute attr[1];
+  if (dH != nullptr) {
+    cudaLaunchConfig_t cfg =
+        small_cfg(dim3((unsigned)((M + kRowsPerBlock - 1) / kRowsPerBlock)), dim3(32 * kRowsPerBlock), stream, attr);
+    const cudaError_t e =
+        layernorm ? cudaLaunchKernelEx(&cfg, postnorm_bwd_rows_kernel<true>, dc, c, g, b, rstd,
+                                       static_cast<__nv_bfloat16*>(dH), M, N)
+                  : cudaLaunchKernelEx(&cfg, postnorm_bwd_rows_kernel<false>, dc, c, g, b, rstd,
+                                       static_cast<__nv_bfloat16*>(dH), M, N);
+    if (e != cudaSuccess) return cuda_fail(e, "post-norm backward row pass launch");
+  }
+  if (dgamma != nullptr || dbeta != nullptr) {
+    const int groups = postnorm_backward_groups(M);
+    cudaLaunchConfig_t cfg = small_cfg(dim3((unsigned)((N / 8 + 255) / 256), (unsigned)groups), dim3(256), stream, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, postnorm_bwd_cols_kernel, dc, c, g, b, part, M, N);
+    if (e != cudaSuccess) return cuda_fail(e, "post-norm backward column pass launch");
+    cfg = small_cfg(dim3((unsigned)((N + 255) / 256)), dim3(256), stream, attr);
+    e = cudaLaunchKernelEx(&cfg, column_sum_kernel, static_cast<const float*>(part), groups, N, dgamma, dbeta);
+    if (e != cudaSuccess) return cuda_fail(e, "column sum launch");
+  }
   return FNORM_OK;
 }
 

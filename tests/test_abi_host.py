@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     for required in ("fnorm_gemm", "fnorm_lazy_prenorm_gemm", "fnorm_gemm_postnorm", "fnorm_rmsnorm",
                      "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
                      "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm", "fnorm_lazy_prenorm_gemm_backward",
-                     "fnorm_gemm_ex", "fnorm_rmsnorm_backward"):
+                     "fnorm_gemm_ex", "fnorm_rmsnorm_backward", "fnorm_gemm_postnorm_backward"):
         assert required in names
 
 
@@ -146,6 +146,13 @@ def test_backward_argument_rules(L):
     # dB reads A^T: M must be a multiple of 8; bad sizes
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, W, W, 100, 64, 64, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, W, W, 128, 60, 64, None) == 1
+    h = L.fnorm_gemm_postnorm_backward
+    # no gradient asked; unknown norm; dH workspace missing; dB with M % 8 != 0
+    assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, None, None, None, None, W, W, 128, 64, 64, None) == 1
+    assert h(FAKE, FAKE, FAKE, FAKE, 3, None, None, FAKE, FAKE, None, None, None, W, W, 128, 64, 64, None) == 1
+    assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, FAKE, None, None, None, None, W, 128, 64, 64, None) == 1
+    assert b"dH" in L.fnorm_last_error()
+    assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, None, FAKE, None, None, W, W, 100, 64, 64, None) == 1
     g = L.fnorm_gemm_ex
     assert g(FAKE, FAKE, FAKE, 100, 64, 64, 1, 0, None) == 1      # A^T needs M % 8 == 0
     assert g(FAKE, FAKE, FAKE, 128, 64, 64, 2, 0, None) == 1

@@ -1,4 +1,5 @@
-"""GPU parity of the backward of the Lazy Pre-RMSNorm GEMM against the fp64 oracle.
+"""GPU parity of the backward of the Lazy Pre-RMSNorm GEMM and of the GEMM
+post-norm against the fp64 oracle.
 
 The forward runs on the GPU (its bf16 output C and fp32 rstd are what a
 training step saves); the backward's dA and dB are compared with the oracle's
@@ -163,3 +164,54 @@ def test_rmsnorm_backward_standalone(M, N):
     # the oracle's backward with B = I: dA_hat = dC, the RMSNorm backward itself
     ref, _, _ = oracle.lazy_prenorm_gemm_backward(to_f64(X), np.eye(N), to_f64(dY), eps)
     assert_out_close(dX, ref, f"rmsnorm_backward {M}x{N}")
+
+
+# ----------------------------------------------------------------------------
+# post-norm backward: dA, dB, dgamma, dbeta of norm(A @ B) * gamma + beta
+# ----------------------------------------------------------------------------
+POSTB = [("layernorm", 256, 64, 256), ("rmsnorm", 200, 128, 72), ("layernorm", 256, 1024, 256),
+         ("rmsnorm", 1000, 200, 128), ("layernorm", 128, 4096, 64), ("layernorm", 8, 8, 8)]
+
+
+def _postb(norm, M, N, K, seed, affine=True):
+    base = "cfg2_n128" if norm == "layernorm" else "cfg4_n1024_rms"
+    w = WORKLOADS[base].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    d = make_inputs(w, seed)
+    g = d["gamma"] if affine else None
+    b = d["beta"] if affine else None
+    dC = torch.from_numpy(np.random.default_rng(seed + 1).standard_normal((M, N), dtype=np.float32)).to(torch.bfloat16)
+    Ad, Bd = d["A"].to(DEV), d["B"].to(DEV)
+    gd = None if g is None else g.to(DEV)
+    bd = None if b is None else b.to(DEV)
+    C, st = fn.gemm_postnorm(Ad, Bd, norm, gd, bd, w.eps, return_stats=True)
+    need = ("dA", "dB", "dgamma", "dbeta") if M % 8 == 0 else ("dA", "dgamma", "dbeta")
+    got = fn.gemm_postnorm_backward(Ad, Bd, C, dC.to(DEV), st["rstd"], norm, gd, bd, need=need)
+    fn.check_status(DEV)
+    ref = oracle.gemm_postnorm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(dC), norm, to_f64(g), to_f64(b), w.eps)
+    return got, ref
+
+
+@pytest.mark.parametrize("norm,M,N,K", POSTB, ids=lambda v: str(v))
+def test_postnorm_backward(norm, M, N, K):
+    got, ref = _postb(norm, M, N, K, seed=M + N + K)
+    assert_out_close(got["dH"], ref["dH"], "dH")
+    assert_out_close(got["dA"], ref["dA"], "dA")
+    if got["dB"] is not None:
+        assert_out_close(got["dB"], ref["dB"], "dB")
+    assert_out_close(got["dgamma"], ref["dgamma"], "dgamma")
+    assert_out_close(got["dbeta"], ref["dbeta"], "dbeta")
+
+
+def test_postnorm_backward_no_affine_and_ragged_M():
+    got, ref = _postb("layernorm", 333, 256, 128, seed=9, affine=False)
+    assert got["dB"] is None
+    assert_out_close(got["dA"], ref["dA"], "dA without affine")
+    assert_out_close(got["dbeta"], ref["dbeta"], "dbeta without affine")
+
+
+def test_postnorm_backward_layernorm_rows_sum_to_zero():
+    # LayerNorm ignores a constant added to a row: each row of dH sums to ~0
+    got, _ = _postb("layernorm", 256, 512, 128, seed=10)
+    h = np64(got["dH"])
+    scale = np.abs(h).sum(axis=1)
+    assert np.all(np.abs(h.sum(axis=1)) <= 2e-2 * scale + 1e-3)

@@ -32,7 +32,7 @@ def _rows(w, outliers, seed):
     return np.unique(np.asarray(picks, dtype=np.int64))
 
 
-@pytest.mark.parametrize("name", sorted(n for n, w in WORKLOADS.items() if w.kind != "prenorm_backward"))
+@pytest.mark.parametrize("name", sorted(n for n, w in WORKLOADS.items() if not w.kind.endswith("_backward")))
 def test_full_size(name):
     w = WORKLOADS[name]
     d = make_inputs(w, 0)

@@ -36,6 +36,8 @@ Forms beyond the five configurations (same distributions where they apply):
   gamma[4096] 1+N(0,0.1), no beta, eps 1e-6.
 * ``prenorm_bwd``  backward of the Lazy Pre-RMSNorm GEMM at cfg3's shape: cfg3's
   A and B and an upstream gradient dC[8192,4096] N(0,1).
+* ``postnorm_bwd``  backward of the GEMM + post-LayerNorm at cfg4_n1024_ln's
+  shape: its A, B, gamma, beta and dC[16384,1024] N(0,1).
 
 Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
 float32 in the order A, row scale, outlier rows, row offset, B, gamma, beta, R
@@ -57,7 +59,8 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "prenorm_backward" | "gemm"
+    kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "prenorm_backward" |
+                              # "postnorm_backward" | "gemm"
     M: int
     K: int
     N: int
@@ -81,7 +84,7 @@ class Workload:
     @property
     def flops(self) -> float:
         """2MNK per GEMM (the backward runs two: dA over N, dB over M)."""
-        return (4.0 if self.kind == "prenorm_backward" else 2.0) * self.M * self.N * self.K
+        return (4.0 if self.kind.endswith("_backward") else 2.0) * self.M * self.N * self.K
 
     @property
     def affine_len(self) -> int:
@@ -93,6 +96,10 @@ class Workload:
         """Bytes one fused launch must move: A + B + C in bf16 (+ R), gamma/beta
         (post-norm) or the folded weight's fp32 column sums and bias row
         (pre-norm with affine), and the fp32 row statistics."""
+        if self.kind == "postnorm_backward":
+            # row pass reads dC, C and writes dH; column pass reads dC, C; the
+            # GEMMs read dH, B and A, dH and write dA, dB
+            return 2.0 * (7 * self.M * self.N + 3 * self.M * self.K + 2 * self.K * self.N) + 4.0 * self.M
         if self.kind == "prenorm_backward":
             # dgrad reads dC, B, C, A, rstd and writes dA; wgrad reads A, dC,
             # rstd and writes dB
@@ -168,6 +175,9 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
     Workload("prenorm_bwd", "prenorm_backward", M=8192, K=4096, N=4096, b_std=1.0 / 64.0, eps=1e-6,
              a_row_scale=True,
              description="backward (dA, dB) of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096]"),
+    Workload("postnorm_bwd", "postnorm_backward", M=16384, K=2048, N=1024, b_std=1.0 / 45.0, eps=1e-5,
+             norm="layernorm", gamma=True, beta=True,
+             description="backward (dA, dB, dgamma, dbeta) of GEMM + post-LayerNorm, A[16384,2048] @ B[2048,1024]"),
 ]}
 
 
@@ -210,7 +220,7 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     if w.residual:
         r = rng.standard_normal((w.M, w.N), dtype=np.float32)
     dc = None
-    if w.kind == "prenorm_backward":
+    if w.kind.endswith("_backward"):
         dc = rng.standard_normal((w.M, w.N), dtype=np.float32)
 
     def bf16(x):
