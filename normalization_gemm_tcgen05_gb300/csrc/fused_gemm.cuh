@@ -464,6 +464,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
+    if (cid < total) {
+      // Warm L2 with the first ring of the first tile while the previous grid
+      // in the stream finishes.  L2 is the point of coherence, so a line
+      // brought in now still sees that grid's later writes; the loads proper
+      // are issued after griddepcontrol.wait.
+      const int m0 = (cid / ngroups) * Cfg::BM;
+      const int n0 = ((cid % ngroups) * C + rank) * cta_cols;
+      const int nk = num_kb < STAGES ? num_kb : STAGES;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (AT) {
+          tma_prefetch_l2_2d(&tmA, m0, kb * BK);
+          tma_prefetch_l2_2d(&tmA, m0 + 64, kb * BK);
+        } else {
+          tma_prefetch_l2_2d(&tmA, kb * BK, m0);
+        }
+        if (BT) {
+          tma_prefetch_l2_2d(&tmB, kb * BK, n0);
+        } else {
+          for (int c = 0; c < BN / 64; ++c) tma_prefetch_l2_2d(&tmB, n0 + c * 64, kb * BK);
+        }
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&aux->tmem_base), Cfg::TMEM_COLS);
