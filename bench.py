@@ -389,6 +389,10 @@ def time_graph(step, K: int, stream, world: int, device, chunk: int = 200) -> fl
     graphs = []
     i = 0
     with torch.cuda.stream(stream):
+        # one eager step on this stream first: per-stream resources (the
+        # wide post-norm's workspace) exist before the capture
+        step(0)
+        stream.synchronize()
         while i < K:
             n = min(chunk, K - i)
             g = torch.cuda.CUDAGraph()

@@ -78,19 +78,35 @@ bool want_resident_b(int64_t M, int64_t N, int64_t K, int bn) {
 //                 (tile width N rounded up to 64);
 //   N <= 1024:    resident cluster of 2 or 4 CTAs, each holding one 128- or
 //                 256-column slice in tensor memory;
-//   wider rows:   spill layout on a cluster of kSpillCluster CTAs, each owning
+//   wider rows:   spill layout with the statistics exchanged grid-wide: units
+//                 of (row block, kGxSlices 256-column slices) spread over all
+//                 SMs; without its workspace (or for the residual form), the
+//                 spill layout on a cluster of kSpillCluster CTAs, each owning
 //                 S = ceil(N / (cluster * 256)) slices of 256 columns.
 // A forced cluster size c keeps the resident layout when each CTA's share fits
 // one tile (256 columns for c <= 4, 128 for c = 8), else uses the spill layout
 // (c <= 4).
 constexpr int kSpillCluster = 4;
+constexpr int kGxSlices = 2;  // default chunk: 512 columns (the launch picks per shape)
+
+// Slices per grid-exchange chunk for an M x N post-norm: the widest chunk
+// (fewer units, fewer exchanges) that still gives every SM six or more units,
+// so that the partial last wave stays small.  Measured on cfg4's shapes:
+// 512-column chunks at N = 4096 and 1024-column chunks at N = 8192.
+int gx_slices_for(int64_t M, int64_t N, int num_sms) {
+  const int64_t row_blocks = (M + 127) / 128;
+  for (int s = 8; s > 1; s >>= 1)
+    if (row_blocks * ((N + 256LL * s - 1) / (256LL * s)) >= 6LL * num_sms) return s;
+  return 1;
+}
 
 struct PostPlan {
   int cluster, bn, slices;
-  bool spill;
+  bool spill, gx;
 };
 
-fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl) {
+fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl, bool allow_gx = true) {
+  pl->gx = false;
   auto resident = [&](int c) -> bool {
     const int64_t w = (N + c - 1) / c;  // columns per CTA
     if (w > 256 || (c > 4 && w > 128)) return false;
@@ -113,6 +129,10 @@ fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl) {
   }
   for (int c : {1, 2, 4})
     if (resident(c)) return FNORM_OK;
+  if (allow_gx) {
+    pl->cluster = 1, pl->bn = 256, pl->slices = kGxSlices, pl->spill = true, pl->gx = true;
+    return FNORM_OK;
+  }
   if (spill(kSpillCluster)) return FNORM_OK;
   set_error("post-norm row of %lld columns is too wide", (long long)N);
   return FNORM_ERR_UNSUPPORTED;
@@ -226,6 +246,29 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   L.slices = plan.slices;
   L.spill = plan.spill;
   L.cluster = plan.cluster;
+  if (plan.gx) {
+    // the grid exchange needs its workspace and (the kernel waits across
+    // CTAs) no pre-norm stage; otherwise the cluster spill layout
+    DeviceInfo dev;
+    FN_TRY(current_device(&dev));
+    plan.slices = gx_slices_for(M, N, dev.num_sms);
+    L.slices = plan.slices;
+    const GxScratch* gx = nullptr;
+    const int units = static_cast<int>((M + 127) / 128 * ((N + 256 * plan.slices - 1) / (256 * plan.slices)));
+    fnorm_status_t gs = pre_rmsnorm ? FNORM_ERR_UNSUPPORTED : gx_scratch_for_stream(L.stream, &gx);
+    if (gs == FNORM_OK && units <= gx->units_cap && (M + 127) / 128 <= gx->rowblocks_cap) {
+      L.gx = gx;
+    } else if (gs == FNORM_OK || gs == FNORM_ERR_UNSUPPORTED) {
+      clear_error();
+      FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
+      L.bn = plan.bn;
+      L.slices = plan.slices;
+      L.spill = plan.spill;
+      L.cluster = plan.cluster;
+    } else {
+      return gs;
+    }
+  }
   L.bres = (plan.cluster == 1 && !plan.spill) && want_resident_b(M, N, K, plan.bn);
   L.eps = eps;
   L.pre_eps = pre_rmsnorm ? pre_eps : 1.0f;
@@ -234,6 +277,7 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   L.mean_out = mean_out;
   L.rstd_out = rstd_out;
   L.pre_rstd_out = pre_rstd_out;
+  if (plan.gx) return launch_fused_post_grid(L);
   return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
 }
 
@@ -304,7 +348,7 @@ fnorm_status_t fnorm_gemm_add_postnorm(const fnorm_bf16* A, const fnorm_bf16* B,
   FN_TRY(check_eps(eps, "eps"));
   if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
   PostPlan plan{};
-  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
   if (M == 0) return FNORM_OK;
   FN_TRY(check_ptr(A, "A", 16, false));
   FN_TRY(check_ptr(B, "B", 16, false));

@@ -68,6 +68,7 @@ enum : int {
   MODE_BT = 512,      // B operand K-major: read from a row-major [N, K] array (B^T of a [K, N] matrix)
   MODE_AT = 1024,     // A operand MN-major: read from a row-major [K, M] array (A^T of an [M, K] matrix)
   MODE_DGRAD = 4096,  // RMSNorm backward epilogue: y = u + c[m] * X[m, n]
+  MODE_GX = 8192,     // spill layout with the row statistics exchanged grid-wide through global memory
 };
 
 struct FusedParams {
@@ -86,6 +87,12 @@ struct FusedParams {
   const __nv_bfloat16* R;     // [M, N] residual (MODE_RES)
   const float* rowcoef;       // MODE_DGRAD: [M] coefficients c of the forward rows
   const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows combined in the epilogue
+  // MODE_GX scratch: per-(row block, chunk) row statistics, per-row-block
+  // counters, the generation word and the CTA finish counter
+  float2* gx_part;
+  unsigned long long* gx_cnt;
+  uint32_t* gx_gen;
+  uint32_t* gx_finish;
   uint32_t* status;
   unsigned long long wait_limit_ns;
 };
@@ -99,7 +106,7 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // Shared-memory control block.  Arrays a mode does not use shrink to one
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff), so each kernel carries only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -108,19 +115,19 @@ struct Aux {
   uint64_t ss_full[2];
   uint64_t ss_empty[2];
   uint64_t xbar[2];
-  uint64_t nstat_full[2];
-  uint64_t nstat_empty[2];
+  uint64_t nstat_full[HD];   // epilogue -> normaliser handoff, HD deep
+  uint64_t nstat_empty[HD];
   uint64_t ebar[4][2];  // bounded barrier of the two epilogue warps of each TMEM lane quarter
   uint64_t teardown;
   uint64_t bres_full;
   uint32_t tmem_base;
   int abort_flag;
-  int nstat_m0[2];
-  int nstat_c0[2];
+  int nstat_m0[HD];
+  int nstat_c0[HD];
   float ss[2][NPART][SSN];    // pre-norm row sums, one slot per norm-warp part
   float ss1[2][NPART][SS1N];  // pre-LayerNorm: shifted sums of the A rows and the shift
   float ssk[2][SS1N];
-  float2 nstat[2][NSN];
+  float2 nstat[HD][NSN];
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
   alignas(16) float gam[GB];
   alignas(16) float bet[GB];
@@ -147,6 +154,7 @@ struct KCfg {
   static constexpr bool BT = (MODE & MODE_BT) != 0;
   static constexpr bool AT = (MODE & MODE_AT) != 0;
   static constexpr bool DGRAD = (MODE & MODE_DGRAD) != 0;
+  static constexpr bool GX = (MODE & MODE_GX) != 0;
   // the spill layout's in-place normalisation runs in its own warps (10-13)
   // unless those warps compute the Lazy Pre-Norm sums of squares
   static constexpr bool NORMW = SPILL && !PRE;
@@ -169,13 +177,16 @@ struct KCfg {
   static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + (BRES ? 0u : B_BYTES);
   static constexpr int SSN = PRE ? 128 : 1, SS1N = PRE_LN ? 128 : 1, NSN = SPILL ? 128 : 1;
+  // depth of the epilogue -> normaliser handoff (a power of two; 4 measured
+  // no faster than 2 for the grid exchange)
+  static constexpr int HDEPTH = 2;
   // norm warps: 4 (one row per thread), or 8 for the pre-LayerNorm, whose
   // shifted sums cost more per element: two parts take half of each row's
   // 16-byte chunks each
   static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
   // that buys a pipeline stage below 4
   static constexpr int stages_with(int bufs) {
@@ -190,7 +201,8 @@ struct KCfg {
 
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage ring");
-  static_assert(!SPILL || (BN == 256 && POST && CLUSTER), "spill layout: 256-column slices, post-norm, cluster");
+  static_assert(!SPILL || (BN == 256 && POST && (CLUSTER || GX)), "spill layout: 256-column slices, post-norm");
+  static_assert(!GX || (SPILL && !CLUSTER && !PRE && !RES), "grid exchange: spill layout, one CTA per unit");
   static_assert(!CLUSTER || (POST && CLMAX_ >= 1 && CLMAX_ <= 8), "clusters serve the post-norm, up to 8 CTAs");
   static_assert(!BRES || !CLUSTER, "resident B serves one CTA per row block");
   static_assert(!(PRE_LN || AFF) || (PRE && !POST), "the folded-affine pre-norm serves the pre-norm GEMM alone");
@@ -407,9 +419,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER, SPILL = Cfg::SPILL;
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
-  constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD;
+  constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD, GX = Cfg::GX;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH>;
+  constexpr int HD = Cfg::HDEPTH;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -451,9 +464,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->ss_full[b]), 4 * Cfg::NPART);
       mbar_init(smem_u32(&aux->ss_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->xbar[b]), 1);
+      for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&aux->ebar[qq][b]), kEpiWarps / 4);
+    }
+    for (int b = 0; b < HD; ++b) {
       mbar_init(smem_u32(&aux->nstat_full[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->nstat_empty[b]), 4);
-      for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&aux->ebar[qq][b]), kEpiWarps / 4);
     }
     mbar_init(smem_u32(&aux->teardown), 1);
     mbar_init(smem_u32(&aux->bres_full), 1);
@@ -741,6 +756,22 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       }
     }
 
+    // grid exchange: publish this CTA's statistics of (row block, chunk g) for
+    // its 128 rows, then count the quarter-warp in (4 per unit)
+    const uint32_t gx_gen = GX ? *reinterpret_cast<volatile uint32_t*>(p.gx_gen) : 0u;
+    auto gx_publish = [&](float part0, float part1, int m0_, int g_) -> bool {
+      const int rb = m0_ / Cfg::BM;
+      if (h == 0) p.gx_part[(static_cast<size_t>(rb) * ngroups + g_) * Cfg::BM + row] = make_float2(part0, part1);
+      __syncwarp();
+      bool ok2 = true;
+      if (h == 0 && lane == 0) {
+        __threadfence();
+        ok2 = grid_count_in(p.gx_cnt + rb, gx_gen);
+        if (!ok2) record_timeout(wc, kSiteGrid);
+      }
+      return __all_sync(0xffffffffu, ok2);
+    };
+
     // spill-layout state: running shifted sums of this half over the current
     // row block, and (inline normalisation only) the pending row block
     float k0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f;
@@ -859,15 +890,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               part0 = pre * pre * sum2;
               part1 = 0.0f;
             }
-            if (!combine_halves(part0, part1, nh[0], nh[1]) || !exchange(part0, part1, g, xit)) {
+            if (!combine_halves(part0, part1, nh[0], nh[1]) ||
+                !(GX ? gx_publish(part0, part1, m0, g) : exchange(part0, part1, g, xit))) {
               ok = false;
               break;
             }
             ++xit;
+            // (grid exchange: the normaliser warps combine the chunks and
+            // write the row statistics)
             const float mean = LN ? part0 : 0.0f;
             const float rstd = rsqrtf((LN ? part1 : part0) / static_cast<float>(N) + p.eps);
             const int m = m0 + row;
-            if (h == 0 && rank == 0 && g == 0 && m < M) {
+            if (!GX && h == 0 && rank == 0 && g == 0 && m < M) {
               if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
               if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
               if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
@@ -875,8 +909,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (NORMW) {
               // hand the row block to the normaliser warps
               const int nb = xit - 1;
-              const int b = nb & 1;
-              if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_empty[b]), (static_cast<uint32_t>(nb >> 1) & 1u) ^ 1u,
+              const int b = nb & (HD - 1);
+              if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_empty[b]), (static_cast<uint32_t>(nb / HD) & 1u) ^ 1u,
                                   kSiteEpilogue)) {
                 ok = false;
                 break;
@@ -1036,17 +1070,41 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     if (lane == 0) bulk_wait_read<0>();  // staging is read; the writes complete with the grid
   } else if (NORMW) {
     // ======================= normaliser warps (spill layout) =======================
+    const uint32_t gx_gen = GX ? *reinterpret_cast<volatile uint32_t*>(p.gx_gen) : 0u;
     const int k = warp - (2 + kEpiWarps);  // rows 32k..32k+31 of each row block
     int nb = 0;
     for (int t = cid; t < total; t += ncl, ++nb) {
-      const int b = nb & 1;
-      if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_full[b]), static_cast<uint32_t>(nb >> 1) & 1u, kSiteEpilogue))
+      const int b = nb & (HD - 1);
+      if (!mbar_wait_warp(wc, smem_u32(&aux->nstat_full[b]), static_cast<uint32_t>(nb / HD) & 1u, kSiteEpilogue))
         break;
-      const float2 st = aux->nstat[b][k * 32 + lane];
+      float2 st = aux->nstat[b][k * 32 + lane];
       const int m0 = aux->nstat_m0[b];
       const int c0 = aux->nstat_c0[b];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&aux->nstat_empty[b]));
+      if (GX) {
+        // wait until every chunk of this row block is published (4 quarter-
+        // warps per chunk), then combine the chunks in order for this row
+        const int rb = m0 / Cfg::BM;
+        const unsigned long long want =
+            (static_cast<unsigned long long>(gx_gen) << 32) | static_cast<unsigned long long>(4 * ngroups);
+        bool ready = true;
+        if (lane == 0) ready = grid_wait_eq(wc, p.gx_cnt + rb, want, kSiteGrid);
+        if (!__all_sync(0xffffffffu, ready)) break;
+        float mean = 0.0f, m2 = 0.0f, n = 0.0f, ssq = 0.0f;
+        for (int qq = 0; qq < ngroups; ++qq) {
+          const float2 v = __ldcg(p.gx_part + (static_cast<size_t>(rb) * ngroups + qq) * Cfg::BM + k * 32 + lane);
+          const float nq = static_cast<float>(min(max(N - qq * cta_cols, 0), cta_cols));
+          if (LN) combine_mean_m2(mean, m2, n, v.x, v.y, nq);
+          else ssq += v.x;
+        }
+        st = make_float2(LN ? mean : 0.0f, rsqrtf((LN ? m2 : ssq) / static_cast<float>(N) + p.eps));
+        const int m = m0 + k * 32 + lane;
+        if (c0 == 0 && m < M) {
+          if (LN && p.mean_out != nullptr) p.mean_out[m] = st.x;
+          if (p.rstd_out != nullptr) p.rstd_out[m] = st.y;
+        }
+      }
       for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
     }
   } else if (PRE) {
@@ -1147,6 +1205,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
   if (CLUSTER) cluster_sync();  // no CTA leaves while a peer may still address it
+  if (GX && threadIdx.x == 0) {
+    // the last CTA of the grid to finish starts the next generation: every
+    // counter this grid touched then reads as zero to the next launch
+    __threadfence();
+    if (atomicAdd(p.gx_finish, 1u) == gridDim.x - 1u) {
+      *reinterpret_cast<volatile uint32_t*>(p.gx_finish) = 0u;
+      __threadfence();
+      atomicAdd(p.gx_gen, 1u);
+    }
+  }
 }
 
 }  // namespace fnorm

@@ -68,6 +68,17 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.bias = L.bias;
   p.R = static_cast<const __nv_bfloat16*>(L.R);
   p.rowcoef = L.rowcoef;
+  if (Cfg::GX) {
+    const int units = ((L.M + Cfg::BM - 1) / Cfg::BM) * ((L.N + Cfg::BN * L.slices - 1) / (Cfg::BN * L.slices));
+    if (L.gx == nullptr || units > L.gx->units_cap || (L.M + Cfg::BM - 1) / Cfg::BM > L.gx->rowblocks_cap) {
+      set_error("internal: grid-exchange workspace missing or too small");
+      return FNORM_ERR_UNSUPPORTED;
+    }
+    p.gx_part = L.gx->part;
+    p.gx_cnt = L.gx->cnt;
+    p.gx_gen = L.gx->gen;
+    p.gx_finish = L.gx->finish;
+  }
   p.X = static_cast<const __nv_bfloat16*>(L.X);
   p.status = dev.status;
   p.wait_limit_ns = wait_limit_ns();
@@ -79,17 +90,23 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   const long long total = (long long)num_m * ngroups;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if (pdl_enabled()) {
+  if (pdl_enabled() && !Cfg::GX) {
     // the kernel's set-up may overlap the previous grid; its first global
     // access waits for that grid (griddepcontrol.wait)
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
+  if (Cfg::GX) {
+    // the grid exchange waits on other CTAs: all of them must be resident
+    attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+    attr[cfg.numAttrs].val.cooperative = 1;
     ++cfg.numAttrs;
   }
   if (Cfg::CLUSTER) {

@@ -37,6 +37,23 @@ fnorm_status_t encode_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t i
                                    uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                                    CUtensorMapSwizzle swizzle);
 
+// Workspace of the grid-exchange spill layout: per-(row block, chunk) row
+// statistics, per-row-block counters, the generation word and the finish
+// counter.  Calls that share one must be ordered (one stream).
+struct GxScratch {
+  float2* part;              // [units][128]
+  unsigned long long* cnt;   // [row blocks]
+  uint32_t* gen;
+  uint32_t* finish;
+  int units_cap;
+  int rowblocks_cap;
+};
+
+// The workspace of (current device, stream), allocated and zeroed by the
+// first call on that pair.  FNORM_ERR_UNSUPPORTED while the stream is being
+// captured and none exists yet (the caller then takes another layout).
+fnorm_status_t gx_scratch_for_stream(cudaStream_t stream, const GxScratch** out);
+
 struct FusedLaunch {
   const void* A;
   const void* B;
@@ -61,6 +78,7 @@ struct FusedLaunch {
   // ([N, K] row-major), as the mode says
   const void* X;          // dgrad: [M, N] forward input combined in the epilogue
   const float* rowcoef;   // dgrad: [M] coefficients c = -rstd^2 (dC . C) / K
+  const GxScratch* gx;    // grid-exchange spill layout's workspace
   cudaStream_t stream;
 };
 
@@ -72,6 +90,7 @@ fnorm_status_t launch_fused_prenorm_affine(const FusedLaunch& L); // lazy pre-no
 fnorm_status_t launch_fused_post_residual(const FusedLaunch& L);  // residual + post-norm, one CTA per row block
 fnorm_status_t launch_fused_post_residual_cluster(const FusedLaunch& L);  // residual + post-norm over a cluster
 fnorm_status_t launch_fused_backward(const FusedLaunch& L);       // backward of the Lazy Pre-RMSNorm GEMM
+fnorm_status_t launch_fused_post_grid(const FusedLaunch& L);      // post-norm, grid-wide statistics exchange
 
 // B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
 fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,

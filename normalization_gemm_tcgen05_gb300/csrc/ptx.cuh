@@ -20,7 +20,7 @@ enum : uint32_t {
 
 enum WaitSite : uint32_t {
   kSiteProducer = 1, kSiteMma = 2, kSiteEpilogue = 3, kSiteNorm = 4, kSiteExchange = 5,
-  kSiteTeardown = 6, kSiteSelfTest = 7
+  kSiteTeardown = 6, kSiteSelfTest = 7, kSiteGrid = 8
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -112,6 +112,43 @@ __device__ __forceinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, uint32
       }
     }
   }
+}
+
+// ---- grid-wide counters (cross-CTA statistics exchange) ----
+// A counter word holds (generation << 32) | count.  Count one arrival in for
+// generation `gen`: a value left by another generation counts as zero.
+// Bounded; false if the CAS never went through (a fault of the protocol).
+__device__ __forceinline__ bool grid_count_in(unsigned long long* c, uint32_t gen) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
+  for (int i = 0; i < (1 << 16); ++i) {
+    const unsigned long long base =
+        (static_cast<uint32_t>(old >> 32) == gen) ? old : (static_cast<unsigned long long>(gen) << 32);
+    const unsigned long long prev = atomicCAS(c, old, base + 1ull);
+    if (prev == old) return true;
+    old = prev;
+  }
+  return false;
+}
+
+// Wait (one lane; bounded by the wait limit and the CTA's abort flag) until
+// the counter reads `want`, then fence so that later loads see what the
+// arrivals published before counting in.
+__device__ __forceinline__ bool grid_wait_eq(const WaitCtx& w, const unsigned long long* c, unsigned long long want,
+                                             uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (*reinterpret_cast<const volatile unsigned long long*>(c) == want) break;
+    if ((i & 15u) == 15u) {
+      if (*w.abort_flag) return false;
+      if (global_timer_ns() - t0 > w.limit_ns) {
+        record_timeout(w, site);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+  __threadfence();
+  return true;
 }
 
 // Warp-collective wait: every lane waits (and so acquires), then the lanes

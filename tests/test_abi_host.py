@@ -171,9 +171,9 @@ def test_norm_rejects_bad_sizes(L):
 
 
 @pytest.mark.parametrize("N,cluster,cols", [(8, 1, 64), (64, 1, 64), (128, 1, 128), (200, 1, 256), (256, 1, 256),
-                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (1032, 4, 512),
-                                            (2048, 4, 512), (2056, 4, 768), (3000, 4, 768), (4096, 4, 1024),
-                                            (8192, 4, 2048), (16384, 4, 4096)])
+                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (1032, 1, 512),
+                                            (2048, 1, 512), (2056, 1, 512), (3000, 1, 512), (4096, 1, 512),
+                                            (8192, 1, 512), (16384, 1, 512)])
 def test_postnorm_plan(L, N, cluster, cols):
     import normalization_gemm_tcgen05_gb300 as fn
     assert fn.postnorm_plan(N) == (cluster, cols)

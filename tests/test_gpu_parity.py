@@ -173,6 +173,50 @@ def test_postnorm_spill(norm, N):
     _post(w, d, norm)
 
 
+@pytest.mark.parametrize("N", [1032, 4096, 8192])
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_postnorm_spill_on_a_cluster(norm, N):
+    # the cluster form of the spill layout (forced), beside the grid-wide
+    # exchange the planner picks for wide rows
+    w, d = _case("cfg4_n4096_ln", N + 3 * (norm == "rmsnorm"), M=300, N=N, K=128)
+    try:
+        fn.set_postnorm_cluster(4)
+        assert fn.postnorm_plan(N)[0] == 4
+        _post(w, d, norm)
+    finally:
+        fn.set_postnorm_cluster(0)
+
+
+def test_grid_exchange_repeats_and_replays():
+    # back-to-back calls reuse the grid-exchange counters (a new generation
+    # each call), and a CUDA graph replays the same launch: every result is
+    # the same as the first, bit for bit, and the status stays clean
+    w, d = _case("cfg4_n4096_ln", 31, M=128 * 170 + 5, N=2048, K=128)
+    A, B, g, b = _dev(d["A"]), _dev(d["B"]), _dev(d["gamma"]), _dev(d["beta"])
+    assert fn.postnorm_plan(2048)[0] == 1
+    C0 = fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps)
+    C1 = fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps)
+    fn.check_status(DEV)
+    assert torch.equal(C0, C1)
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", to_f64(d["gamma"]),
+                               to_f64(d["beta"]), w.eps)
+    assert_out_close(C0, ref["C"], "grid exchange vs oracle")
+    stream = torch.cuda.Stream(DEV)
+    out = torch.empty_like(C0)
+    with torch.cuda.stream(stream):
+        fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps, out=out)  # the stream's workspace, before capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps, out=out)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, C0)
+    fn.check_status(DEV)
+
+
 def test_postnorm_cluster_with_pre():
     w, d = _case("cfg5", 13, M=400, N=1024, K=256)
     _post(w, d, "layernorm", pre=True)
