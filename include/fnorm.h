@@ -18,7 +18,10 @@
  *     16-bit storage (fnorm_bf16).  Accumulation is fp32; row statistics are
  *     fp32 arrays of length M.
  *   - Every pointer is DEVICE memory on the current CUDA device, owned by
- *     the caller.  The library never frees, retains or allocates per call.
+ *     the caller.  The library never frees or retains caller memory and
+ *     allocates nothing per call; the one allocation it makes is the 16 MB
+ *     workspace of the wide-row post-norm, once per (device, stream) on the
+ *     first fnorm_gemm_postnorm call that needs it (fnorm_gemm_postnorm).
  *     Base addresses of A, B, C, X, Y, gamma and beta must be 16-byte
  *     aligned; fp32 statistic outputs 4-byte aligned.  A misaligned pointer
  *     is an argument error.
@@ -117,7 +120,15 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
  *   CTA writes its un-normalised slices to C in bf16, then normalises them in
  *   place once the statistics are known; those outputs are normalised from
  *   bf16-rounded values (relative error <= 2^-9 of the value before the norm).
- *   C is therefore also read by this call.
+ *   C is therefore also read by this call.  By default the spill layout runs
+ *   grid-wide: (row block, column chunk) units over every SM publish their
+ *   chunk statistics to a 16 MB workspace that belongs to the calling
+ *   (device, stream) pair and is allocated by the first such call on it;
+ *   make that first call before capturing the stream into a CUDA graph (a
+ *   capture without a workspace, a pre-norm, or a shape past the workspace,
+ *   takes the cluster form of the spill layout instead).  Calls on one
+ *   stream are ordered, so they may share it; calls on different streams
+ *   use different workspaces.
  *   norm:        FNORM_LAYERNORM or FNORM_RMSNORM.
  *   gamma, beta: [N] bf16 device arrays, or NULL (gamma = 1, beta = 0).
  *   eps:         epsilon of the post-norm, inside the square root.
