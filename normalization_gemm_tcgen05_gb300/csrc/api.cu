@@ -95,8 +95,11 @@ constexpr int kGxSlices = 2;  // default chunk: 512 columns (the launch picks pe
 // 512-column chunks at N = 4096 and 1024-column chunks at N = 8192.
 int gx_slices_for(int64_t M, int64_t N, int num_sms) {
   const int64_t row_blocks = (M + 127) / 128;
-  for (int s = 8; s > 1; s >>= 1)
-    if (row_blocks * ((N + 256LL * s - 1) / (256LL * s)) >= 6LL * num_sms) return s;
+  const int64_t smax = (N + 255) / 256;  // no chunk wider than the row
+  for (int64_t s = 8; s > 1; s >>= 1) {
+    const int64_t sc = s < smax ? s : smax;
+    if (row_blocks * ((N + 256 * sc - 1) / (256 * sc)) >= 6LL * num_sms) return static_cast<int>(sc);
+  }
   return 1;
 }
 
