@@ -182,6 +182,28 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
                                                 int64_t N, int64_t K, void* stream);
 
 /*
+ * fnorm_gemm_postnorm_noalloc — fnorm_gemm_postnorm (same arguments, same
+ * results) that allocates nothing, ever.  The pages have no counterpart: it
+ * exists for callers that must not let a library allocate device memory.
+ *   The wide-row grid exchange keeps its statistics in a fixed device array
+ *   of the library (2048 (row block, chunk) units, 8192 row blocks: about
+ *   2.1 MB) instead of the per-stream workspace.  A shape whose grid exchange
+ *   needs more is rejected with FNORM_ERR_UNSUPPORTED and a message naming
+ *   the limit (fnorm_gemm_postnorm takes it).  Shapes that need no exchange
+ *   workspace (N <= 1024, or a pre-norm) run exactly as fnorm_gemm_postnorm.
+ *   The first call on a device takes the array's address and clears its
+ *   counters (on the call's stream): make it before capturing a stream into
+ *   a CUDA graph.  All calls of a device share the array: calls that
+ *   overlap in time (different streams, or graphs replayed concurrently)
+ *   race and give wrong results; order them on one stream.
+ */
+fnorm_status_t fnorm_gemm_postnorm_noalloc(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
+                                           int64_t M, int64_t N, int64_t K, fnorm_norm_t norm,
+                                           const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                           int pre_rmsnorm, float pre_eps, float* mean_out, float* rstd_out,
+                                           float* pre_rstd_out, void* stream);
+
+/*
  * fnorm_gemm_postnorm_backward — gradients of C = norm(A @ B) * gamma + beta
  * (fnorm_gemm_postnorm without the pre-norm) given dC = dL/dC.  The forward
  * never materialised H = A @ B; its normalised rows are rebuilt from the

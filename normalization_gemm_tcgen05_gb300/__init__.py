@@ -35,7 +35,7 @@ import torch
 
 __all__ = [
     "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm",
-    "gemm_postnorm_backward", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "gemm_postnorm_backward", "gemm_postnorm_noalloc", "lazy_prenorm_gemm_backward", "gemm_postnorm",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
@@ -76,6 +76,8 @@ _SIGNATURES = {
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
     "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
+    "fnorm_gemm_postnorm_noalloc": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
+                                                ctypes.c_int, _f32, _p, _p, _p, _p]),
     "fnorm_gemm_postnorm_backward": (_c_status, [_p, _p, _p, _p, ctypes.c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                                  _i64, _i64, _i64, _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
@@ -316,6 +318,31 @@ def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Opt
             1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
             _ptr(stats.get("pre_rstd")), _stream(A.device)))
     return (C, stats) if return_stats else C
+
+
+def gemm_postnorm_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, norm="layernorm",
+                          gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None, eps: float = 1e-5,
+                          pre_rmsnorm: bool = False, pre_eps: float = 1e-6, mean_out: Optional[torch.Tensor] = None,
+                          rstd_out: Optional[torch.Tensor] = None, pre_rstd_out: Optional[torch.Tensor] = None):
+    """``gemm_postnorm`` through the entry point that allocates nothing: every
+    output (``out`` and the optional fp32 [M] statistics) is the caller's, and
+    nothing is allocated here either."""
+    M, N, K = _ab(A, B)
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    gamma = _vec(gamma, N, "gamma", A.device)
+    beta = _vec(beta, N, "beta", A.device)
+    _out(out, (M, N), A.device)
+    for t, name in ((mean_out, "mean_out"), (rstd_out, "rstd_out"), (pre_rstd_out, "pre_rstd_out")):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != M or not t.is_contiguous()
+                              or t.device != A.device):
+            raise ValueError(f"{name} must be a contiguous float32 vector of length {M} on {A.device}")
+    with torch.cuda.device(A.device):
+        _check(lib().fnorm_gemm_postnorm_noalloc(
+            _ptr(A), _ptr(B), _ptr(out), M, N, K, _NORMS[norm], _ptr(gamma), _ptr(beta), float(eps),
+            1 if pre_rmsnorm else 0, float(pre_eps), _ptr(mean_out), _ptr(rstd_out), _ptr(pre_rstd_out),
+            _stream(A.device)))
+    return out
 
 
 def gemm_postnorm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC: torch.Tensor, rstd: torch.Tensor,

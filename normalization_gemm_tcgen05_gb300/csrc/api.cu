@@ -220,10 +220,16 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
   return launch_fused_plain(L);
 }
 
-fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
-                                   int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
-                                   const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
-                                   float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
+}  // extern "C"
+
+namespace fnorm {
+namespace {
+// fnorm_gemm_postnorm and its allocation-free twin: they differ only in where
+// the wide-row grid exchange keeps its statistics
+fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M, int64_t N,
+                                  int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma, const fnorm_bf16* beta,
+                                  float eps, int pre_rmsnorm, float pre_eps, float* mean_out, float* rstd_out,
+                                  float* pre_rstd_out, void* stream, bool noalloc) {
   clear_error();
   FN_TRY(check_mnk(M, N, K));
   if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
@@ -258,8 +264,16 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
     L.slices = plan.slices;
     const GxScratch* gx = nullptr;
     const int units = static_cast<int>((M + 127) / 128 * ((N + 256 * plan.slices - 1) / (256 * plan.slices)));
-    fnorm_status_t gs = pre_rmsnorm ? FNORM_ERR_UNSUPPORTED : gx_scratch_for_stream(L.stream, &gx);
-    if (gs == FNORM_OK && units <= gx->units_cap && (M + 127) / 128 <= gx->rowblocks_cap) {
+    fnorm_status_t gs = pre_rmsnorm ? FNORM_ERR_UNSUPPORTED
+                                    : (noalloc ? noalloc_scratch(L.stream, &gx) : gx_scratch_for_stream(L.stream, &gx));
+    const bool fits = gs == FNORM_OK && units <= gx->units_cap && (M + 127) / 128 <= gx->rowblocks_cap;
+    if (noalloc && gs == FNORM_OK && !fits) {
+      set_error("fnorm_gemm_postnorm_noalloc: %d units of %d rows x 256*%d columns (%lld row blocks) exceed its "
+                "fixed workspace (%d units, %d row blocks); use fnorm_gemm_postnorm",
+                units, 128, plan.slices, (long long)((M + 127) / 128), gx->units_cap, gx->rowblocks_cap);
+      return FNORM_ERR_UNSUPPORTED;
+    }
+    if (fits) {
       L.gx = gx;
     } else if (gs == FNORM_OK || gs == FNORM_ERR_UNSUPPORTED) {
       clear_error();
@@ -283,6 +297,27 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
   if (plan.gx) return launch_fused_post_grid(L);
   return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
 }
+}  // namespace
+}  // namespace fnorm
+
+extern "C" {
+
+fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
+                                   int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                   const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
+                                   float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
+  return gemm_postnorm_impl(A, B, C, M, N, K, norm, gamma, beta, eps, pre_rmsnorm, pre_eps, mean_out, rstd_out,
+                            pre_rstd_out, stream, false);
+}
+
+fnorm_status_t fnorm_gemm_postnorm_noalloc(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
+                                           int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                           const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
+                                           float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
+  return gemm_postnorm_impl(A, B, C, M, N, K, norm, gamma, beta, eps, pre_rmsnorm, pre_eps, mean_out, rstd_out,
+                            pre_rstd_out, stream, true);
+}
+
 
 fnorm_status_t fnorm_fold_prenorm_affine(const fnorm_bf16* B, int64_t K, int64_t N, const fnorm_bf16* gamma,
                                          const fnorm_bf16* beta, fnorm_bf16* B_folded, float* colsum, float* bias,

@@ -54,6 +54,11 @@ struct GxScratch {
 // captured and none exists yet (the caller then takes another layout).
 fnorm_status_t gx_scratch_for_stream(cudaStream_t stream, const GxScratch** out);
 
+// The fixed workspace of fnorm_gemm_postnorm_noalloc (a device array, no
+// allocation): address taken and counters cleared by the first call per
+// device.  Calls sharing it must not overlap.
+fnorm_status_t noalloc_scratch(cudaStream_t stream, const GxScratch** out);
+
 struct FusedLaunch {
   const void* A;
   const void* B;

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     for required in ("fnorm_gemm", "fnorm_lazy_prenorm_gemm", "fnorm_gemm_postnorm", "fnorm_rmsnorm",
                      "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
                      "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm", "fnorm_lazy_prenorm_gemm_backward",
-                     "fnorm_gemm_ex", "fnorm_rmsnorm_backward", "fnorm_gemm_postnorm_backward"):
+                     "fnorm_gemm_ex", "fnorm_rmsnorm_backward", "fnorm_gemm_postnorm_backward",
+                     "fnorm_gemm_postnorm_noalloc"):
         assert required in names
 
 
