@@ -187,12 +187,16 @@ struct KCfg {
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
       (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH>) + 15) / 16 * 16;
-  // epilogue staging: 8 warps x STG_BUFS store boxes; one box per warp when
-  // that buys a pipeline stage below 4
+  // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
+  // that buys a pipeline stage and either the ring is below 4 stages or a
+  // warp stores only one box per tile (64-column tiles), so that nothing
+  // waits on the single buffer within a tile: a narrow tile streams A at a
+  // rate set by the bytes its ring keeps in flight.
   static constexpr int stages_with(int bufs) {
     return (int)((kSmemLimit - 1024 - BRES_BYTES - kEpiWarps * bufs * kBoxBytes - AUX_BYTES) / STAGE_BYTES);
   }
-  static constexpr int STG_BUFS = (stages_with(2) < 4 && stages_with(1) > stages_with(2)) ? 1 : 2;
+  static constexpr int STG_BUFS =
+      ((stages_with(2) < 4 || NCH == 1) && stages_with(1) > stages_with(2) && stages_with(2) < kMaxStages) ? 1 : 2;
   static constexpr uint32_t STG_BYTES = kEpiWarps * STG_BUFS * kBoxBytes;
   static constexpr int STAGES = stages_with(STG_BUFS) < kMaxStages ? stages_with(STG_BUFS) : kMaxStages;
   static constexpr uint32_t SMEM_BYTES = 1024 + BRES_BYTES + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;

@@ -7,7 +7,7 @@ namespace fnorm {
 
 // Pipeline depths the streaming kernels are tuned for (stage = A + B tile).
 static_assert(KCfg<256, MODE_PRE>::STAGES >= 4, "Lazy Pre-Norm, 256-column tiles");
-static_assert(KCfg<128, 0>::STAGES >= 5 && KCfg<64, 0>::STAGES >= 7, "GEMM, narrow tiles");
+static_assert(KCfg<128, 0>::STAGES >= 5 && KCfg<64, 0>::STAGES >= 8, "GEMM, narrow tiles");
 
 namespace {
 template <int BN>

@@ -5,7 +5,7 @@
 
 namespace fnorm {
 
-static_assert(KCfg<128, MODE_POST | MODE_LN>::STAGES >= 5 && KCfg<64, MODE_POST | MODE_LN>::STAGES >= 7,
+static_assert(KCfg<128, MODE_POST | MODE_LN>::STAGES >= 5 && KCfg<64, MODE_POST | MODE_LN>::STAGES >= 8,
               "post-norm, narrow tiles");
 static_assert(KCfg<256, MODE_POST | MODE_LN | MODE_PRE | MODE_BRES>::STAGES >= 4, "pre + post-norm, resident B");
 
