@@ -221,7 +221,9 @@ struct KCfg {
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
 // (columns c0..c0+255) of C, re-read from L2.  Lane l owns columns
 // c0+8l..c0+8l+7; mean and rstd of row r0+i are held by lane lane_off+i.
-template <bool LN>
+// RIF rows of loads are in flight per lane: the pass is bound by L2 round
+// trips, nrows / RIF of them.
+template <bool LN, int RIF = 8>
 __device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, int nrows, int lane_off, int c0,
                                                 float mean, float rstd, int lane) {
   const int col = c0 + lane * 8;
@@ -249,16 +251,16 @@ __device__ __forceinline__ void normalize_slice(const FusedParams& p, int r0, in
     b2[h] = f2(bv[2 * h], bv[2 * h + 1]);
   }
 #pragma unroll 1
-  for (int rr = 0; rr < nrows; rr += 8) {
-    uint4 v[8];  // eight rows of loads in flight per lane
+  for (int rr = 0; rr < nrows; rr += RIF) {
+    uint4 v[RIF];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < RIF; ++u) {
       const int m = r0 + rr + u;
       v[u] = make_uint4(0, 0, 0, 0);
       if (colok && rr + u < nrows && m < p.M) v[u] = ld_global_cg_v4(p.C + static_cast<size_t>(m) * p.N + col);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < RIF; ++u) {
       const float mu = __shfl_sync(0xffffffffu, mean, (lane_off + rr + u) & 31);
       const float rs = __shfl_sync(0xffffffffu, rstd, (lane_off + rr + u) & 31);
       const int m = r0 + rr + u;
@@ -1109,7 +1111,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           if (p.rstd_out != nullptr) p.rstd_out[m] = st.y;
         }
       }
-      for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
+      for (int s = 0; s < S; ++s)
+        normalize_slice<LN, GX ? 16 : 8>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
     }
   } else if (PRE) {
     // ======================= norm warps (Lazy Pre-Norm) =======================
