@@ -643,16 +643,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint32_t sbuf = 0;
     int it = 0;
 
-    if (POST && !SPILL) {
-      // resident post-norm CTAs own one fixed BN-column slice of every row
-      const int n0 = rank * BN;
-      for (int j = etid; j < BN; j += 32 * kEpiWarps) {
-        const int n = n0 + j;
-        aux->gam[j] = (p.gamma != nullptr && n < N) ? __bfloat162float(p.gamma[n]) : 1.0f;
-        aux->bet[j] = (p.beta != nullptr && n < N) ? __bfloat162float(p.beta[n]) : 0.0f;
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
-    }
 
     // stage one [32 rows x 32 columns] bf16 box of this warp's rows (64-byte
     // swizzle) and store it with TMA
@@ -760,6 +750,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[i2]));
       }
+    }
+    if (POST && !SPILL) {
+      // resident post-norm CTAs own one fixed BN-column slice of every row
+      // (after the residual preload, which the first MMA waits for)
+      const int n0 = rank * BN;
+      for (int j = etid; j < BN; j += 32 * kEpiWarps) {
+        const int n = n0 + j;
+        aux->gam[j] = (p.gamma != nullptr && n < N) ? __bfloat162float(p.gamma[n]) : 1.0f;
+        aux->bet[j] = (p.beta != nullptr && n < N) ? __bfloat162float(p.beta[n]) : 0.0f;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
     }
 
     // grid exchange: publish this CTA's statistics of (row block, chunk g) for
