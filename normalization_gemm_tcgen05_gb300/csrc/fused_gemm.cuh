@@ -105,8 +105,9 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 
 // Shared-memory control block.  Arrays a mode does not use shrink to one
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
-// spill-layout handoff), so each kernel carries only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD>
+// spill-layout handoff, NBR: resident-B k-blocks), so each kernel carries
+// only what it needs.
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -119,7 +120,7 @@ struct Aux {
   uint64_t nstat_empty[HD];
   uint64_t ebar[4][2];  // bounded barrier of the two epilogue warps of each TMEM lane quarter
   uint64_t teardown;
-  uint64_t bres_full;
+  uint64_t bres_full[NBR];  // one per k-block of resident B
   uint32_t tmem_base;
   int abort_flag;
   int nstat_m0[HD];
@@ -186,7 +187,7 @@ struct KCfg {
   static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1)>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
   // that buys a pipeline stage and either the ring is below 4 stages or a
   // warp stores only one box per tile (64-column tiles), so that nothing
@@ -427,7 +428,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD, GX = Cfg::GX;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
-  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH>;
+  using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
+                   (Cfg::BRES ? Cfg::KB_MAX : 1)>;
   constexpr int HD = Cfg::HDEPTH;
 
   extern __shared__ uint8_t smem_raw[];
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->nstat_empty[b]), 4);
     }
     mbar_init(smem_u32(&aux->teardown), 1);
-    mbar_init(smem_u32(&aux->bres_full), 1);
+    for (int kb = 0; kb < (BRES ? Cfg::KB_MAX : 1); ++kb) mbar_init(smem_u32(&aux->bres_full[kb]), 1);
     aux->abort_flag = 0;
     fence_mbar_init();
   }
@@ -526,16 +528,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     // ======================= TMA producer =======================
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, filled = 0, fill_par = 0;
+      int bres_issued = 0;  // resident-B k-blocks issued (each on its own barrier)
       bool ok = true;
-      if (BRES && cid < total) {
-        // all of B once: num_kb k-blocks x BN/64 chunks of [64 x 64]
-        const uint32_t bf = smem_u32(&aux->bres_full);
-        mbar_arrive_expect_tx(bf, static_cast<uint32_t>(num_kb) * Cfg::B_BYTES);
-        for (int kb = 0; kb < num_kb; ++kb)
-#pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_2d(bres_base + kb * Cfg::B_BYTES + c * (BK * 128), &tmB, c * 64, kb * BK, bf);
-      }
       for (int t = cid; t < total && ok; t += ncl) {
         const int m0 = (t / ngroups) * Cfg::BM;
         for (int s = 0; s < S && ok; ++s) {
@@ -544,6 +538,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
               ok = false;
               break;
+            }
+            if (BRES && t == cid) {
+              // all of B once, during the first tile: k-block kb just ahead
+              // of the A stage that pairs with it, so the first MMAs need not
+              // wait for the whole of B
+              const uint32_t bf = smem_u32(&aux->bres_full[kb]);
+              mbar_arrive_expect_tx(bf, Cfg::B_BYTES);
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(bres_base + kb * Cfg::B_BYTES + c * (BK * 128), &tmB, c * 64, kb * BK, bf);
+              bres_issued = kb + 1;
             }
             const uint32_t full = smem_u32(&aux->full[stage]);
             mbar_arrive_expect_tx(full, STAGE_BYTES);
@@ -578,7 +583,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u)
           mbar_wait<false, true>(wc, smem_u32(&aux->full[s]), (fill_par >> s) & 1u, kSiteTeardown);
-      if (BRES && cid < total) mbar_wait<false, true>(wc, smem_u32(&aux->bres_full), 0, kSiteTeardown);
+      for (int kb = 0; kb < bres_issued; ++kb)
+        mbar_wait<false, true>(wc, smem_u32(&aux->bres_full[kb]), 0, kSiteTeardown);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -586,7 +592,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
-      if (BRES && cid < total) ok = mbar_wait(wc, smem_u32(&aux->bres_full), 0, kSiteMma);
       for (int t = cid; t < total && ok; t += ncl) {
         for (int s = 0; s < S && ok; ++s, ++it) {
           const int buf = it & 1;
@@ -600,7 +605,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * BN);
           for (int kb = 0; kb < num_kb; ++kb) {
-            if (!mbar_wait(wc, smem_u32(&aux->full[stage]), phase, kSiteMma)) {
+            if (!mbar_wait(wc, smem_u32(&aux->full[stage]), phase, kSiteMma) ||
+                (BRES && it == 0 && !mbar_wait(wc, smem_u32(&aux->bres_full[kb]), 0, kSiteMma))) {
               ok = false;
               break;
             }
