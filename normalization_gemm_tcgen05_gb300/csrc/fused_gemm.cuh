@@ -412,8 +412,9 @@ __device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n
   if (nb <= 0.0f) return;
   const float nn = n + nb;
   const float d = mean_b - mean;
-  mean += d * (nb / nn);
-  m2 += m2_b + d * d * (n * nb / nn);
+  const float w = nb / nn;
+  mean += d * w;
+  m2 += m2_b + d * d * (n * w);
   n = nn;
 }
 
@@ -455,6 +456,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const int cid = static_cast<int>(blockIdx.x) / C;
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_kb = (K + BK - 1) / BK;
+  // The per-row statistics multiply by 1/N and 1/K (correctly rounded
+  // reciprocals: exact, as a division would be, whenever N and K are powers
+  // of two) instead of dividing; a division costs far more on the epilogue's
+  // critical path.  Recomputed where used, so no register holds them.
+  auto inv_N = [&]() { return __frcp_rn(static_cast<float>(N)); };
+  auto inv_K = [&]() { return __frcp_rn(static_cast<float>(K)); };
 
   const WaitCtx wc{p.wait_limit_ns, p.status, &aux->abort_flag};
 
@@ -699,7 +706,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       if (!esync()) return false;
       const float2 a = aux->hstat[hp][0][row];
       const float2 b = aux->hstat[hp][1][row];
-      if (LN) {
+      if (LN && nh0 == nh1 && nh0 > 0.0f) {
+        // equal halves (every full tile): the combination's weights are
+        // exactly 1/2 and nh/2, the same values without its divisions
+        const float d = b.x - a.x;
+        part0 = a.x + d * 0.5f;
+        part1 = a.y + (b.y + d * d * (nh0 * 0.5f));
+      } else if (LN) {
         float mean = 0.0f, m2 = 0.0f, n = 0.0f;
         combine_mean_m2(mean, m2, n, a.x, a.y, nh0);
         combine_mean_m2(mean, m2, n, b.x, b.y, nh1);
@@ -834,16 +847,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           }
           const float ss = Cfg::NPART == 2 ? aux->ss[sb][0][row] + aux->ss[sb][Cfg::NPART - 1][row]
                                            : aux->ss[sb][0][row];
-          const float kf = static_cast<float>(K);
           if (PRE_LN) {
             // LayerNorm of the A row from its shifted sums (shift: ssk)
             const float s1 = Cfg::NPART == 2 ? aux->ss1[sb][0][row] + aux->ss1[sb][Cfg::NPART - 1][row]
                                              : aux->ss1[sb][0][row];
-            pre_mean = aux->ssk[sb][row] + s1 / kf;
-            const float var = fmaxf(ss / kf - (s1 / kf) * (s1 / kf), 0.0f);
+            const float mu = s1 * inv_K();
+            pre_mean = aux->ssk[sb][row] + mu;
+            const float var = fmaxf(ss * inv_K() - mu * mu, 0.0f);
             pre = rsqrtf(var + p.pre_eps);
           } else {
-            pre = rsqrtf(ss / kf + p.pre_eps);
+            pre = rsqrtf(ss * inv_K() + p.pre_eps);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&aux->ss_empty[sb]));
@@ -897,8 +910,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const float nmine = nh[h];
             float part0, part1;  // statistics of the pre-scaled values v = pre * u
             if (LN) {
-              part0 = nmine > 0.0f ? pre * (k0 + sum1 / nmine) : 0.0f;
-              part1 = nmine > 0.0f ? pre * pre * fmaxf(sum2 - sum1 * sum1 / nmine, 0.0f) : 0.0f;
+              const float inv_nm = nmine > 0.0f ? 1.0f / nmine : 0.0f;
+              part0 = nmine > 0.0f ? pre * (k0 + sum1 * inv_nm) : 0.0f;
+              part1 = nmine > 0.0f ? pre * pre * fmaxf(sum2 - sum1 * sum1 * inv_nm, 0.0f) : 0.0f;
             } else {
               part0 = pre * pre * sum2;
               part1 = 0.0f;
@@ -912,7 +926,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             // (grid exchange: the normaliser warps combine the chunks and
             // write the row statistics)
             const float mean = LN ? part0 : 0.0f;
-            const float rstd = rsqrtf((LN ? part1 : part0) / static_cast<float>(N) + p.eps);
+            const float rstd = rsqrtf((LN ? part1 : part0) * inv_N() + p.eps);
             const int m = m0 + row;
             if (!GX && h == 0 && rank == 0 && g == 0 && m < M) {
               if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
@@ -990,8 +1004,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           const float nf = static_cast<float>(nvh);
           float part0, part1;  // statistics of the pre-scaled values v = pre * u
           if (LN) {
-            part0 = nvh > 0 ? pre * (kk + s1 / nf) : 0.0f;
-            part1 = nvh > 0 ? pre * pre * fmaxf(s2 - s1 * s1 / nf, 0.0f) : 0.0f;
+            const float inv_nf = nvh == HALF ? 1.0f / static_cast<float>(HALF) : (nvh > 0 ? 1.0f / nf : 0.0f);
+            part0 = nvh > 0 ? pre * (kk + s1 * inv_nf) : 0.0f;
+            part1 = nvh > 0 ? pre * pre * fmaxf(s2 - s1 * s1 * inv_nf, 0.0f) : 0.0f;
           } else {
             part0 = pre * pre * s2;
             part1 = 0.0f;
@@ -1011,9 +1026,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           }
           if (LN) {
             mean = part0;
-            rstd = rsqrtf(part1 / static_cast<float>(N) + p.eps);
+            rstd = rsqrtf(part1 * inv_N() + p.eps);
           } else {
-            rstd = rsqrtf(part0 / static_cast<float>(N) + p.eps);
+            rstd = rsqrtf(part0 * inv_N() + p.eps);
           }
         }
 
@@ -1111,7 +1126,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           if (LN) combine_mean_m2(mean, m2, n, v.x, v.y, nq);
           else ssq += v.x;
         }
-        st = make_float2(LN ? mean : 0.0f, rsqrtf((LN ? m2 : ssq) / static_cast<float>(N) + p.eps));
+        st = make_float2(LN ? mean : 0.0f, rsqrtf((LN ? m2 : ssq) * inv_N() + p.eps));
         const int m = m0 + k * 32 + lane;
         if (c0 == 0 && m < M) {
           if (LN && p.mean_out != nullptr) p.mean_out[m] = st.x;
