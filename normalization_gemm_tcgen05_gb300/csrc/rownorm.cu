@@ -243,7 +243,9 @@ __global__ void __launch_bounds__(256) backward_rows_kernel(const __nv_bfloat16*
 //   RMSNorm:   dH = rstd * (dh - h_hat * mean_n(dh * h_hat))
 //   dgamma = sum_m dC * h_hat,   dbeta = sum_m dC.
 // Row pass: one warp per row, two sweeps over the row (sums, then dH; the
-// second sweep reads from L2), 16-byte loads, any N.
+// second sweep reads from L2), 16-byte loads, any N.  The first sweep's
+// dh * h_hat is dC * (C - beta), with no division; the second multiplies by
+// correctly rounded reciprocals of gamma instead of dividing by it.
 constexpr int kRowsPerBlock = 8;
 
 __device__ __forceinline__ float bf16_at(const uint4& v, int e) {
@@ -272,10 +274,9 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) postnorm_bwd_rows_kernel(
     if (beta != nullptr) b = *reinterpret_cast<const uint4*>(beta + vi * 8);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float gm = bf16_at(g, e);
-      const float d = bf16_at(u, e) * gm;
-      s1 += d;
-      s2 = fmaf(d, (bf16_at(v, e) - bf16_at(b, e)) / gm, s2);
+      const float du = bf16_at(u, e);
+      s1 = fmaf(du, bf16_at(g, e), s1);
+      s2 = fmaf(du, bf16_at(v, e) - bf16_at(b, e), s2);  // (dC * gamma) * (C - beta) / gamma
     }
   }
 #pragma unroll
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) postnorm_bwd_rows_kernel(
       for (int q = 0; q < 2; ++q) {
         const int e = 2 * h + q;
         const float gm = bf16_at(g, e);
-        const float hat = (bf16_at(v, e) - bf16_at(b, e)) / gm;
+        const float hat = (bf16_at(v, e) - bf16_at(b, e)) * __frcp_rn(gm);
         y[q] = r * (bf16_at(u, e) * gm - m1 - hat * m2);
       }
       o[h] = pack_bf16x2(y[0], y[1]);
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(256) postnorm_bwd_cols_kernel(const __nv_bfloa
   float ig[8], bt[8], ag[8], ab[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    ig[e] = 1.0f / bf16_at(g, e);
+    ig[e] = __frcp_rn(bf16_at(g, e));
     bt[e] = bf16_at(b, e);
     ag[e] = ab[e] = 0.0f;
   }
