@@ -63,6 +63,19 @@ int round64(int64_t x) { return static_cast<int>((x + 63) / 64 * 64); }
 
 int gemm_tile_n(int64_t N) { return N <= 64 ? 64 : (N <= 128 ? 128 : 256); }
 
+// Tile width for the transposed and backward GEMMs: the widest tile that
+// covers N, halved while a grid of such tiles fills less than one wave of
+// SMs and the halved one still fits in one.  (A [2048 x 1024] weight
+// gradient: 64 tiles of 128 x 256 would leave 88 of 152 SMs idle.)
+int fill_tile_n(int64_t M, int64_t N) {
+  int bn = gemm_tile_n(N);
+  DeviceInfo dev;
+  if (current_device(&dev) != FNORM_OK) return bn;
+  auto tiles = [&](int b) { return ((M + 127) / 128) * ((N + b - 1) / b); };
+  while (bn > 64 && tiles(bn) < dev.num_sms && tiles(bn / 2) <= dev.num_sms) bn /= 2;
+  return bn;
+}
+
 // Keep all of B in shared memory when it is one tile wide (N <= bn), at most
 // 128 KB, and each CTA will visit several row blocks (more row blocks than
 // SMs), so B is read once per CTA instead of once per tile.
@@ -197,7 +210,7 @@ fnorm_status_t fnorm_gemm_ex(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf1
   if (!trans_a && !trans_b) return fnorm_gemm(A, B, C, M, N, K, stream);
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   L.mode = (trans_a ? MODE_AT : 0) | (trans_b ? MODE_BT : 0);
-  L.bn = gemm_tile_n(N);
+  L.bn = fill_tile_n(M, N);
   return launch_fused_transposed(L);
 }
 
@@ -456,7 +469,7 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
     // backward's row term in its epilogue
     FusedLaunch L = base_launch(dCs, B, dA, M, K, N, stream);
     L.mode = MODE_DGRAD | MODE_BT;
-    L.bn = gemm_tile_n(K);
+    L.bn = fill_tile_n(M, K);
     L.X = A;
     L.rowcoef = rowcoef;
     FN_TRY(launch_fused_backward(L));
@@ -465,7 +478,7 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
     // dB [K,N] = A^T @ dCs: a GEMM over M reading A^T straight from A
     FusedLaunch L = base_launch(A, dCs, dB, K, N, M, stream);
     L.mode = MODE_AT;
-    L.bn = gemm_tile_n(N);
+    L.bn = fill_tile_n(K, N);
     FN_TRY(launch_fused_transposed(L));
   }
   return FNORM_OK;

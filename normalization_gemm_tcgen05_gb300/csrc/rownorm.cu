@@ -363,20 +363,41 @@ __global__ void __launch_bounds__(256) postnorm_bwd_cols_kernel(const __nv_bfloa
   }
 }
 
-// dgamma[n] = sum_g part[g][0][n], dbeta[n] = sum_g part[g][1][n], in group order
-__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ part, int ngroups, int N,
-                                                         float* __restrict__ dgamma, float* __restrict__ dbeta) {
+// dgamma[n] = sum_g part[g][0][n], dbeta[n] = sum_g part[g][1][n].  A block
+// takes kSumCols columns; each of its kSumRows thread rows sums every
+// kSumRows-th group (loads coalesced along n, several in flight), and the
+// rows' sums are then added in row order, so the result is the same on every
+// run.
+constexpr int kSumCols = 32, kSumRows = 32;
+
+__global__ void __launch_bounds__(kSumCols * kSumRows) column_sum_kernel(const float* __restrict__ part, int ngroups,
+                                                                         int N, float* __restrict__ dgamma,
+                                                                         float* __restrict__ dbeta) {
+  __shared__ float ra[kSumRows][kSumCols + 1], rb[kSumRows][kSumCols + 1];
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+  const int tx = static_cast<int>(threadIdx.x) % kSumCols, ty = static_cast<int>(threadIdx.x) / kSumCols;
+  const int n = blockIdx.x * kSumCols + tx;
   float a = 0.0f, b = 0.0f;
-  for (int k = 0; k < ngroups; ++k) {
-    a += part[static_cast<size_t>(k) * 2 * N + n];
-    b += part[static_cast<size_t>(k) * 2 * N + N + n];
+  if (n < N) {
+#pragma unroll 4
+    for (int k = ty; k < ngroups; k += kSumRows) {
+      a += part[static_cast<size_t>(k) * 2 * N + n];
+      b += part[static_cast<size_t>(k) * 2 * N + N + n];
+    }
   }
-  if (dgamma != nullptr) dgamma[n] = a;
-  if (dbeta != nullptr) dbeta[n] = b;
+  ra[ty][tx] = a;
+  rb[ty][tx] = b;
+  __syncthreads();
+  if (ty == 0 && n < N) {
+    float sa = 0.0f, sb = 0.0f;
+    for (int r = 0; r < kSumRows; ++r) {
+      sa += ra[r][tx];
+      sb += rb[r][tx];
+    }
+    if (dgamma != nullptr) dgamma[n] = sa;
+    if (dbeta != nullptr) dbeta[n] = sb;
+  }
 }
 
 }  // namespace
@@ -482,6 +503,7 @@ fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, cons
   const auto* g = static_cast<const __nv_bfloat16*>(gamma);
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
   cudaLaunchAttribute attr[1];
+  const bool cols = dgamma != nullptr || dbeta != nullptr;
   if (dH != nullptr) {
     cudaLaunchConfig_t cfg =
         small_cfg(dim3((unsigned)((M + kRowsPerBlock - 1) / kRowsPerBlock)), dim3(32 * kRowsPerBlock), stream, attr);
@@ -492,12 +514,12 @@ fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, cons
                                        static_cast<__nv_bfloat16*>(dH), M, N);
     if (e != cudaSuccess) return cuda_fail(e, "post-norm backward row pass launch");
   }
-  if (dgamma != nullptr || dbeta != nullptr) {
+  if (cols) {
     const int groups = postnorm_backward_groups(M);
     cudaLaunchConfig_t cfg = small_cfg(dim3((unsigned)((N / 8 + 255) / 256), (unsigned)groups), dim3(256), stream, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, postnorm_bwd_cols_kernel, dc, c, g, b, part, M, N);
     if (e != cudaSuccess) return cuda_fail(e, "post-norm backward column pass launch");
-    cfg = small_cfg(dim3((unsigned)((N + 255) / 256)), dim3(256), stream, attr);
+    cfg = small_cfg(dim3((unsigned)((N + kSumCols - 1) / kSumCols)), dim3(kSumCols * kSumRows), stream, attr);
     e = cudaLaunchKernelEx(&cfg, column_sum_kernel, static_cast<const float*>(part), groups, N, dgamma, dbeta);
     if (e != cudaSuccess) return cuda_fail(e, "column sum launch");
   }
