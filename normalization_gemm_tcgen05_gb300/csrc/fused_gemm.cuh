@@ -121,6 +121,7 @@ struct Aux {
   uint64_t ebar[4][2];  // bounded barrier of the two epilogue warps of each TMEM lane quarter
   uint64_t teardown;
   uint64_t bres_full[NBR];  // one per k-block of resident B
+  uint64_t rload;           // the first residual tile, loaded by TMA (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort_flag;
   int nstat_m0[HD];
@@ -422,7 +423,8 @@ __device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
+                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                      const FusedParams p) {
   constexpr int BK = Cfg::BK, BN = Cfg::BN, STAGES = Cfg::STAGES, HALF = Cfg::HALF, NCH = Cfg::NCH;
   constexpr bool PRE = Cfg::PRE, POST = Cfg::POST, LN = Cfg::LN, CLUSTER = Cfg::CLUSTER, SPILL = Cfg::SPILL;
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
@@ -487,6 +489,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     }
     mbar_init(smem_u32(&aux->teardown), 1);
     for (int kb = 0; kb < (BRES ? Cfg::KB_MAX : 1); ++kb) mbar_init(smem_u32(&aux->bres_full[kb]), 1);
+    mbar_init(smem_u32(&aux->rload), kEpiWarps);
     aux->abort_flag = 0;
     fence_mbar_init();
   }
@@ -761,10 +764,70 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       preload_residual<NCH>(p, tb2, (t2 / ngroups) * Cfg::BM + row, n0b + h * HALF);
       return true;
     };
+    // The first tile's residual by TMA, when a warp's staging buffers hold its
+    // half of a tile: each warp loads its [32 x 32] boxes of R (the C store
+    // layout, zero-filled past M and N), then every lane moves its row into
+    // tensor memory.  One bulk copy per box instead of a 16-byte load per row
+    // segment, so the first MMA, which waits for this, is not held up behind
+    // the ring's loads.  Returns 1 when loaded, 0 with no tile, -1 if the
+    // wait gave up.
+    constexpr bool RTMA = RES && !CLUSTER && !SPILL && NCH <= Cfg::STG_BUFS;
+    auto preload_first_tma = [&]() -> int {
+      if (cid >= total) return 0;
+      const int n0b = ((cid % ngroups) * C + rank) * cta_cols + h * HALF;
+      const int r0 = (cid / ngroups) * Cfg::BM + q * 32;
+      const uint32_t bar = smem_u32(&aux->rload);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NCH) * kBoxBytes);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) tma_load_2d(stg + c * kBoxBytes, &tmR, n0b + c * 32, r0, bar);
+      }
+      if (!mbar_wait_warp(wc, bar, 0u, kSiteEpilogue)) {
+        // gave up (or another role did): the copies in flight land before
+        // this CTA can exit (bounded teardown drain)
+        if (lane == 0) mbar_wait<false, true>(wc, bar, 0u, kSiteTeardown);
+        __syncwarp();
+        return -1;
+      }
+      const uint32_t tb0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * HALF);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        // row `lane` of box c: 16-byte chunk ch at chunk ch ^ ((row >> 1) & 3)
+        const uint32_t rbase = stg + c * kBoxBytes + static_cast<uint32_t>(lane) * 64u;
+        uint32_t v[32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t x0, x1, x2, x3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                       : "r"(rbase + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4))
+                       : "memory");
+          const uint32_t in[4] = {x0, x1, x2, x3};
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            v[ch * 8 + 2 * hh] = __float_as_uint(bf16_lo(in[hh]));
+            v[ch * 8 + 2 * hh + 1] = __float_as_uint(bf16_hi(in[hh]));
+          }
+        }
+        tmem_st_32x32b_x32(tb0 + c * 32, v);
+      }
+      tmem_st_wait();
+      return 1;
+    };
+    bool preload_ok = true;
     if (RES) {
       // the first two tiles' buffers start out holding their residual
       for (int i2 = 0; i2 < 2; ++i2) {
-        if (!preload_iter(i2)) break;
+        if (RTMA && i2 == 0) {
+          const int r = preload_first_tma();
+          if (r < 0) {
+            preload_ok = false;
+            break;
+          }
+          if (r == 0) break;
+        } else if (!preload_iter(i2)) {
+          break;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[i2]));
@@ -805,7 +868,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     int pm0 = 0, pc0 = 0, pnext = 0;
     float pmean = 0.0f, prstd = 1.0f;
     int xit = 0;  // row-block statistics completed so far
-    bool ok = true;
+    bool ok = preload_ok;
 
     for (int t = cid; t < total && ok; t += ncl) {
       const int m0 = (t / ngroups) * Cfg::BM;

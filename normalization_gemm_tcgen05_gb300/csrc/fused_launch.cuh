@@ -49,6 +49,14 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   st = encode_tmap_bf16_2d(&tc, L.C, (uint64_t)L.N, (uint64_t)L.M, (uint64_t)L.N * 2, 32, 32,
                            CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != FNORM_OK) return st;
+  // the residual R [M,N] in the same [32 x 32] boxes (read by the first tile
+  // of the single-CTA residual layouts); otherwise unused
+  CUtensorMap tr = tc;
+  if (Cfg::RES) {
+    st = encode_tmap_bf16_2d(&tr, L.R, (uint64_t)L.N, (uint64_t)L.M, (uint64_t)L.N * 2, 32, 32,
+                             CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != FNORM_OK) return st;
+  }
 
   FusedParams p;
   p.M = L.M;
@@ -142,7 +150,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     const long long grid = total < dev.num_sms ? total : dev.num_sms;
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tr, p);
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
   return FNORM_OK;
 }

@@ -170,7 +170,13 @@ def test_rmsnorm_backward_standalone(M, N):
 # post-norm backward: dA, dB, dgamma, dbeta of norm(A @ B) * gamma + beta
 # ----------------------------------------------------------------------------
 POSTB = [("layernorm", 256, 64, 256), ("rmsnorm", 200, 128, 72), ("layernorm", 256, 1024, 256),
-         ("rmsnorm", 1000, 200, 128), ("layernorm", 128, 4096, 64), ("layernorm", 8, 8, 8)]
+         ("rmsnorm", 1000, 200, 128), ("layernorm", 128, 4096, 64), ("layernorm", 8, 8, 8),
+         # 41 groups of 64 rows (the column sum's thread rows wrap), N not a
+         # multiple of 32 (a ragged last block of columns)
+         ("layernorm", 2568, 200, 64),
+         # a [2048 x 1024] weight gradient: 64 tiles of 128 x 256 would not
+         # fill the GPU, so it runs as 128 tiles of 128 x 128
+         ("rmsnorm", 512, 1024, 2048)]
 
 
 def _postb(norm, M, N, K, seed, affine=True):
