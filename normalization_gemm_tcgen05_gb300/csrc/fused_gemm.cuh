@@ -501,10 +501,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       // Warm L2 with the first ring of the first tile while the previous grid
       // in the stream finishes.  L2 is the point of coherence, so a line
       // brought in now still sees that grid's later writes; the loads proper
-      // are issued after griddepcontrol.wait.
+      // are issued after griddepcontrol.wait.  (The residual layouts warm two
+      // k-blocks only: their first MMA waits for the residual tile, whose
+      // loads a deeper warm-up would delay; measured 10.7 -> 10.3 us.)
       const int m0 = (cid / ngroups) * Cfg::BM;
       const int n0 = ((cid % ngroups) * C + rank) * cta_cols;
-      const int nk = num_kb < STAGES ? num_kb : STAGES;
+      constexpr int kWarm = RES ? 2 : STAGES;
+      const int nk = num_kb < kWarm ? num_kb : kWarm;
       for (int kb = 0; kb < nk; ++kb) {
         if (AT) {
           tma_prefetch_l2_2d(&tmA, m0, kb * BK);
