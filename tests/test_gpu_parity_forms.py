@@ -29,6 +29,8 @@ def _dev(t):
 RES_CASES = [  # (norm, M, N, K): one CTA, resident cluster, spill layout
     ("layernorm", 256, 64, 256), ("rmsnorm", 200, 128, 72), ("layernorm", 333, 200, 1000),
     ("layernorm", 256, 256, 512), ("rmsnorm", 129, 8, 64),
+    # first-tile residual by TMA: a half's box partly past N (128- and 64-column tiles)
+    ("layernorm", 200, 72, 128), ("rmsnorm", 131, 40, 64),
     ("layernorm", 256, 320, 256), ("rmsnorm", 300, 512, 512), ("layernorm", 256, 1024, 256),
     ("layernorm", 256, 1032, 256), ("rmsnorm", 256, 2048, 128), ("layernorm", 130, 4096, 256),
 ]
