@@ -111,10 +111,15 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 # helpers
 # --------------------------------------------------------------------------
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: whole-line // comments and blank lines
+    are left out, so that editing a comment does not count as a new kernel."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "normalization_gemm_tcgen05_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+            for line in f.read().splitlines():
+                t = line.strip()
+                if t and not t.startswith(b"//"):
+                    h.update(line + b"\n")
     return h.hexdigest()[:16]
 
 

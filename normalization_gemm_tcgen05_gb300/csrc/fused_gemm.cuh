@@ -11,7 +11,7 @@
 //   * epilogue post-norm, C = norm(A @ B) * gamma + beta, LayerNorm or RMSNorm
 //     ([FNF-ru] "Multi-CTA Norm Fusion": a norm is a row reduction plus an
 //     element-wise step, only the reduction needs the whole row, and its
-//     result is one scalar per row).  Three layouts of a row block:
+//     result is one scalar per row).  Four layouts of a row block:
 //       - resident, one CTA: the CTA's accumulator spans the whole row;
 //       - resident, cluster: the CTAs of a cluster split the row along N, each
 //         keeps its slice in tensor memory, pushes its per-row partial
@@ -22,8 +22,20 @@
 //         to C un-normalised while its statistics accumulate, and once the row
 //         block's statistics are exchanged the slices are re-read from L2 and
 //         normalised in place while the next row block's MMAs run.  Rows of
-//         any width, on small clusters.
-//   * both at once: norm(rmsnorm(A) @ B).
+//         any width, on small clusters;
+//       - spill, grid-wide: the same slices in units of S x 256 columns, one
+//         CTA per unit, the row statistics exchanged between all CTAs through
+//         global memory (published partials and per-row-block counters, a
+//         cooperative launch);
+//   * both at once: norm(rmsnorm(A) @ B);
+//   * residual: norm(A @ B + R), R written into the accumulator before the
+//     tile's MMAs accumulate onto it;
+//   * pre-norm with the affine folded into B: (norm(A) * gamma + beta) @ B
+//     as rstd * (A @ B' - mean * colsum(B')) + beta @ B, the LayerNorm's
+//     shifted sums of the A rows taken by the norm warps;
+//   * the backward's GEMMs: B^T and A^T operands read straight from their
+//     row-major arrays, and the Lazy Pre-RMSNorm's dgrad epilogue
+//     y = u + c_m * x.
 //
 // Warp roles (one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: A [128 x 64] and B [64 x BN] tiles into an
@@ -37,9 +49,10 @@
 //               tcgen05.ld of 32-column register subtiles, statistics (the two
 //               halves combine theirs through shared memory), normalise /
 //               scale, bf16, swizzled shared-memory staging, TMA stores.
-//   warps 10-13 Lazy Pre-Norm: sum of squares of the staged A rows; spill
-//               layout (without Lazy Pre-Norm): the in-place normalisation of
-//               finished row blocks, from L2.
+//   warps 10-13 Lazy Pre-Norm: sum of squares of the staged A rows (warps
+//               10-17 for the pre-LayerNorm, each row's chunks in two parts);
+//               spill layouts (without Lazy Pre-Norm): the in-place
+//               normalisation of finished row blocks, from L2.
 // A stage is released when the MMA commit and (for Lazy Pre-Norm) the four
 // norm warps have all arrived on its "empty" barrier.
 //
