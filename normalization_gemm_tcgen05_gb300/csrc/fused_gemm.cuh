@@ -481,13 +481,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const WaitCtx wc{p.wait_limit_ns, p.status, &aux->abort_flag};
 
   // ---------------- set-up ----------------
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+  if (warp == 0) {
+    // the barriers, initialised by the 32 lanes of warp 0 in parallel
+    for (int s = lane; s < STAGES; s += 32) {
       mbar_init(smem_u32(&aux->full[s]), 1);
       // the MMA's commit, and for the lazy pre-norm the norm warps' reads
       mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 * Cfg::NPART : 0));
     }
-    for (int b = 0; b < 2; ++b) {
+    if (lane < 2) {
+      const int b = lane;
       mbar_init(smem_u32(&aux->acc_full[b]), 1);
       mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps);
       // handoffs between warp groups: one arrival per warp, after __syncwarp
@@ -496,17 +498,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->xbar[b]), 1);
       for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&aux->ebar[qq][b]), kEpiWarps / 4);
     }
-    for (int b = 0; b < HD; ++b) {
-      mbar_init(smem_u32(&aux->nstat_full[b]), kEpiWarps);
-      mbar_init(smem_u32(&aux->nstat_empty[b]), 4);
+    if (lane >= 2 && lane < 2 + HD) {
+      mbar_init(smem_u32(&aux->nstat_full[lane - 2]), kEpiWarps);
+      mbar_init(smem_u32(&aux->nstat_empty[lane - 2]), 4);
     }
-    mbar_init(smem_u32(&aux->teardown), 1);
-    for (int kb = 0; kb < (BRES ? Cfg::KB_MAX : 1); ++kb) mbar_init(smem_u32(&aux->bres_full[kb]), 1);
-    mbar_init(smem_u32(&aux->rload), kEpiWarps);
-    aux->abort_flag = 0;
+    for (int kb = lane; kb < (BRES ? Cfg::KB_MAX : 1); kb += 32) mbar_init(smem_u32(&aux->bres_full[kb]), 1);
+    if (lane == 31) {
+      mbar_init(smem_u32(&aux->teardown), 1);
+      mbar_init(smem_u32(&aux->rload), kEpiWarps);
+      aux->abort_flag = 0;
+    }
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 2 && lane == 0) {
+    // (an epilogue warp, idle until the set-up ends, so that the warm-up
+    // starts at kernel entry rather than after the barrier set-up)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
