@@ -11,6 +11,8 @@
 // registers, then the row is normalised and written with 16-byte stores.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -363,6 +365,117 @@ __global__ void __launch_bounds__(256) postnorm_bwd_cols_kernel(const __nv_bfloa
   }
 }
 
+// Row and column passes in one (N <= 1024, both wanted).  A block takes one
+// kColRows-row group and a warp every kRowsPerBlock-th row of it; a lane keeps
+// its columns' dC and C of the current row in registers between the two
+// sweeps (each read once), and adds its columns' dgamma/dbeta contributions
+// into its warp's own slice of shared memory.  The block then sums the
+// warps' slices in warp order into part[group] (the column pass's layout).
+template <bool LN, int VPL>
+__global__ void __launch_bounds__(32 * kRowsPerBlock, 2) postnorm_bwd_fused_kernel(
+    const __nv_bfloat16* __restrict__ dC, const __nv_bfloat16* __restrict__ C, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ beta, const float* __restrict__ rstd_in, __nv_bfloat16* __restrict__ dH,
+    float* __restrict__ part, int M, int N) {
+  extern __shared__ float red[];  // [kRowsPerBlock][2][N]
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = blockIdx.x;
+  const int nvec = N >> 3;
+  float* pw = red + static_cast<size_t>(warp) * 2 * N;
+  for (int n = lane; n < 2 * N; n += 32) pw[n] = 0.0f;
+  __syncwarp();
+  // gamma and beta of this lane's columns, re-read each row through the
+  // read-only cache rather than held in registers
+  auto gb = [&](int j, uint4& g, uint4& b) {
+    const int vi = lane + 32 * j;
+    g = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+    b = make_uint4(0, 0, 0, 0);
+    if (vi < nvec && gamma != nullptr) g = __ldg(reinterpret_cast<const uint4*>(gamma + vi * 8));
+    if (vi < nvec && beta != nullptr) b = __ldg(reinterpret_cast<const uint4*>(beta + vi * 8));
+  };
+  const float inv_n = 1.0f / static_cast<float>(N);
+  for (int i = warp; i < kColRows; i += kRowsPerBlock) {
+    const int row = grp * kColRows + i;
+    if (row >= M) break;
+    const size_t off = static_cast<size_t>(row) * N;
+    uint4 u[VPL], v[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int vi = lane + 32 * j;
+      u[j] = v[j] = make_uint4(0, 0, 0, 0);  // columns past N add zero
+      if (vi < nvec) {
+        u[j] = ld_stream(dC + off + vi * 8);
+        v[j] = ld_stream(C + off + vi * 8);
+      }
+    }
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      uint4 g, b;
+      gb(j, g, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float du = bf16_at(u[j], e);
+        s1 = fmaf(du, bf16_at(g, e), s1);
+        s2 = fmaf(du, bf16_at(v[j], e) - bf16_at(b, e), s2);  // (dC * gamma) * (C - beta) / gamma
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    const float r = rstd_in[row];
+    const float m1 = LN ? s1 * inv_n : 0.0f, m2 = s2 * inv_n;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int vi = lane + 32 * j;
+      if (vi >= nvec) continue;
+      uint4 g, b;
+      gb(j, g, b);
+      float hat[8];
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float y[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int e = 2 * h + q;
+          const float gm = bf16_at(g, e);
+          hat[e] = (bf16_at(v[j], e) - bf16_at(b, e)) * __frcp_rn(gm);
+          y[q] = r * (bf16_at(u[j], e) * gm - m1 - hat[e] * m2);
+        }
+        o[h] = pack_bf16x2(y[0], y[1]);
+      }
+      *reinterpret_cast<uint4*>(dH + off + vi * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+      float4* pg = reinterpret_cast<float4*>(pw + vi * 8);
+      float4* pb = reinterpret_cast<float4*>(pw + N + vi * 8);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float4 ga = pg[hh], ba = pb[hh];
+        ga.x = fmaf(bf16_at(u[j], 4 * hh), hat[4 * hh], ga.x);
+        ga.y = fmaf(bf16_at(u[j], 4 * hh + 1), hat[4 * hh + 1], ga.y);
+        ga.z = fmaf(bf16_at(u[j], 4 * hh + 2), hat[4 * hh + 2], ga.z);
+        ga.w = fmaf(bf16_at(u[j], 4 * hh + 3), hat[4 * hh + 3], ga.w);
+        ba.x += bf16_at(u[j], 4 * hh);
+        ba.y += bf16_at(u[j], 4 * hh + 1);
+        ba.z += bf16_at(u[j], 4 * hh + 2);
+        ba.w += bf16_at(u[j], 4 * hh + 3);
+        pg[hh] = ga;
+        pb[hh] = ba;
+      }
+    }
+  }
+  __syncthreads();
+  float* pgo = part + static_cast<size_t>(grp) * 2 * N;
+  for (int n = threadIdx.x; n < 2 * N; n += blockDim.x) {
+    float acc = 0.0f;
+    for (int w = 0; w < kRowsPerBlock; ++w) acc += red[static_cast<size_t>(w) * 2 * N + n];
+    pgo[n] = acc;
+  }
+}
+
 // dgamma[n] = sum_g part[g][0][n], dbeta[n] = sum_g part[g][1][n].  A block
 // takes kSumCols columns; each of its kSumRows thread rows sums every
 // kSumRows-th group (loads coalesced along n, several in flight), and the
@@ -492,6 +605,25 @@ cudaLaunchConfig_t small_cfg(dim3 grid, dim3 block, cudaStream_t stream, cudaLau
 
 int postnorm_backward_groups(int M) { return (M + kColRows - 1) / kColRows; }
 
+namespace {
+// the fused row and column pass: 64 N bytes of shared memory (opted in once
+// per device, up to 64 KB at N = 1024)
+template <bool LN, int VPL>
+cudaError_t launch_postnorm_fused(cudaLaunchConfig_t& cfg, int dev_id, const __nv_bfloat16* dc,
+                                  const __nv_bfloat16* c, const __nv_bfloat16* g, const __nv_bfloat16* b,
+                                  const float* rstd, __nv_bfloat16* dh, float* part, int M, int N) {
+  auto kern = postnorm_bwd_fused_kernel<LN, VPL>;
+  static std::atomic<uint64_t> configured{0};  // one bit per device
+  if (!((configured.load(std::memory_order_acquire) >> dev_id) & 1ull)) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(1ull << dev_id, std::memory_order_acq_rel);
+  }
+  cfg.dynamicSmemBytes = static_cast<size_t>(kRowsPerBlock) * 2 * N * sizeof(float);
+  return cudaLaunchKernelEx(&cfg, kern, dc, c, g, b, rstd, dh, part, M, N);
+}
+}  // namespace
+
 fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, const void* gamma, const void* beta,
                                              const float* rstd, bool layernorm, void* dH, float* part, float* dgamma,
                                              float* dbeta, int M, int N, cudaStream_t stream) {
@@ -504,6 +636,28 @@ fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, cons
   const auto* b = static_cast<const __nv_bfloat16*>(beta);
   cudaLaunchAttribute attr[1];
   const bool cols = dgamma != nullptr || dbeta != nullptr;
+  if (dH != nullptr && cols && N <= 1024) {
+    // both passes in one kernel (each row of dC and C read once), then the column sum
+    const int groups = postnorm_backward_groups(M);
+    const int vpl = (N / 8 + 31) / 32;
+    cudaLaunchConfig_t cfg = small_cfg(dim3((unsigned)groups), dim3(32 * kRowsPerBlock), stream, attr);
+    auto* dh = static_cast<__nv_bfloat16*>(dH);
+    cudaError_t e;
+    if (vpl <= 1)
+      e = layernorm ? launch_postnorm_fused<true, 1>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N)
+                    : launch_postnorm_fused<false, 1>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N);
+    else if (vpl <= 2)
+      e = layernorm ? launch_postnorm_fused<true, 2>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N)
+                    : launch_postnorm_fused<false, 2>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N);
+    else
+      e = layernorm ? launch_postnorm_fused<true, 4>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N)
+                    : launch_postnorm_fused<false, 4>(cfg, dev.id, dc, c, g, b, rstd, dh, part, M, N);
+    if (e != cudaSuccess) return cuda_fail(e, "post-norm backward row and column pass launch");
+    cfg = small_cfg(dim3((unsigned)((N + kSumCols - 1) / kSumCols)), dim3(kSumCols * kSumRows), stream, attr);
+    e = cudaLaunchKernelEx(&cfg, column_sum_kernel, static_cast<const float*>(part), groups, N, dgamma, dbeta);
+    if (e != cudaSuccess) return cuda_fail(e, "column sum launch");
+    return FNORM_OK;
+  }
   if (dH != nullptr) {
     cudaLaunchConfig_t cfg =
         small_cfg(dim3((unsigned)((M + kRowsPerBlock - 1) / kRowsPerBlock)), dim3(32 * kRowsPerBlock), stream, attr);
