@@ -471,6 +471,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const int cid = static_cast<int>(blockIdx.x) / C;
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_kb = (K + BK - 1) / BK;
+  // The k-th tile of this CTA (t = row block * ngroups + column group):
+  // cid + k * ncl.  The lazy pre-norm GEMMs without a post-norm whose rows
+  // span several column groups take pairs of neighbouring tiles instead:
+  // iterations 2q and 2q + 1 take tiles 2 * (q * ncl + cid) and the next one,
+  // mostly of one row block, so the norm warps sum its rows once per pair; a
+  // round of pairs still spans only 2 * ncl consecutive tiles (a few row
+  // blocks of A), and the last, partial round goes back to single tiles.
+  constexpr bool PAIRS = PRE && !POST && !CLUSTER && !SPILL;
+  const int full_rounds = PAIRS && ngroups > 1 ? total / (2 * ncl) : 0;
+  auto tile_of = [&](int k) -> int {
+    if (k < 2 * full_rounds) return 2 * ((k >> 1) * ncl + cid) + (k & 1);
+    return 2 * full_rounds * ncl + cid + (k - 2 * full_rounds) * ncl;
+  };
   // The per-row statistics multiply by 1/N and 1/K (correctly rounded
   // reciprocals: exact, as a division would be, whenever N and K are powers
   // of two) instead of dividing; a division costs far more on the epilogue's
@@ -516,15 +529,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    if (cid < total) {
+    if (tile_of(0) < total) {
       // Warm L2 with the first ring of the first tile while the previous grid
       // in the stream finishes.  L2 is the point of coherence, so a line
       // brought in now still sees that grid's later writes; the loads proper
       // are issued after griddepcontrol.wait.  (The residual layouts warm two
       // k-blocks only: their first MMA waits for the residual tile, whose
       // loads a deeper warm-up would delay; measured 10.7 -> 10.3 us.)
-      const int m0 = (cid / ngroups) * Cfg::BM;
-      const int n0 = ((cid % ngroups) * C + rank) * cta_cols;
+      const int t0 = tile_of(0);
+      const int m0 = (t0 / ngroups) * Cfg::BM;
+      const int n0 = ((t0 % ngroups) * C + rank) * cta_cols;
       constexpr int kWarm = RES ? 2 : STAGES;
       const int nk = num_kb < kWarm ? num_kb : kWarm;
       for (int kb = 0; kb < nk; ++kb) {
@@ -562,7 +576,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, filled = 0, fill_par = 0;
       int bres_issued = 0;  // resident-B k-blocks issued (each on its own barrier)
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl) {
+      for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
         const int m0 = (t / ngroups) * Cfg::BM;
         for (int s = 0; s < S && ok; ++s) {
           const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN;
@@ -571,7 +585,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               ok = false;
               break;
             }
-            if (BRES && t == cid) {
+            if (BRES && k == 0) {
               // all of B once, during the first tile: k-block kb just ahead
               // of the A stage that pairs with it, so the first MMAs need not
               // wait for the whole of B
@@ -624,7 +638,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl) {
+      for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
         for (int s = 0; s < S && ok; ++s, ++it) {
           const int buf = it & 1;
           const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
@@ -892,7 +906,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     int xit = 0;  // row-block statistics completed so far
     bool ok = preload_ok;
 
-    for (int t = cid; t < total && ok; t += ncl) {
+    for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
       const int m0 = (t / ngroups) * Cfg::BM;
       const int g = t % ngroups;
       for (int s = 0; s < S && ok; ++s, ++it) {
@@ -1236,7 +1250,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0;
     int it = 0;
     bool ok = true;
-    for (int t = cid; t < total && ok; t += ncl) {
+    // the previous tile's row block and this row's sums over it: a tile of the
+    // same row block (the second of a pair) reuses them, still waiting for and
+    // releasing every stage as the MMA does
+    int held_rb = -1;
+    float held_s2 = 0.0f, held_s1 = 0.0f, held_shift = 0.0f;
+    for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
+      const bool reuse = PAIRS && t / ngroups == held_rb;
+      held_rb = t / ngroups;
       for (int s = 0; s < S && ok; ++s, ++it) {
         // packed pairs of partial sums: acc = sum of squares (of a - shift for
         // the pre-LayerNorm), lsum = sum of (a - shift)
@@ -1249,14 +1270,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             break;
           }
           const uint8_t* arow = smem + stage * STAGE_BYTES + row * ROW_BYTES;
-          if (PRE_LN && kb == 0) {
+          if (PRE_LN && kb == 0 && !reuse) {
             // the shift is the row's first element, a[row][0] (logical chunk 0),
             // the same for both parts
             shift = bf16_lo(*reinterpret_cast<const uint32_t*>(arow + (swz << 4)));
             sh2 = f2(shift, shift);
           }
 #pragma unroll
-          for (int c = 0; c < CPP; ++c) {
+          for (int c = 0; c < (reuse ? 0 : CPP); ++c) {
             // visit the part's chunks in a bank-conflict-free order (the
             // lanes' rows have distinct swizzle phases); sums do not depend
             // on the order
@@ -1291,8 +1312,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           break;
         }
         float s2t = (f2_lo(acc[0]) + f2_hi(acc[0])) + (f2_lo(acc[1]) + f2_hi(acc[1]));
+        float s1t = 0.0f;
         if (PRE_LN) {
-          float s1t = (f2_lo(lsum[0]) + f2_hi(lsum[0])) + (f2_lo(lsum[1]) + f2_hi(lsum[1]));
+          s1t = (f2_lo(lsum[0]) + f2_hi(lsum[0])) + (f2_lo(lsum[1]) + f2_hi(lsum[1]));
           if (part == 0) {
             // the zero-filled tail of the last k-block added (0 - shift) per
             // element to one part or the other; both share the shift, so part
@@ -1300,8 +1322,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const float pad = static_cast<float>(num_kb * BK - K);
             s1t += pad * shift;
             s2t -= pad * shift * shift;
-            aux->ssk[sb][row] = shift;
           }
+        }
+        if (reuse) {
+          s2t = held_s2;
+          s1t = held_s1;
+          shift = held_shift;
+        } else {
+          held_s2 = s2t;
+          held_s1 = s1t;
+          held_shift = shift;
+        }
+        if (PRE_LN) {
+          if (part == 0) aux->ssk[sb][row] = shift;
           aux->ss1[sb][part][row] = s1t;
         }
         aux->ss[sb][part][row] = s2t;
