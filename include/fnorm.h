@@ -390,6 +390,21 @@ fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta);
 fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size);
 
 /*
+ * fnorm_set_pair_mma — choose when fnorm_gemm, fnorm_lazy_prenorm_gemm and
+ * fnorm_prenorm_gemm run their 256-column tiles as two-CTA MMAs (a cluster of
+ * two CTAs computes a [256 x 256] tile with tcgen05 cta_group::2; each CTA
+ * stages its 128 rows of A and half of the tile's B columns, and the second
+ * CTA's copies complete on the first CTA's barriers).  mode: 1 = whenever the
+ * tile is 256 columns wide and B is not resident; 0 = never; -1 = automatic,
+ * the default, which keeps the one-CTA tiles (on GB300 they measured as fast
+ * or faster on every shape tried).  It changes the schedule, not the
+ * arithmetic: every output is the same sum over K in the same order, and the
+ * two forms agree bit for bit.  Process-wide.  Any other mode returns
+ * FNORM_ERR_INVALID_ARG.
+ */
+fnorm_status_t fnorm_set_pair_mma(int mode);
+
+/*
  * fnorm_debug_wait_timeout — failure-detection self test.  Launches one small
  * kernel that waits, with a bound of limit_ns, on a barrier that nothing
  * arrives on; the wait runs out, the kernel records a timeout in the device

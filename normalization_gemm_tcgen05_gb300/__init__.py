@@ -38,7 +38,7 @@ __all__ = [
     "gemm_postnorm_backward", "gemm_postnorm_noalloc", "lazy_prenorm_gemm_backward", "gemm_postnorm",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
-    "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster",
+    "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster", "set_pair_mma",
     "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
 ]
 
@@ -92,6 +92,7 @@ _SIGNATURES = {
     "fnorm_set_wait_limit_ns": (_c_status, [ctypes.c_uint64]),
     "fnorm_postnorm_plan": (_c_status, [_i64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "fnorm_set_postnorm_cluster": (_c_status, [ctypes.c_int]),
+    "fnorm_set_pair_mma": (_c_status, [ctypes.c_int]),
     "fnorm_debug_wait_timeout": (_c_status, [ctypes.c_uint64, _p]),
     "fnorm_version": (ctypes.c_int, []),
 }
@@ -535,6 +536,11 @@ def postnorm_plan(N: int) -> tuple[int, int]:
 def set_postnorm_cluster(cluster_size: int) -> None:
     """Force the post-norm cluster size (0 = automatic)."""
     _check(lib().fnorm_set_postnorm_cluster(int(cluster_size)))
+
+
+def set_pair_mma(mode: int) -> None:
+    """When 256-column GEMM tiles run as two-CTA MMAs: -1 automatic, 0 never, 1 always (see fnorm_set_pair_mma)."""
+    _check(lib().fnorm_set_pair_mma(int(mode)))
 
 
 def debug_wait_timeout(limit_ns: int = 50_000_000, device=None) -> None:

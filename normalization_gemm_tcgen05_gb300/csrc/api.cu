@@ -17,6 +17,7 @@ fnorm_status_t read_and_clear_status(cudaStream_t stream);
 
 namespace {
 std::atomic<int> g_forced_cluster{0};
+std::atomic<int> g_pair_mode{-1};  // fnorm_set_pair_mma: -1 automatic, 0 never, 1 whenever eligible
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
 
@@ -84,6 +85,19 @@ bool want_resident_b(int64_t M, int64_t N, int64_t K, int bn) {
   if (current_device(&dev) != FNORM_OK) return false;
   const int64_t kb_max = 131072 / (64LL * bn * 2);
   return N <= bn && (K + 63) / 64 <= kb_max && (M + 127) / 128 > dev.num_sms;
+}
+
+// Two-CTA MMA for a 256-column GEMM tile, on request only (fnorm_set_pair_mma).
+// The pair halves what each SM takes in per tile, but on GB300 it measured no
+// faster than the one-CTA tile on any shape tried (8192 x 4096 x 4096: 160 us
+// against 158 us; 16384 x 4096 x 2048: 188 us against 177 us): the one-CTA
+// mainloop waits on the latency of its loads, not on their bytes, and the
+// pair's loads complete later.  Automatic selection therefore keeps one CTA.
+bool want_pair(int64_t M, int64_t N, int64_t K, int bn, bool bres) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return g_pair_mode.load(std::memory_order_relaxed) == 1 && bn == 256 && !bres;
 }
 
 // How a post-norm row of width N is laid out over the CTAs.
@@ -194,6 +208,7 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
   L.mode = 0;
   L.bn = gemm_tile_n(N);
   L.bres = want_resident_b(M, N, K, L.bn);
+  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_plain(L);
 }
 
@@ -230,6 +245,7 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
   L.bres = want_resident_b(M, N, K, L.bn);
   L.pre_eps = eps;
   L.rstd_out = rstd_out;
+  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_plain(L);
 }
 
@@ -380,12 +396,14 @@ fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folde
   if (!ln && bias == nullptr) {
     // RMSNorm with gamma only: the folded B makes it the plain lazy pre-norm
     L.mode = MODE_PRE;
+    if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
     return launch_fused_plain(L);
   }
   L.mode = MODE_PRE | MODE_AFF | (ln ? MODE_PRE_LN : 0);
   L.colsum = ln ? colsum : nullptr;
   L.bias = bias;
   L.mean_out = ln ? mean_out : nullptr;
+  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_prenorm_affine(L);
 }
 
@@ -631,6 +649,13 @@ fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size) {
   if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8)
     return bad("cluster size must be 0 (automatic), 1, 2, 4 or 8");
   g_forced_cluster.store(cluster_size, std::memory_order_relaxed);
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_set_pair_mma(int mode) {
+  clear_error();
+  if (mode < -1 || mode > 1) return bad("pair MMA mode must be -1 (automatic), 0 (never) or 1 (whenever eligible)");
+  g_pair_mode.store(mode, std::memory_order_relaxed);
   return FNORM_OK;
 }
 

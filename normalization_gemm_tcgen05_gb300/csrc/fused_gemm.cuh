@@ -35,7 +35,13 @@
 //     shifted sums of the A rows taken by the norm warps;
 //   * the backward's GEMMs: B^T and A^T operands read straight from their
 //     row-major arrays, and the Lazy Pre-RMSNorm's dgrad epilogue
-//     y = u + c_m * x.
+//     y = u + c_m * x;
+//   * the plain and lazy pre-norm GEMMs on a CTA pair (tcgen05 cta_group::2):
+//     a 2-CTA cluster computes each [256 x 256] tile, each CTA staging its 128
+//     rows of A and 128 of the tile's B columns; the second CTA's copies
+//     complete on the first CTA's full barriers, the first CTA issues the
+//     MMAs of both, and their commits release the stages (and accumulators)
+//     of both.
 //
 // Warp roles (one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: A [128 x 64] and B [64 x BN] tiles into an
@@ -43,7 +49,7 @@
 //               all of B is resident in shared memory.
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, M = 128,
 //               N = BN, K = 16, fp32 accumulators in tensor memory, double
-//               buffered.
+//               buffered (CTA pair: M = 256, issued by the first CTA).
 //   warps 2-9   epilogue, two warps per TMEM lane quarter: warps 2-5 own the
 //               first BN/2 columns of a tile, warps 6-9 the second half.
 //               tcgen05.ld of 32-column register subtiles, statistics (the two
@@ -82,6 +88,10 @@ enum : int {
   MODE_AT = 1024,     // A operand MN-major: read from a row-major [K, M] array (A^T of an [M, K] matrix)
   MODE_DGRAD = 4096,  // RMSNorm backward epilogue: y = u + c[m] * X[m, n]
   MODE_GX = 8192,     // spill layout with the row statistics exchanged grid-wide through global memory
+  // two-CTA MMA: the two CTAs of a cluster compute one [256 x BN] tile with
+  // tcgen05 cta_group::2, each staging its own 128 rows of A and half of B's
+  // BN columns, so that each SM takes in a third less per tile
+  MODE_CTA2 = 16384,
 };
 
 struct FusedParams {
@@ -124,6 +134,7 @@ template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART,
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
+  uint64_t mdone[STAGES_];  // CTA pair, rank 1: the MMAs have read the stage (its norm warps' signal)
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t ss_full[2];
@@ -170,6 +181,10 @@ struct KCfg {
   static constexpr bool AT = (MODE & MODE_AT) != 0;
   static constexpr bool DGRAD = (MODE & MODE_DGRAD) != 0;
   static constexpr bool GX = (MODE & MODE_GX) != 0;
+  static constexpr bool CTA2 = (MODE & MODE_CTA2) != 0;
+  static constexpr int CG = CTA2 ? 2 : 1;      // CTA group of every tcgen05 instruction
+  static constexpr int RB = CTA2 ? 256 : 128;  // rows of one tile (a row block)
+  static constexpr int BNS = CTA2 ? BN / 2 : BN;  // columns of B this CTA stages
   // the spill layout's in-place normalisation runs in its own warps (10-13)
   // unless those warps compute the Lazy Pre-Norm sums of squares
   static constexpr bool NORMW = SPILL && !PRE;
@@ -186,7 +201,7 @@ struct KCfg {
   static constexpr int GB = (POST && !SPILL) ? BN : 1;  // gamma/beta kept in shared memory
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BK * BN * 2;
+  static constexpr uint32_t B_BYTES = BK * BNS * 2;
   // resident B: up to 128 KB, i.e. KB_MAX k-blocks of [64 x BN]
   static constexpr int KB_MAX = BRES ? (int)(131072u / B_BYTES) : 0;
   static constexpr uint32_t BRES_BYTES = (uint32_t)KB_MAX * B_BYTES;
@@ -203,20 +218,24 @@ struct KCfg {
   static constexpr uint32_t AUX_BYTES =
       (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1)>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
-  // that buys a pipeline stage and either the ring is below 4 stages or a
+  // that buys a pipeline stage and either the ring is below 4 stages, or a
   // warp stores only one box per tile (64-column tiles), so that nothing
-  // waits on the single buffer within a tile: a narrow tile streams A at a
-  // rate set by the bytes its ring keeps in flight.
+  // waits on the single buffer within a tile (a narrow tile streams A at a
+  // rate set by the bytes its ring keeps in flight), or the tile is a CTA
+  // pair's (six stages measured 160 us against 169 us for five on an
+  // 8192 x 4096 x 4096 GEMM).
   static constexpr int stages_with(int bufs) {
     return (int)((kSmemLimit - 1024 - BRES_BYTES - kEpiWarps * bufs * kBoxBytes - AUX_BYTES) / STAGE_BYTES);
   }
   static constexpr int STG_BUFS =
-      ((stages_with(2) < 4 || NCH == 1) && stages_with(1) > stages_with(2) && stages_with(2) < kMaxStages) ? 1 : 2;
+      ((stages_with(2) < 4 || NCH == 1 || CTA2) && stages_with(1) > stages_with(2) && stages_with(2) < kMaxStages)
+          ? 1
+          : 2;
   static constexpr uint32_t STG_BYTES = kEpiWarps * STG_BUFS * kBoxBytes;
   static constexpr int STAGES = stages_with(STG_BUFS) < kMaxStages ? stages_with(STG_BUFS) : kMaxStages;
   static constexpr uint32_t SMEM_BYTES = 1024 + BRES_BYTES + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;
   static constexpr int NUM_THREADS = 32 * (2 + kEpiWarps + AUX_WARPS);
-  static constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, !BT, AT);
+  static constexpr uint32_t IDESC = make_idesc_bf16_f32(RB, BN, !BT, AT);
 
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage ring");
@@ -231,6 +250,8 @@ struct KCfg {
                 "backward operand layouts serve the plain and lazy GEMMs");
   static_assert(!DGRAD || (BT && !AT && !PRE), "the dgrad: B^T operand, per-row coefficients from memory");
   static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
+  static_assert(!CTA2 || (BN == 256 && !POST && !BRES && !RES && !BT && !AT && !DGRAD),
+                "two-CTA MMA: 256-column tiles of the plain and lazy pre-norm GEMMs");
 };
 
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
@@ -443,6 +464,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD, GX = Cfg::GX;
+  constexpr bool CTA2 = Cfg::CTA2;
+  constexpr int CG = Cfg::CG, RB = Cfg::RB;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
                    (Cfg::BRES ? Cfg::KB_MAX : 1)>;
@@ -463,13 +486,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const int C = CLUSTER ? p.cluster : 1;
   const int S = SPILL ? p.slices : 1;
   const int rank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
-  const int num_m = (M + Cfg::BM - 1) / Cfg::BM;
+  // CTA pair: rank 0 issues the MMAs of both CTAs; each CTA owns rows
+  // prank * 128 .. + 127 of every 256-row tile
+  const int prank = CTA2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool issuer = prank == 0;
+  const int num_m = (M + RB - 1) / RB;
   const int cta_cols = S * BN;
   const int group_cols = cta_cols * C;
   const int ngroups = (N + group_cols - 1) / group_cols;
   const int total = num_m * ngroups;  // row blocks (x column groups) to visit
-  const int cid = static_cast<int>(blockIdx.x) / C;
-  const int ncl = static_cast<int>(gridDim.x) / C;
+  const int CP = CTA2 ? 2 : C;  // CTAs that share each tile sequence
+  const int cid = static_cast<int>(blockIdx.x) / CP;
+  const int ncl = static_cast<int>(gridDim.x) / CP;
   const int num_kb = (K + BK - 1) / BK;
   // The k-th tile of this CTA (t = row block * ngroups + column group):
   // cid + k * ncl.  The lazy pre-norm GEMMs without a post-norm whose rows
@@ -498,13 +526,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     // the barriers, initialised by the 32 lanes of warp 0 in parallel
     for (int s = lane; s < STAGES; s += 32) {
       mbar_init(smem_u32(&aux->full[s]), 1);
+      mbar_init(smem_u32(&aux->mdone[s]), 1);
       // the MMA's commit, and for the lazy pre-norm the norm warps' reads
       mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 * Cfg::NPART : 0));
     }
     if (lane < 2) {
       const int b = lane;
       mbar_init(smem_u32(&aux->acc_full[b]), 1);
-      mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps);
+      // (CTA pair: the epilogue warps of both CTAs, on rank 0's barrier)
+      mbar_init(smem_u32(&aux->acc_empty[b]), kEpiWarps * CG);
       // handoffs between warp groups: one arrival per warp, after __syncwarp
       mbar_init(smem_u32(&aux->ss_full[b]), 4 * Cfg::NPART);
       mbar_init(smem_u32(&aux->ss_empty[b]), kEpiWarps);
@@ -537,10 +567,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       // k-blocks only: their first MMA waits for the residual tile, whose
       // loads a deeper warm-up would delay; measured 10.7 -> 10.3 us.)
       const int t0 = tile_of(0);
-      const int m0 = (t0 / ngroups) * Cfg::BM;
-      const int n0 = ((t0 % ngroups) * C + rank) * cta_cols;
+      const int m0 = (t0 / ngroups) * RB + prank * Cfg::BM;
+      const int n0 = ((t0 % ngroups) * C + rank) * cta_cols + prank * Cfg::BNS;
       constexpr int kWarm = RES ? 2 : STAGES;
-      const int nk = num_kb < kWarm ? num_kb : kWarm;
+      const int nk = m0 < M ? (num_kb < kWarm ? num_kb : kWarm) : 0;
       for (int kb = 0; kb < nk; ++kb) {
         if (AT) {
           tma_prefetch_l2_2d(&tmA, m0, kb * BK);
@@ -551,18 +581,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (BT) {
           tma_prefetch_l2_2d(&tmB, kb * BK, n0);
         } else {
-          for (int c = 0; c < BN / 64; ++c) tma_prefetch_l2_2d(&tmB, n0 + c * 64, kb * BK);
+          for (int c = 0; c < Cfg::BNS / 64; ++c) tma_prefetch_l2_2d(&tmB, n0 + c * 64, kb * BK);
         }
       }
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&aux->tmem_base), Cfg::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(&aux->tmem_base), Cfg::TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
-  if (CLUSTER) cluster_sync();  // peers' barriers are initialised before any remote arrive
+  if (CLUSTER || CTA2) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_base;
   // Set-up above overlaps the previous grid in the stream; every global
@@ -575,12 +605,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, filled = 0, fill_par = 0;
       int bres_issued = 0;  // resident-B k-blocks issued (each on its own barrier)
+      // CTA pair, rank 1: rank 0's full barrier of a stage, and the copies
+      // into this CTA's shared memory that complete on it
+      auto peer_full0 = [&](uint32_t st) { return mapa_shared(smem_u32(&aux->full[st]), 0); };
+      auto load_pair = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint32_t bar) {
+        if (issuer) tma_load_2d(dst, m, c0, c1, bar);
+        else tma_load_2d_pair(dst, m, c0, c1, bar);
+      };
       bool ok = true;
       for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
-        const int m0 = (t / ngroups) * Cfg::BM;
+        const int m0 = (t / ngroups) * RB + prank * Cfg::BM;
         for (int s = 0; s < S && ok; ++s) {
-          const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN;
+          // (CTA pair: this CTA's half of the tile's B columns)
+          const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + prank * Cfg::BNS;
           for (int kb = 0; kb < num_kb; ++kb) {
+            // (CTA pair: the stage is released by rank 0's MMA commit)
             if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
               ok = false;
               break;
@@ -596,10 +635,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 tma_load_2d(bres_base + kb * Cfg::B_BYTES + c * (BK * 128), &tmB, c * 64, kb * BK, bf);
               bres_issued = kb + 1;
             }
-            const uint32_t full = smem_u32(&aux->full[stage]);
-            mbar_arrive_expect_tx(full, STAGE_BYTES);
+            // CTA pair: both CTAs' copies complete on rank 0's full barrier,
+            // which rank 0 arms with the bytes of both (rank 1's may land
+            // first: the transaction count runs negative until rank 0 arrives)
+            const uint32_t full = (CTA2 && !issuer) ? peer_full0(stage) : smem_u32(&aux->full[stage]);
+            if (!CTA2 || issuer) mbar_arrive_expect_tx(full, CTA2 ? 2u * STAGE_BYTES : STAGE_BYTES);
             const uint32_t sa = base + stage * STAGE_BYTES;
-            if (AT) {
+            if (CTA2) {
+              load_pair(sa, &tmA, kb * BK, m0, full);
+            } else if (AT) {
               // A^T: two MN-major chunks of [64 k-rows x 64 m] from the [K, M] array
               tma_load_2d(sa, &tmA, m0, kb * BK, full);
               tma_load_2d(sa + BK * 128, &tmA, m0 + 64, kb * BK, full);
@@ -613,7 +657,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 tma_load_2d(sb, &tmB, kb * BK, n0, full);
               } else {
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                for (int c = 0; c < Cfg::BNS / 64; ++c) {
+                  if (CTA2) load_pair(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                  else tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                }
               }
             }
             filled |= 1u << stage;
@@ -626,15 +673,20 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
       }
       // teardown drain: every copy issued into shared memory lands before exit
+      // (CTA pair, rank 1: its copies complete on rank 0's barriers; it waits
+      // instead until the MMAs have read each stage it filled)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u)
-          mbar_wait<false, true>(wc, smem_u32(&aux->full[s]), (fill_par >> s) & 1u, kSiteTeardown);
+          mbar_wait<false, true>(wc, smem_u32((CTA2 && !issuer) ? (PRE ? &aux->mdone[s] : &aux->empty[s]) : &aux->full[s]),
+                                 (fill_par >> s) & 1u, kSiteTeardown);
       for (int kb = 0; kb < bres_issued; ++kb)
         mbar_wait<false, true>(wc, smem_u32(&aux->bres_full[kb]), 0, kSiteTeardown);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
-    if (lane == 0) {
+    // (CTA pair: rank 0 issues for both CTAs; rank 1's warp 1 only holds its
+    // share of the tensor memory)
+    if (lane == 0 && issuer) {
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
@@ -644,7 +696,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
           // with the residual, the epilogue releases each buffer once more
           // up front, after writing the first tile's R into it
-          if (!mbar_wait(wc, smem_u32(&aux->acc_empty[buf]), RES ? aph : aph ^ 1u, kSiteMma)) {
+          if (!mbar_wait<CTA2>(wc, smem_u32(&aux->acc_empty[buf]), RES ? aph : aph ^ 1u, kSiteMma)) {
             ok = false;
             break;
           }
@@ -670,19 +722,28 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                      : make_smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
               const uint64_t db = BT ? make_smem_desc(sb + ks * 32, 16, 1024, kSwizzle128B)
                                      : make_smem_desc(sb + ks * (16 * 128), BK * 128, 1024, kSwizzle128B);
-              umma_bf16(d0, da, db, Cfg::IDESC, (RES || (kb | ks) != 0) ? 1u : 0u);
+              umma_bf16<CG>(d0, da, db, Cfg::IDESC, (RES || (kb | ks) != 0) ? 1u : 0u);
             }
-            umma_commit(smem_u32(&aux->empty[stage]));
+            if (CTA2) {
+              umma_commit_pair(smem_u32(&aux->empty[stage]), 0x3);  // both CTAs' stage
+              // rank 1's norm warps read its A rows once the stage is known complete
+              if (PRE) umma_commit_pair(smem_u32(&aux->mdone[stage]), 0x2);
+            } else {
+              umma_commit(smem_u32(&aux->empty[stage]));
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          if (ok) umma_commit(smem_u32(&aux->acc_full[buf]));
+          if (ok) {
+            if (CTA2) umma_commit_pair(smem_u32(&aux->acc_full[buf]), 0x3);
+            else umma_commit(smem_u32(&aux->acc_full[buf]));
+          }
         }
       }
       // every MMA issued has completed before tensor memory is released
-      umma_commit(smem_u32(&aux->teardown));
+      umma_commit<CG>(smem_u32(&aux->teardown));
       mbar_wait<false, true>(wc, smem_u32(&aux->teardown), 0, kSiteTeardown);
     }
   } else if (warp < 2 + kEpiWarps) {
@@ -721,6 +782,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         bulk_commit();
       }
       if (Cfg::STG_BUFS == 2) sbuf ^= 1u;
+    };
+
+    // give an accumulator buffer back to the MMA issuer (CTA pair: on rank 0's
+    // barrier, released at cluster scope; rank 0's MMAs write both CTAs'
+    // tensor memory)
+    auto release_acc = [&](int b) {
+      if (lane == 0) {
+        if (CTA2 && !issuer) mbar_arrive_remote(mapa_shared(smem_u32(&aux->acc_empty[b]), 0));
+        else mbar_arrive(smem_u32(&aux->acc_empty[b]));
+      }
     };
 
     // barrier of the two epilogue warps that share this TMEM lane quarter
@@ -907,7 +978,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     bool ok = preload_ok;
 
     for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
-      const int m0 = (t / ngroups) * Cfg::BM;
+      const int m0 = (t / ngroups) * RB + prank * Cfg::BM;  // first row of this CTA's tile rows
       const int g = t % ngroups;
       for (int s = 0; s < S && ok; ++s, ++it) {
         const int n0 = (g * C + rank) * cta_cols + s * BN;  // first column of the tile
@@ -991,7 +1062,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           if (RES) preload_iter(it + 2);  // this buffer's next tile starts from its residual
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
+          release_acc(buf);
 
           // ---- (inline) one slice of the pending row block's normalisation ----
           if (!NORMW && pend) {
@@ -1170,7 +1241,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (RES) preload_iter(it + 2);  // this buffer's next tile starts from its residual
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[buf]));
+        release_acc(buf);
 
         // ---- row statistics ----
         const int m = m0 + row;
@@ -1265,7 +1336,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         float shift = 0.0f;
         uint64_t sh2 = 0ull;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait_warp(wc, smem_u32(&aux->full[stage]), phase, kSiteNorm)) {
+          // (CTA pair, rank 1: this CTA's copies complete on rank 0's barrier;
+          // the MMAs' commit says the stage is complete)
+          if (!mbar_wait_warp(wc, smem_u32((CTA2 && !issuer) ? &aux->mdone[stage] : &aux->full[stage]), phase,
+                              kSiteNorm)) {
             ok = false;
             break;
           }
@@ -1347,11 +1421,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   // ---------------- teardown ----------------
   tc_fence_before();
   __syncthreads();
+  // CTA pair: rank 0 reaches this after its last MMA completed, so neither
+  // CTA's tensor memory is still being written when it is released
+  if (CTA2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
   }
-  if (CLUSTER) cluster_sync();  // no CTA leaves while a peer may still address it
+  if (CLUSTER || CTA2) cluster_sync();  // no CTA leaves while a peer may still address it
   if (GX && threadIdx.x == 0) {
     // the last CTA of the grid to finish starts the next generation: every
     // counter this grid touched then reads as zero to the next launch

@@ -92,7 +92,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.wait_limit_ns = wait_limit_ns();
 
   const int C = p.cluster;
-  const int num_m = (L.M + Cfg::BM - 1) / Cfg::BM;
+  const int num_m = (L.M + Cfg::RB - 1) / Cfg::RB;
   const int group_cols = Cfg::BN * p.slices * C;
   const int ngroups = (L.N + group_cols - 1) / group_cols;
   const long long total = (long long)num_m * ngroups;
@@ -117,35 +117,37 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     attr[cfg.numAttrs].val.cooperative = 1;
     ++cfg.numAttrs;
   }
-  if (Cfg::CLUSTER) {
-    if (C < 1 || C > Cfg::CLMAX) {
+  if (Cfg::CLUSTER || Cfg::CTA2) {
+    // post-norm: C CTAs along N; two-CTA MMA: the CTA pair of each tile
+    const int CL = Cfg::CTA2 ? 2 : C;
+    if (Cfg::CLUSTER && (C < 1 || C > Cfg::CLMAX)) {
       set_error("cluster size %d outside 1..%d for this kernel", C, Cfg::CLMAX);
       return FNORM_ERR_UNSUPPORTED;
     }
     cudaLaunchAttribute& ca = attr[cfg.numAttrs++];
     ca.id = cudaLaunchAttributeClusterDimension;
-    ca.val.clusterDim.x = (unsigned)C;
+    ca.val.clusterDim.x = (unsigned)CL;
     ca.val.clusterDim.y = 1;
     ca.val.clusterDim.z = 1;
     // co-resident clusters, cached per device and cluster size
     static std::atomic<int> max_clusters[64][9];
-    int mc = max_clusters[dev.id][C].load(std::memory_order_relaxed);
+    int mc = max_clusters[dev.id][CL].load(std::memory_order_relaxed);
     if (mc == 0) {
       cudaLaunchConfig_t q = cfg;  // occupancy query: the cluster attribute only
-      q.gridDim = dim3((unsigned)C, 1, 1);
+      q.gridDim = dim3((unsigned)CL, 1, 1);
       q.attrs = &ca;
       q.numAttrs = 1;
       cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, (void*)kern, &q);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
       if (mc <= 0) {
-        set_error("no cluster of %d CTAs (%u bytes of shared memory each) fits on this device", C,
+        set_error("no cluster of %d CTAs (%u bytes of shared memory each) fits on this device", CL,
                   Cfg::SMEM_BYTES);
         return FNORM_ERR_UNSUPPORTED;
       }
-      max_clusters[dev.id][C].store(mc, std::memory_order_relaxed);
+      max_clusters[dev.id][CL].store(mc, std::memory_order_relaxed);
     }
     const long long nclusters = total < mc ? total : mc;
-    cfg.gridDim = dim3((unsigned)(nclusters * C), 1, 1);
+    cfg.gridDim = dim3((unsigned)(nclusters * CL), 1, 1);
   } else {
     const long long grid = total < dev.num_sms ? total : dev.num_sms;
     cfg.gridDim = dim3((unsigned)grid, 1, 1);

@@ -96,6 +96,7 @@ fnorm_status_t launch_fused_post_residual(const FusedLaunch& L);  // residual + 
 fnorm_status_t launch_fused_post_residual_cluster(const FusedLaunch& L);  // residual + post-norm over a cluster
 fnorm_status_t launch_fused_backward(const FusedLaunch& L);       // backward of the Lazy Pre-RMSNorm GEMM
 fnorm_status_t launch_fused_post_grid(const FusedLaunch& L);      // post-norm, grid-wide statistics exchange
+fnorm_status_t launch_fused_pair(const FusedLaunch& L);           // GEMM, lazy pre-norms: two-CTA MMA (256-row tiles)
 
 // B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
 fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,

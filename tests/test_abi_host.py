@@ -200,6 +200,18 @@ def test_forced_cluster(L):
     assert fn.postnorm_plan(1024) == (4, 256)
 
 
+def test_pair_mma_setter(L):
+    import normalization_gemm_tcgen05_gb300 as fn
+    try:
+        for mode in (-1, 0, 1):
+            fn.set_pair_mma(mode)
+        for bad in (2, -2, 16):
+            with pytest.raises(fn.FnormError):
+                fn.set_pair_mma(bad)
+    finally:
+        fn.set_pair_mma(-1)
+
+
 def test_wait_limit_setter(L):
     assert L.fnorm_set_wait_limit_ns(0) == 0
     assert L.fnorm_set_wait_limit_ns(5_000_000) == 0
