@@ -93,10 +93,7 @@ bool want_resident_b(int64_t M, int64_t N, int64_t K, int bn) {
 // against 158 us; 16384 x 4096 x 2048: 188 us against 177 us): the one-CTA
 // mainloop waits on the latency of its loads, not on their bytes, and the
 // pair's loads complete later.  Automatic selection therefore keeps one CTA.
-bool want_pair(int64_t M, int64_t N, int64_t K, int bn, bool bres) {
-  (void)M;
-  (void)N;
-  (void)K;
+bool want_pair(int bn, bool bres) {
   return g_pair_mode.load(std::memory_order_relaxed) == 1 && bn == 256 && !bres;
 }
 
@@ -208,7 +205,7 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
   L.mode = 0;
   L.bn = gemm_tile_n(N);
   L.bres = want_resident_b(M, N, K, L.bn);
-  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_plain(L);
 }
 
@@ -245,7 +242,7 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
   L.bres = want_resident_b(M, N, K, L.bn);
   L.pre_eps = eps;
   L.rstd_out = rstd_out;
-  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_plain(L);
 }
 
@@ -396,14 +393,14 @@ fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folde
   if (!ln && bias == nullptr) {
     // RMSNorm with gamma only: the folded B makes it the plain lazy pre-norm
     L.mode = MODE_PRE;
-    if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
+    if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
     return launch_fused_plain(L);
   }
   L.mode = MODE_PRE | MODE_AFF | (ln ? MODE_PRE_LN : 0);
   L.colsum = ln ? colsum : nullptr;
   L.bias = bias;
   L.mean_out = ln ? mean_out : nullptr;
-  if (want_pair(M, N, K, L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
   return launch_fused_prenorm_affine(L);
 }
 
