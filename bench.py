@@ -148,11 +148,11 @@ def load_traffic(name: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks, throttle reasons and the board's power limit, sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.limit")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -182,6 +182,7 @@ class ClockSampler:
 
     def summary(self) -> dict:
         rows = []
+        limits = []
         for line in (self.out or "").splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -191,6 +192,10 @@ class ClockSampler:
                              "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
             except ValueError:
                 continue
+            try:
+                limits.append(float(parts[9]))
+            except (IndexError, ValueError):
+                pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         loaded = [r for r in rows if r["power"] > 250.0] or rows
@@ -202,7 +207,7 @@ class ClockSampler:
                     reasons.add(label)
         return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": max(r["power"] for r in rows)}
+                "power_w_max": max(r["power"] for r in rows), "power_limit_w": max(limits) if limits else None}
 
 
 # --------------------------------------------------------------------------
