@@ -1,18 +1,24 @@
 """Benchmark of the fused normalization + GEMM path on one GB300 (or N replicas).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload cfg2|cfg1|cfg3|cfg4|cfg5|all]
+                [--workload main|cfg1|cfg2|cfg3|cfg4|cfg5|res|preaff|bwd|all]
 
-Workload groups: cfg1..cfg5 (the five configurations), res (residual-add
-post-norm), preaff (pre-norm with its affine folded into B), bwd (backward of
-the Lazy Pre-RMSNorm GEMM: 4MNK FLOPs a step), all.
+Workload groups: main (the default: all five configurations in one step),
+cfg1..cfg5 (one configuration each), res (residual-add post-norm), preaff
+(pre-norm with its affine folded into B), bwd (backward of the Lazy
+Pre-RMSNorm GEMM and of the GEMM + post-LayerNorm), all (main, res, preaff,
+bwd: one line each).
 
-Default workload (one JSON line on stdout): GEMM + post-LayerNorm with affine,
-A[16384,1024] @ B[1024,N] for N = 64 and N = 128 (both launches make one step).
-Metric: fused norm-GEMM TFLOP/s (2*M*N*K per launch), with the roofline of the
-dominant kernel, the fraction of the unfused norm's latency that fusion hides,
-an end-to-end number through the public API with host buffers, and the fp64
-oracle timed on the host cores.
+Default workload (one JSON line on stdout): one step is one fused launch of
+every sub-workload of the five configurations: the Lazy Pre-RMSNorm GEMMs
+(256x512x128 and 8192x4096x4096), the GEMM + post-LayerNorm at N = 64 and
+128, the GEMM + post-LayerNorm and post-RMSNorm of A[16384,2048] at N = 1024,
+4096 and 8192, and the pre-RMSNorm + post-LayerNorm block at 65536x256x256.
+Metric: fused norm-GEMM TFLOP/s (2*M*N*K per launch, summed over the step),
+with the roofline of the dominant kernel (the one with the largest share of
+the step), per sub-workload the fraction of the unfused norm's latency that
+fusion hides and its own roofline fraction, an end-to-end number through the
+public API with host buffers, and the fp64 oracle timed on the host cores.
 
 Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and torch.cuda.synchronize() on both sides and timed
@@ -50,7 +56,10 @@ from workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
 
 METRIC = "fused norm-GEMM TFLOP/s and % of roofline; % unfused-norm latency hidden (1×GB300)"
 
+MAIN = ["cfg1", "cfg2_n64", "cfg2_n128", "cfg3", "cfg4_n1024_ln", "cfg4_n1024_rms", "cfg4_n4096_ln",
+        "cfg4_n4096_rms", "cfg4_n8192_ln", "cfg4_n8192_rms", "cfg5"]
 GROUPS = {
+    "main": MAIN,
     "cfg1": ["cfg1"],
     "cfg2": ["cfg2_n64", "cfg2_n128"],
     "cfg3": ["cfg3"],
@@ -62,11 +71,15 @@ GROUPS = {
     "bwd": ["prenorm_bwd", "postnorm_bwd"],
 }
 GROUP_TEXT = {
+    "main": "the five configurations, one fused launch of each sub-workload per step: Lazy Pre-RMSNorm GEMM "
+            "256x512x128 and 8192x4096x4096; GEMM + post-LayerNorm(affine) A[16384,1024] @ B[1024,N], N in "
+            "{64,128}; GEMM + post-LayerNorm(affine) and post-RMSNorm(gamma) A[16384,2048] @ B[2048,N], N in "
+            "{1024,4096,8192}; pre-RMSNorm + GEMM + post-LayerNorm(affine) A[65536,256] @ B[256,256]",
     "cfg1": "Lazy Pre-RMSNorm GEMM, A[256,512] @ B[512,128], eps 1e-6",
     "cfg2": "GEMM + post-LayerNorm(affine), A[16384,1024] @ B[1024,N], N in {64,128}, eps 1e-5",
     "cfg3": "Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], eps 1e-6",
-    "cfg4": "GEMM + post-LayerNorm and post-RMSNorm over a CTA cluster, A[16384,2048] @ B[2048,N], "
-            "N in {1024,4096,8192}",
+    "cfg4": "GEMM + post-LayerNorm and post-RMSNorm of rows split over CTAs (a cluster at N = 1024, the "
+            "grid-wide exchange beyond), A[16384,2048] @ B[2048,N], N in {1024,4096,8192}",
     "cfg5": "pre-RMSNorm + GEMM + post-LayerNorm(affine) in one kernel, A[65536,256] @ B[256,256]",
     "res": "GEMM + residual + post-norm: LayerNorm(affine) A[16384,1024] @ B[1024,128] + R, "
            "RMSNorm(gamma) A[16384,2048] @ B[2048,1024] + R",
@@ -301,6 +314,21 @@ class Case:
             return
         self.fn.gemm(self.A[j], self.B[j], out=self.C[j])
 
+    def cublas_gemm(self, i: int):
+        """The same GEMM(s) by cuBLAS (torch.matmul): context for the GEMM half of
+        the unfused comparison, not a product path."""
+        w, j = self.w, i % self.R
+        if w.kind in ("postnorm_backward", "prenorm_backward"):
+            if self._cub is None:
+                self._cub = (torch.empty((w.M, w.K), dtype=torch.bfloat16, device=self.dev),
+                             torch.empty((w.K, w.N), dtype=torch.bfloat16, device=self.dev))
+            torch.matmul(self.dC[j], self.B[j].t(), out=self._cub[0])
+            torch.matmul(self.A[j].t(), self.dC[j], out=self._cub[1])
+            return
+        torch.matmul(self.A[j], self.B[j], out=self.C[j])
+
+    _cub = None
+
     def norm_only(self, i: int):
         """The standalone norm kernel(s) the fusion replaces, on rotating inputs."""
         w, fn, j = self.w, self.fn, i % self.Rn
@@ -448,6 +476,7 @@ def run_ours(args, names, world, rank, local):
             c.gemm_only(i)
             c.norm_only(i)
             c.unfused_pipeline(i)
+            c.cublas_gemm(i)
     torch.cuda.synchronize()
     fn.check_status(device)
 
@@ -456,6 +485,7 @@ def run_ours(args, names, world, rank, local):
         gemm_t = [time_graph(c.gemm_only, K, stream, world, device) for c in cases]
         norm_t = [time_graph(c.norm_only, K, stream, world, device) for c in cases]
         pipe_t = [time_graph(c.unfused_pipeline, K, stream, world, device) for c in cases]
+        cub_t = [time_graph(c.cublas_gemm, K, stream, world, device) for c in cases]
     fn.check_status(device)
 
     # ---- end to end through the public API with pinned host buffers ----
@@ -467,15 +497,20 @@ def run_ours(args, names, world, rank, local):
     dom = max(range(len(cases)), key=lambda k: fused_t[k])
     dc = cases[dom]
     per_launch = fused_t[dom] / K
-    ai = dc.w.flops / dc.w.algorithmic_bytes
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if ai < ridge:
-        achieved = dc.w.algorithmic_bytes / per_launch / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        achieved = dc.w.flops / per_launch / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+
+    def roofline_of(w, t):
+        """(bound, achieved, peak, unit) of one launch of w taking t seconds."""
+        if w.flops / w.algorithmic_bytes < ridge:
+            return "hbm", w.algorithmic_bytes / t / 1e9, peaks["hbm_gbs"], "GB/s"
+        return "tensor", w.flops / t / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+
+    bound, achieved, peak, unit = roofline_of(dc.w, per_launch)
+    roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    if bound == "tensor":
+        # context: the same against the measured sustained (power-capped) rate
+        roof["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
     roof["traffic"] = load_traffic(dc.w.name)
     roof["kernel"] = (f"fused backward (row pass + dgrad + wgrad: one call, three launches), {dc.w.name}"
                       if dc.w.kind == "prenorm_backward" else f"fused kernel, {dc.w.name}")
@@ -485,6 +520,8 @@ def run_ours(args, names, world, rank, local):
     hidden = {}
     for k, c in enumerate(cases):
         tf, tg, tn, tp = fused_t[k] / K, gemm_t[k] / K, norm_t[k] / K, pipe_t[k] / K
+        tc = cub_t[k] / K
+        b_k, a_k, p_k, _ = roofline_of(c.w, tf)
         hidden[c.w.name] = {
             "t_fused_us": round(tf * 1e6, 3), "t_gemm_us": round(tg * 1e6, 3), "t_norm_us": round(tn * 1e6, 3),
             "t_unfused_pipeline_us": round(tp * 1e6, 3),
@@ -492,6 +529,12 @@ def run_ours(args, names, world, rank, local):
             "hidden_vs_pipeline": round((tp - tf) / (tp - tg), 4) if tp > tg else None,
             "fused_tflops": round(c.w.flops / tf / 1e12, 2),
             "fused_gbs": round(c.w.algorithmic_bytes / tf / 1e9, 1),
+            "roofline": {"bound": b_k, "frac": round(a_k / p_k, 4)},
+            # context only, not the product path: the same GEMM by cuBLAS
+            # (torch.matmul), and "hidden" against cuBLAS + this library's
+            # standalone norm
+            "context_t_cublas_gemm_us": round(tc * 1e6, 3),
+            "context_hidden_vs_cublas_plus_norm": round((tc + tn - tf) / tn, 4),
         }
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -511,6 +554,25 @@ def run_ours(args, names, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(names, args.cpu_seconds)
     return line
+
+
+def link_rates(device, nbytes: int = 64 << 20, reps: int = 5) -> tuple:
+    """Best-of-`reps` GB/s of one pinned host -> device and one device -> host
+    copy of `nbytes` (tensor.copy_, i.e. cudaMemcpyAsync), CUDA events."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    best = [float("inf"), float("inf")]
+    for _ in range(reps):
+        for k, (dst, src) in enumerate(((d, h), (h, d))):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            best[k] = min(best[k], e0.elapsed_time(e1) / 1e3)
+    return nbytes / best[0] / 1e9, nbytes / best[1] / 1e9
 
 
 def run_e2e(cases, K, W, world, device) -> dict:
@@ -595,8 +657,13 @@ def run_e2e(cases, K, W, world, device) -> dict:
     barrier(world)
     t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     flops = sum(c.w.flops for c in cases)
+    h2d_gbs, d2h_gbs = link_rates(device)
     return {"value": round(world * K * flops / t / 1e12, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(t / K * 1e3, 4)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(t / K * 1e3, 4),
+            # the host link, measured on this machine: one 64 MiB pinned copy each
+            # way, and the step's copies at those rates
+            "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+            "copies_ms_at_link_rate": round((h2d / h2d_gbs + d2h / d2h_gbs) / 1e6, 4)}
 
 
 # --------------------------------------------------------------------------
@@ -716,7 +783,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="cfg2", choices=sorted(GROUPS) + ["all"])
+    ap.add_argument("--workload", default="main", choices=sorted(GROUPS) + ["all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", default=None, choices=sorted(WORKLOADS),
@@ -734,7 +801,7 @@ def main(argv=None):
             raise SystemExit("bench.py needs a CUDA device (the fused path has no CPU fallback)")
         torch.cuda.set_device(local)
         init_dist(world, "nccl")
-    groups = sorted(GROUPS) if args.workload == "all" else [args.workload]
+    groups = ["main", "res", "preaff", "bwd"] if args.workload == "all" else [args.workload]
     for gname in groups:
         args.workload = gname
         names = GROUPS[gname]

@@ -18,11 +18,11 @@
  *     16-bit storage (fnorm_bf16).  Accumulation is fp32; row statistics are
  *     fp32 arrays of length M.
  *   - Every pointer is DEVICE memory on the current CUDA device, owned by
- *     the caller.  The library never frees or retains caller memory and
- *     allocates nothing per call; the one allocation it makes is the 16 MB
- *     workspace of the wide-row post-norm, once per (device, stream) on the
- *     first fnorm_gemm_postnorm call that needs it (fnorm_gemm_postnorm).
- *     Base addresses of A, B, C, X, Y, gamma and beta must be 16-byte
+ *     the caller.  The library never frees or retains caller memory, and no
+ *     call allocates device memory or synchronises the host (except
+ *     fnorm_check_status, whose job is to synchronise).  Workspaces are the
+ *     caller's and passed in (fnorm_gemm_postnorm_ws and the backward
+ *     entry points).  Base addresses of A, B, C, X, Y, gamma and beta must be 16-byte
  *     aligned; fp32 statistic outputs 4-byte aligned.  A misaligned pointer
  *     is an argument error.
  *   - Sizes: M >= 0 (M == 0 is a valid empty call that does nothing);
@@ -49,6 +49,7 @@
 #ifndef FNORM_H
 #define FNORM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -117,18 +118,12 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
  *   statistics through distributed shared memory and each normalises its own
  *   slice (fnorm_postnorm_plan reports the split).  Rows wider than the
  *   cluster's tensor memory (N > 1024 by default) use a spill layout: each
- *   CTA writes its un-normalised slices to C in bf16, then normalises them in
- *   place once the statistics are known; those outputs are normalised from
- *   bf16-rounded values (relative error <= 2^-9 of the value before the norm).
- *   C is therefore also read by this call.  By default the spill layout runs
- *   grid-wide: (row block, column chunk) units over every SM publish their
- *   chunk statistics to a 16 MB workspace that belongs to the calling
- *   (device, stream) pair and is allocated by the first such call on it;
- *   make that first call before capturing the stream into a CUDA graph (a
- *   capture without a workspace, a pre-norm, or a shape past the workspace,
- *   takes the cluster form of the spill layout instead).  Calls on one
- *   stream are ordered, so they may share it; calls on different streams
- *   use different workspaces.
+ *   CTA of a 4-CTA cluster writes its un-normalised slices to C in bf16, then
+ *   normalises them in place once the statistics are known; those outputs
+ *   are normalised from bf16-rounded values (relative error <= 2^-9 of the
+ *   value before the norm), and C is therefore also read by this call.  This
+ *   entry point needs no workspace; fnorm_gemm_postnorm_ws takes one and
+ *   computes wide rows faster, without the spill.
  *   norm:        FNORM_LAYERNORM or FNORM_RMSNORM.
  *   gamma, beta: [N] bf16 device arrays, or NULL (gamma = 1, beta = 0).
  *   eps:         epsilon of the post-norm, inside the square root.
@@ -145,6 +140,54 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
                                    int pre_rmsnorm, float pre_eps,
                                    float* mean_out, float* rstd_out, float* pre_rstd_out,
                                    void* stream);
+
+/*
+ * fnorm_gemm_postnorm_ws — fnorm_gemm_postnorm with a caller-owned workspace
+ * for the statistics exchange of wide rows.
+ *   [FNF-ru] "Multi-CTA Norm Fusion" (the CTAs that share a row combine one
+ *   pair of scalars per row), with the exchange made grid-wide: for a row of
+ *   more than 1024 columns, every 256-column tile of the plain GEMM stays in
+ *   tensor memory; the tiles of a 128-row block, on any CTAs of the grid,
+ *   publish their per-row partial statistics (mean and sum of squared
+ *   deviations for LayerNorm, sum of squares for RMSNorm) to the workspace
+ *   and count in on the row block's counter; each tile then combines all of
+ *   them in tile order (so every tile of a row derives the same statistics)
+ *   and normalises itself straight from the fp32 accumulator.  Nothing is
+ *   written to C before it is normalised.  The kernel is a cooperative launch
+ *   (all its CTAs co-resident); a row of more tiles than the device has SMs
+ *   (N > 256 * SMs) takes fnorm_gemm_postnorm's spill layout instead, as do
+ *   rows of at most 1024 columns, which need no workspace.
+ *   workspace:       device memory of at least workspace_bytes, 16-byte
+ *                    aligned, owned by the caller, or NULL (then this is
+ *                    fnorm_gemm_postnorm).  fnorm_postnorm_workspace_size
+ *                    gives the bytes an M x N call needs (0: none used).  It
+ *                    must be zero-filled before its first use (for instance
+ *                    cudaMemsetAsync on the calls' stream); each call leaves
+ *                    it ready for the next one (a generation counter), so it
+ *                    is cleared once, not per call.  Calls that share a
+ *                    workspace must not overlap in time (order them on one
+ *                    stream); after a call that ended in FNORM_ERR_TIMEOUT
+ *                    it must be cleared again.
+ *   workspace_bytes: its size; smaller than the call needs is
+ *                    FNORM_ERR_INVALID_ARG.
+ *   Other arguments and results as fnorm_gemm_postnorm.
+ */
+fnorm_status_t fnorm_gemm_postnorm_ws(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C,
+                                      int64_t M, int64_t N, int64_t K, fnorm_norm_t norm,
+                                      const fnorm_bf16* gamma, const fnorm_bf16* beta, float eps,
+                                      int pre_rmsnorm, float pre_eps,
+                                      float* mean_out, float* rstd_out, float* pre_rstd_out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fnorm_postnorm_workspace_size — bytes of the workspace fnorm_gemm_postnorm_ws
+ * uses for an M x N post-norm, into *bytes: 1024 per (128-row block,
+ * 256-column tile), 8 per row block, and 256; 0 when the row needs no
+ * exchange workspace (N <= 1024, M == 0, or a forced cluster size).  A
+ * workspace sized for M x N serves every call with at most as many row
+ * blocks and tiles.  Host only; launches nothing.
+ */
+fnorm_status_t fnorm_postnorm_workspace_size(int64_t M, int64_t N, size_t* bytes);
 
 /*
  * fnorm_lazy_prenorm_gemm_backward — gradients of C = rmsnorm(A) @ B
@@ -182,15 +225,18 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
                                                 int64_t N, int64_t K, void* stream);
 
 /*
- * fnorm_gemm_postnorm_noalloc — fnorm_gemm_postnorm (same arguments, same
- * results) that allocates nothing, ever.  The pages have no counterpart: it
- * exists for callers that must not let a library allocate device memory.
+ * fnorm_gemm_postnorm_noalloc — fnorm_gemm_postnorm_ws (same arguments but
+ * the workspace, same results) that allocates nothing, ever, and needs no
+ * workspace from the caller.  The pages have no counterpart: it exists for
+ * callers that must not allocate device memory at all, not even through
+ * their own allocator, and so have no workspace to hand over.
  *   The wide-row grid exchange keeps its statistics in a fixed device array
- *   of the library (2048 (row block, chunk) units, 8192 row blocks: about
- *   2.1 MB) instead of the per-stream workspace.  A shape whose grid exchange
- *   needs more is rejected with FNORM_ERR_UNSUPPORTED and a message naming
- *   the limit (fnorm_gemm_postnorm takes it).  Shapes that need no exchange
- *   workspace (N <= 1024, or a pre-norm) run exactly as fnorm_gemm_postnorm.
+ *   of the library (2048 (row block, 256-column tile) units, 8192 row
+ *   blocks: about 2.1 MB) instead of the caller's workspace.  A shape whose
+ *   grid exchange needs more is rejected with FNORM_ERR_UNSUPPORTED and a
+ *   message naming the limit (fnorm_gemm_postnorm and fnorm_gemm_postnorm_ws
+ *   take it).  Shapes that need no exchange workspace (N <= 1024) run
+ *   exactly as fnorm_gemm_postnorm.
  *   The first call on a device takes the array's address and clears its
  *   counters (on the call's stream): make it before capturing a stream into
  *   a CUDA graph.  All calls of a device share the array: calls that
@@ -372,10 +418,12 @@ const char* fnorm_last_error(void);
 fnorm_status_t fnorm_set_wait_limit_ns(uint64_t ns);
 
 /*
- * fnorm_postnorm_plan — how fnorm_gemm_postnorm splits a row of width N:
- * *cluster receives the CTAs per cluster along N and *cols_per_cta the
- * columns each CTA owns (a multiple of 64; more than 256 means the spill
- * layout).  Host only; launches nothing.
+ * fnorm_postnorm_plan — how fnorm_gemm_postnorm (no workspace) splits a row
+ * of width N: *cluster receives the CTAs per cluster along N and
+ * *cols_per_cta the columns each CTA owns (a multiple of 64; more than 256
+ * means the spill layout).  With a workspace, rows of more than 1024 columns
+ * are instead 256-column tiles over the whole grid
+ * (fnorm_postnorm_workspace_size > 0).  Host only; launches nothing.
  */
 fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta);
 

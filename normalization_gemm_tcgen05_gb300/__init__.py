@@ -14,7 +14,9 @@ Forms (see the header for the full contract):
 * ``lazy_prenorm_gemm(A, B, eps)``    C = rmsnorm(A) @ B = (A @ B) * rstd(A)
 * ``lazy_prenorm_gemm_backward(A, B, C, dC, rstd)``  its dA and dB
 * ``gemm_postnorm(A, B, norm, ...)``  C = norm(A @ B) * gamma + beta, optionally
-  norm(rmsnorm(A) @ B); rows wider than one CTA tile are split over a cluster
+  norm(rmsnorm(A) @ B); rows wider than one CTA tile are split over a cluster,
+  rows wider than 1024 columns over the whole grid (with a workspace this
+  binding keeps per device and stream)
 * ``gemm_add_postnorm(A, B, R, norm, ...)``  C = norm(A @ B + R) * gamma + beta
 * ``fold_prenorm_affine(B, gamma, beta)``  B' = bf16(diag(gamma) B), colsum(B'), beta @ B
 * ``prenorm_gemm(A, B', norm, colsum, bias)``  C = (norm(A) * gamma + beta) @ B,
@@ -36,6 +38,7 @@ import torch
 __all__ = [
     "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm",
     "gemm_postnorm_backward", "gemm_postnorm_noalloc", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "postnorm_workspace_size",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster", "set_pair_mma",
@@ -75,6 +78,9 @@ _SIGNATURES = {
     "fnorm_lazy_prenorm_gemm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, _f32, _p, _p]),
     "fnorm_gemm_postnorm": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                         ctypes.c_int, _f32, _p, _p, _p, _p]),
+    "fnorm_gemm_postnorm_ws": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
+                                           ctypes.c_int, _f32, _p, _p, _p, _p, ctypes.c_size_t, _p]),
+    "fnorm_postnorm_workspace_size": (_c_status, [_i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "fnorm_lazy_prenorm_gemm_backward": (_c_status, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
     "fnorm_gemm_postnorm_noalloc": (_c_status, [_p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                                 ctypes.c_int, _f32, _p, _p, _p, _p]),
@@ -292,14 +298,45 @@ def lazy_prenorm_gemm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor
     return dA, dB
 
 
+def postnorm_workspace_size(M: int, N: int) -> int:
+    """Bytes of the grid-exchange workspace an M x N post-norm uses (0: none)."""
+    n = ctypes.c_size_t(0)
+    _check(lib().fnorm_postnorm_workspace_size(int(M), int(N), ctypes.byref(n)))
+    return int(n.value)
+
+
+# Grid-exchange workspaces, one per (device, stream handle), zero-filled on
+# the stream when made and grown when a larger call needs more.  Calls on one
+# stream are ordered, so they share it; different streams never do.
+_workspaces = {}
+
+
+def _workspace(M: int, N: int, device) -> Optional[torch.Tensor]:
+    need = postnorm_workspace_size(M, N)
+    if need == 0:
+        return None
+    key = (device.index, _stream(device))
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Optional[torch.Tensor] = None,
                   beta: Optional[torch.Tensor] = None, eps: float = 1e-5, pre_rmsnorm: bool = False,
-                  pre_eps: float = 1e-6, out: Optional[torch.Tensor] = None, return_stats: bool = False):
+                  pre_eps: float = 1e-6, out: Optional[torch.Tensor] = None, return_stats: bool = False,
+                  workspace: bool = True):
     """C = norm(A @ B) * gamma + beta, or norm(rmsnorm(A) @ B) * gamma + beta.
 
     ``norm`` is "layernorm" or "rmsnorm".  With ``return_stats`` also returns a
     dict of fp32 [M] tensors: "rstd", "mean" (LayerNorm) and "pre_rstd"
-    (``pre_rmsnorm``).
+    (``pre_rmsnorm``).  Rows of more than 1024 columns use the grid-wide
+    statistics exchange through ``fnorm_gemm_postnorm_ws`` with a workspace
+    kept per device and stream (made, zero-filled, on the first such call on
+    a stream: make it before capturing that stream into a CUDA graph);
+    ``workspace=False`` calls ``fnorm_gemm_postnorm`` (no workspace: the
+    cluster spill layout for wide rows).
     """
     M, N, K = _ab(A, B)
     if norm not in _NORMS:
@@ -314,10 +351,17 @@ def gemm_postnorm(A: torch.Tensor, B: torch.Tensor, norm="layernorm", gamma: Opt
         stats["mean"] = _stat(M, A.device) if nid == LAYERNORM else None
         stats["pre_rstd"] = _stat(M, A.device) if pre_rmsnorm else None
     with torch.cuda.device(A.device):
-        _check(lib().fnorm_gemm_postnorm(
-            _ptr(A), _ptr(B), _ptr(C), M, N, K, nid, _ptr(gamma), _ptr(beta), float(eps),
-            1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
-            _ptr(stats.get("pre_rstd")), _stream(A.device)))
+        ws = _workspace(M, N, A.device) if workspace else None
+        if ws is None:
+            _check(lib().fnorm_gemm_postnorm(
+                _ptr(A), _ptr(B), _ptr(C), M, N, K, nid, _ptr(gamma), _ptr(beta), float(eps),
+                1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
+                _ptr(stats.get("pre_rstd")), _stream(A.device)))
+        else:
+            _check(lib().fnorm_gemm_postnorm_ws(
+                _ptr(A), _ptr(B), _ptr(C), M, N, K, nid, _ptr(gamma), _ptr(beta), float(eps),
+                1 if pre_rmsnorm else 0, float(pre_eps), _ptr(stats.get("mean")), _ptr(stats.get("rstd")),
+                _ptr(stats.get("pre_rstd")), ws.data_ptr(), ws.numel(), _stream(A.device)))
     return (C, stats) if return_stats else C
 
 

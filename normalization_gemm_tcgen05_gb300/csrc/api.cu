@@ -102,37 +102,24 @@ bool want_pair(int bn, bool bres) {
 //                 (tile width N rounded up to 64);
 //   N <= 1024:    resident cluster of 2 or 4 CTAs, each holding one 128- or
 //                 256-column slice in tensor memory;
-//   wider rows:   spill layout with the statistics exchanged grid-wide: units
-//                 of (row block, kGxSlices 256-column slices) spread over all
-//                 SMs; without its workspace (or for the residual form), the
-//                 spill layout on a cluster of kSpillCluster CTAs, each owning
-//                 S = ceil(N / (cluster * 256)) slices of 256 columns.
+//   wider rows:   with a grid-exchange workspace (fnorm_gemm_postnorm_ws,
+//                 fnorm_gemm_postnorm_noalloc), the plain GEMM's 256-column
+//                 tiles over the whole grid, resident in tensor memory, the
+//                 row statistics exchanged through the workspace; without
+//                 one (fnorm_gemm_postnorm), the spill layout on a cluster of
+//                 kSpillCluster CTAs, each owning S = ceil(N / (cluster *
+//                 256)) slices of 256 columns.
 // A forced cluster size c keeps the resident layout when each CTA's share fits
 // one tile (256 columns for c <= 4, 128 for c = 8), else uses the spill layout
 // (c <= 4).
 constexpr int kSpillCluster = 4;
-constexpr int kGxSlices = 2;  // default chunk: 512 columns (the launch picks per shape)
-
-// Slices per grid-exchange chunk for an M x N post-norm: the widest chunk
-// (fewer units, fewer exchanges) that still gives every SM six or more units,
-// so that the partial last wave stays small.  Measured on cfg4's shapes:
-// 512-column chunks at N = 4096 and 1024-column chunks at N = 8192.
-int gx_slices_for(int64_t M, int64_t N, int num_sms) {
-  const int64_t row_blocks = (M + 127) / 128;
-  const int64_t smax = (N + 255) / 256;  // no chunk wider than the row
-  for (int64_t s = 8; s > 1; s >>= 1) {
-    const int64_t sc = s < smax ? s : smax;
-    if (row_blocks * ((N + 256 * sc - 1) / (256 * sc)) >= 6LL * num_sms) return static_cast<int>(sc);
-  }
-  return 1;
-}
 
 struct PostPlan {
   int cluster, bn, slices;
   bool spill, gx;
 };
 
-fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl, bool allow_gx = true) {
+fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl, bool allow_gx) {
   pl->gx = false;
   auto resident = [&](int c) -> bool {
     const int64_t w = (N + c - 1) / c;  // columns per CTA
@@ -157,7 +144,7 @@ fnorm_status_t plan_postnorm(int64_t N, int forced, PostPlan* pl, bool allow_gx 
   for (int c : {1, 2, 4})
     if (resident(c)) return FNORM_OK;
   if (allow_gx) {
-    pl->cluster = 1, pl->bn = 256, pl->slices = kGxSlices, pl->spill = true, pl->gx = true;
+    pl->cluster = 1, pl->bn = 256, pl->slices = 1, pl->spill = false, pl->gx = true;
     return FNORM_OK;
   }
   if (spill(kSpillCluster)) return FNORM_OK;
@@ -250,12 +237,17 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
 
 namespace fnorm {
 namespace {
-// fnorm_gemm_postnorm and its allocation-free twin: they differ only in where
-// the wide-row grid exchange keeps its statistics
+// Where the wide-row grid exchange keeps its statistics: nowhere (the call
+// takes the cluster spill layout), the caller's workspace, or the library's
+// fixed device array.
+enum class Ws { kNone, kCaller, kFixed };
+
+// fnorm_gemm_postnorm and its workspace and allocation-free twins: they
+// differ only in where the wide-row grid exchange keeps its statistics
 fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M, int64_t N,
                                   int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma, const fnorm_bf16* beta,
                                   float eps, int pre_rmsnorm, float pre_eps, float* mean_out, float* rstd_out,
-                                  float* pre_rstd_out, void* stream, bool noalloc) {
+                                  float* pre_rstd_out, void* workspace, size_t workspace_bytes, void* stream, Ws ws) {
   clear_error();
   FN_TRY(check_mnk(M, N, K));
   if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
@@ -264,8 +256,9 @@ fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnor
   if (pre_rmsnorm) FN_TRY(check_eps(pre_eps, "pre_eps"));
   if (norm == FNORM_RMSNORM && mean_out != nullptr) return bad("mean_out is only defined for LayerNorm");
   if (!pre_rmsnorm && pre_rstd_out != nullptr) return bad("pre_rstd_out needs pre_rmsnorm = 1");
+  if (ws == Ws::kCaller && workspace == nullptr) ws = Ws::kNone;
   PostPlan plan{};
-  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, ws != Ws::kNone));
   if (M == 0) return FNORM_OK;
   FN_TRY(check_ptr(A, "A", 16, false));
   FN_TRY(check_ptr(B, "B", 16, false));
@@ -276,43 +269,37 @@ fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnor
   FN_TRY(check_ptr(rstd_out, "rstd_out", 4, true));
   FN_TRY(check_ptr(pre_rstd_out, "pre_rstd_out", 4, true));
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
+  GxScratch caller_gx{};
+  if (plan.gx && ws == Ws::kCaller) FN_TRY(gx_scratch_from(workspace, workspace_bytes, M, N, &caller_gx));
+  if (plan.gx) {
+    // one CTA per tile of a row at least (no CTA may hold two tiles of the
+    // row block it waits on); a row with more tiles than SMs takes the
+    // cluster spill layout instead
+    DeviceInfo dev;
+    FN_TRY(current_device(&dev));
+    if ((N + 255) / 256 > dev.num_sms) {
+      FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
+    } else if (ws == Ws::kFixed) {
+      const GxScratch* gx = nullptr;
+      FN_TRY(noalloc_scratch(L.stream, &gx));
+      const int64_t rb = (M + 127) / 128, units = rb * ((N + 255) / 256);
+      if (units > gx->units_cap || rb > gx->rowblocks_cap) {
+        set_error("fnorm_gemm_postnorm_noalloc: %lld tiles of 128 x 256 (%lld row blocks) exceed its fixed "
+                  "workspace (%d tiles, %d row blocks); use fnorm_gemm_postnorm or fnorm_gemm_postnorm_ws",
+                  (long long)units, (long long)rb, gx->units_cap, gx->rowblocks_cap);
+        return FNORM_ERR_UNSUPPORTED;
+      }
+      L.gx = gx;
+    } else {
+      L.gx = &caller_gx;
+    }
+  }
   L.mode = MODE_POST | (norm == FNORM_LAYERNORM ? MODE_LN : 0) | (pre_rmsnorm ? MODE_PRE : 0);
   L.bn = plan.bn;
   L.slices = plan.slices;
   L.spill = plan.spill;
   L.cluster = plan.cluster;
-  if (plan.gx) {
-    // the grid exchange needs its workspace and (the kernel waits across
-    // CTAs) no pre-norm stage; otherwise the cluster spill layout
-    DeviceInfo dev;
-    FN_TRY(current_device(&dev));
-    plan.slices = gx_slices_for(M, N, dev.num_sms);
-    L.slices = plan.slices;
-    const GxScratch* gx = nullptr;
-    const int units = static_cast<int>((M + 127) / 128 * ((N + 256 * plan.slices - 1) / (256 * plan.slices)));
-    fnorm_status_t gs = pre_rmsnorm ? FNORM_ERR_UNSUPPORTED
-                                    : (noalloc ? noalloc_scratch(L.stream, &gx) : gx_scratch_for_stream(L.stream, &gx));
-    const bool fits = gs == FNORM_OK && units <= gx->units_cap && (M + 127) / 128 <= gx->rowblocks_cap;
-    if (noalloc && gs == FNORM_OK && !fits) {
-      set_error("fnorm_gemm_postnorm_noalloc: %d units of %d rows x 256*%d columns (%lld row blocks) exceed its "
-                "fixed workspace (%d units, %d row blocks); use fnorm_gemm_postnorm",
-                units, 128, plan.slices, (long long)((M + 127) / 128), gx->units_cap, gx->rowblocks_cap);
-      return FNORM_ERR_UNSUPPORTED;
-    }
-    if (fits) {
-      L.gx = gx;
-    } else if (gs == FNORM_OK || gs == FNORM_ERR_UNSUPPORTED) {
-      clear_error();
-      FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
-      L.bn = plan.bn;
-      L.slices = plan.slices;
-      L.spill = plan.spill;
-      L.cluster = plan.cluster;
-    } else {
-      return gs;
-    }
-  }
-  L.bres = (plan.cluster == 1 && !plan.spill) && want_resident_b(M, N, K, plan.bn);
+  L.bres = (plan.cluster == 1 && !plan.spill && !plan.gx) && want_resident_b(M, N, K, plan.bn);
   L.eps = eps;
   L.pre_eps = pre_rmsnorm ? pre_eps : 1.0f;
   L.gamma = gamma;
@@ -333,7 +320,26 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
                                    const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
                                    float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
   return gemm_postnorm_impl(A, B, C, M, N, K, norm, gamma, beta, eps, pre_rmsnorm, pre_eps, mean_out, rstd_out,
-                            pre_rstd_out, stream, false);
+                            pre_rstd_out, nullptr, 0, stream, Ws::kNone);
+}
+
+fnorm_status_t fnorm_gemm_postnorm_ws(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
+                                      int64_t N, int64_t K, fnorm_norm_t norm, const fnorm_bf16* gamma,
+                                      const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
+                                      float* mean_out, float* rstd_out, float* pre_rstd_out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return gemm_postnorm_impl(A, B, C, M, N, K, norm, gamma, beta, eps, pre_rmsnorm, pre_eps, mean_out, rstd_out,
+                            pre_rstd_out, workspace, workspace_bytes, stream, Ws::kCaller);
+}
+
+fnorm_status_t fnorm_postnorm_workspace_size(int64_t M, int64_t N, size_t* bytes) {
+  clear_error();
+  if (bytes == nullptr) return bad("bytes must not be NULL");
+  FN_TRY(check_mnk(M, N, 8));
+  PostPlan plan{};
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, true));
+  *bytes = (plan.gx && M > 0) ? gx_workspace_bytes(M, N) : 0;
+  return FNORM_OK;
 }
 
 fnorm_status_t fnorm_gemm_postnorm_noalloc(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
@@ -341,7 +347,7 @@ fnorm_status_t fnorm_gemm_postnorm_noalloc(const fnorm_bf16* A, const fnorm_bf16
                                            const fnorm_bf16* beta, float eps, int pre_rmsnorm, float pre_eps,
                                            float* mean_out, float* rstd_out, float* pre_rstd_out, void* stream) {
   return gemm_postnorm_impl(A, B, C, M, N, K, norm, gamma, beta, eps, pre_rmsnorm, pre_eps, mean_out, rstd_out,
-                            pre_rstd_out, stream, true);
+                            pre_rstd_out, nullptr, 0, stream, Ws::kFixed);
 }
 
 
@@ -635,7 +641,7 @@ fnorm_status_t fnorm_postnorm_plan(int64_t N, int* cluster, int* cols_per_cta) {
   if (cluster == nullptr || cols_per_cta == nullptr) return bad("output pointers must not be NULL");
   if (N < 8 || N > kMaxDim || N % 8 != 0) return bad("N must be a multiple of 8 in [8, 2^31)");
   PostPlan plan{};
-  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan));
+  FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
   *cluster = plan.cluster;
   *cols_per_cta = plan.bn * plan.slices;
   return FNORM_OK;

@@ -22,11 +22,14 @@
 //         to C un-normalised while its statistics accumulate, and once the row
 //         block's statistics are exchanged the slices are re-read from L2 and
 //         normalised in place while the next row block's MMAs run.  Rows of
-//         any width, on small clusters;
-//       - spill, grid-wide: the same slices in units of S x 256 columns, one
-//         CTA per unit, the row statistics exchanged between all CTAs through
-//         global memory (published partials and per-row-block counters, a
-//         cooperative launch);
+//         any width, on small clusters, with no workspace;
+//       - resident, grid-wide: the plain GEMM's 256-column tiles, each kept in
+//         tensor memory until the row block's statistics are known; the tiles
+//         of a row block, on any CTAs of the grid, publish their per-row
+//         partial statistics to a global workspace and count in on the row
+//         block's counter, then each combines all of them in tile order and
+//         normalises its tile from tensor memory (a cooperative launch; the
+//         other accumulator buffer keeps the tensor cores busy meanwhile);
 //   * both at once: norm(rmsnorm(A) @ B);
 //   * residual: norm(A @ B + R), R written into the accumulator before the
 //     tile's MMAs accumulate onto it;
@@ -57,7 +60,7 @@
 //               scale, bf16, swizzled shared-memory staging, TMA stores.
 //   warps 10-13 Lazy Pre-Norm: sum of squares of the staged A rows (warps
 //               10-17 for the pre-LayerNorm, each row's chunks in two parts);
-//               spill layouts (without Lazy Pre-Norm): the in-place
+//               spill layout (without Lazy Pre-Norm): the in-place
 //               normalisation of finished row blocks, from L2.
 // A stage is released when the MMA commit and (for Lazy Pre-Norm) the four
 // norm warps have all arrived on its "empty" barrier.
@@ -87,7 +90,11 @@ enum : int {
   MODE_BT = 512,      // B operand K-major: read from a row-major [N, K] array (B^T of a [K, N] matrix)
   MODE_AT = 1024,     // A operand MN-major: read from a row-major [K, M] array (A^T of an [M, K] matrix)
   MODE_DGRAD = 4096,  // RMSNorm backward epilogue: y = u + c[m] * X[m, n]
-  MODE_GX = 8192,     // spill layout with the row statistics exchanged grid-wide through global memory
+  // post-norm of rows wider than a cluster holds: the row statistics are
+  // exchanged grid-wide through global memory (a cooperative launch), each
+  // CTA keeping one 256-column tile in tensor memory while the row block's
+  // other tiles, on any CTAs of the grid, publish theirs
+  MODE_GX = 8192,
   // two-CTA MMA: the two CTAs of a cluster compute one [256 x BN] tile with
   // tcgen05 cta_group::2, each staging its own 128 rows of A and half of B's
   // BN columns, so that each SM takes in a third less per tile
@@ -110,7 +117,7 @@ struct FusedParams {
   const __nv_bfloat16* R;     // [M, N] residual (MODE_RES)
   const float* rowcoef;       // MODE_DGRAD: [M] coefficients c of the forward rows
   const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows combined in the epilogue
-  // MODE_GX scratch: per-(row block, chunk) row statistics, per-row-block
+  // MODE_GX workspace: per-(row block, tile) row statistics, per-row-block
   // counters, the generation word and the CTA finish counter
   float2* gx_part;
   unsigned long long* gx_cnt;
@@ -130,7 +137,7 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff, NBR: resident-B k-blocks), so each kernel carries
 // only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR, int GW>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -157,6 +164,10 @@ struct Aux {
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
   alignas(16) float gam[GB];
   alignas(16) float bet[GB];
+  // resident grid exchange: each epilogue warp's gamma/beta for the columns
+  // of its half of the current tile (tiles change column group)
+  alignas(16) float wgam[GW > 1 ? 8 : 1][GW];
+  alignas(16) float wbet[GW > 1 ? 8 : 1][GW];
   float2 xstat[2][CLMAX > 0 ? CLMAX : 1][128];
 };
 
@@ -195,10 +206,11 @@ struct KCfg {
   // register budget allows (320 threads: 168 registers), else two (448
   // threads: 128 registers; cluster exchange code needs the room too)
   static constexpr int LDB = DGRAD ? 1  // (the dgrad also holds its X values)
-                             : (AUXW || (CLUSTER && NCH > 2)) ? (NCH < 2 ? NCH : 2) : NCH;
+                             : (AUXW || ((CLUSTER || GX) && NCH > 2)) ? (NCH < 2 ? NCH : 2) : NCH;
   static constexpr bool KEEP = (LDB == NCH);  // one TMEM read serves statistics and output
   static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
-  static constexpr int GB = (POST && !SPILL) ? BN : 1;  // gamma/beta kept in shared memory
+  static constexpr int GB = (POST && !SPILL && !GX) ? BN : 1;  // gamma/beta kept in shared memory
+  static constexpr int GW = GX ? HALF : 1;  // grid exchange: per-warp gamma/beta of a half tile
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BK * BNS * 2;
@@ -216,7 +228,7 @@ struct KCfg {
   static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1)>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1), GW>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
   // that buys a pipeline stage and either the ring is below 4 stages, or a
   // warp stores only one box per tile (64-column tiles), so that nothing
@@ -239,8 +251,9 @@ struct KCfg {
 
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage ring");
-  static_assert(!SPILL || (BN == 256 && POST && (CLUSTER || GX)), "spill layout: 256-column slices, post-norm");
-  static_assert(!GX || (SPILL && !CLUSTER && !PRE && !RES), "grid exchange: spill layout, one CTA per unit");
+  static_assert(!SPILL || (BN == 256 && POST && CLUSTER), "spill layout: 256-column slices, post-norm, a cluster");
+  static_assert(!GX || (POST && BN == 256 && !CLUSTER && !SPILL && !RES && !BRES),
+                "grid exchange: resident 256-column tiles, no cluster");
   static_assert(!CLUSTER || (POST && CLMAX_ >= 1 && CLMAX_ <= 8), "clusters serve the post-norm, up to 8 CTAs");
   static_assert(!BRES || !CLUSTER, "resident B serves one CTA per row block");
   static_assert(!(PRE_LN || AFF) || (PRE && !POST), "the folded-affine pre-norm serves the pre-norm GEMM alone");
@@ -468,7 +481,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr int CG = Cfg::CG, RB = Cfg::RB;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
-                   (Cfg::BRES ? Cfg::KB_MAX : 1)>;
+                   (Cfg::BRES ? Cfg::KB_MAX : 1), Cfg::GW>;
   constexpr int HD = Cfg::HDEPTH;
 
   extern __shared__ uint8_t smem_raw[];
@@ -940,7 +953,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(smem_u32(&aux->acc_empty[i2]));
       }
     }
-    if (POST && !SPILL) {
+    if (POST && !SPILL && !GX) {
       // resident post-norm CTAs own one fixed BN-column slice of every row
       // (after the residual preload, which the first MMA waits for)
       const int n0 = rank * BN;
@@ -952,8 +965,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
     }
 
-    // grid exchange: publish this CTA's statistics of (row block, chunk g) for
-    // its 128 rows, then count the quarter-warp in (4 per unit)
+    // grid exchange: publish the statistics of tile (row block, column group
+    // g) for its 128 rows, then count the quarter-warp in (4 per tile)
     const uint32_t gx_gen = GX ? *reinterpret_cast<volatile uint32_t*>(p.gx_gen) : 0u;
     auto gx_publish = [&](float part0, float part1, int m0_, int g_) -> bool {
       const int rb = m0_ / Cfg::BM;
@@ -966,6 +979,42 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (!ok2) record_timeout(wc, kSiteGrid);
       }
       return __all_sync(0xffffffffu, ok2);
+    };
+
+    // resident grid exchange: publish this tile's statistics, wait until every
+    // tile of its row block has published, then combine all of them in tile
+    // order (the same arithmetic in every tile of the row, so every tile
+    // derives the same mean and rstd); false if a wait gave up
+    auto gx_exchange = [&](float& part0, float& part1, int m0_, int g_) -> bool {
+      if (!gx_publish(part0, part1, m0_, g_)) return false;
+      const int rb = m0_ / Cfg::BM;
+      const unsigned long long want =
+          (static_cast<unsigned long long>(gx_gen) << 32) | static_cast<unsigned long long>(4 * ngroups);
+      bool ready = true;
+      if (lane == 0) ready = grid_wait_eq(wc, p.gx_cnt + rb, want, kSiteGrid);
+      if (!__all_sync(0xffffffffu, ready)) return false;
+      __syncwarp();  // lane 0's acquire (the fence after the counter) orders every lane's loads below
+      const float2* src = p.gx_part + static_cast<size_t>(rb) * ngroups * Cfg::BM + row;
+      float mean = 0.0f, m2 = 0.0f, n = 0.0f, ssq = 0.0f;
+      for (int q0 = 0; q0 < ngroups; q0 += 8) {
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = q0 + u < ngroups ? __ldcg(src + static_cast<size_t>(q0 + u) * Cfg::BM) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (q0 + u >= ngroups) break;
+          if (LN) {
+            const float nq = static_cast<float>(min(max(N - (q0 + u) * cta_cols, 0), cta_cols));
+            combine_mean_m2(mean, m2, n, v[u].x, v[u].y, nq);
+          } else {
+            ssq += v[u].x;
+          }
+        }
+      }
+      part0 = LN ? mean : ssq;
+      part1 = m2;
+      return true;
     };
 
     // spill-layout state: running shifted sums of this half over the current
@@ -985,6 +1034,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int c0h = n0 + h * HALF;                      // first column of this half
         const int buf = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        // resident grid exchange: this half's gamma (lanes 0-15) and beta
+        // (lanes 16-31), 8 columns per lane, loaded while the tile's MMAs run
+        uint4 gbv = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);  // bf16 1.0 pairs
+        if (GX) {
+          const int col = c0h + (lane & 15) * 8;
+          const __nv_bfloat16* src = lane < 16 ? p.gamma : p.beta;
+          if (lane >= 16) gbv = make_uint4(0u, 0u, 0u, 0u);
+          if (src != nullptr && col < N) gbv = __ldg(reinterpret_cast<const uint4*>(src + col));
+        }
         // dgrad: this half's X values, loaded while the tile's MMAs run
         uint4 xv[DGRAD ? NCH : 1][4];
         if (DGRAD) {
@@ -1087,18 +1145,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               part0 = pre * pre * sum2;
               part1 = 0.0f;
             }
-            if (!combine_halves(part0, part1, nh[0], nh[1]) ||
-                !(GX ? gx_publish(part0, part1, m0, g) : exchange(part0, part1, g, xit))) {
+            if (!combine_halves(part0, part1, nh[0], nh[1]) || !exchange(part0, part1, g, xit)) {
               ok = false;
               break;
             }
             ++xit;
-            // (grid exchange: the normaliser warps combine the chunks and
-            // write the row statistics)
             const float mean = LN ? part0 : 0.0f;
             const float rstd = rsqrtf((LN ? part1 : part0) * inv_N() + p.eps);
             const int m = m0 + row;
-            if (!GX && h == 0 && rank == 0 && g == 0 && m < M) {
+            if (h == 0 && rank == 0 && g == 0 && m < M) {
               if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
               if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
               if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
@@ -1193,6 +1248,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               break;
             }
             ++xit;
+          } else if (GX) {
+            if (!gx_exchange(part0, part1, m0, g)) {
+              ok = false;
+              break;
+            }
           }
           if (LN) {
             mean = part0;
@@ -1202,6 +1262,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           }
         }
 
+        // resident grid exchange: this warp's gamma/beta of the tile into its
+        // own shared-memory slice (read back as float4 broadcasts)
+        const int ew = warp - 2;
+        if (GX) {
+          float* dst = (lane < 16 ? &aux->wgam[ew][0] : &aux->wbet[ew][0]) + (lane & 15) * 8;
+          const uint32_t gw[4] = {gbv.x, gbv.y, gbv.z, gbv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dst[2 * e] = bf16_lo(gw[e]);
+            dst[2 * e + 1] = bf16_hi(gw[e]);
+          }
+          __syncwarp();
+        }
         // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
         for (int cb = 0; cb < NBATCH; ++cb) {
           if (c0h + cb * LDB * 32 >= N) break;
@@ -1214,8 +1287,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t w[16];
             if (POST) {
               // y = (v - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta, v = pre * u
-              affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f, &aux->gam[h * HALF + c * 32],
-                          &aux->bet[h * HALF + c * 32], w);
+              affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f,
+                          GX ? &aux->wgam[ew][c * 32] : &aux->gam[h * HALF + c * 32],
+                          GX ? &aux->wbet[ew][c * 32] : &aux->bet[h * HALF + c * 32], w);
             } else if (DGRAD) {
               // y = u + c * x
               const uint64_t cc = f2(pre_mean, pre_mean);
@@ -1247,7 +1321,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int m = m0 + row;
         if (h == 0 && m < M) {
           if (POST) {
-            if (rank == 0) {
+            if (rank == 0 && (!GX || g == 0)) {
               if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
               if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;
               if (PRE && p.pre_rstd_out != nullptr) p.pre_rstd_out[m] = pre;
@@ -1268,7 +1342,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     if (lane == 0) bulk_wait_read<0>();  // staging is read; the writes complete with the grid
   } else if (NORMW) {
     // ======================= normaliser warps (spill layout) =======================
-    const uint32_t gx_gen = GX ? *reinterpret_cast<volatile uint32_t*>(p.gx_gen) : 0u;
     const int k = warp - (2 + kEpiWarps);  // rows 32k..32k+31 of each row block
     int nb = 0;
     for (int t = cid; t < total; t += ncl, ++nb) {
@@ -1280,31 +1353,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       const int c0 = aux->nstat_c0[b];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&aux->nstat_empty[b]));
-      if (GX) {
-        // wait until every chunk of this row block is published (4 quarter-
-        // warps per chunk), then combine the chunks in order for this row
-        const int rb = m0 / Cfg::BM;
-        const unsigned long long want =
-            (static_cast<unsigned long long>(gx_gen) << 32) | static_cast<unsigned long long>(4 * ngroups);
-        bool ready = true;
-        if (lane == 0) ready = grid_wait_eq(wc, p.gx_cnt + rb, want, kSiteGrid);
-        if (!__all_sync(0xffffffffu, ready)) break;
-        float mean = 0.0f, m2 = 0.0f, n = 0.0f, ssq = 0.0f;
-        for (int qq = 0; qq < ngroups; ++qq) {
-          const float2 v = __ldcg(p.gx_part + (static_cast<size_t>(rb) * ngroups + qq) * Cfg::BM + k * 32 + lane);
-          const float nq = static_cast<float>(min(max(N - qq * cta_cols, 0), cta_cols));
-          if (LN) combine_mean_m2(mean, m2, n, v.x, v.y, nq);
-          else ssq += v.x;
-        }
-        st = make_float2(LN ? mean : 0.0f, rsqrtf((LN ? m2 : ssq) * inv_N() + p.eps));
-        const int m = m0 + k * 32 + lane;
-        if (c0 == 0 && m < M) {
-          if (LN && p.mean_out != nullptr) p.mean_out[m] = st.x;
-          if (p.rstd_out != nullptr) p.rstd_out[m] = st.y;
-        }
-      }
-      for (int s = 0; s < S; ++s)
-        normalize_slice<LN, GX ? 16 : 8>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
+      for (int s = 0; s < S; ++s) normalize_slice<LN>(p, m0 + k * 32, 32, 0, c0 + s * BN, st.x, st.y, lane);
     }
   } else if (PRE) {
     // ======================= norm warps (Lazy Pre-Norm) =======================

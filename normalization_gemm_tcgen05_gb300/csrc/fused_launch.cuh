@@ -77,7 +77,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.R = static_cast<const __nv_bfloat16*>(L.R);
   p.rowcoef = L.rowcoef;
   if (Cfg::GX) {
-    const int units = ((L.M + Cfg::BM - 1) / Cfg::BM) * ((L.N + Cfg::BN * L.slices - 1) / (Cfg::BN * L.slices));
+    const int units = ((L.M + Cfg::BM - 1) / Cfg::BM) * ((L.N + Cfg::BN - 1) / Cfg::BN);
     if (L.gx == nullptr || units > L.gx->units_cap || (L.M + Cfg::BM - 1) / Cfg::BM > L.gx->rowblocks_cap) {
       set_error("internal: grid-exchange workspace missing or too small");
       return FNORM_ERR_UNSUPPORTED;
@@ -150,6 +150,12 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     cfg.gridDim = dim3((unsigned)(nclusters * CL), 1, 1);
   } else {
     const long long grid = total < dev.num_sms ? total : dev.num_sms;
+    if (Cfg::GX && ngroups > grid) {
+      // every tile of a row block must be able to publish while the others
+      // wait: no CTA may hold two tiles of one row block
+      set_error("internal: a grid exchange over %d tiles per row needs as many CTAs (grid %lld)", ngroups, grid);
+      return FNORM_ERR_UNSUPPORTED;
+    }
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tr, p);

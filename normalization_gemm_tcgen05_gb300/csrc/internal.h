@@ -37,7 +37,7 @@ fnorm_status_t encode_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t i
                                    uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                                    CUtensorMapSwizzle swizzle);
 
-// Workspace of the grid-exchange spill layout: per-(row block, chunk) row
+// Workspace of the grid-exchange post-norm: per-(row block, tile) row
 // statistics, per-row-block counters, the generation word and the finish
 // counter.  Calls that share one must be ordered (one stream).
 struct GxScratch {
@@ -49,10 +49,11 @@ struct GxScratch {
   int rowblocks_cap;
 };
 
-// The workspace of (current device, stream), allocated and zeroed by the
-// first call on that pair.  FNORM_ERR_UNSUPPORTED while the stream is being
-// captured and none exists yet (the caller then takes another layout).
-fnorm_status_t gx_scratch_for_stream(cudaStream_t stream, const GxScratch** out);
+// Bytes of the caller's grid-exchange workspace for an M x N post-norm, and
+// its layout over a given buffer (FNORM_ERR_INVALID_ARG if it is too small or
+// misaligned).  Nothing is allocated.
+size_t gx_workspace_bytes(int64_t M, int64_t N);
+fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t N, GxScratch* out);
 
 // The fixed workspace of fnorm_gemm_postnorm_noalloc (a device array, no
 // allocation): address taken and counters cleared by the first call per
@@ -83,7 +84,7 @@ struct FusedLaunch {
   // ([N, K] row-major), as the mode says
   const void* X;          // dgrad: [M, N] forward input combined in the epilogue
   const float* rowcoef;   // dgrad: [M] coefficients c = -rstd^2 (dC . C) / K
-  const GxScratch* gx;    // grid-exchange spill layout's workspace
+  const GxScratch* gx;    // grid-exchange post-norm's workspace
   cudaStream_t stream;
 };
 

@@ -4,7 +4,6 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
-#include <map>
 #include <mutex>
 #include <string>
 
@@ -90,51 +89,34 @@ fnorm_status_t current_device(DeviceInfo* out) {
   return FNORM_OK;
 }
 
-namespace {
-// grid-exchange workspaces: one per (device, stream), allocated by the first
-// call on that pair and kept for the life of the process
-constexpr int kGxUnitsCap = 16384;      // (row block, chunk) units: 16 MB of statistics
-constexpr int kGxRowBlocksCap = 16384;  // 128-row blocks: M up to 2^21
-std::mutex g_gx_mutex;
-std::map<std::pair<int, cudaStream_t>, GxScratch> g_gx;
-}  // namespace
+// Layout of a grid-exchange workspace for an M x N post-norm: the per-tile
+// row statistics [row blocks][tiles per row][128] float2, the per-row-block
+// counters, then 256 bytes holding the generation word and the finish count.
+size_t gx_workspace_bytes(int64_t M, int64_t N) {
+  const int64_t rb = (M + 127) / 128, tiles = (N + 255) / 256;
+  return static_cast<size_t>(rb * tiles) * 128 * sizeof(float2) + static_cast<size_t>(rb) * sizeof(uint64_t) + 256;
+}
 
-fnorm_status_t gx_scratch_for_stream(cudaStream_t stream, const GxScratch** out) {
-  DeviceInfo dev;
-  fnorm_status_t st = current_device(&dev);
-  if (st != FNORM_OK) return st;
-  std::lock_guard<std::mutex> lock(g_gx_mutex);
-  auto it = g_gx.find({dev.id, stream});
-  if (it != g_gx.end()) {
-    *out = &it->second;
-    return FNORM_OK;
+fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t N, GxScratch* out) {
+  const size_t need = gx_workspace_bytes(M, N);
+  if (workspace == nullptr || bytes < need) {
+    set_error("the grid-exchange workspace of a %lld x %lld post-norm needs %zu bytes (given %zu)", (long long)M,
+              (long long)N, need, workspace == nullptr ? (size_t)0 : bytes);
+    return FNORM_ERR_INVALID_ARG;
   }
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-  if (cap != cudaStreamCaptureStatusNone) {
-    set_error("no grid-exchange workspace for this stream yet (make one call before capturing it)");
-    return FNORM_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) {
+    set_error("workspace must be 16-byte aligned");
+    return FNORM_ERR_INVALID_ARG;
   }
-  const size_t part_bytes = static_cast<size_t>(kGxUnitsCap) * 128 * sizeof(float2);
-  const size_t cnt_bytes = static_cast<size_t>(kGxRowBlocksCap) * sizeof(unsigned long long);
-  const size_t bytes = part_bytes + cnt_bytes + 256;
-  void* base = nullptr;
-  e = cudaMalloc(&base, bytes);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(grid-exchange workspace)");
-  // counters, generation and finish count start at zero
-  e = cudaMemset(static_cast<char*>(base) + part_bytes, 0, cnt_bytes + 256);
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the grid-exchange workspace");
-  GxScratch g;
-  g.part = static_cast<float2*>(base);
-  g.cnt = reinterpret_cast<unsigned long long*>(static_cast<char*>(base) + part_bytes);
-  g.gen = reinterpret_cast<uint32_t*>(static_cast<char*>(base) + part_bytes + cnt_bytes);
-  g.finish = g.gen + 32;
-  g.units_cap = kGxUnitsCap;
-  g.rowblocks_cap = kGxRowBlocksCap;
-  auto res = g_gx.emplace(std::make_pair(dev.id, stream), g);
-  *out = &res.first->second;
+  const int64_t rb = (M + 127) / 128, tiles = (N + 255) / 256;
+  char* base = static_cast<char*>(workspace);
+  const size_t part_bytes = static_cast<size_t>(rb * tiles) * 128 * sizeof(float2);
+  out->part = reinterpret_cast<float2*>(base);
+  out->cnt = reinterpret_cast<unsigned long long*>(base + part_bytes);
+  out->gen = reinterpret_cast<uint32_t*>(base + part_bytes + static_cast<size_t>(rb) * sizeof(uint64_t));
+  out->finish = out->gen + 32;
+  out->units_cap = static_cast<int>(rb * tiles);
+  out->rowblocks_cap = static_cast<int>(rb);
   return FNORM_OK;
 }
 

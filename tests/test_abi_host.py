@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
                      "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
                      "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm", "fnorm_lazy_prenorm_gemm_backward",
                      "fnorm_gemm_ex", "fnorm_rmsnorm_backward", "fnorm_gemm_postnorm_backward",
-                     "fnorm_gemm_postnorm_noalloc"):
+                     "fnorm_gemm_postnorm_noalloc", "fnorm_gemm_postnorm_ws", "fnorm_postnorm_workspace_size"):
         assert required in names
 
 
@@ -172,12 +172,78 @@ def test_norm_rejects_bad_sizes(L):
 
 
 @pytest.mark.parametrize("N,cluster,cols", [(8, 1, 64), (64, 1, 64), (128, 1, 128), (200, 1, 256), (256, 1, 256),
-                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (1032, 1, 512),
-                                            (2048, 1, 512), (2056, 1, 512), (3000, 1, 512), (4096, 1, 512),
-                                            (8192, 1, 512), (16384, 1, 512)])
+                                            (320, 2, 256), (512, 2, 256), (1024, 4, 256), (1032, 4, 512),
+                                            (2048, 4, 512), (2056, 4, 768), (3000, 4, 768), (4096, 4, 1024),
+                                            (8192, 4, 2048), (16384, 4, 4096)])
 def test_postnorm_plan(L, N, cluster, cols):
+    # without a workspace: one CTA, a resident cluster, or the spill layout on
+    # a cluster of 4 (ceil(N / 1024) slices of 256 columns per CTA)
     import normalization_gemm_tcgen05_gb300 as fn
     assert fn.postnorm_plan(N) == (cluster, cols)
+
+
+@pytest.mark.parametrize("M,N", [(16384, 8192), (16384, 4096), (300, 1032), (1, 2048), (16384, 1024), (0, 4096),
+                                 (65536, 256)])
+def test_postnorm_workspace_size(L, M, N):
+    # 1 KB per (128-row block, 256-column tile), 8 bytes per row block, 256;
+    # nothing for rows a cluster holds (N <= 1024) or an empty call
+    import normalization_gemm_tcgen05_gb300 as fn
+    rb, tiles = -(-M // 128), -(-N // 256)
+    want = rb * tiles * 1024 + rb * 8 + 256 if (N > 1024 and M > 0) else 0
+    assert fn.postnorm_workspace_size(M, N) == want
+
+
+def test_postnorm_workspace_size_follows_a_forced_cluster(L):
+    import normalization_gemm_tcgen05_gb300 as fn
+    try:
+        fn.set_postnorm_cluster(4)
+        assert fn.postnorm_workspace_size(1024, 4096) == 0   # the forced cluster spill needs none
+    finally:
+        fn.set_postnorm_cluster(0)
+    assert fn.postnorm_workspace_size(1024, 4096) > 0
+
+
+def test_postnorm_ws_argument_rules(L):
+    f = L.fnorm_gemm_postnorm_ws
+    W = ctypes.c_void_p(0x800000)
+    need = (4 * 16) * 1024 + 4 * 8 + 256   # M = 512, N = 4096
+    # too small, misaligned
+    assert f(FAKE, FAKE, FAKE, 512, 4096, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None, W, need - 1, None) == 1
+    assert b"workspace" in L.fnorm_last_error()
+    assert f(FAKE, FAKE, FAKE, 512, 4096, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None,
+             ctypes.c_void_p(0x800008), need, None) == 1
+    # the shared post-norm rules still apply
+    assert f(FAKE, FAKE, FAKE, 512, 4096, 64, 0, None, None, 1e-5, 0, 1e-6, FAKE, None, None, W, need, None) == 1
+    # M == 0: nothing to do, no workspace needed
+    assert f(None, None, None, 0, 4096, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None, None, 0, None) == 0
+    n = ctypes.c_size_t(0)
+    assert L.fnorm_postnorm_workspace_size(512, 4096, ctypes.byref(n)) == 0 and n.value == need
+    assert L.fnorm_postnorm_workspace_size(512, 4096, None) == 1
+    assert L.fnorm_postnorm_workspace_size(512, 4092, ctypes.byref(n)) == 1
+
+
+def test_no_call_allocates_or_synchronises():
+    # No entry point may allocate device memory or synchronise the host,
+    # except fnorm_check_status (which synchronises its stream by contract):
+    # the library's sources name no allocation or device-wide synchronisation
+    # at all, and the only blocking copies are in the status read.
+    csrc = os.path.join(ROOT, "normalization_gemm_tcgen05_gb300", "csrc")
+    banned = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cudaDeviceSynchronize|cudaMallocAsync|cudaHostAlloc|"
+                        r"cudaMallocHost|cuMemAlloc\w*|cudaMemset|cudaStreamSynchronize|cudaMemcpy)\s*\(")
+    allowed = {("runtime.cu", "cudaStreamSynchronize"), ("runtime.cu", "cudaMemcpy")}
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        text = open(os.path.join(csrc, name)).read()
+        code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+        for m in banned.finditer(code):
+            assert (name, m.group(1)) in allowed, f"{name} calls {m.group(1)}"
+    # and the blocking calls that remain sit in the status read alone
+    rt = open(os.path.join(csrc, "runtime.cu")).read()
+    body = rt[rt.index("fnorm_status_t read_and_clear_status"):]
+    body = body[:body.index("\n}\n") + 3]
+    code = re.sub(r"//[^\n]*", "", rt.replace(body, ""))
+    assert not re.search(r"\b(cudaStreamSynchronize|cudaMemcpy)\s*\(", code)
 
 
 def test_forced_cluster(L):

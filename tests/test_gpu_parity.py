@@ -114,11 +114,11 @@ POST1 = [("layernorm", 64), ("layernorm", 128), ("rmsnorm", 64), ("rmsnorm", 128
          ("layernorm", 256), ("rmsnorm", 256), ("layernorm", 200), ("rmsnorm", 8)]
 
 
-def _post(w, d, norm, pre=False, affine=True):
+def _post(w, d, norm, pre=False, affine=True, workspace=True):
     gamma = d["gamma"] if affine else None
     beta = d["beta"] if (affine and norm == "layernorm") else None
     C, st = fn.gemm_postnorm(_dev(d["A"]), _dev(d["B"]), norm, _dev(gamma), _dev(beta), w.eps,
-                             pre_rmsnorm=pre, pre_eps=w.pre_eps, return_stats=True)
+                             pre_rmsnorm=pre, pre_eps=w.pre_eps, return_stats=True, workspace=workspace)
     ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), norm, to_f64(gamma), to_f64(beta), w.eps,
                                pre_rmsnorm=pre, pre_eps=w.pre_eps)
     assert_out_close(C, ref["C"], f"post-{norm} C")
@@ -155,7 +155,8 @@ def test_pre_and_post_in_one_kernel(norm):
 # GEMM + post-norm over a cluster along N (DSMEM row-statistics exchange)
 # ----------------------------------------------------------------------------
 CLUSTER_N = [320, 512, 640, 1024]                  # resident slices, 2 or 4 CTAs
-SPILL_N = [1032, 2048, 3000, 4096, 8192, 12288]    # spill layout, 4 CTAs, 2..12 slices each
+WIDE_N = [1032, 2048, 3000, 4096, 8192, 12288]     # grid exchange (5..48 tiles a row) or, with no
+                                                   # workspace, the spill layout (4 CTAs, 2..12 slices)
 
 
 @pytest.mark.parametrize("N", CLUSTER_N)
@@ -167,24 +168,36 @@ def test_postnorm_cluster(norm, N):
     _post(w, d, norm)
 
 
-@pytest.mark.parametrize("N", SPILL_N)
+@pytest.mark.parametrize("N", WIDE_N)
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_postnorm_grid_exchange(norm, N):
+    # with a workspace: 256-column tiles resident in tensor memory over the
+    # whole grid, the row statistics exchanged through the workspace
+    w, d = _case("cfg4_n4096_ln", N + 7 * (norm == "rmsnorm"), M=520, N=N, K=192)
+    assert fn.postnorm_workspace_size(520, N) > 0
+    _post(w, d, norm)
+
+
+@pytest.mark.parametrize("N", WIDE_N)
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
 def test_postnorm_spill(norm, N):
+    # without a workspace (fnorm_gemm_postnorm): the spill layout on a cluster
     w, d = _case("cfg4_n4096_ln", N + 7 * (norm == "rmsnorm"), M=520, N=N, K=192)
     c, cols = fn.postnorm_plan(N)
-    assert cols > 256
-    _post(w, d, norm)
+    assert c == 4 and cols > 256
+    _post(w, d, norm, workspace=False)
 
 
 @pytest.mark.parametrize("N", [1032, 4096, 8192])
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
-def test_postnorm_spill_on_a_cluster(norm, N):
-    # the cluster form of the spill layout (forced), beside the grid-wide
-    # exchange the planner picks for wide rows
+def test_postnorm_spill_on_a_forced_cluster(norm, N):
+    # a forced cluster size takes the spill layout even where a workspace is
+    # offered (the binding then passes none)
     w, d = _case("cfg4_n4096_ln", N + 3 * (norm == "rmsnorm"), M=300, N=N, K=128)
     try:
         fn.set_postnorm_cluster(4)
         assert fn.postnorm_plan(N)[0] == 4
+        assert fn.postnorm_workspace_size(300, N) == 0
         _post(w, d, norm)
     finally:
         fn.set_postnorm_cluster(0)
@@ -196,7 +209,7 @@ def test_grid_exchange_repeats_and_replays():
     # the same as the first, bit for bit, and the status stays clean
     w, d = _case("cfg4_n4096_ln", 31, M=128 * 170 + 5, N=2048, K=128)
     A, B, g, b = _dev(d["A"]), _dev(d["B"]), _dev(d["gamma"]), _dev(d["beta"])
-    assert fn.postnorm_plan(2048)[0] == 1
+    assert fn.postnorm_workspace_size(w.M, 2048) > 0
     C0 = fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps)
     C1 = fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps)
     fn.check_status(DEV)
@@ -225,17 +238,79 @@ def test_postnorm_cluster_with_pre():
     _post(w, d, "layernorm", pre=True)
 
 
-def test_postnorm_spill_with_pre_and_no_affine():
+@pytest.mark.parametrize("workspace", [True, False])
+def test_postnorm_wide_with_pre_and_no_affine(workspace):
     w, d = _case("cfg5", 14, M=300, N=4096, K=256)
-    _post(w, d, "layernorm", pre=True)
-    _post(w, d, "rmsnorm", pre=True, affine=False)
+    _post(w, d, "layernorm", pre=True, workspace=workspace)
+    _post(w, d, "rmsnorm", pre=True, affine=False, workspace=workspace)
 
 
-def test_postnorm_spill_many_row_blocks():
-    # more row blocks than co-resident clusters: every CTA carries a pending
-    # normalisation across row blocks
+@pytest.mark.parametrize("workspace", [True, False])
+def test_postnorm_wide_many_row_blocks(workspace):
+    # more row blocks than CTAs: the grid exchange's CTAs hold a tile of one
+    # row block while computing the next; the spill layout's CTAs carry a
+    # pending normalisation across row blocks
     w, d = _case("cfg4_n4096_ln", 15, M=128 * 160 + 37, N=3072, K=64)
-    _post(w, d, "layernorm")
+    _post(w, d, "layernorm", workspace=workspace)
+
+
+def test_grid_exchange_and_spill_agree():
+    # the two wide-row layouts split the row statistics differently: equal up
+    # to fp32 summation order
+    w, d = _case("cfg4_n4096_ln", 41, M=384, N=4096, K=256)
+    _, s1 = _post(w, d, "layernorm", workspace=True)
+    _, s2 = _post(w, d, "layernorm", workspace=False)
+    assert np.max(np.abs(np64(s1["rstd"]) - np64(s2["rstd"])) / np64(s2["rstd"])) < 1e-5
+
+
+def test_grid_exchange_row_wider_than_the_grid():
+    # a row of more 256-column tiles than SMs cannot be exchanged grid-wide
+    # (a CTA would hold two tiles of the row block it waits on): the call
+    # takes the spill layout even with a workspace, and is still correct
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    N = 256 * (sms + 1)
+    w, d = _case("cfg4_n4096_ln", 43, M=130, N=N, K=64)
+    _post(w, d, "rmsnorm", workspace=True)
+
+
+def test_postnorm_without_workspace_allocates_nothing_and_captures():
+    # fnorm_gemm_postnorm on a fresh stream, through the C ABI: no device
+    # memory changes hands, and its very first call captures into a CUDA
+    # graph whose replays equal the eager result bit for bit
+    w, d = _case("cfg4_n4096_ln", 47, M=512, N=4096, K=256)
+    A, B, g, b = _dev(d["A"]), _dev(d["B"]), _dev(d["gamma"]), _dev(d["beta"])
+    C0 = torch.empty(512, 4096, dtype=torch.bfloat16, device=DEV)
+    C1 = torch.empty_like(C0)
+    L = fn.lib()
+
+    def call(C, stream):
+        st = L.fnorm_gemm_postnorm(A.data_ptr(), B.data_ptr(), C.data_ptr(), 512, 4096, 256, fn.LAYERNORM,
+                                   g.data_ptr(), b.data_ptr(), w.eps, 0, 1e-6, None, None, None,
+                                   stream.cuda_stream)
+        assert st == fn.OK, fn.last_error()
+
+    call(C0, torch.cuda.current_stream(DEV))  # loads the kernel (lazy module loading takes device memory)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(DEV)
+    alloc0 = torch.cuda.memory_allocated(DEV)
+    s1 = torch.cuda.Stream(DEV)
+    call(C0, s1)
+    s1.synchronize()
+    free1, _ = torch.cuda.mem_get_info(DEV)
+    assert free1 == free0 and torch.cuda.memory_allocated(DEV) == alloc0
+    s2 = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s2):
+        call(C1, s2)
+    for _ in range(2):
+        C1.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(C1, C0)
+    fn.check_status(DEV)
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", to_f64(d["gamma"]),
+                               to_f64(d["beta"]), w.eps)
+    assert_out_close(C0, ref["C"], "fnorm_gemm_postnorm, no workspace")
 
 
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])

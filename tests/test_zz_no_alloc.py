@@ -1,11 +1,13 @@
 """The allocation-free post-norm entry point (collected last on purpose: it
-must agree with fnorm_gemm_postnorm whether it runs alone or after every
-other test, i.e. whatever state the library's fixed workspace was left in).
+must agree with the workspace entry point whether it runs alone or after
+every other test, i.e. whatever state the library's fixed workspace was left
+in; each test also runs a differently shaped call first, so the fixed
+workspace's counters are never fresh when the compared calls start).
 
 fnorm_gemm_postnorm_noalloc keeps the wide-row grid exchange's statistics in
-a fixed device array instead of a per-stream workspace; results must equal
-fnorm_gemm_postnorm's bit for bit (same kernels, same plan), on two calls in a
-row, and shapes past the array must be refused with a clear error.
+a fixed device array instead of a caller's workspace; results must equal
+fnorm_gemm_postnorm_ws's bit for bit (same kernels, same plan), on two calls
+in a row, and shapes past the array must be refused with a clear error.
 """
 import numpy as np
 import pytest
@@ -34,6 +36,11 @@ def test_noalloc_matches_postnorm_twice(norm, M, N, K):
     g = d["gamma"].to(DEV)
     b = d["beta"].to(DEV) if norm == "layernorm" else None
     C0, st0 = fn.gemm_postnorm(A, B, norm, g, b, w.eps, return_stats=True)
+    # a wide RMSNorm call of another shape through the fixed workspace first
+    Mw, Nw = 384, 8192
+    Aw = torch.randn(Mw, 64, device=DEV).to(torch.bfloat16)
+    Bw = torch.randn(64, Nw, device=DEV).to(torch.bfloat16)
+    fn.gemm_postnorm_noalloc(Aw, Bw, torch.empty(Mw, Nw, dtype=torch.bfloat16, device=DEV), "rmsnorm")
     for _ in range(2):  # two calls in a row: the second reuses the counters
         C = torch.empty_like(C0)
         rstd = torch.empty(M, dtype=torch.float32, device=DEV)
