@@ -155,8 +155,9 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
  *   and normalises itself straight from the fp32 accumulator.  Nothing is
  *   written to C before it is normalised.  The kernel is a cooperative launch
  *   (all its CTAs co-resident); a row of more tiles than the device has SMs
- *   (N > 256 * SMs) takes fnorm_gemm_postnorm's spill layout instead, as do
- *   rows of at most 1024 columns, which need no workspace.
+ *   (N > 256 * SMs) or more than 2^21 rows take fnorm_gemm_postnorm's spill
+ *   layout instead, as do rows of at most 1024 columns, which need no
+ *   workspace.
  *   workspace:       device memory of at least workspace_bytes, 16-byte
  *                    aligned, owned by the caller, or NULL (then this is
  *                    fnorm_gemm_postnorm).  fnorm_postnorm_workspace_size
@@ -181,11 +182,13 @@ fnorm_status_t fnorm_gemm_postnorm_ws(const fnorm_bf16* A, const fnorm_bf16* B, 
 
 /*
  * fnorm_postnorm_workspace_size — bytes of the workspace fnorm_gemm_postnorm_ws
- * uses for an M x N post-norm, into *bytes: 1024 per (128-row block,
- * 256-column tile), 8 per row block, and 256; 0 when the row needs no
- * exchange workspace (N <= 1024, M == 0, or a forced cluster size).  A
- * workspace sized for M x N serves every call with at most as many row
- * blocks and tiles.  Host only; launches nothing.
+ * uses for an M x N post-norm, into *bytes: 256 + 8 * 16384 (a header and
+ * the counters of up to 16384 row blocks, at the same place whatever the
+ * call's shape) plus 1024 per (128-row block, 256-column tile); 0 when the
+ * call needs no exchange workspace (N <= 1024, M == 0, M > 2^21 rows, or a
+ * forced cluster size).  A workspace sized for M x N serves every call with
+ * at most as many (row block, tile) pairs, whatever their shapes.  Host only;
+ * launches nothing.
  */
 fnorm_status_t fnorm_postnorm_workspace_size(int64_t M, int64_t N, size_t* bytes);
 
@@ -451,6 +454,21 @@ fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size);
  * FNORM_ERR_INVALID_ARG.
  */
 fnorm_status_t fnorm_set_pair_mma(int mode);
+
+/*
+ * fnorm_set_b_multicast — choose when fnorm_gemm, fnorm_lazy_prenorm_gemm,
+ * fnorm_prenorm_gemm and the grid exchange of fnorm_gemm_postnorm_ws share
+ * B between the two CTAs of a 2-CTA cluster along M: the CTAs compute the
+ * tiles of two neighbouring 128-row blocks at the same 256 columns, each
+ * with its own one-CTA MMAs, and each loads half of every k-block's B tile
+ * into both CTAs' shared memory with one TMA multicast (a third less read
+ * from L2 per SM).  mode: 1 = whenever the tile is 256 columns wide and B is
+ * not resident; 0 = never; -1 = automatic, the default (the same, for more
+ * than one row block).  It changes the schedule, not the arithmetic: every
+ * output is the same sum in the same order as with one-CTA tiles.
+ * Process-wide.  Any other mode returns FNORM_ERR_INVALID_ARG.
+ */
+fnorm_status_t fnorm_set_b_multicast(int mode);
 
 /*
  * fnorm_debug_wait_timeout — failure-detection self test.  Launches one small

@@ -41,7 +41,7 @@ __all__ = [
     "postnorm_workspace_size",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
-    "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster", "set_pair_mma",
+    "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster", "set_pair_mma", "set_b_multicast",
     "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
 ]
 
@@ -99,6 +99,7 @@ _SIGNATURES = {
     "fnorm_postnorm_plan": (_c_status, [_i64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "fnorm_set_postnorm_cluster": (_c_status, [ctypes.c_int]),
     "fnorm_set_pair_mma": (_c_status, [ctypes.c_int]),
+    "fnorm_set_b_multicast": (_c_status, [ctypes.c_int]),
     "fnorm_debug_wait_timeout": (_c_status, [ctypes.c_uint64, _p]),
     "fnorm_version": (ctypes.c_int, []),
 }
@@ -585,6 +586,12 @@ def set_postnorm_cluster(cluster_size: int) -> None:
 def set_pair_mma(mode: int) -> None:
     """When 256-column GEMM tiles run as two-CTA MMAs: -1 automatic, 0 never, 1 always (see fnorm_set_pair_mma)."""
     _check(lib().fnorm_set_pair_mma(int(mode)))
+
+
+def set_b_multicast(mode: int) -> None:
+    """When 256-column tiles share B over a 2-CTA cluster (TMA multicast): -1 automatic, 0 never,
+    1 always (see fnorm_set_b_multicast)."""
+    _check(lib().fnorm_set_b_multicast(int(mode)))
 
 
 def debug_wait_timeout(limit_ns: int = 50_000_000, device=None) -> None:

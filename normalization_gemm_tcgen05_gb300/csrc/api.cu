@@ -18,6 +18,7 @@ fnorm_status_t read_and_clear_status(cudaStream_t stream);
 namespace {
 std::atomic<int> g_forced_cluster{0};
 std::atomic<int> g_pair_mode{-1};  // fnorm_set_pair_mma: -1 automatic, 0 never, 1 whenever eligible
+std::atomic<int> g_mcb_mode{-1};   // fnorm_set_b_multicast: -1 automatic, 0 never, 1 whenever eligible
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
 
@@ -95,6 +96,14 @@ bool want_resident_b(int64_t M, int64_t N, int64_t K, int bn) {
 // pair's loads complete later.  Automatic selection therefore keeps one CTA.
 bool want_pair(int bn, bool bres) {
   return g_pair_mode.load(std::memory_order_relaxed) == 1 && bn == 256 && !bres;
+}
+
+// B shared by a 2-CTA cluster along M (TMA multicast) for 256-column tiles
+// with B streamed: each SM then reads a third less from L2 per k-block.
+// Automatic selection takes it whenever there are two row blocks to pair.
+bool want_mcb(int64_t M, int bn, bool bres) {
+  const int mode = g_mcb_mode.load(std::memory_order_relaxed);
+  return mode != 0 && bn == 256 && !bres && (mode == 1 || M > 128);
 }
 
 // How a post-norm row of width N is laid out over the CTAs.
@@ -193,6 +202,7 @@ fnorm_status_t fnorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* 
   L.bn = gemm_tile_n(N);
   L.bres = want_resident_b(M, N, K, L.bn);
   if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_mcb(M, L.bn, L.bres)) return launch_fused_mcb(L);
   return launch_fused_plain(L);
 }
 
@@ -230,6 +240,7 @@ fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B,
   L.pre_eps = eps;
   L.rstd_out = rstd_out;
   if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_mcb(M, L.bn, L.bres)) return launch_fused_mcb(L);
   return launch_fused_plain(L);
 }
 
@@ -270,14 +281,15 @@ fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnor
   FN_TRY(check_ptr(pre_rstd_out, "pre_rstd_out", 4, true));
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   GxScratch caller_gx{};
-  if (plan.gx && ws == Ws::kCaller) FN_TRY(gx_scratch_from(workspace, workspace_bytes, M, N, &caller_gx));
+  if (plan.gx && ws == Ws::kCaller && (M + 127) / 128 <= kGxMaxRowBlocks)
+    FN_TRY(gx_scratch_from(workspace, workspace_bytes, M, N, &caller_gx));
   if (plan.gx) {
     // one CTA per tile of a row at least (no CTA may hold two tiles of the
     // row block it waits on); a row with more tiles than SMs takes the
     // cluster spill layout instead
     DeviceInfo dev;
     FN_TRY(current_device(&dev));
-    if ((N + 255) / 256 > dev.num_sms) {
+    if ((N + 255) / 256 > dev.num_sms || (M + 127) / 128 > kGxMaxRowBlocks) {
       FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, false));
     } else if (ws == Ws::kFixed) {
       const GxScratch* gx = nullptr;
@@ -307,7 +319,16 @@ fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnor
   L.mean_out = mean_out;
   L.rstd_out = rstd_out;
   L.pre_rstd_out = pre_rstd_out;
-  if (plan.gx) return launch_fused_post_grid(L);
+  if (plan.gx) {
+    if (want_mcb(M, L.bn, L.bres)) {
+      // a device that will not launch a cooperative grid of clusters takes
+      // the one-CTA grid exchange
+      const fnorm_status_t st = launch_fused_mcb_grid(L);
+      if (st != FNORM_ERR_UNSUPPORTED) return st;
+      clear_error();
+    }
+    return launch_fused_post_grid(L);
+  }
   return (plan.cluster == 1 && !plan.spill) ? launch_fused_post_single(L) : launch_fused_post_cluster(L);
 }
 }  // namespace
@@ -338,7 +359,7 @@ fnorm_status_t fnorm_postnorm_workspace_size(int64_t M, int64_t N, size_t* bytes
   FN_TRY(check_mnk(M, N, 8));
   PostPlan plan{};
   FN_TRY(plan_postnorm(N, forced_postnorm_cluster(), &plan, true));
-  *bytes = (plan.gx && M > 0) ? gx_workspace_bytes(M, N) : 0;
+  *bytes = (plan.gx && M > 0 && (M + 127) / 128 <= kGxMaxRowBlocks) ? gx_workspace_bytes(M, N) : 0;
   return FNORM_OK;
 }
 
@@ -400,6 +421,7 @@ fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folde
     // RMSNorm with gamma only: the folded B makes it the plain lazy pre-norm
     L.mode = MODE_PRE;
     if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
+    if (want_mcb(M, L.bn, L.bres)) return launch_fused_mcb(L);
     return launch_fused_plain(L);
   }
   L.mode = MODE_PRE | MODE_AFF | (ln ? MODE_PRE_LN : 0);
@@ -407,6 +429,7 @@ fnorm_status_t fnorm_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B_folde
   L.bias = bias;
   L.mean_out = ln ? mean_out : nullptr;
   if (want_pair(L.bn, L.bres)) return launch_fused_pair(L);
+  if (want_mcb(M, L.bn, L.bres)) return launch_fused_mcb(L);
   return launch_fused_prenorm_affine(L);
 }
 
@@ -659,6 +682,13 @@ fnorm_status_t fnorm_set_pair_mma(int mode) {
   clear_error();
   if (mode < -1 || mode > 1) return bad("pair MMA mode must be -1 (automatic), 0 (never) or 1 (whenever eligible)");
   g_pair_mode.store(mode, std::memory_order_relaxed);
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_set_b_multicast(int mode) {
+  clear_error();
+  if (mode < -1 || mode > 1) return bad("B multicast mode must be -1 (automatic), 0 (never) or 1 (whenever eligible)");
+  g_mcb_mode.store(mode, std::memory_order_relaxed);
   return FNORM_OK;
 }
 

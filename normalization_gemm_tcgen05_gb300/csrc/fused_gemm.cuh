@@ -99,6 +99,12 @@ enum : int {
   // tcgen05 cta_group::2, each staging its own 128 rows of A and half of B's
   // BN columns, so that each SM takes in a third less per tile
   MODE_CTA2 = 16384,
+  // B shared by a 2-CTA cluster along M: the two CTAs compute the tiles of
+  // two neighbouring row blocks at the same columns, each with its own
+  // one-CTA MMAs, and each loads half of every stage's B tile with a TMA
+  // multicast into both CTAs' shared memory, so each SM takes in a third less
+  // per k-block; a stage is free again once both CTAs' MMAs have read it
+  MODE_MCB = 32768,
 };
 
 struct FusedParams {
@@ -193,8 +199,10 @@ struct KCfg {
   static constexpr bool DGRAD = (MODE & MODE_DGRAD) != 0;
   static constexpr bool GX = (MODE & MODE_GX) != 0;
   static constexpr bool CTA2 = (MODE & MODE_CTA2) != 0;
+  static constexpr bool MCB = (MODE & MODE_MCB) != 0;
+  static constexpr bool PAIR = CTA2 || MCB;    // a 2-CTA cluster along M shares each tile sequence
   static constexpr int CG = CTA2 ? 2 : 1;      // CTA group of every tcgen05 instruction
-  static constexpr int RB = CTA2 ? 256 : 128;  // rows of one tile (a row block)
+  static constexpr int RB = PAIR ? 256 : 128;  // rows of one tile sequence unit (one or two row blocks)
   static constexpr int BNS = CTA2 ? BN / 2 : BN;  // columns of B this CTA stages
   // the spill layout's in-place normalisation runs in its own warps (10-13)
   // unless those warps compute the Lazy Pre-Norm sums of squares
@@ -265,6 +273,9 @@ struct KCfg {
   static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
   static_assert(!CTA2 || (BN == 256 && !POST && !BRES && !RES && !BT && !AT && !DGRAD),
                 "two-CTA MMA: 256-column tiles of the plain and lazy pre-norm GEMMs");
+  static_assert(!MCB || (!CTA2 && (BN == 128 || BN == 256) && !CLUSTER && !SPILL && !BRES && !RES && !BT && !AT &&
+                         !DGRAD && (!POST || GX)),
+                "B multicast: the plain, lazy pre-norm and grid-exchange post-norm GEMMs");
 };
 
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD, GX = Cfg::GX;
-  constexpr bool CTA2 = Cfg::CTA2;
+  constexpr bool CTA2 = Cfg::CTA2, MCB = Cfg::MCB, PAIR = Cfg::PAIR;
   constexpr int CG = Cfg::CG, RB = Cfg::RB;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
@@ -501,14 +512,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   const int rank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
   // CTA pair: rank 0 issues the MMAs of both CTAs; each CTA owns rows
   // prank * 128 .. + 127 of every 256-row tile
-  const int prank = CTA2 ? static_cast<int>(cluster_ctarank()) : 0;
-  const bool issuer = prank == 0;
+  // (B multicast: the same rows split, but each CTA issues its own MMAs)
+  const int prank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool issuer = !CTA2 || prank == 0;
   const int num_m = (M + RB - 1) / RB;
   const int cta_cols = S * BN;
   const int group_cols = cta_cols * C;
   const int ngroups = (N + group_cols - 1) / group_cols;
   const int total = num_m * ngroups;  // row blocks (x column groups) to visit
-  const int CP = CTA2 ? 2 : C;  // CTAs that share each tile sequence
+  const int CP = PAIR ? 2 : C;  // CTAs that share each tile sequence
   const int cid = static_cast<int>(blockIdx.x) / CP;
   const int ncl = static_cast<int>(gridDim.x) / CP;
   const int num_kb = (K + BK - 1) / BK;
@@ -540,8 +552,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     for (int s = lane; s < STAGES; s += 32) {
       mbar_init(smem_u32(&aux->full[s]), 1);
       mbar_init(smem_u32(&aux->mdone[s]), 1);
-      // the MMA's commit, and for the lazy pre-norm the norm warps' reads
-      mbar_init(smem_u32(&aux->empty[s]), 1 + (PRE ? 4 * Cfg::NPART : 0));
+      // the MMA's commit (B multicast: both CTAs' MMAs, which read what this
+      // CTA's multicast wrote), and for the lazy pre-norm the norm warps' reads
+      mbar_init(smem_u32(&aux->empty[s]), (MCB ? 2 : 1) + (PRE ? 4 * Cfg::NPART : 0));
     }
     if (lane < 2) {
       const int b = lane;
@@ -581,7 +594,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       // loads a deeper warm-up would delay; measured 10.7 -> 10.3 us.)
       const int t0 = tile_of(0);
       const int m0 = (t0 / ngroups) * RB + prank * Cfg::BM;
-      const int n0 = ((t0 % ngroups) * C + rank) * cta_cols + prank * Cfg::BNS;
+      const int n0 = ((t0 % ngroups) * C + rank) * cta_cols + (CTA2 ? prank * Cfg::BNS : 0);
       constexpr int kWarm = RES ? 2 : STAGES;
       const int nk = m0 < M ? (num_kb < kWarm ? num_kb : kWarm) : 0;
       for (int kb = 0; kb < nk; ++kb) {
@@ -605,7 +618,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CLUSTER || CTA2) cluster_sync();  // peers' barriers are initialised before any remote arrive
+  if (CLUSTER || PAIR) cluster_sync();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = aux->tmem_base;
   // Set-up above overlaps the previous grid in the stream; every global
@@ -630,7 +643,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int m0 = (t / ngroups) * RB + prank * Cfg::BM;
         for (int s = 0; s < S && ok; ++s) {
           // (CTA pair: this CTA's half of the tile's B columns)
-          const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + prank * Cfg::BNS;
+          const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + (CTA2 ? prank * Cfg::BNS : 0);
           for (int kb = 0; kb < num_kb; ++kb) {
             // (CTA pair: the stage is released by rank 0's MMA commit)
             if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
@@ -671,8 +684,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               } else {
 #pragma unroll
                 for (int c = 0; c < Cfg::BNS / 64; ++c) {
-                  if (CTA2) load_pair(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
-                  else tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                  if (CTA2) {
+                    load_pair(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                  } else if (MCB) {
+                    // this CTA's half of the tile's B boxes, into both CTAs
+                    // (same offset; each CTA's full barrier counts all of B)
+                    if (c / (BN / 128) == prank)
+                      tma_load_2d_mc(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, 0x3);
+                  } else {
+                    tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
+                  }
                 }
               }
             }
@@ -741,6 +762,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               umma_commit_pair(smem_u32(&aux->empty[stage]), 0x3);  // both CTAs' stage
               // rank 1's norm warps read its A rows once the stage is known complete
               if (PRE) umma_commit_pair(smem_u32(&aux->mdone[stage]), 0x2);
+            } else if (MCB) {
+              umma_commit_mc(smem_u32(&aux->empty[stage]), 0x3);  // both CTAs' stage (B written by both)
             } else {
               umma_commit(smem_u32(&aux->empty[stage]));
             }
@@ -1248,7 +1271,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               break;
             }
             ++xit;
-          } else if (GX) {
+          } else if (GX && m0 < M) {
+            // (B multicast: the second row block of the last pair may lie
+            // past M; it has no statistics to exchange and stores nothing)
             if (!gx_exchange(part0, part1, m0, g)) {
               ok = false;
               break;
@@ -1477,7 +1502,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
   }
-  if (CLUSTER || CTA2) cluster_sync();  // no CTA leaves while a peer may still address it
+  if (CLUSTER || PAIR) cluster_sync();  // no CTA leaves while a peer may still address it
   if (GX && threadIdx.x == 0) {
     // the last CTA of the grid to finish starts the next generation: every
     // counter this grid touched then reads as zero to the next launch

@@ -117,9 +117,10 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     attr[cfg.numAttrs].val.cooperative = 1;
     ++cfg.numAttrs;
   }
-  if (Cfg::CLUSTER || Cfg::CTA2) {
-    // post-norm: C CTAs along N; two-CTA MMA: the CTA pair of each tile
-    const int CL = Cfg::CTA2 ? 2 : C;
+  if (Cfg::CLUSTER || Cfg::PAIR) {
+    // post-norm: C CTAs along N; two-CTA MMA and B multicast: the CTA pair of
+    // each 256-row unit
+    const int CL = Cfg::PAIR ? 2 : C;
     if (Cfg::CLUSTER && (C < 1 || C > Cfg::CLMAX)) {
       set_error("cluster size %d outside 1..%d for this kernel", C, Cfg::CLMAX);
       return FNORM_ERR_UNSUPPORTED;
@@ -147,6 +148,10 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
       max_clusters[dev.id][CL].store(mc, std::memory_order_relaxed);
     }
     const long long nclusters = total < mc ? total : mc;
+    if (Cfg::GX && ngroups > nclusters) {
+      set_error("internal: a grid exchange over %d tiles per row needs as many clusters (%lld)", ngroups, nclusters);
+      return FNORM_ERR_UNSUPPORTED;
+    }
     cfg.gridDim = dim3((unsigned)(nclusters * CL), 1, 1);
   } else {
     const long long grid = total < dev.num_sms ? total : dev.num_sms;
@@ -159,6 +164,15 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tr, p);
+  if (e != cudaSuccess && Cfg::GX && Cfg::PAIR &&
+      (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration ||
+       e == cudaErrorCooperativeLaunchTooLarge)) {
+    // a cooperative launch of clusters refused before anything ran: the
+    // caller takes the one-CTA grid exchange
+    (void)cudaGetLastError();
+    set_error("cooperative launch of a clustered grid exchange not available: %s", cudaGetErrorString(e));
+    return FNORM_ERR_UNSUPPORTED;
+  }
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
   return FNORM_OK;
 }

@@ -51,7 +51,11 @@ struct GxScratch {
 
 // Bytes of the caller's grid-exchange workspace for an M x N post-norm, and
 // its layout over a given buffer (FNORM_ERR_INVALID_ARG if it is too small or
-// misaligned).  Nothing is allocated.
+// misaligned).  Nothing is allocated.  The counters have a fixed capacity of
+// kGxMaxRowBlocks 128-row blocks (M up to 2^21); taller calls take the
+// cluster spill layout.
+constexpr size_t kGxHeaderBytes = 256;
+constexpr int kGxMaxRowBlocks = 16384;
 size_t gx_workspace_bytes(int64_t M, int64_t N);
 fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t N, GxScratch* out);
 
@@ -98,6 +102,8 @@ fnorm_status_t launch_fused_post_residual_cluster(const FusedLaunch& L);  // res
 fnorm_status_t launch_fused_backward(const FusedLaunch& L);       // backward of the Lazy Pre-RMSNorm GEMM
 fnorm_status_t launch_fused_post_grid(const FusedLaunch& L);      // post-norm, grid-wide statistics exchange
 fnorm_status_t launch_fused_pair(const FusedLaunch& L);           // GEMM, lazy pre-norms: two-CTA MMA (256-row tiles)
+fnorm_status_t launch_fused_mcb(const FusedLaunch& L);            // GEMM, lazy pre-norms: B multicast over a 2-CTA cluster
+fnorm_status_t launch_fused_mcb_grid(const FusedLaunch& L);       // grid-exchange post-norm, B multicast
 
 // B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
 fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,

@@ -89,12 +89,16 @@ fnorm_status_t current_device(DeviceInfo* out) {
   return FNORM_OK;
 }
 
-// Layout of a grid-exchange workspace for an M x N post-norm: the per-tile
-// row statistics [row blocks][tiles per row][128] float2, the per-row-block
-// counters, then 256 bytes holding the generation word and the finish count.
+// Layout of a caller's grid-exchange workspace, the same for every call that
+// uses it whatever its shape (so counters and the generation word are always
+// found where earlier calls left them): 256 bytes holding the generation word
+// (offset 0) and the finish count (offset 128), then kGxMaxRowBlocks
+// per-row-block counters, then the per-tile row statistics
+// [row blocks][tiles per row][128] float2 of the call.
 size_t gx_workspace_bytes(int64_t M, int64_t N) {
   const int64_t rb = (M + 127) / 128, tiles = (N + 255) / 256;
-  return static_cast<size_t>(rb * tiles) * 128 * sizeof(float2) + static_cast<size_t>(rb) * sizeof(uint64_t) + 256;
+  return kGxHeaderBytes + static_cast<size_t>(kGxMaxRowBlocks) * sizeof(uint64_t) +
+         static_cast<size_t>(rb * tiles) * 128 * sizeof(float2);
 }
 
 fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t N, GxScratch* out) {
@@ -108,15 +112,14 @@ fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t
     set_error("workspace must be 16-byte aligned");
     return FNORM_ERR_INVALID_ARG;
   }
-  const int64_t rb = (M + 127) / 128, tiles = (N + 255) / 256;
   char* base = static_cast<char*>(workspace);
-  const size_t part_bytes = static_cast<size_t>(rb * tiles) * 128 * sizeof(float2);
-  out->part = reinterpret_cast<float2*>(base);
-  out->cnt = reinterpret_cast<unsigned long long*>(base + part_bytes);
-  out->gen = reinterpret_cast<uint32_t*>(base + part_bytes + static_cast<size_t>(rb) * sizeof(uint64_t));
+  out->gen = reinterpret_cast<uint32_t*>(base);
   out->finish = out->gen + 32;
-  out->units_cap = static_cast<int>(rb * tiles);
-  out->rowblocks_cap = static_cast<int>(rb);
+  out->cnt = reinterpret_cast<unsigned long long*>(base + kGxHeaderBytes);
+  out->part = reinterpret_cast<float2*>(base + kGxHeaderBytes + static_cast<size_t>(kGxMaxRowBlocks) * 8);
+  const size_t units = (bytes - kGxHeaderBytes - static_cast<size_t>(kGxMaxRowBlocks) * 8) / (128 * sizeof(float2));
+  out->units_cap = static_cast<int>(units < 0x7fffffffu ? units : 0x7fffffffu);
+  out->rowblocks_cap = kGxMaxRowBlocks;
   return FNORM_OK;
 }
 

@@ -183,13 +183,14 @@ def test_postnorm_plan(L, N, cluster, cols):
 
 
 @pytest.mark.parametrize("M,N", [(16384, 8192), (16384, 4096), (300, 1032), (1, 2048), (16384, 1024), (0, 4096),
-                                 (65536, 256)])
+                                 (65536, 256), (128 * 16384, 2048), (128 * 16384 + 1, 2048)])
 def test_postnorm_workspace_size(L, M, N):
-    # 1 KB per (128-row block, 256-column tile), 8 bytes per row block, 256;
-    # nothing for rows a cluster holds (N <= 1024) or an empty call
+    # a 256-byte header, 16384 row-block counters, then 1 KB per (128-row
+    # block, 256-column tile); nothing for rows a cluster holds (N <= 1024)
+    # or an empty call
     import normalization_gemm_tcgen05_gb300 as fn
     rb, tiles = -(-M // 128), -(-N // 256)
-    want = rb * tiles * 1024 + rb * 8 + 256 if (N > 1024 and M > 0) else 0
+    want = 256 + 8 * 16384 + rb * tiles * 1024 if (N > 1024 and 0 < M and rb <= 16384) else 0
     assert fn.postnorm_workspace_size(M, N) == want
 
 
@@ -206,7 +207,7 @@ def test_postnorm_workspace_size_follows_a_forced_cluster(L):
 def test_postnorm_ws_argument_rules(L):
     f = L.fnorm_gemm_postnorm_ws
     W = ctypes.c_void_p(0x800000)
-    need = (4 * 16) * 1024 + 4 * 8 + 256   # M = 512, N = 4096
+    need = 256 + 8 * 16384 + (4 * 16) * 1024   # M = 512, N = 4096
     # too small, misaligned
     assert f(FAKE, FAKE, FAKE, 512, 4096, 64, 1, None, None, 1e-5, 0, 1e-6, None, None, None, W, need - 1, None) == 1
     assert b"workspace" in L.fnorm_last_error()

@@ -1,0 +1,121 @@
+"""B shared by a 2-CTA cluster along M (TMA multicast): the same arithmetic as
+the one-CTA tiles, so every output and statistic must agree bit for bit, on
+row-block counts that pair up and on odd ones (the second CTA of the last
+cluster then has no rows), and match the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normalization_gemm_tcgen05_gb300 as fn
+import oracle
+from gpu_util import assert_out_close, assert_rstd_close
+from workloads import WORKLOADS, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _both(call):
+    """call() with B multicast forced off, then on; returns both results."""
+    out = []
+    try:
+        for mode in (0, 1):
+            fn.set_b_multicast(mode)
+            out.append(call())
+            fn.check_status(DEV)
+    finally:
+        fn.set_b_multicast(-1)
+    return out
+
+
+def _equal(a, b, what):
+    if isinstance(a, torch.Tensor):
+        assert torch.equal(a, b), f"{what}: B multicast differs from one-CTA tiles"
+    elif isinstance(a, dict):
+        for k in a:
+            if a[k] is not None:
+                _equal(a[k], b[k], f"{what} {k}")
+    else:
+        for i, (x, y) in enumerate(zip(a, b)):
+            _equal(x, y, f"{what}[{i}]")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (384, 512, 320), (1000, 768, 256), (129, 1024, 64),
+                                   (2048, 4096, 512), (1, 256, 64)], ids=lambda v: str(v))
+def test_gemm_multicast(M, N, K):
+    w = WORKLOADS["cfg3"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K), a_row_scale=False)
+    d = make_inputs(w, M + N + K)
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    c0, c1 = _both(lambda: fn.gemm(A, B))
+    _equal(c0, c1, "gemm")
+    assert_out_close(c1, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])), f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 1024, 512), (640, 4096, 256), (333, 512, 1024), (8192, 2048, 128)],
+                         ids=lambda v: str(v))
+def test_lazy_prenorm_multicast(M, N, K):
+    w = WORKLOADS["cfg1"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    d = make_inputs(w, M * 3 + K)
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    r0, r1 = _both(lambda: fn.lazy_prenorm_gemm(A, B, w.eps, return_rstd=True))
+    _equal(r0, r1, "lazy prenorm")
+    Cr, rr = oracle.lazy_prenorm_gemm(to_f64(d["A"]), to_f64(d["B"]), w.eps)
+    assert_out_close(r1[0], Cr, "lazy prenorm C")
+    assert_rstd_close(r1[1], rr, "lazy prenorm rstd")
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_prenorm_affine_multicast(norm):
+    w = WORKLOADS["preln_affine" if norm == "layernorm" else "prerms_gamma"].scaled(M=520, K=512, N=768)
+    d = make_inputs(w, 61)
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    g = d["gamma"].to(DEV)
+    b = None if d["beta"] is None else d["beta"].to(DEV)
+    Bf, colsum, bias = fn.fold_prenorm_affine(B, g, b)
+    r0, r1 = _both(lambda: fn.prenorm_gemm(A, Bf, norm, colsum if norm == "layernorm" else None, bias, w.eps,
+                                           return_stats=True))
+    _equal(r0, r1, "prenorm affine")
+    Cr, _, rr = oracle.prenorm_affine_gemm(to_f64(d["A"]), to_f64(d["B"]), norm, to_f64(d["gamma"]),
+                                           to_f64(d["beta"]), w.eps)
+    assert_out_close(r1[0], Cr, "prenorm affine C")
+    assert_rstd_close(r1[1]["rstd"], rr, "prenorm affine rstd")
+
+
+@pytest.mark.parametrize("M,N", [(520, 4096), (128 * 33, 2048), (300, 8192), (128 * 160 + 37, 3072)],
+                         ids=lambda v: str(v))
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_grid_exchange_multicast(norm, M, N):
+    w = WORKLOADS["cfg4_n4096_ln"].scaled(M=M, N=N, K=128)
+    d = make_inputs(w, M + N + (norm == "rmsnorm"))
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    g = d["gamma"].to(DEV)
+    b = d["beta"].to(DEV) if norm == "layernorm" else None
+    r0, r1 = _both(lambda: fn.gemm_postnorm(A, B, norm, g, b, w.eps, return_stats=True))
+    _equal(r0, r1, "grid exchange")
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), norm, to_f64(d["gamma"]),
+                               to_f64(d["beta"]) if norm == "layernorm" else None, w.eps)
+    assert_out_close(r1[0], ref["C"], f"grid exchange {norm} C")
+    assert_rstd_close(r1[1]["rstd"], ref["rstd"], f"grid exchange {norm} rstd")
+
+
+def test_grid_exchange_multicast_with_pre():
+    w = WORKLOADS["cfg5"].scaled(M=700, N=4096, K=256)
+    d = make_inputs(w, 71)
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    g, b = d["gamma"].to(DEV), d["beta"].to(DEV)
+    r0, r1 = _both(lambda: fn.gemm_postnorm(A, B, "layernorm", g, b, w.eps, pre_rmsnorm=True, pre_eps=w.pre_eps,
+                                            return_stats=True))
+    _equal(r0, r1, "grid exchange with pre-norm")
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", to_f64(d["gamma"]),
+                               to_f64(d["beta"]), w.eps, pre_rmsnorm=True, pre_eps=w.pre_eps)
+    assert_out_close(r1[0], ref["C"], "grid exchange with pre-norm C")
+    assert_rstd_close(r1[1]["pre_rstd"], ref["pre_rstd"], "pre rstd")
+
+
+def test_multicast_setter_rejects_bad_modes():
+    for bad in (2, -2):
+        with pytest.raises(fn.FnormError):
+            fn.set_b_multicast(bad)
+    fn.set_b_multicast(-1)
