@@ -255,7 +255,10 @@ struct KCfg {
   static constexpr int STAGES = stages_with(STG_BUFS) < kMaxStages ? stages_with(STG_BUFS) : kMaxStages;
   static constexpr uint32_t SMEM_BYTES = 1024 + BRES_BYTES + STAGES * STAGE_BYTES + STG_BYTES + AUX_BYTES;
   static constexpr int NUM_THREADS = 32 * (2 + kEpiWarps + AUX_WARPS);
-  static constexpr uint32_t IDESC = make_idesc_bf16_f32(RB, BN, !BT, AT);
+  // M of each MMA: 256 only for the CTA pair's cta_group::2 MMAs; every
+  // one-CTA MMA (B multicast included) is M = 128
+  static constexpr uint32_t IDESC = make_idesc_bf16_f32(CG * BM, BN, !BT, AT);
+  static_assert(((IDESC >> 24) & 31u) * 16u == (CTA2 ? 256u : 128u), "MMA M: 128 per CTA, 256 for a CTA pair");
 
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N in 64..256, step 64");
   static_assert(STAGES >= 2, "shared memory too small for a 2-stage ring");
@@ -715,6 +718,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                  (fill_par >> s) & 1u, kSiteTeardown);
       for (int kb = 0; kb < bres_issued; ++kb)
         mbar_wait<false, true>(wc, smem_u32(&aux->bres_full[kb]), 0, kSiteTeardown);
+      // B multicast: the peer's MMA commits arrive on this CTA's empty
+      // barriers; once both CTAs' MMAs have released the last fill of every
+      // stage, none of them is still on its way here
+      if (MCB)
+        for (int s = 0; s < STAGES; ++s)
+          if ((filled >> s) & 1u) mbar_wait<false, true>(wc, smem_u32(&aux->empty[s]), (fill_par >> s) & 1u, kSiteTeardown);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
