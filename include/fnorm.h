@@ -164,8 +164,8 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
  *                    gives the bytes an M x N call needs (0: none used).  It
  *                    must be zero-filled before its first use (for instance
  *                    cudaMemsetAsync on the calls' stream); each call leaves
- *                    it ready for the next one (a generation counter), so it
- *                    is cleared once, not per call.  Calls that share a
+ *                    its counters zero again, so it is cleared once, not per
+ *                    call.  Calls that share a
  *                    workspace must not overlap in time (order them on one
  *                    stream); after a call that ended in FNORM_ERR_TIMEOUT
  *                    it must be cleared again.

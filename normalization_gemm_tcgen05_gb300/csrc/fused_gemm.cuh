@@ -124,10 +124,10 @@ struct FusedParams {
   const float* rowcoef;       // MODE_DGRAD: [M] coefficients c of the forward rows
   const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows combined in the epilogue
   // MODE_GX workspace: per-(row block, tile) row statistics, per-row-block
-  // counters, the generation word and the CTA finish counter
+  // arrival counters (zero at launch; the last CTA to finish zeroes them
+  // again) and the CTA finish counter
   float2* gx_part;
   unsigned long long* gx_cnt;
-  uint32_t* gx_gen;
   uint32_t* gx_finish;
   uint32_t* status;
   unsigned long long wait_limit_ns;
@@ -161,6 +161,8 @@ struct Aux {
   uint64_t rload;           // the first residual tile, loaded by TMA (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort_flag;
+  int gx_ready;  // grid exchange: tiles whose row block the polling lane has seen complete
+  int gx_last;   // grid exchange: this CTA finished last
   int nstat_m0[HD];
   int nstat_c0[HD];
   float ss[2][NPART][SSN];    // pre-norm row sums, one slot per norm-warp part
@@ -579,6 +581,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->teardown), 1);
       mbar_init(smem_u32(&aux->rload), kEpiWarps);
       aux->abort_flag = 0;
+      aux->gx_ready = 0;
     }
     fence_mbar_init();
   }
@@ -997,35 +1000,37 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
     }
 
-    // grid exchange: publish the statistics of tile (row block, column group
-    // g) for its 128 rows, then count the quarter-warp in (4 per tile)
-    const uint32_t gx_gen = GX ? *reinterpret_cast<volatile uint32_t*>(p.gx_gen) : 0u;
-    auto gx_publish = [&](float part0, float part1, int m0_, int g_) -> bool {
+    // Grid exchange of tile (row block, column group g): the column-half-0
+    // warps publish the tile's statistics for its 128 rows and each counts
+    // in on the row block's counter (4 arrivals per tile, atomic adds); one
+    // lane of the CTA polls the counter until every tile of the row block
+    // has arrived and passes that on through shared memory (one poller per
+    // CTA keeps the counter's L2 line quiet for the arrivals); then every
+    // warp combines all the tiles' statistics in tile order (the same
+    // arithmetic in every tile of the row, so every tile derives the same
+    // mean and rstd).  xk counts this CTA's exchanges.  False if a wait gave
+    // up.
+    int xk = 0;
+    auto gx_exchange = [&](float& part0, float& part1, int m0_, int g_) -> bool {
       const int rb = m0_ / Cfg::BM;
       if (h == 0) p.gx_part[(static_cast<size_t>(rb) * ngroups + g_) * Cfg::BM + row] = make_float2(part0, part1);
       __syncwarp();
-      bool ok2 = true;
       if (h == 0 && lane == 0) {
-        __threadfence();
-        ok2 = grid_count_in(p.gx_cnt + rb, gx_gen);
-        if (!ok2) record_timeout(wc, kSiteGrid);
+        __threadfence();  // the statistics are visible before the arrival
+        atomicAdd(p.gx_cnt + rb, 1ull);
       }
-      return __all_sync(0xffffffffu, ok2);
-    };
-
-    // resident grid exchange: publish this tile's statistics, wait until every
-    // tile of its row block has published, then combine all of them in tile
-    // order (the same arithmetic in every tile of the row, so every tile
-    // derives the same mean and rstd); false if a wait gave up
-    auto gx_exchange = [&](float& part0, float& part1, int m0_, int g_) -> bool {
-      if (!gx_publish(part0, part1, m0_, g_)) return false;
-      const int rb = m0_ / Cfg::BM;
-      const unsigned long long want =
-          (static_cast<unsigned long long>(gx_gen) << 32) | static_cast<unsigned long long>(4 * ngroups);
       bool ready = true;
-      if (lane == 0) ready = grid_wait_eq(wc, p.gx_cnt + rb, want, kSiteGrid);
+      ++xk;
+      if (lane == 0) {
+        if (warp == 2) {
+          ready = grid_wait_eq(wc, p.gx_cnt + rb, static_cast<unsigned long long>(4 * ngroups), kSiteGrid);
+          if (ready) *reinterpret_cast<volatile int*>(&aux->gx_ready) = xk;
+        } else {
+          ready = wait_flag_ge(wc, &aux->gx_ready, xk, kSiteGrid);
+        }
+      }
       if (!__all_sync(0xffffffffu, ready)) return false;
-      __syncwarp();  // lane 0's acquire (the fence after the counter) orders every lane's loads below
+      __syncwarp();  // lane 0's acquire (the fence after its wait) orders every lane's loads below
       const float2* src = p.gx_part + static_cast<size_t>(rb) * ngroups * Cfg::BM + row;
       float mean = 0.0f, m2 = 0.0f, n = 0.0f, ssq = 0.0f;
       for (int q0 = 0; q0 < ngroups; q0 += 8) {
@@ -1512,14 +1517,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
   }
   if (CLUSTER || PAIR) cluster_sync();  // no CTA leaves while a peer may still address it
-  if (GX && threadIdx.x == 0) {
-    // the last CTA of the grid to finish starts the next generation: every
-    // counter this grid touched then reads as zero to the next launch
-    __threadfence();
-    if (atomicAdd(p.gx_finish, 1u) == gridDim.x - 1u) {
-      *reinterpret_cast<volatile uint32_t*>(p.gx_finish) = 0u;
+  if (GX) {
+    // the last CTA of the grid to finish zeroes every counter this grid used
+    // (and the finish count): the next launch on the workspace starts from
+    // zero; every other CTA has finished its waits by then
+    if (threadIdx.x == 0) {
       __threadfence();
-      atomicAdd(p.gx_gen, 1u);
+      aux->gx_last = atomicAdd(p.gx_finish, 1u) == gridDim.x - 1u;
+    }
+    __syncthreads();
+    if (aux->gx_last) {
+      const int nrb = (M + Cfg::BM - 1) / Cfg::BM;
+      for (int i = static_cast<int>(threadIdx.x); i < nrb; i += static_cast<int>(blockDim.x)) p.gx_cnt[i] = 0ull;
+      if (threadIdx.x == 0) *reinterpret_cast<volatile uint32_t*>(p.gx_finish) = 0u;
     }
   }
 }

@@ -84,7 +84,6 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     }
     p.gx_part = L.gx->part;
     p.gx_cnt = L.gx->cnt;
-    p.gx_gen = L.gx->gen;
     p.gx_finish = L.gx->finish;
   }
   p.X = static_cast<const __nv_bfloat16*>(L.X);

@@ -38,12 +38,11 @@ fnorm_status_t encode_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t i
                                    CUtensorMapSwizzle swizzle);
 
 // Workspace of the grid-exchange post-norm: per-(row block, tile) row
-// statistics, per-row-block counters, the generation word and the finish
-// counter.  Calls that share one must be ordered (one stream).
+// statistics, per-row-block arrival counters and the finish counter (both
+// zero between calls).  Calls that share one must be ordered (one stream).
 struct GxScratch {
   float2* part;              // [units][128]
   unsigned long long* cnt;   // [row blocks]
-  uint32_t* gen;
   uint32_t* finish;
   int units_cap;
   int rowblocks_cap;

@@ -50,14 +50,13 @@ fnorm_status_t noalloc_scratch(cudaStream_t stream, const GxScratch** out) {
       cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess) throw SetupError{cuda_fail(e, "cudaGetSymbolAddress(no-alloc workspace)")};
       char* base = static_cast<char*>(p);
-      // counters, generation word and finish count start at zero (ordered
-      // before this call's kernel on its stream)
+      // counters and finish count start at zero (ordered before this call's
+      // kernel on its stream); every call leaves them zero
       e = cudaMemsetAsync(base + kPartBytes, 0, kCntBytes + 256, stream);
       if (e != cudaSuccess) throw SetupError{cuda_fail(e, "clearing the no-alloc workspace")};
       s.gx.part = reinterpret_cast<float2*>(base);
       s.gx.cnt = reinterpret_cast<unsigned long long*>(base + kPartBytes);
-      s.gx.gen = reinterpret_cast<uint32_t*>(base + kPartBytes + kCntBytes);
-      s.gx.finish = s.gx.gen + 32;
+      s.gx.finish = reinterpret_cast<uint32_t*>(base + kPartBytes + kCntBytes);
       s.gx.units_cap = kNoAllocUnits;
       s.gx.rowblocks_cap = kNoAllocRowBlocks;
     });

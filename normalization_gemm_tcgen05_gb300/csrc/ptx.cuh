@@ -121,21 +121,6 @@ __device__ __forceinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, uint32
 }
 
 // ---- grid-wide counters (cross-CTA statistics exchange) ----
-// A counter word holds (generation << 32) | count.  Count one arrival in for
-// generation `gen`: a value left by another generation counts as zero.
-// Bounded; false if the CAS never went through (a fault of the protocol).
-__device__ __forceinline__ bool grid_count_in(unsigned long long* c, uint32_t gen) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
-  for (int i = 0; i < (1 << 16); ++i) {
-    const unsigned long long base =
-        (static_cast<uint32_t>(old >> 32) == gen) ? old : (static_cast<unsigned long long>(gen) << 32);
-    const unsigned long long prev = atomicCAS(c, old, base + 1ull);
-    if (prev == old) return true;
-    old = prev;
-  }
-  return false;
-}
-
 // Wait (one lane; bounded by the wait limit and the CTA's abort flag) until
 // the counter reads `want`, then fence so that later loads see what the
 // arrivals published before counting in.
@@ -152,6 +137,25 @@ __device__ __forceinline__ bool grid_wait_eq(const WaitCtx& w, const unsigned lo
       }
     }
     __nanosleep(64);
+  }
+  __threadfence();
+  return true;
+}
+
+// Wait (one lane; bounded) until the shared-memory word `flag` reads at
+// least v, then fence so that later loads see what the writer had observed
+// before it set the flag.
+__device__ __forceinline__ bool wait_flag_ge(const WaitCtx& w, const int* flag, int v, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (*reinterpret_cast<const volatile int*>(flag) >= v) break;
+    if ((i & 63u) == 63u) {
+      if (*w.abort_flag) return false;
+      if (global_timer_ns() - t0 > w.limit_ns) {
+        record_timeout(w, site);
+        return false;
+      }
+    }
   }
   __threadfence();
   return true;

@@ -90,11 +90,10 @@ fnorm_status_t current_device(DeviceInfo* out) {
 }
 
 // Layout of a caller's grid-exchange workspace, the same for every call that
-// uses it whatever its shape (so counters and the generation word are always
-// found where earlier calls left them): 256 bytes holding the generation word
-// (offset 0) and the finish count (offset 128), then kGxMaxRowBlocks
-// per-row-block counters, then the per-tile row statistics
-// [row blocks][tiles per row][128] float2 of the call.
+// uses it whatever its shape (so the counters are always where the last
+// call left them, zeroed): 256 bytes holding the finish count (offset 0),
+// then kGxMaxRowBlocks per-row-block arrival counters, then the per-tile row
+// statistics [row blocks][tiles per row][128] float2 of the call.
 size_t gx_workspace_bytes(int64_t M, int64_t N) {
   const int64_t rb = (M + 127) / 128, tiles = (N + 255) / 256;
   return kGxHeaderBytes + static_cast<size_t>(kGxMaxRowBlocks) * sizeof(uint64_t) +
@@ -113,8 +112,7 @@ fnorm_status_t gx_scratch_from(void* workspace, size_t bytes, int64_t M, int64_t
     return FNORM_ERR_INVALID_ARG;
   }
   char* base = static_cast<char*>(workspace);
-  out->gen = reinterpret_cast<uint32_t*>(base);
-  out->finish = out->gen + 32;
+  out->finish = reinterpret_cast<uint32_t*>(base);
   out->cnt = reinterpret_cast<unsigned long long*>(base + kGxHeaderBytes);
   out->part = reinterpret_cast<float2*>(base + kGxHeaderBytes + static_cast<size_t>(kGxMaxRowBlocks) * 8);
   const size_t units = (bytes - kGxHeaderBytes - static_cast<size_t>(kGxMaxRowBlocks) * 8) / (128 * sizeof(float2));
