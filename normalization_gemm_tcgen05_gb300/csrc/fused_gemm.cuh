@@ -1015,41 +1015,55 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       const int rb = m0_ / Cfg::BM;
       if (h == 0) p.gx_part[(static_cast<size_t>(rb) * ngroups + g_) * Cfg::BM + row] = make_float2(part0, part1);
       __syncwarp();
-      if (h == 0 && lane == 0) {
-        __threadfence();  // the statistics are visible before the arrival
-        atomicAdd(p.gx_cnt + rb, 1ull);
-      }
+      if (h == 0 && lane == 0) grid_arrive(p.gx_cnt + rb);
       bool ready = true;
       ++xk;
       if (lane == 0) {
         if (warp == 2) {
           ready = grid_wait_eq(wc, p.gx_cnt + rb, static_cast<unsigned long long>(4 * ngroups), kSiteGrid);
-          if (ready) *reinterpret_cast<volatile int*>(&aux->gx_ready) = xk;
+          if (ready) flag_release(&aux->gx_ready, xk);
         } else {
           ready = wait_flag_ge(wc, &aux->gx_ready, xk, kSiteGrid);
         }
       }
       if (!__all_sync(0xffffffffu, ready)) return false;
-      __syncwarp();  // lane 0's acquire (the fence after its wait) orders every lane's loads below
+      __syncwarp();  // lane 0's acquire orders every lane's loads below
+      // Combine the tiles' statistics in tile order, XB per batch of loads in
+      // flight (fewer where the norm warps leave fewer registers).
+      // LayerNorm in two passes over them, without a division per step:
+      // mean = sum_q n_q mean_q / N, then M2 = sum_q (M2_q + n_q (mean_q - mean)^2).
+      constexpr int XB = Cfg::AUXW ? 8 : 32;
       const float2* src = p.gx_part + static_cast<size_t>(rb) * ngroups * Cfg::BM + row;
-      float mean = 0.0f, m2 = 0.0f, n = 0.0f, ssq = 0.0f;
-      for (int q0 = 0; q0 < ngroups; q0 += 8) {
-        float2 v[8];
+      auto nq = [&](int qq) { return static_cast<float>(min(max(N - qq * cta_cols, 0), cta_cols)); };
+      float acc = 0.0f;  // LayerNorm: sum n_q mean_q; RMSNorm: sum of squares
+      float2 v[XB];
+      for (int q0 = 0; q0 < ngroups; q0 += XB) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < XB; ++u)
           v[u] = q0 + u < ngroups ? __ldcg(src + static_cast<size_t>(q0 + u) * Cfg::BM) : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (q0 + u >= ngroups) break;
-          if (LN) {
-            const float nq = static_cast<float>(min(max(N - (q0 + u) * cta_cols, 0), cta_cols));
-            combine_mean_m2(mean, m2, n, v[u].x, v[u].y, nq);
-          } else {
-            ssq += v[u].x;
-          }
+        for (int u = 0; u < XB; ++u) acc = LN ? fmaf(nq(q0 + u), v[u].x, acc) : acc + v[u].x;
+      }
+      if (!LN) {
+        part0 = acc;
+        part1 = 0.0f;
+        return true;
+      }
+      const float mean = acc * inv_N();
+      float m2 = 0.0f;
+      for (int q0 = 0; q0 < ngroups; q0 += XB) {
+        if (q0 > 0 || ngroups > XB) {  // (one batch: its values are still in registers)
+#pragma unroll
+          for (int u = 0; u < XB; ++u)
+            v[u] = q0 + u < ngroups ? __ldcg(src + static_cast<size_t>(q0 + u) * Cfg::BM) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < XB; ++u) {
+          const float d = v[u].x - mean;
+          m2 += v[u].y + nq(q0 + u) * (d * d);
         }
       }
-      part0 = LN ? mean : ssq;
+      part0 = mean;
       part1 = m2;
       return true;
     };
@@ -1248,6 +1262,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         constexpr int LDB = Cfg::LDB, NBATCH = NCH / LDB;
         uint32_t r[LDB][32];
         if (Cfg::KEEP) tmem_load_batch<LDB>(tb, r);  // the whole half, once
+        // grid exchange: this warp's gamma/beta of the tile into its own
+        // shared-memory slice (read back as float4 broadcasts after the
+        // exchange; the previous tile's reads of the slice are complete)
+        if (GX) {
+          float* dst = (lane < 16 ? &aux->wgam[warp - 2][0] : &aux->wbet[warp - 2][0]) + (lane & 15) * 8;
+          const uint32_t gw[4] = {gbv.x, gbv.y, gbv.z, gbv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dst[2 * e] = bf16_lo(gw[e]);
+            dst[2 * e + 1] = bf16_hi(gw[e]);
+          }
+          __syncwarp();
+        }
         float mean = 0.0f, rstd = 1.0f;
         if (POST) {
           float kk = 0.0f;
@@ -1301,19 +1328,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           }
         }
 
-        // resident grid exchange: this warp's gamma/beta of the tile into its
-        // own shared-memory slice (read back as float4 broadcasts)
         const int ew = warp - 2;
-        if (GX) {
-          float* dst = (lane < 16 ? &aux->wgam[ew][0] : &aux->wbet[ew][0]) + (lane & 15) * 8;
-          const uint32_t gw[4] = {gbv.x, gbv.y, gbv.z, gbv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dst[2 * e] = bf16_lo(gw[e]);
-            dst[2 * e + 1] = bf16_hi(gw[e]);
-          }
-          __syncwarp();
-        }
         // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
         for (int cb = 0; cb < NBATCH; ++cb) {
           if (c0h + cb * LDB * 32 >= N) break;

@@ -121,14 +121,23 @@ __device__ __forceinline__ bool mbar_wait(const WaitCtx& w, uint32_t bar, uint32
 }
 
 // ---- grid-wide counters (cross-CTA statistics exchange) ----
+// Count one arrival in on a grid-wide counter, releasing at GPU scope every
+// write that happens before it (in particular the warp's writes ordered by
+// a __syncwarp before this lane's call).
+__device__ __forceinline__ void grid_arrive(unsigned long long* c) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(c) : "memory");
+}
+
 // Wait (one lane; bounded by the wait limit and the CTA's abort flag) until
-// the counter reads `want`, then fence so that later loads see what the
-// arrivals published before counting in.
+// the counter reads `want`, with acquire loads at GPU scope: later accesses
+// of this thread see what the arrivals released.
 __device__ __forceinline__ bool grid_wait_eq(const WaitCtx& w, const unsigned long long* c, unsigned long long want,
                                              uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 0;; ++i) {
-    if (*reinterpret_cast<const volatile unsigned long long*>(c) == want) break;
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(c) : "memory");
+    if (v == want) return true;
     if ((i & 15u) == 15u) {
       if (*w.abort_flag) return false;
       if (global_timer_ns() - t0 > w.limit_ns) {
@@ -136,19 +145,25 @@ __device__ __forceinline__ bool grid_wait_eq(const WaitCtx& w, const unsigned lo
         return false;
       }
     }
-    __nanosleep(64);
+    __nanosleep(32);
   }
-  __threadfence();
-  return true;
+}
+
+// Hand a value to the other warps of the CTA through a shared-memory word,
+// releasing (at CTA scope) everything this thread has seen, including what
+// it acquired at GPU scope.
+__device__ __forceinline__ void flag_release(int* flag, int v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(flag)), "r"(v) : "memory");
 }
 
 // Wait (one lane; bounded) until the shared-memory word `flag` reads at
-// least v, then fence so that later loads see what the writer had observed
-// before it set the flag.
+// least v, with acquire loads at CTA scope (pairs with flag_release).
 __device__ __forceinline__ bool wait_flag_ge(const WaitCtx& w, const int* flag, int v, uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 0;; ++i) {
-    if (*reinterpret_cast<const volatile int*>(flag) >= v) break;
+    int x;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(x) : "r"(smem_u32(flag)) : "memory");
+    if (x >= v) return true;
     if ((i & 63u) == 63u) {
       if (*w.abort_flag) return false;
       if (global_timer_ns() - t0 > w.limit_ns) {
@@ -157,8 +172,6 @@ __device__ __forceinline__ bool wait_flag_ge(const WaitCtx& w, const int* flag, 
       }
     }
   }
-  __threadfence();
-  return true;
 }
 
 // Warp-collective wait: every lane waits (and so acquires), then the lanes
