@@ -464,7 +464,8 @@ fnorm_status_t fnorm_set_pair_mma(int mode);
  * into both CTAs' shared memory with one TMA multicast (a third less read
  * from L2 per SM).  mode: 1 = whenever the tile is 256 columns wide and B is
  * not resident; 0 = never; -1 = automatic, the default (the same, for more
- * than one row block).  It changes the schedule, not the arithmetic: every
+ * than one row block, except the grid exchange of fnorm_gemm_postnorm_ws,
+ * which keeps one-CTA tiles unless the mode is 1).  It changes the schedule, not the arithmetic: every
  * output is the same sum in the same order as with one-CTA tiles.
  * Process-wide.  Any other mode returns FNORM_ERR_INVALID_ARG.
  */

@@ -320,9 +320,13 @@ fnorm_status_t gemm_postnorm_impl(const fnorm_bf16* A, const fnorm_bf16* B, fnor
   L.rstd_out = rstd_out;
   L.pre_rstd_out = pre_rstd_out;
   if (plan.gx) {
-    if (want_mcb(M, L.bn, L.bres)) {
-      // a device that will not launch a cooperative grid of clusters takes
-      // the one-CTA grid exchange
+    // The grid exchange with B multicast is a cooperative launch of clusters;
+    // it runs only when B multicast is forced (fnorm_set_b_multicast(1)): an
+    // ncu capture of it faulted where its plain runs never did, so automatic
+    // selection keeps the one-CTA cooperative kernel (about 3 % slower at
+    // N = 8192).  A device that will not launch a cooperative grid of
+    // clusters takes the one-CTA kernel too.
+    if (g_mcb_mode.load(std::memory_order_relaxed) == 1 && want_mcb(M, L.bn, L.bres)) {
       const fnorm_status_t st = launch_fused_mcb_grid(L);
       if (st != FNORM_ERR_UNSUPPORTED) return st;
       clear_error();
