@@ -600,58 +600,96 @@ def run_e2e(cases, K, W, world, device) -> dict:
     d2h = sum(h[5].numel() * h[5].element_size() for h in host if h[5] is not None)
     d2h += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][3:])
 
+    # Three streams, so that the host link carries inputs in and results out
+    # at the same time and the kernels run meanwhile: per sub-workload, the
+    # H2D copies of its inputs (after its previous call has read them), the
+    # fused call (after its inputs are in and its previous output has been
+    # read back), then the D2H copy of its output.
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in cases]
+    ev_cmp = [torch.cuda.Event() for _ in cases]
+    ev_out = [torch.cuda.Event() for _ in cases]
+    for k in range(len(cases)):
+        for ev, st in ((ev_in[k], s_in), (ev_cmp[k], s_cmp), (ev_out[k], s_out)):
+            ev.record(st)
+
     def step():
-        for c, (hA, hB, hg, hb, hR, hC, bwd) in zip(cases, host):
+        for k, (c, (hA, hB, hg, hb, hR, hC, bwd)) in enumerate(zip(cases, host)):
             dA, dB = c.A[0], c.B[0]
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            if hg is not None:
-                c.g.copy_(hg, non_blocking=True)
-            if hb is not None:
-                c.b.copy_(hb, non_blocking=True)
-            if hR is not None:
-                c.Rres[0].copy_(hR, non_blocking=True)
             w = c.w
-            if bwd is not None:
-                hCf, hr, hdC, hdA, hdB = bwd
-                c.Cf[0].copy_(hCf, non_blocking=True)
-                c.rstd[0].copy_(hr, non_blocking=True)
-                c.dC[0].copy_(hdC, non_blocking=True)
-                if w.kind == "prenorm_backward":
-                    fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
-                                                  work=c.work[0])
-                    hdA.copy_(c.dA[0], non_blocking=True)
-                    hdB.copy_(c.dB[0], non_blocking=True)
+            s_in.wait_event(ev_cmp[k])
+            with torch.cuda.stream(s_in):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                if hg is not None:
+                    c.g.copy_(hg, non_blocking=True)
+                if hb is not None:
+                    c.b.copy_(hb, non_blocking=True)
+                if hR is not None:
+                    c.Rres[0].copy_(hR, non_blocking=True)
+                if bwd is not None:
+                    c.Cf[0].copy_(bwd[0], non_blocking=True)
+                    c.rstd[0].copy_(bwd[1], non_blocking=True)
+                    c.dC[0].copy_(bwd[2], non_blocking=True)
+                ev_in[k].record(s_in)
+            s_cmp.wait_event(ev_in[k])
+            s_cmp.wait_event(ev_out[k])
+            with torch.cuda.stream(s_cmp):
+                if bwd is not None:
+                    if w.kind == "prenorm_backward":
+                        fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
+                                                      work=c.work[0])
+                        outs = (c.dA[0], c.dB[0])
+                    else:
+                        g = fn.gemm_postnorm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], w.norm, c.g, c.b,
+                                                      need=("dA", "dB"))
+                        outs = (g["dA"], g["dB"])
+                elif w.kind == "prenorm":
+                    fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
+                    outs = (c.C[0],)
+                elif w.kind == "prenorm_affine":
+                    # the weight arrives from the host every step: fold, then the fused GEMM
+                    Bf, cs, bias = c.fold[0]
+                    fn.fold_prenorm_affine(dB, c.g, c.b, out=Bf, colsum_out=cs, bias_out=bias)
+                    fn.prenorm_gemm(dA, Bf, w.norm, cs if w.norm == "layernorm" else None, bias, w.eps,
+                                    out=c.C[0])
+                    outs = (c.C[0],)
+                elif w.residual:
+                    fn.gemm_add_postnorm(dA, dB, c.Rres[0], w.norm, c.g, c.b, w.eps, out=c.C[0])
+                    outs = (c.C[0],)
                 else:
-                    g = fn.gemm_postnorm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], w.norm, c.g, c.b,
-                                                  need=("dA", "dB"))
-                    hdA.copy_(g["dA"], non_blocking=True)
-                    hdB.copy_(g["dB"], non_blocking=True)
-                continue
-            if w.kind == "prenorm":
-                fn.lazy_prenorm_gemm(dA, dB, w.eps, out=c.C[0])
-            elif w.kind == "prenorm_affine":
-                # the weight arrives from the host every step: fold, then the fused GEMM
-                Bf, cs, bias = c.fold[0]
-                fn.fold_prenorm_affine(dB, c.g, c.b, out=Bf, colsum_out=cs, bias_out=bias)
-                fn.prenorm_gemm(dA, Bf, w.norm, cs if w.norm == "layernorm" else None, bias, w.eps, out=c.C[0])
-            elif w.residual:
-                fn.gemm_add_postnorm(dA, dB, c.Rres[0], w.norm, c.g, c.b, w.eps, out=c.C[0])
-            else:
-                fn.gemm_postnorm(dA, dB, w.norm, c.g, c.b, w.eps, pre_rmsnorm=w.pre_rmsnorm, pre_eps=w.pre_eps,
-                                 out=c.C[0])
-            hC.copy_(c.C[0], non_blocking=True)
+                    fn.gemm_postnorm(dA, dB, w.norm, c.g, c.b, w.eps, pre_rmsnorm=w.pre_rmsnorm,
+                                     pre_eps=w.pre_eps, out=c.C[0])
+                    outs = (c.C[0],)
+                ev_cmp[k].record(s_cmp)
+            s_out.wait_event(ev_cmp[k])
+            with torch.cuda.stream(s_out):
+                dsts = (bwd[3], bwd[4]) if bwd is not None else (hC,)
+                for dst, src in zip(dsts, outs):
+                    src.record_stream(s_out)  # (the backward's outputs are fresh allocations)
+                    dst.copy_(src, non_blocking=True)
+                ev_out[k].record(s_out)
+
+    def join():
+        # the default stream waits for the three streams' work so far
+        cur = torch.cuda.current_stream(device)
+        for st in (s_in, s_cmp, s_out):
+            cur.wait_stream(st)
 
     for _ in range(W):
         step()
+    join()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
+    for st in (s_in, s_cmp, s_out):  # nothing of the timed steps starts before e0
+        st.wait_stream(torch.cuda.current_stream(device))
     for _ in range(K):
         step()
+    join()
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -661,9 +699,12 @@ def run_e2e(cases, K, W, world, device) -> dict:
     return {"value": round(world * K * flops / t / 1e12, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(t / K * 1e3, 4),
             # the host link, measured on this machine: one 64 MiB pinned copy each
-            # way, and the step's copies at those rates
+            # way, and the step's copies at those rates (each direction on its
+            # own stream, the two directions overlapping)
             "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
-            "copies_ms_at_link_rate": round((h2d / h2d_gbs + d2h / d2h_gbs) / 1e6, 4)}
+            "h2d_ms_at_link_rate": round(h2d / h2d_gbs / 1e6, 4),
+            "d2h_ms_at_link_rate": round(d2h / d2h_gbs / 1e6, 4),
+            "streams": "inputs in, compute and results out on three streams"}
 
 
 # --------------------------------------------------------------------------
