@@ -264,6 +264,16 @@ def test_grid_exchange_and_spill_agree():
     assert np.max(np.abs(np64(s1["rstd"]) - np64(s2["rstd"])) / np64(s2["rstd"])) < 1e-5
 
 
+@pytest.mark.parametrize("M", [1, 127, 129])
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_grid_exchange_few_rows(norm, M):
+    # one (partial) row block or two: as many CTAs as tiles of the row, the
+    # rows past M zero-filled and never stored
+    w, d = _case("cfg4_n4096_ln", 50 + M, M=M, N=2048, K=256)
+    _post(w, d, norm)
+    _post(w, d, norm, affine=False)
+
+
 def test_grid_exchange_row_wider_than_the_grid():
     # a row of more 256-column tiles than SMs cannot be exchanged grid-wide
     # (a CTA would hold two tiles of the row block it waits on): the call
