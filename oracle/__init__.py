@@ -33,4 +33,5 @@ from .fnorm_oracle import (  # noqa: F401
     gemm_add_postnorm,
     lazy_prenorm_gemm_backward,
     gemm_postnorm_backward,
+    gemm_postnorm_backward_regrouped,
 )

@@ -23,7 +23,8 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm", "gemm_postnorm", "prenorm_affine_gemm",
-           "gemm_add_postnorm", "lazy_prenorm_gemm_backward", "gemm_postnorm_backward"]
+           "gemm_add_postnorm", "lazy_prenorm_gemm_backward", "gemm_postnorm_backward",
+           "gemm_postnorm_backward_regrouped"]
 
 
 def _f64(x) -> np.ndarray:
@@ -231,3 +232,29 @@ def gemm_postnorm_backward(A, B, dC, norm: str, gamma=None, beta=None, eps: floa
         dH = rstd[:, None] * (dh - h_hat * proj[:, None])
     return {"dA": gemm(dH, B.T), "dB": gemm(A.T, dH), "dH": dH, "dgamma": dgamma, "dbeta": dbeta,
             "mean": mean, "rstd": rstd}
+
+
+def gemm_postnorm_backward_regrouped(G, W, A, B, norm: str, gamma=None, beta=None, eps: float = 1e-5,
+                                     trans_w: bool = False) -> dict:
+    """The post-norm's backward when the gradient reaching its output comes
+    from the GEMM of the layer that consumes it.
+
+    [TFN] ("fusion regrouping": in the backward a norm is fused with a
+    different linear layer than in the forward, so that the backward also
+    gets an epilogue fusion).  The forward is two layers,
+
+        Y = norm(A @ B) * gamma + beta,    Z = Y @ op(W),
+
+    with op(W) = W ([N, J]) or, with trans_w, W^T (W stored as [J, N]); G is
+    dL/dZ [M, J].  The gradient at the post-norm's output is the consumer's
+    data-gradient GEMM, dY = G @ op(W)^T, and from there the chain rule of
+    gemm_postnorm_backward.  The oracle materialises dY in float64.
+
+    Returns gemm_postnorm_backward's dict plus "dC" (= dY).
+    """
+    G = _f64(G)
+    W = _f64(W)
+    dY = gemm(G, W if trans_w else W.T)
+    d = gemm_postnorm_backward(A, B, dY, norm, gamma, beta, eps)
+    d["dC"] = dY
+    return d

@@ -449,6 +449,37 @@ def check_postnorm_backward_shift_invariance(o):
     _close(np.sum(d["dH"], axis=1), np.zeros(4), 0, 1e-12, "post-LN dH rows sum to zero")
 
 
+def check_postnorm_backward_regrouped_autograd(o):
+    # two layers, Y = norm(A @ B) * gamma + beta and Z = Y @ op(W), differentiated
+    # by autograd from dL/dZ = G: the regrouped backward starts from G and W
+    rng = _rng(21)
+    M, K, N = 6, 10, 12
+    A = rng.standard_normal((M, K))
+    B = rng.standard_normal((K, N)) / 3
+    gam = 1 + 0.1 * rng.standard_normal(N)
+    bet = 0.1 * rng.standard_normal(N)
+    for J, trans_w in ((12, False), (12, True), (7, False), (5, True)):
+        W = rng.standard_normal((J, N) if trans_w else (N, J)) / 3
+        G = rng.standard_normal((M, J))
+        for norm in ("layernorm", "rmsnorm"):
+            b = bet if norm == "layernorm" else None
+            d = o.gemm_postnorm_backward_regrouped(G, W, A, B, norm, gam, b, 1e-4, trans_w=trans_w)
+            At, Bt = _t(A).requires_grad_(True), _t(B).requires_grad_(True)
+            gt, bt = _t(gam).requires_grad_(True), _t(bet).requires_grad_(True)
+            H = At @ Bt
+            Y = F.layer_norm(H, (N,), gt, bt, 1e-4) if norm == "layernorm" else F.rms_norm(H, (N,), gt, 1e-4)
+            Y.retain_grad()
+            Z = Y @ (_t(W).T if trans_w else _t(W))
+            Z.backward(_t(G))
+            what = f"regrouped post-{norm}, J={J}, trans_w={trans_w}"
+            _close(d["dC"], Y.grad.numpy(), 1e-12, 1e-12, f"{what}: dC vs autograd")
+            _close(d["dA"], At.grad.numpy(), 1e-10, 1e-12, f"{what}: dA vs autograd")
+            _close(d["dB"], Bt.grad.numpy(), 1e-10, 1e-12, f"{what}: dB vs autograd")
+            _close(d["dgamma"], gt.grad.numpy(), 1e-10, 1e-12, f"{what}: dgamma vs autograd")
+            if norm == "layernorm":
+                _close(d["dbeta"], bt.grad.numpy(), 1e-12, 1e-12, f"{what}: dbeta vs autograd")
+
+
 ALL_CHECKS = [
     check_gemm_bruteforce, check_gemm_torch,
     check_rmsnorm_golden, check_rmsnorm_torch, check_rmsnorm_unit_rms,
@@ -463,4 +494,5 @@ ALL_CHECKS = [
     check_add_postnorm_torch, check_add_postnorm_cancel,
     check_prenorm_backward_autograd, check_prenorm_backward_finite_diff, check_prenorm_backward_scale_invariance,
     check_postnorm_backward_autograd, check_postnorm_backward_shift_invariance,
+    check_postnorm_backward_regrouped_autograd,
 ]

@@ -11,7 +11,8 @@ from oracle_pins import ALL_CHECKS
 
 _real = {name: getattr(O, name) for name in ("gemm", "rmsnorm", "layernorm", "lazy_prenorm_gemm",
                                              "gemm_postnorm", "prenorm_affine_gemm", "gemm_add_postnorm",
-                                             "lazy_prenorm_gemm_backward", "gemm_postnorm_backward")}
+                                             "lazy_prenorm_gemm_backward", "gemm_postnorm_backward",
+                                             "gemm_postnorm_backward_regrouped")}
 
 
 def _gemm_transposed(A, B):          # transposed operand
@@ -130,6 +131,18 @@ def _postnorm_bwd_gamma_ignored(A, B, dC, norm, gamma=None, beta=None, eps=1e-5)
     return _real["gemm_postnorm_backward"](A, B, dC, norm, None, beta, eps)
 
 
+def _regrouped_w_flipped(G, W, A, B, norm, gamma=None, beta=None, eps=1e-5, trans_w=False):
+    # the consumer's weight taken the wrong way round
+    return _real["gemm_postnorm_backward_regrouped"](G, W, A, B, norm, gamma, beta, eps, not trans_w)
+
+
+def _regrouped_consumer_skipped(G, W, A, B, norm, gamma=None, beta=None, eps=1e-5, trans_w=False):
+    # G used as the post-norm's output gradient, without the consumer's GEMM
+    d = _real["gemm_postnorm_backward"](A, B, G, norm, gamma, beta, eps)
+    d["dC"] = np.asarray(G, np.float64)
+    return d
+
+
 MUTANTS = {
     "gemm_transposed_B": ("gemm", _gemm_transposed),
     "gemm_dropped_k_term": ("gemm", _gemm_dropped_k),
@@ -149,6 +162,8 @@ MUTANTS = {
     "prenorm_backward_dB_not_rebuilt": ("lazy_prenorm_gemm_backward", _prenorm_bwd_dB_unscaled),
     "postnorm_backward_mean_term_dropped": ("gemm_postnorm_backward", _postnorm_bwd_no_mean_term),
     "postnorm_backward_gamma_ignored": ("gemm_postnorm_backward", _postnorm_bwd_gamma_ignored),
+    "regrouped_backward_w_flipped": ("gemm_postnorm_backward_regrouped", _regrouped_w_flipped),
+    "regrouped_backward_consumer_skipped": ("gemm_postnorm_backward_regrouped", _regrouped_consumer_skipped),
 }
 
 
