@@ -68,7 +68,7 @@ GROUPS = {
     "cfg5": ["cfg5"],
     "res": ["res_ln_n128", "res_rms_n1024"],
     "preaff": ["preln_affine", "prerms_gamma"],
-    "bwd": ["prenorm_bwd", "postnorm_bwd"],
+    "bwd": ["prenorm_bwd", "postnorm_bwd", "postnorm_bwd_rg"],
 }
 GROUP_TEXT = {
     "main": "the five configurations, one fused launch of each sub-workload per step: Lazy Pre-RMSNorm GEMM "
@@ -261,12 +261,19 @@ class Case:
             self.G = [torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
             self.work = [(torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device),
                           torch.empty(w.M, dtype=torch.float32, device=device)) for _ in range(self.R)]
-        if w.kind == "postnorm_backward":
+        if w.kind in ("postnorm_backward", "postnorm_regrouped_backward"):
             fwd = [fn.gemm_postnorm(Aj, Bj, w.norm, self.g, self.b, w.eps, return_stats=True)
                    for Aj, Bj in zip(self.A, self.B)]
             self.Cf = [c for c, _ in fwd]
             self.rstd = [st["rstd"] for _, st in fwd]
-            self.dC = [d["dC"].to(device) for _ in range(self.R)]
+            if w.kind == "postnorm_backward":
+                self.dC = [d["dC"].to(device) for _ in range(self.R)]
+            else:
+                # the consumer's gradient and weight; dC is materialised only
+                # by the unfused comparison
+                self.Gr = [d["G"].to(device) for _ in range(self.R)]
+                self.Wr = [d["W"].to(device) for _ in range(self.R)]
+                self.dC = [fn.gemm_ex(Gj, Wj, trans_b=True) for Gj, Wj in zip(self.Gr, self.Wr)]
         self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         self.Y = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.R)]
         nst = 3
@@ -293,6 +300,9 @@ class Case:
         elif w.kind == "postnorm_backward":
             fn.gemm_postnorm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j], w.norm, self.g,
                                       self.b)
+        elif w.kind == "postnorm_regrouped_backward":
+            fn.gemm_postnorm_backward_regrouped(self.Gr[j], self.Wr[j], self.A[j], self.B[j], self.Cf[j],
+                                                self.rstd[j], w.norm, self.g, self.b)
         elif w.residual:
             fn.gemm_add_postnorm(self.A[j], self.B[j], self.Rres[j], w.norm, self.g, self.b, w.eps, out=self.C[j])
         elif w.kind == "postnorm":
@@ -304,6 +314,11 @@ class Case:
 
     def gemm_only(self, i: int):
         j = i % self.R
+        if self.w.kind == "postnorm_regrouped_backward":  # the consumer's G @ W^T, then the two GEMMs
+            self.fn.gemm_ex(self.Gr[j], self.Wr[j], trans_b=True, out=self.dC[j])
+            self.fn.gemm_ex(self.dC[j], self.B[j], trans_b=True)
+            self.fn.gemm_ex(self.A[j], self.dC[j], trans_a=True)
+            return
         if self.w.kind == "postnorm_backward":  # the two GEMMs: dH @ B^T, A^T @ dH (dH: dC's shape)
             self.fn.gemm_ex(self.dC[j], self.B[j], trans_b=True)
             self.fn.gemm_ex(self.A[j], self.dC[j], trans_a=True)
@@ -318,7 +333,9 @@ class Case:
         """The same GEMM(s) by cuBLAS (torch.matmul): context for the GEMM half of
         the unfused comparison, not a product path."""
         w, j = self.w, i % self.R
-        if w.kind in ("postnorm_backward", "prenorm_backward"):
+        if w.kind in ("postnorm_backward", "prenorm_backward", "postnorm_regrouped_backward"):
+            if w.kind == "postnorm_regrouped_backward":
+                torch.matmul(self.Gr[j], self.Wr[j].t(), out=self.dC[j])
             if self._cub is None:
                 self._cub = (torch.empty((w.M, w.K), dtype=torch.bfloat16, device=self.dev),
                              torch.empty((w.K, w.N), dtype=torch.bfloat16, device=self.dev))
@@ -338,8 +355,8 @@ class Case:
         elif w.kind == "prenorm_affine":
             k = i % self.R
             self._pre_norm(k, self.A[k], self._pre_out(k))
-        elif w.kind == "postnorm_backward":
-            # the norm backward's passes alone (dgamma, dbeta and dH)
+        elif w.kind in ("postnorm_backward", "postnorm_regrouped_backward"):
+            # the norm backward's passes alone (dH, dgamma and dbeta)
             k = i % self.R
             fn.gemm_postnorm_backward(self.A[k], self.B[k], self.Cf[k], self.dC[k], self.rstd[k], w.norm, self.g,
                                       self.b, need=("dgamma", "dbeta"))
@@ -371,6 +388,11 @@ class Case:
             fn.gemm(self._pre_out(j), self.B[j], out=self.C[j])
         elif w.kind == "postnorm_backward":
             # the same decomposition: the norm backward's passes, then the GEMMs
+            fn.gemm_postnorm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j], w.norm, self.g,
+                                      self.b)
+        elif w.kind == "postnorm_regrouped_backward":
+            # the consumer's GEMM writes dC, then the unfused post-norm backward
+            fn.gemm_ex(self.Gr[j], self.Wr[j], trans_b=True, out=self.dC[j])
             fn.gemm_postnorm_backward(self.A[j], self.B[j], self.Cf[j], self.dC[j], self.rstd[j], w.norm, self.g,
                                       self.b)
         elif w.kind == "prenorm_backward":
@@ -413,7 +435,10 @@ class Case:
         if w.kind == "prenorm_backward":
             return {"fused": 3, "gemm": 2, "norm": 2}.get(what, 4)
         if w.kind == "postnorm_backward":
-            return {"fused": 5, "gemm": 2, "norm": 2}.get(what, 5)
+            return {"fused": 4, "gemm": 2, "norm": 2}.get(what, 4)
+        if w.kind == "postnorm_regrouped_backward":
+            # fused: the GEMM with the norm backward's epilogue, the column sum, dA, dB
+            return {"fused": 4, "gemm": 3, "norm": 2}.get(what, 5)
         if what == "fused" or what == "gemm":
             return 1
         if what == "norm":
@@ -589,16 +614,21 @@ def run_e2e(cases, K, W, world, device) -> dict:
         hC = torch.empty((c.w.M, c.w.N), dtype=torch.bfloat16).pin_memory()
         bwd = None
         if c.w.kind.endswith("_backward"):
-            # the backward's inputs (forward output, rstd, dC) in, dA and dB out
-            bwd = (c.Cf[0].cpu().pin_memory(), c.rstd[0].cpu().pin_memory(), c.host["dC"].pin_memory(),
-                   torch.empty((c.w.M, c.w.K), dtype=torch.bfloat16).pin_memory(),
-                   torch.empty((c.w.K, c.w.N), dtype=torch.bfloat16).pin_memory())
+            # the backward's inputs in (forward output, rstd, and the upstream
+            # gradient: dC, or for the regrouped form G and W), dA and dB out
+            ins = [(c.Cf[0].cpu().pin_memory(), c.Cf[0]), (c.rstd[0].cpu().pin_memory(), c.rstd[0])]
+            if c.w.kind == "postnorm_regrouped_backward":
+                ins += [(c.host["G"].pin_memory(), c.Gr[0]), (c.host["W"].pin_memory(), c.Wr[0])]
+            else:
+                ins += [(c.host["dC"].pin_memory(), c.dC[0])]
+            bwd = (ins, (torch.empty((c.w.M, c.w.K), dtype=torch.bfloat16).pin_memory(),
+                         torch.empty((c.w.K, c.w.N), dtype=torch.bfloat16).pin_memory()))
             hC = None
         host.append((hA, hB, hg, hb, hR, hC, bwd))
     h2d = sum(t.numel() * t.element_size() for h in host for t in h[:5] if t is not None)
-    h2d += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][:3])
+    h2d += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t, _ in h[6][0])
     d2h = sum(h[5].numel() * h[5].element_size() for h in host if h[5] is not None)
-    d2h += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][3:])
+    d2h += sum(t.numel() * t.element_size() for h in host if h[6] is not None for t in h[6][1])
 
     # Three streams, so that the host link carries inputs in and results out
     # at the same time and the kernels run meanwhile: per sub-workload, the
@@ -628,9 +658,8 @@ def run_e2e(cases, K, W, world, device) -> dict:
                 if hR is not None:
                     c.Rres[0].copy_(hR, non_blocking=True)
                 if bwd is not None:
-                    c.Cf[0].copy_(bwd[0], non_blocking=True)
-                    c.rstd[0].copy_(bwd[1], non_blocking=True)
-                    c.dC[0].copy_(bwd[2], non_blocking=True)
+                    for src, dst in bwd[0]:
+                        dst.copy_(src, non_blocking=True)
                 ev_in[k].record(s_in)
             s_cmp.wait_event(ev_in[k])
             s_cmp.wait_event(ev_out[k])
@@ -640,6 +669,10 @@ def run_e2e(cases, K, W, world, device) -> dict:
                         fn.lazy_prenorm_gemm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], dA=c.dA[0], dB=c.dB[0],
                                                       work=c.work[0])
                         outs = (c.dA[0], c.dB[0])
+                    elif w.kind == "postnorm_regrouped_backward":
+                        g = fn.gemm_postnorm_backward_regrouped(c.Gr[0], c.Wr[0], dA, dB, c.Cf[0], c.rstd[0],
+                                                                w.norm, c.g, c.b, need=("dA", "dB"))
+                        outs = (g["dA"], g["dB"])
                     else:
                         g = fn.gemm_postnorm_backward(dA, dB, c.Cf[0], c.dC[0], c.rstd[0], w.norm, c.g, c.b,
                                                       need=("dA", "dB"))
@@ -664,7 +697,7 @@ def run_e2e(cases, K, W, world, device) -> dict:
                 ev_cmp[k].record(s_cmp)
             s_out.wait_event(ev_cmp[k])
             with torch.cuda.stream(s_out):
-                dsts = (bwd[3], bwd[4]) if bwd is not None else (hC,)
+                dsts = bwd[1] if bwd is not None else (hC,)
                 for dst, src in zip(dsts, outs):
                     src.record_stream(s_out)  # (the backward's outputs are fresh allocations)
                     dst.copy_(src, non_blocking=True)
@@ -719,6 +752,9 @@ def oracle_step(w: Workload, d: dict, rows: np.ndarray):
         oracle.lazy_prenorm_gemm_backward(A, d["B64"], d["dC64"][rows], w.eps)
     elif w.kind == "postnorm_backward":
         oracle.gemm_postnorm_backward(A, d["B64"], d["dC64"][rows], w.norm, d["g64"], d["b64"], w.eps)
+    elif w.kind == "postnorm_regrouped_backward":
+        oracle.gemm_postnorm_backward_regrouped(d["G64"][rows], d["W64"], A, d["B64"], w.norm, d["g64"], d["b64"],
+                                                w.eps)
     elif w.kind == "prenorm_affine":
         oracle.prenorm_affine_gemm(A, d["B64"], w.norm, d["g64"], d["b64"], w.eps)
     elif w.residual:
@@ -737,7 +773,8 @@ def _oracle_inputs(names):
         w = WORKLOADS[n]
         d = make_inputs(w, 0)
         out.append((w, {"A64": to_f64(d["A"]), "B64": to_f64(d["B"]), "g64": to_f64(d["gamma"]),
-                        "b64": to_f64(d["beta"]), "R64": to_f64(d["R"]), "dC64": to_f64(d["dC"])}))
+                        "b64": to_f64(d["beta"]), "R64": to_f64(d["R"]), "dC64": to_f64(d["dC"]),
+                        "G64": to_f64(d["G"]), "W64": to_f64(d["W"])}))
     return out
 
 

@@ -273,7 +273,8 @@ fnorm_status_t fnorm_gemm_postnorm_noalloc(const fnorm_bf16* A, const fnorm_bf16
  *   dA [M,K], dB [K,N], dgamma [N] fp32, dbeta [N] fp32: outputs, each NULL
  *   to skip (dB needs M to be a multiple of 8; with M == 0 dB, dgamma and
  *   dbeta are zeroed).
- *   dH: [M,N] bf16 workspace, needed with dA or dB; receives dH.
+ *   dH: [M,N] bf16, receives dH whenever given; needed with dA or dB (their
+ *   GEMMs read it).
  *   part: fp32 workspace of 2 * N * ceil(M / 64) values, needed with dgamma
  *   or dbeta.
  */
@@ -282,6 +283,44 @@ fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf1
                                            const fnorm_bf16* beta, const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
                                            float* dgamma, float* dbeta, fnorm_bf16* dH, float* part, int64_t M,
                                            int64_t N, int64_t K, void* stream);
+
+/*
+ * fnorm_gemm_postnorm_backward_regrouped — fnorm_gemm_postnorm_backward when
+ * the gradient at the post-norm's output comes from the GEMM of the layer that
+ * consumes it, Z = C @ op(W): dC = G @ op(W)^T with G = dL/dZ [M, J].
+ *   [TFN] ("fusion regrouping": in the backward the norm is fused with a
+ *   different linear layer than in the forward, so that the backward also
+ *   gets an epilogue fusion).  dC is the accumulator of one fused GEMM and is
+ *   never written: its epilogue rebuilds h_hat = (C - beta) / gamma from the
+ *   forward output, takes the norm backward's two row sums (exchanged between
+ *   the CTAs of a cluster for rows wider than 256 columns), writes dH, and
+ *   writes per-32-row column partials of dC * h_hat and dC, which a
+ *   fixed-order column sum turns into dgamma and dbeta (deterministic).  Then
+ *   dA = dH @ B^T and dB = A^T @ dH as in fnorm_gemm_postnorm_backward.
+ *   G: [M, J] bf16, 16-byte aligned.
+ *   W: the consumer's bf16 weight, read in place as stored:
+ *     trans_w = 0: W is [N, J] and the consumer computes Z = C @ W (this
+ *                  library's B layout); dC = G @ W^T.
+ *     trans_w = 1: W is [J, N] (a linear layer's [out, in] weight) and the
+ *                  consumer computes Z = C @ W^T; dC = G @ W.
+ *   J: the consumer's output width, a multiple of 8.
+ *   A, B, C, norm, gamma, beta, rstd, dA, dB, dgamma, dbeta, M, N, K: as
+ *   fnorm_gemm_postnorm_backward.
+ *   dH: [M,N] bf16 output (always needed): receives dH.
+ *   part: fp32 workspace of 2 * N * ceil(M / 32) values, needed with dgamma or
+ *   dbeta.
+ *   Rows of up to 1024 columns (FNORM_ERR_UNSUPPORTED beyond: take fnorm_gemm_ex
+ *   and fnorm_gemm_postnorm_backward); a cluster size forced through
+ *   fnorm_set_postnorm_cluster must be 1, 2 or 4 and leave at most 256 columns
+ *   per CTA.
+ */
+fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const fnorm_bf16* W, int64_t J,
+                                                     int trans_w, const fnorm_bf16* A, const fnorm_bf16* B,
+                                                     const fnorm_bf16* C, fnorm_norm_t norm,
+                                                     const fnorm_bf16* gamma, const fnorm_bf16* beta,
+                                                     const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
+                                                     float* dgamma, float* dbeta, fnorm_bf16* dH, float* part,
+                                                     int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
  * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual

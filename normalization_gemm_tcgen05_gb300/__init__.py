@@ -37,7 +37,7 @@ import torch
 
 __all__ = [
     "FnormError", "lib", "LIB_PATH", "gemm", "gemm_ex", "rmsnorm_backward", "lazy_prenorm_gemm",
-    "gemm_postnorm_backward", "gemm_postnorm_noalloc", "lazy_prenorm_gemm_backward", "gemm_postnorm",
+    "gemm_postnorm_backward", "gemm_postnorm_backward_regrouped", "gemm_postnorm_noalloc", "lazy_prenorm_gemm_backward", "gemm_postnorm",
     "postnorm_workspace_size",
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
@@ -86,6 +86,9 @@ _SIGNATURES = {
                                                 ctypes.c_int, _f32, _p, _p, _p, _p]),
     "fnorm_gemm_postnorm_backward": (_c_status, [_p, _p, _p, _p, ctypes.c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                                  _i64, _i64, _i64, _p]),
+    "fnorm_gemm_postnorm_backward_regrouped": (_c_status, [_p, _p, _i64, ctypes.c_int, _p, _p, _p, ctypes.c_int,
+                                                           _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64,
+                                                           _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                             _p, _p, _p]),
     "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
@@ -420,6 +423,47 @@ def gemm_postnorm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC
             _ptr(A), _ptr(B), _ptr(C), _ptr(dC), _NORMS[norm], _ptr(gamma), _ptr(beta), _ptr(rstd),
             _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dgamma"]), _ptr(out["dbeta"]), _ptr(out["dH"]), _ptr(part),
             M, N, K, _stream(dev)))
+    return out
+
+
+def gemm_postnorm_backward_regrouped(G: torch.Tensor, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                                     C: torch.Tensor, rstd: torch.Tensor, norm="layernorm",
+                                     gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None,
+                                     trans_w: bool = False, need=("dA", "dB", "dgamma", "dbeta")) -> dict:
+    """gemm_postnorm_backward with the output gradient produced by the
+    consuming layer's GEMM inside the same fused kernel: dC = G @ W^T for a
+    consumer Z = C @ W (W [N, J]), or dC = G @ W with ``trans_w`` for a
+    consumer Z = C @ W^T (W [J, N]).  G is dL/dZ [M, J].  Returns a dict with
+    the gradients named in ``need`` and "dH"."""
+    M, N, K = _ab(A, B)
+    _mat(G, "G")
+    _mat(W, "W")
+    if G.shape[0] != M or G.device != A.device:
+        raise ValueError(f"G must have {M} rows on {A.device}")
+    J = G.shape[1]
+    if tuple(W.shape) != ((J, N) if trans_w else (N, J)) or W.device != A.device:
+        raise ValueError(f"W must have shape {(J, N) if trans_w else (N, J)} on {A.device}")
+    _mat(C, "C")
+    if tuple(C.shape) != (M, N) or C.device != A.device:
+        raise ValueError(f"C must have shape {(M, N)} on {A.device}")
+    if rstd.dtype != torch.float32 or rstd.numel() != M or not rstd.is_contiguous() or rstd.device != A.device:
+        raise ValueError(f"rstd must be a contiguous float32 vector of length {M} on {A.device}")
+    if norm not in _NORMS:
+        raise ValueError("norm must be 'layernorm' or 'rmsnorm'")
+    gamma = _vec(gamma, N, "gamma", A.device)
+    beta = _vec(beta, N, "beta", A.device)
+    dev = A.device
+    out = {"dA": torch.empty((M, K), dtype=torch.bfloat16, device=dev) if "dA" in need else None,
+           "dB": torch.empty((K, N), dtype=torch.bfloat16, device=dev) if "dB" in need else None,
+           "dgamma": torch.empty(N, dtype=torch.float32, device=dev) if "dgamma" in need else None,
+           "dbeta": torch.empty(N, dtype=torch.float32, device=dev) if "dbeta" in need else None}
+    out["dH"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    part = torch.empty(2 * N * ((M + 31) // 32), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().fnorm_gemm_postnorm_backward_regrouped(
+            _ptr(G), _ptr(W), J, 1 if trans_w else 0, _ptr(A), _ptr(B), _ptr(C), _NORMS[norm], _ptr(gamma),
+            _ptr(beta), _ptr(rstd), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dgamma"]), _ptr(out["dbeta"]),
+            _ptr(out["dH"]), _ptr(part), M, N, K, _stream(dev)))
     return out
 
 

@@ -540,13 +540,14 @@ fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf1
   clear_error();
   FN_TRY(check_mnk(M, N, K));
   if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
-  if (dA == nullptr && dB == nullptr && dgamma == nullptr && dbeta == nullptr) return bad("no gradient asked for");
+  if (dA == nullptr && dB == nullptr && dgamma == nullptr && dbeta == nullptr && dH == nullptr)
+    return bad("no gradient asked for");
   FN_TRY(check_ptr(dA, "dA", 16, true));
   FN_TRY(check_ptr(dB, "dB", 16, true));
   FN_TRY(check_ptr(dgamma, "dgamma", 4, true));
   FN_TRY(check_ptr(dbeta, "dbeta", 4, true));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool need_dh = dA != nullptr || dB != nullptr;
+  const bool need_dh = dA != nullptr || dB != nullptr || dH != nullptr;
   const bool need_cols = dgamma != nullptr || dbeta != nullptr;
   if (M == 0) {
     // an empty batch: zero dB, dgamma, dbeta
@@ -570,10 +571,80 @@ fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf1
   FN_TRY(check_ptr(gamma, "gamma", 16, true));
   FN_TRY(check_ptr(beta, "beta", 16, true));
   FN_TRY(check_ptr(rstd, "rstd", 4, !need_dh));
-  FN_TRY(check_ptr(dH, "dH", 16, !need_dh));
+  FN_TRY(check_ptr(dH, "dH", 16, dA == nullptr && dB == nullptr));
   FN_TRY(check_ptr(part, "part", 16, !need_cols));
   FN_TRY(launch_postnorm_backward_rows(dC, C, gamma, beta, rstd, norm == FNORM_LAYERNORM, need_dh ? dH : nullptr,
                                        part, dgamma, dbeta, static_cast<int>(M), static_cast<int>(N), st));
+  if (dA != nullptr) FN_TRY(fnorm_gemm_ex(dH, B, dA, M, K, N, 0, 1, stream));   // dH @ B^T
+  if (dB != nullptr) FN_TRY(fnorm_gemm_ex(A, dH, dB, K, N, M, 1, 0, stream));   // A^T @ dH
+  return FNORM_OK;
+}
+
+fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const fnorm_bf16* W, int64_t J,
+                                                     int trans_w, const fnorm_bf16* A, const fnorm_bf16* B,
+                                                     const fnorm_bf16* C, fnorm_norm_t norm,
+                                                     const fnorm_bf16* gamma, const fnorm_bf16* beta,
+                                                     const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
+                                                     float* dgamma, float* dbeta, fnorm_bf16* dH, float* part,
+                                                     int64_t M, int64_t N, int64_t K, void* stream) {
+  clear_error();
+  FN_TRY(check_mnk(M, N, K));
+  if (J < 8 || J > kMaxDim || J % 8 != 0) return bad("J must be a multiple of 8 in [8, 2^31)");
+  if (trans_w != 0 && trans_w != 1) return bad("trans_w must be 0 or 1");
+  if (norm != FNORM_RMSNORM && norm != FNORM_LAYERNORM) return bad("norm must be FNORM_RMSNORM or FNORM_LAYERNORM");
+  FN_TRY(check_ptr(dA, "dA", 16, true));
+  FN_TRY(check_ptr(dB, "dB", 16, true));
+  FN_TRY(check_ptr(dgamma, "dgamma", 4, true));
+  FN_TRY(check_ptr(dbeta, "dbeta", 4, true));
+  // rows of up to 256 columns in one CTA's tile; up to 1024 over a cluster
+  // of 2 or 4 CTAs of 256 columns (the exchange of the two row sums)
+  const int forced = forced_postnorm_cluster();
+  const int c = forced != 0 ? forced : (N <= 256 ? 1 : (N <= 512 ? 2 : 4));
+  if ((c != 1 && c != 2 && c != 4) || (N + c - 1) / c > 256) {
+    set_error("the regrouped post-norm backward covers rows of up to 1024 columns (a cluster of up to 4 CTAs of 256 "
+              "columns); N = %lld%s: use fnorm_gemm_ex and fnorm_gemm_postnorm_backward",
+              (long long)N, forced != 0 ? " with the forced cluster size" : "");
+    return FNORM_ERR_UNSUPPORTED;
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool cols = dgamma != nullptr || dbeta != nullptr;
+  if (M == 0) {
+    // an empty batch: zero dB, dgamma, dbeta
+    struct Z {
+      void* p;
+      size_t n;
+    } z[3] = {{dB, static_cast<size_t>(K) * N * 2}, {dgamma, static_cast<size_t>(N) * 4},
+              {dbeta, static_cast<size_t>(N) * 4}};
+    for (auto& e : z)
+      if (e.p != nullptr) {
+        cudaError_t err = cudaMemsetAsync(e.p, 0, e.n, st);
+        if (err != cudaSuccess) return cuda_fail(err, "cudaMemsetAsync");
+      }
+    return FNORM_OK;
+  }
+  if (dB != nullptr && M % 8 != 0) return bad("dB needs M to be a multiple of 8 (dH is read transposed)");
+  FN_TRY(check_ptr(G, "G", 16, false));
+  FN_TRY(check_ptr(W, "W", 16, false));
+  FN_TRY(check_ptr(A, "A", 16, dB == nullptr));
+  FN_TRY(check_ptr(B, "B", 16, dA == nullptr));
+  FN_TRY(check_ptr(C, "C", 16, false));
+  FN_TRY(check_ptr(gamma, "gamma", 16, true));
+  FN_TRY(check_ptr(beta, "beta", 16, true));
+  FN_TRY(check_ptr(rstd, "rstd", 4, false));
+  FN_TRY(check_ptr(dH, "dH", 16, false));
+  FN_TRY(check_ptr(part, "part", 16, !cols));
+  // dC = G @ op(W)^T in the accumulator: W [N, J] is the B^T operand, W [J, N] the plain one
+  FusedLaunch L = base_launch(G, W, dH, M, N, J, stream);
+  L.mode = MODE_POST | MODE_NBWD | (norm == FNORM_LAYERNORM ? MODE_LN : 0) | (trans_w ? 0 : MODE_BT);
+  L.cluster = c;
+  L.bn = (c == 1 && N <= 128) ? 128 : 256;
+  L.gamma = gamma;
+  L.beta = beta;
+  L.X = C;
+  L.rstd_in = rstd;
+  L.cpart = cols ? part : nullptr;
+  FN_TRY(launch_fused_norm_backward(L));
+  if (cols) FN_TRY(launch_column_sum(part, static_cast<int>((M + 31) / 32), static_cast<int>(N), dgamma, dbeta, st));
   if (dA != nullptr) FN_TRY(fnorm_gemm_ex(dH, B, dA, M, K, N, 0, 1, stream));   // dH @ B^T
   if (dB != nullptr) FN_TRY(fnorm_gemm_ex(A, dH, dB, K, N, M, 1, 0, stream));   // A^T @ dH
   return FNORM_OK;

@@ -39,6 +39,12 @@
 //   * the backward's GEMMs: B^T and A^T operands read straight from their
 //     row-major arrays, and the Lazy Pre-RMSNorm's dgrad epilogue
 //     y = u + c_m * x;
+//   * the post-norm's backward regrouped onto the GEMM that produces its
+//     output gradient ([TFN] "fusion regrouping": the consuming layer's
+//     data-gradient GEMM): the accumulator holds dC, the epilogue rebuilds
+//     the normalised rows from the forward output, takes the row reductions
+//     of the norm's backward (exchanged like the forward's statistics), writes
+//     dH and the per-32-row column partials of dgamma and dbeta;
 //   * the plain and lazy pre-norm GEMMs on a CTA pair (tcgen05 cta_group::2):
 //     a 2-CTA cluster computes each [256 x 256] tile, each CTA staging its 128
 //     rows of A and 128 of the tile's B columns; the second CTA's copies
@@ -105,6 +111,14 @@ enum : int {
   // multicast into both CTAs' shared memory, so each SM takes in a third less
   // per k-block; a stage is free again once both CTAs' MMAs have read it
   MODE_MCB = 32768,
+  // post-norm backward epilogue on the GEMM whose accumulator is dC = dL/dC
+  // (with MODE_POST; MODE_LN for LayerNorm): with h_hat = (X - beta) / gamma
+  // rebuilt from the forward output X and dh = dC * gamma,
+  //   dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+  // (RMSNorm: no mean_n(dh) term), rstd the forward's; the two row sums are
+  // exchanged like the forward's statistics.  Column partials of dC * h_hat
+  // (dgamma) and dC (dbeta) over each 32 rows go to a workspace.
+  MODE_NBWD = 65536,
 };
 
 struct FusedParams {
@@ -122,7 +136,9 @@ struct FusedParams {
   const float* bias;          // [N] beta @ B, or NULL (MODE_AFF)
   const __nv_bfloat16* R;     // [M, N] residual (MODE_RES)
   const float* rowcoef;       // MODE_DGRAD: [M] coefficients c of the forward rows
-  const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows combined in the epilogue
+  const __nv_bfloat16* X;     // MODE_DGRAD: [M, N] forward input rows; MODE_NBWD: [M, N] forward output
+  const float* rstd_in;       // MODE_NBWD: [M] the forward's rstd
+  float* cpart;               // MODE_NBWD: [ceil(M/32)][2][N] column partials (dgamma, dbeta), or NULL
   // MODE_GX workspace: per-(row block, tile) row statistics, per-row-block
   // arrival counters (zero at launch; the last CTA to finish zeroes them
   // again) and the CTA finish counter
@@ -143,7 +159,7 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff, NBR: resident-B k-blocks), so each kernel carries
 // only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR, int GW>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR, int GW, int GI>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -172,6 +188,7 @@ struct Aux {
   float2 hstat[2][2][128];  // [parity][column half][row]: partial statistics of each half
   alignas(16) float gam[GB];
   alignas(16) float bet[GB];
+  alignas(16) float igam[GI];  // post-norm backward: 1 / gamma of the CTA's columns (bet: -beta / gamma)
   // resident grid exchange: each epilogue warp's gamma/beta for the columns
   // of its half of the current tile (tiles change column group)
   alignas(16) float wgam[GW > 1 ? 8 : 1][GW];
@@ -202,6 +219,7 @@ struct KCfg {
   static constexpr bool GX = (MODE & MODE_GX) != 0;
   static constexpr bool CTA2 = (MODE & MODE_CTA2) != 0;
   static constexpr bool MCB = (MODE & MODE_MCB) != 0;
+  static constexpr bool NBWD = (MODE & MODE_NBWD) != 0;
   static constexpr bool PAIR = CTA2 || MCB;    // a 2-CTA cluster along M shares each tile sequence
   static constexpr int CG = CTA2 ? 2 : 1;      // CTA group of every tcgen05 instruction
   static constexpr int RB = PAIR ? 256 : 128;  // rows of one tile sequence unit (one or two row blocks)
@@ -215,12 +233,13 @@ struct KCfg {
   // 32-column subtiles loaded from TMEM per wait: the whole half when the
   // register budget allows (320 threads: 168 registers), else two (448
   // threads: 128 registers; cluster exchange code needs the room too)
-  static constexpr int LDB = DGRAD ? 1  // (the dgrad also holds its X values)
+  static constexpr int LDB = (DGRAD || NBWD) ? 1  // (these also hold their X values)
                              : (AUXW || ((CLUSTER || GX) && NCH > 2)) ? (NCH < 2 ? NCH : 2) : NCH;
   static constexpr bool KEEP = (LDB == NCH);  // one TMEM read serves statistics and output
   static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
   static constexpr int GB = (POST && !SPILL && !GX) ? BN : 1;  // gamma/beta kept in shared memory
   static constexpr int GW = GX ? HALF : 1;  // grid exchange: per-warp gamma/beta of a half tile
+  static constexpr int GI = NBWD ? BN : 1;   // post-norm backward: 1 / gamma
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BK * BNS * 2;
@@ -238,7 +257,7 @@ struct KCfg {
   static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1), GW>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1), GW, GI>) + 15) / 16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
   // that buys a pipeline stage and either the ring is below 4 stages, or a
   // warp stores only one box per tile (64-column tiles), so that nothing
@@ -272,8 +291,10 @@ struct KCfg {
   static_assert(!(PRE_LN || AFF) || (PRE && !POST), "the folded-affine pre-norm serves the pre-norm GEMM alone");
   static_assert(!PRE_LN || AFF, "the pre-LayerNorm needs its column sums");
   static_assert(!RES || (POST && !PRE), "the residual serves the post-norm");
-  static_assert(!(BT || AT || DGRAD) || (!POST && !BRES && !AFF && !RES),
-                "backward operand layouts serve the plain and lazy GEMMs");
+  static_assert(!(BT || AT || DGRAD) || ((!POST || (NBWD && !AT && !DGRAD)) && !BRES && !AFF && !RES),
+                "backward operand layouts serve the plain and lazy GEMMs and the post-norm backward");
+  static_assert(!NBWD || (POST && !PRE && !RES && !SPILL && !GX && !BRES && !MCB && !CTA2 && HALF <= 128),
+                "post-norm backward: resident tiles (one CTA or a cluster), X values of a half tile in registers");
   static_assert(!DGRAD || (BT && !AT && !PRE), "the dgrad: B^T operand, per-row coefficients from memory");
   static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
   static_assert(!CTA2 || (BN == 256 && !POST && !BRES && !RES && !BT && !AT && !DGRAD),
@@ -482,6 +503,31 @@ __device__ __forceinline__ void combine_mean_m2(float& mean, float& m2, float& n
   n = nn;
 }
 
+// Column sums over the 32 rows a warp holds (one row per lane): v[j] is this
+// lane's value of column j; lane l returns the sum of column l.  Five
+// butterfly rounds, each halving the columns a lane keeps (16 + 8 + 4 + 2 + 1
+// shuffles); the additions run in a fixed order, so the sums are the same on
+// every run.  v is consumed.
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float keep = upper ? v[j + w] : v[j];
+      const float send = upper ? v[j] : v[j + w];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// element e (0..7) of eight bf16 values packed in a uint4, widened to fp32
+__device__ __forceinline__ float bf16_of(const uint4& v, int e) {
+  const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+  return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
 // ---------------------------------------------------------------------------
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
@@ -493,11 +539,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool BRES = Cfg::BRES, NORMW = Cfg::NORMW;
   constexpr bool PRE_LN = Cfg::PRE_LN, AFF = Cfg::AFF, RES = Cfg::RES;
   constexpr bool BT = Cfg::BT, AT = Cfg::AT, DGRAD = Cfg::DGRAD, GX = Cfg::GX;
-  constexpr bool CTA2 = Cfg::CTA2, MCB = Cfg::MCB, PAIR = Cfg::PAIR;
+  constexpr bool CTA2 = Cfg::CTA2, MCB = Cfg::MCB, PAIR = Cfg::PAIR, NBWD = Cfg::NBWD;
   constexpr int CG = Cfg::CG, RB = Cfg::RB;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
-                   (Cfg::BRES ? Cfg::KB_MAX : 1), Cfg::GW>;
+                   (Cfg::BRES ? Cfg::KB_MAX : 1), Cfg::GW, Cfg::GI>;
   constexpr int HD = Cfg::HDEPTH;
 
   extern __shared__ uint8_t smem_raw[];
@@ -698,7 +744,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                   } else if (MCB) {
                     // this CTA's half of the tile's B boxes, into both CTAs
                     // (same offset; each CTA's full barrier counts all of B)
-                    if (c / (BN / 128) == prank)
+                    if (c / (BN >= 128 ? BN / 128 : 1) == prank)
                       tma_load_2d_mc(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, 0x3);
                   } else {
                     tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
@@ -874,7 +920,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       if (!esync()) return false;
       const float2 a = aux->hstat[hp][0][row];
       const float2 b = aux->hstat[hp][1][row];
-      if (LN && nh0 == nh1 && nh0 > 0.0f) {
+      if (NBWD) {
+        // the norm backward's row reductions are plain sums
+        part0 = a.x + b.x;
+        part1 = a.y + b.y;
+      } else if (LN && nh0 == nh1 && nh0 > 0.0f) {
         // equal halves (every full tile): the combination's weights are
         // exactly 1/2 and nh/2, the same values without its divisions
         const float d = b.x - a.x;
@@ -909,10 +959,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       for (int r2 = 0; r2 < C; ++r2) {
         const float2 v = aux->xstat[xp][r2][row];
         const int nq = min(max(N - (g * C + r2) * cta_cols, 0), cta_cols);
-        if (LN) combine_mean_m2(m_acc, q_acc, n_acc, v.x, v.y, static_cast<float>(nq));
-        else q_acc += v.x;
+        if (NBWD) {
+          m_acc += v.x;
+          q_acc += v.y;
+        } else if (LN) {
+          combine_mean_m2(m_acc, q_acc, n_acc, v.x, v.y, static_cast<float>(nq));
+        } else {
+          q_acc += v.x;
+        }
       }
-      part0 = LN ? m_acc : q_acc;
+      part0 = (LN || NBWD) ? m_acc : q_acc;
       part1 = q_acc;
       return true;
     };
@@ -1006,6 +1062,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const int n = n0 + j;
         aux->gam[j] = (p.gamma != nullptr && n < N) ? __bfloat162float(p.gamma[n]) : 1.0f;
         aux->bet[j] = (p.beta != nullptr && n < N) ? __bfloat162float(p.beta[n]) : 0.0f;
+        if (NBWD) {
+          // h_hat = (x - beta) / gamma as x * (1/gamma) + (-beta/gamma)
+          aux->igam[j] = __frcp_rn(aux->gam[j]);
+          aux->bet[j] = -aux->bet[j] * aux->igam[j];
+        }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps, before any wait
     }
@@ -1104,9 +1165,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           if (lane >= 16) gbv = make_uint4(0u, 0u, 0u, 0u);
           if (src != nullptr && col < N) gbv = __ldg(reinterpret_cast<const uint4*>(src + col));
         }
-        // dgrad: this half's X values, loaded while the tile's MMAs run
-        uint4 xv[DGRAD ? NCH : 1][4];
-        if (DGRAD) {
+        // dgrad, post-norm backward: this half's X values (and the forward
+        // rstd of the row), loaded while the tile's MMAs run
+        uint4 xv[(DGRAD || NBWD) ? NCH : 1][4];
+        const float rstd_row = (NBWD && m0 + row < M) ? __ldg(p.rstd_in + m0 + row) : 0.0f;
+        if (DGRAD || NBWD) {
 #pragma unroll
           for (int c = 0; c < NCH; ++c)
 #pragma unroll
@@ -1285,8 +1348,74 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           }
           __syncwarp();
         }
-        float mean = 0.0f, rstd = 1.0f;
-        if (POST) {
+        float mean = 0.0f, rstd = 1.0f, proj = 0.0f;
+        if constexpr (NBWD) {
+          float part0 = 0.0f, part1 = 0.0f;
+          // post-norm backward: the row sums of dh = u * gamma and dh * h_hat,
+          // h_hat = (x - beta) / gamma, over this half's columns; the column
+          // sums of u * h_hat and u over this warp's 32 rows (u is exactly zero
+          // past M and N: those A rows and B columns are zero-filled)
+          const int lim0 = m0 + row < M ? nvh : 0;
+          const bool cols = p.cpart != nullptr;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            if (c * 32 >= nvh) break;
+            tmem_load_batch<1>(tb + c * 32, r);
+            // (gamma, 1/gamma, -beta/gamma as float4 broadcasts)
+            const float4* gm = reinterpret_cast<const float4*>(&aux->gam[h * HALF + c * 32]);
+            const float4* be = reinterpret_cast<const float4*>(&aux->bet[h * HALF + c * 32]);
+            const float4* ig = reinterpret_cast<const float4*>(&aux->igam[h * HALF + c * 32]);
+            float va[32];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 g4 = gm[j4], b4 = be[j4], i4 = ig[j4];
+              const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+              const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+              const float iv[4] = {i4.x, i4.y, i4.z, i4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                const float u = j < lim0 - c * 32 ? __uint_as_float(r[0][j]) : 0.0f;
+                const float hh = fmaf(bf16_of(xv[c][j >> 3], j & 7), iv[e], bv[e]);
+                const float dh = u * gv[e];
+                part0 += dh;
+                part1 = fmaf(dh, hh, part1);
+                va[j] = u * hh;
+                r[0][j] = __float_as_uint(u);
+              }
+            }
+            if (cols) {
+              float vb[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) vb[j] = __uint_as_float(r[0][j]);
+              const float sg = warp_column_sums(va, lane);
+              const float sb = warp_column_sums(vb, lane);
+              const int col = c0h + c * 32 + lane;
+              if (m0 + q * 32 < M && col < N) {
+                float* cp = p.cpart + static_cast<size_t>((m0 >> 5) + q) * 2 * N;
+                cp[col] = sg;
+                cp[N + col] = sb;
+              }
+            }
+          }
+          const float n_h0 = static_cast<float>(min(max(N - n0, 0), HALF));
+          const float n_h1 = static_cast<float>(min(max(N - n0 - HALF, 0), HALF));
+          if (!combine_halves(part0, part1, n_h0, n_h1)) {
+            ok = false;
+            break;
+          }
+          if (CLUSTER) {
+            if (!exchange(part0, part1, g, xit)) {
+              ok = false;
+              break;
+            }
+            ++xit;
+          }
+          // dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+          mean = LN ? part0 * inv_N() : 0.0f;
+          proj = part1 * inv_N();
+          rstd = rstd_row;
+        } else if (POST) {
           float kk = 0.0f;
           float a1[2] = {0.f, 0.f}, a2[2] = {0.f, 0.f};
           for (int cb = 0; cb < NBATCH; ++cb) {
@@ -1340,40 +1469,72 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
         const int ew = warp - 2;
         // ---- normalise / scale, bf16, stage, TMA store: 32 columns at a time ----
-        for (int cb = 0; cb < NBATCH; ++cb) {
-          if (c0h + cb * LDB * 32 >= N) break;
-          if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
+        if constexpr (NBWD) {
+          // dH = rstd * (u * gamma - mean_n(dh) - h_hat * mean_n(dh * h_hat))
+          const float rm = -rstd * mean, rp = -rstd * proj;
 #pragma unroll
-          for (int b = 0; b < LDB; ++b) {
-            const int c = cb * LDB + b;
+          for (int c = 0; c < NCH; ++c) {
             const int col0 = c0h + c * 32;
             if (col0 >= N) break;
+            tmem_load_batch<1>(tb + c * 32, r);
+            const float4* gm = reinterpret_cast<const float4*>(&aux->gam[h * HALF + c * 32]);
+            const float4* be = reinterpret_cast<const float4*>(&aux->bet[h * HALF + c * 32]);
+            const float4* ig = reinterpret_cast<const float4*>(&aux->igam[h * HALF + c * 32]);
             uint32_t w[16];
-            if (POST) {
-              // y = (v - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta, v = pre * u
-              affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f,
-                          GX ? &aux->wgam[ew][c * 32] : &aux->gam[h * HALF + c * 32],
-                          GX ? &aux->wbet[ew][c * 32] : &aux->bet[h * HALF + c * 32], w);
-            } else if (DGRAD) {
-              // y = u + c * x
-              const uint64_t cc = f2(pre_mean, pre_mean);
 #pragma unroll
-              for (int g8 = 0; g8 < 4; ++g8) {
-                const uint32_t xw[4] = {xv[c][g8].x, xv[c][g8].y, xv[c][g8].z, xv[c][g8].w};
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 g4 = gm[j4], b4 = be[j4], i4 = ig[j4];
+              const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+              const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+              const float iv[4] = {i4.x, i4.y, i4.z, i4.w};
+              float y[4];
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                  const int jj = g8 * 8 + 2 * hh;
-                  w[jj >> 1] = pack_bf16x2_f2(f2_fma(f2(bf16_lo(xw[hh]), bf16_hi(xw[hh])), cc, f2u(r[b][jj], r[b][jj + 1])));
-                }
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                const float hh = fmaf(bf16_of(xv[c][j >> 3], j & 7), iv[e], bv[e]);
+                y[e] = fmaf(__uint_as_float(r[0][j]) * gv[e], rstd, fmaf(hh, rp, rm));
               }
-            } else if (AFF) {
-              // lazy pre-norm with folded affine: y = rstd * (u - mean * colsum_n) + bias_n
-              prenorm_pack<PRE_LN>(r[b], pre, -pre_mean * pre, p.colsum + col0,
-                                   p.bias == nullptr ? nullptr : p.bias + col0, N - col0, w);
-            } else {
-              scale_pack<PRE>(r[b], pre, w);
+              w[2 * j4] = pack_bf16x2(y[0], y[1]);
+              w[2 * j4 + 1] = pack_bf16x2(y[2], y[3]);
             }
             store_box(w, col0, m0);
+          }
+        } else {
+          for (int cb = 0; cb < NBATCH; ++cb) {
+            if (c0h + cb * LDB * 32 >= N) break;
+            if (!Cfg::KEEP) tmem_load_batch<LDB>(tb + cb * LDB * 32, r);
+#pragma unroll
+            for (int b = 0; b < LDB; ++b) {
+              const int c = cb * LDB + b;
+              const int col0 = c0h + c * 32;
+              if (col0 >= N) break;
+              uint32_t w[16];
+              if (POST) {
+                // y = (v - mean) * rstd * gamma + beta = (u*a + b) * gamma + beta, v = pre * u
+                affine_pack(r[b], pre * rstd, LN ? -mean * rstd : 0.0f,
+                            GX ? &aux->wgam[ew][c * 32] : &aux->gam[h * HALF + c * 32],
+                            GX ? &aux->wbet[ew][c * 32] : &aux->bet[h * HALF + c * 32], w);
+              } else if (DGRAD) {
+                // y = u + c * x
+                const uint64_t cc = f2(pre_mean, pre_mean);
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                  const uint32_t xw[4] = {xv[c][g8].x, xv[c][g8].y, xv[c][g8].z, xv[c][g8].w};
+#pragma unroll
+                  for (int hh = 0; hh < 4; ++hh) {
+                    const int jj = g8 * 8 + 2 * hh;
+                    w[jj >> 1] = pack_bf16x2_f2(f2_fma(f2(bf16_lo(xw[hh]), bf16_hi(xw[hh])), cc, f2u(r[b][jj], r[b][jj + 1])));
+                  }
+                }
+              } else if (AFF) {
+                // lazy pre-norm with folded affine: y = rstd * (u - mean * colsum_n) + bias_n
+                prenorm_pack<PRE_LN>(r[b], pre, -pre_mean * pre, p.colsum + col0,
+                                     p.bias == nullptr ? nullptr : p.bias + col0, N - col0, w);
+              } else {
+                scale_pack<PRE>(r[b], pre, w);
+              }
+              store_box(w, col0, m0);
+            }
           }
         }
         if (RES) preload_iter(it + 2);  // this buffer's next tile starts from its residual
@@ -1384,7 +1545,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // ---- row statistics ----
         const int m = m0 + row;
         if (h == 0 && m < M) {
-          if (POST) {
+          if (POST && !NBWD) {
             if (rank == 0 && (!GX || g == 0)) {
               if (LN && p.mean_out != nullptr) p.mean_out[m] = mean;
               if (p.rstd_out != nullptr) p.rstd_out[m] = rstd;

@@ -87,6 +87,8 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
     p.gx_finish = L.gx->finish;
   }
   p.X = static_cast<const __nv_bfloat16*>(L.X);
+  p.rstd_in = L.rstd_in;
+  p.cpart = L.cpart;
   p.status = dev.status;
   p.wait_limit_ns = wait_limit_ns();
 

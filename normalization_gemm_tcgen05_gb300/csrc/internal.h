@@ -87,6 +87,8 @@ struct FusedLaunch {
   // ([N, K] row-major), as the mode says
   const void* X;          // dgrad: [M, N] forward input combined in the epilogue
   const float* rowcoef;   // dgrad: [M] coefficients c = -rstd^2 (dC . C) / K
+  const float* rstd_in;   // post-norm backward: [M] the forward's rstd (X is then the forward output)
+  float* cpart;           // post-norm backward: [ceil(M/32)][2][N] column partials, or NULL
   const GxScratch* gx;    // grid-exchange post-norm's workspace
   cudaStream_t stream;
 };
@@ -103,6 +105,7 @@ fnorm_status_t launch_fused_post_grid(const FusedLaunch& L);      // post-norm, 
 fnorm_status_t launch_fused_pair(const FusedLaunch& L);           // GEMM, lazy pre-norms: two-CTA MMA (256-row tiles)
 fnorm_status_t launch_fused_mcb(const FusedLaunch& L);            // GEMM, lazy pre-norms: B multicast over a 2-CTA cluster
 fnorm_status_t launch_fused_mcb_grid(const FusedLaunch& L);       // grid-exchange post-norm, B multicast
+fnorm_status_t launch_fused_norm_backward(const FusedLaunch& L);  // post-norm backward on the dC-producing GEMM
 
 // B' = bf16(gamma_k * B[k, n]), colsum[n] = sum_k B'[k, n], bias[n] = sum_k beta_k * B[k, n]
 fnorm_status_t launch_fold_prenorm_affine(const void* B, int K, int N, const void* gamma, const void* beta,
@@ -119,6 +122,10 @@ fnorm_status_t launch_backward_rows(const void* dC, const void* C, const float* 
 // post-norm backward: dH from dC and the forward output (h_hat = (C - beta) /
 // gamma), and dgamma/dbeta through per-64-row partials in part[groups][2][N]
 int postnorm_backward_groups(int M);
+// dgamma[n] = sum_g part[g][0][n], dbeta[n] = sum_g part[g][1][n] over `groups`
+// row groups, in a fixed order (either output may be NULL)
+fnorm_status_t launch_column_sum(const float* part, int groups, int N, float* dgamma, float* dbeta,
+                                 cudaStream_t stream);
 fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, const void* gamma, const void* beta,
                                              const float* rstd, bool layernorm, void* dH, float* part, float* dgamma,
                                              float* dbeta, int M, int N, cudaStream_t stream);

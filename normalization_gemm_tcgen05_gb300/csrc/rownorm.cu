@@ -680,6 +680,16 @@ fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, cons
   return FNORM_OK;
 }
 
+fnorm_status_t launch_column_sum(const float* part, int groups, int N, float* dgamma, float* dbeta,
+                                 cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg =
+      small_cfg(dim3((unsigned)((N + kSumCols - 1) / kSumCols)), dim3(kSumCols * kSumRows), stream, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, column_sum_kernel, part, groups, N, dgamma, dbeta);
+  if (e != cudaSuccess) return cuda_fail(e, "column sum launch");
+  return FNORM_OK;
+}
+
 fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const float* rstd, void* dX, int M, int N,
                                        cudaStream_t stream) {
   DeviceInfo dev;

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
                      "fnorm_layernorm", "fnorm_check_status", "fnorm_last_error", "fnorm_gemm_add_postnorm",
                      "fnorm_fold_prenorm_affine", "fnorm_prenorm_gemm", "fnorm_lazy_prenorm_gemm_backward",
                      "fnorm_gemm_ex", "fnorm_rmsnorm_backward", "fnorm_gemm_postnorm_backward",
-                     "fnorm_gemm_postnorm_noalloc", "fnorm_gemm_postnorm_ws", "fnorm_postnorm_workspace_size"):
+                     "fnorm_gemm_postnorm_noalloc", "fnorm_gemm_postnorm_ws", "fnorm_postnorm_workspace_size",
+                     "fnorm_gemm_postnorm_backward_regrouped"):
         assert required in names
 
 
@@ -149,7 +150,7 @@ def test_backward_argument_rules(L):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, W, W, 128, 60, 64, None) == 1
     h = L.fnorm_gemm_postnorm_backward
     # no gradient asked; unknown norm; dH workspace missing; dB with M % 8 != 0
-    assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, None, None, None, None, W, W, 128, 64, 64, None) == 1
+    assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, None, None, None, None, None, W, 128, 64, 64, None) == 1
     assert h(FAKE, FAKE, FAKE, FAKE, 3, None, None, FAKE, FAKE, None, None, None, W, W, 128, 64, 64, None) == 1
     assert h(FAKE, FAKE, FAKE, FAKE, 1, None, None, FAKE, FAKE, None, None, None, None, W, 128, 64, 64, None) == 1
     assert b"dH" in L.fnorm_last_error()
@@ -160,6 +161,34 @@ def test_backward_argument_rules(L):
     assert g(FAKE, FAKE, FAKE, 128, 64, 64, 0, -1, None) == 1
     assert L.fnorm_rmsnorm_backward(FAKE, FAKE, FAKE, FAKE, 16, 32768, None) == 1
     assert L.fnorm_rmsnorm_backward(FAKE, FAKE, None, FAKE, 16, 64, None) == 1
+
+
+def test_regrouped_backward_rejects_bad_arguments(L):
+    h = L.fnorm_gemm_postnorm_backward_regrouped
+    W = FAKE
+
+    def call(G=FAKE, J=64, trans_w=0, norm=1, dA=FAKE, dB=FAKE, dgamma=None, dbeta=None, dH=FAKE, part=None,
+             M=128, N=256, K=64):
+        return h(G, W, J, trans_w, FAKE, FAKE, FAKE, norm, None, None, FAKE, dA, dB, dgamma, dbeta, dH, part, M, N,
+                 K, None)
+
+    assert call(J=60) == 1 and b"J" in L.fnorm_last_error()
+    assert call(trans_w=2) == 1
+    assert call(norm=3) == 1
+    assert call(N=60) == 1
+    # rows wider than a cluster of 4 x 256 columns: refused before any device work
+    assert call(N=1032) == 2 and b"1024" in L.fnorm_last_error()
+    assert call(M=100) == 1 and b"multiple of 8" in L.fnorm_last_error()    # dB reads dH transposed
+    assert call(dH=None) == 1 and b"dH" in L.fnorm_last_error()
+    assert call(dgamma=FAKE) == 1 and b"part" in L.fnorm_last_error()
+    assert call(G=ctypes.c_void_p(0x10002)) == 1 and b"G" in L.fnorm_last_error()
+    assert call(dgamma=ctypes.c_void_p(0x10002), part=FAKE) == 1
+    # a forced cluster size that leaves more than 256 columns per CTA
+    L.fnorm_set_postnorm_cluster(2)
+    try:
+        assert call(N=1024) == 2
+    finally:
+        L.fnorm_set_postnorm_cluster(0)
 
 
 def test_norm_rejects_bad_sizes(L):

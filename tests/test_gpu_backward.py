@@ -221,3 +221,90 @@ def test_postnorm_backward_layernorm_rows_sum_to_zero():
     h = np64(got["dH"])
     scale = np.abs(h).sum(axis=1)
     assert np.all(np.abs(h.sum(axis=1)) <= 2e-2 * scale + 1e-3)
+
+
+# ----------------------------------------------------------------------------
+# the post-norm backward regrouped onto the consuming layer's data-gradient
+# GEMM: dC = G @ op(W)^T lives only in the fused kernel's accumulator
+# ----------------------------------------------------------------------------
+def _rg(norm, M, N, K, J, trans_w, seed, affine=True, need=("dA", "dB", "dgamma", "dbeta")):
+    base = "cfg2_n128" if norm == "layernorm" else "cfg4_n1024_rms"
+    w = WORKLOADS[base].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    d = make_inputs(w, seed)
+    rng = np.random.default_rng(seed + 2)
+    G = torch.from_numpy(rng.standard_normal((M, J), dtype=np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy(rng.standard_normal((J, N) if trans_w else (N, J), dtype=np.float32)
+                         / np.float32(np.sqrt(J))).to(torch.bfloat16)
+    g = d["gamma"] if affine else None
+    b = d["beta"] if affine and norm == "layernorm" else None
+    Ad, Bd = d["A"].to(DEV), d["B"].to(DEV)
+    gd = None if g is None else g.to(DEV)
+    bd = None if b is None else b.to(DEV)
+    C, st = fn.gemm_postnorm(Ad, Bd, norm, gd, bd, w.eps, return_stats=True)
+    if M % 8 != 0:
+        need = tuple(x for x in need if x != "dB")
+    got = fn.gemm_postnorm_backward_regrouped(G.to(DEV), W.to(DEV), Ad, Bd, C, st["rstd"], norm, gd, bd,
+                                              trans_w=trans_w, need=need)
+    fn.check_status(DEV)
+    ref = oracle.gemm_postnorm_backward_regrouped(to_f64(G), to_f64(W), to_f64(d["A"]), to_f64(d["B"]), norm,
+                                                  to_f64(g), to_f64(b), w.eps, trans_w=trans_w)
+    return got, ref, (G, W, C, st, Ad, Bd, gd, bd)
+
+
+RG = [("layernorm", 256, 64, 256, 128, False),   # one CTA, 128-column tile, half past N
+      ("rmsnorm", 200, 128, 72, 96, True),       # ragged M
+      ("layernorm", 333, 200, 128, 256, False),  # a partial 32-row group; a ragged 256-column tile
+      ("layernorm", 256, 256, 128, 520, True),
+      ("rmsnorm", 384, 512, 256, 264, False),    # a cluster of 2
+      ("layernorm", 1000, 1024, 128, 256, True),  # a cluster of 4, ragged M
+      ("rmsnorm", 136, 1000, 64, 64, False),     # a cluster of 4, ragged N
+      ("layernorm", 8, 8, 8, 8, False)]
+
+
+@pytest.mark.parametrize("norm,M,N,K,J,trans_w", RG, ids=lambda v: str(v))
+def test_postnorm_backward_regrouped(norm, M, N, K, J, trans_w):
+    got, ref, _ = _rg(norm, M, N, K, J, trans_w, seed=M + N + K + J)
+    assert_out_close(got["dH"], ref["dH"], "dH")
+    assert_out_close(got["dA"], ref["dA"], "dA")
+    if got["dB"] is not None:
+        assert_out_close(got["dB"], ref["dB"], "dB")
+    assert_out_close(got["dgamma"], ref["dgamma"], "dgamma")
+    assert_out_close(got["dbeta"], ref["dbeta"], "dbeta")
+
+
+def test_postnorm_backward_regrouped_no_affine_and_partial_need():
+    got, ref, _ = _rg("layernorm", 520, 384, 64, 128, True, seed=31, affine=False, need=("dgamma", "dbeta"))
+    assert got["dA"] is None and got["dB"] is None
+    assert_out_close(got["dH"], ref["dH"], "dH without affine")
+    assert_out_close(got["dgamma"], ref["dgamma"], "dgamma without affine")
+    assert_out_close(got["dbeta"], ref["dbeta"], "dbeta without affine")
+
+
+def test_postnorm_backward_regrouped_matches_unfused_pipeline():
+    # the consumer's GEMM to a bf16 dC, then the unfused post-norm backward:
+    # the same gradients up to dC's rounding to bf16
+    got, ref, (G, W, C, st, Ad, Bd, gd, bd) = _rg("layernorm", 512, 1024, 256, 512, False, seed=33)
+    dC = fn.gemm_ex(G.to(DEV), W.to(DEV), trans_b=True)
+    un = fn.gemm_postnorm_backward(Ad, Bd, C, dC, st["rstd"], "layernorm", gd, bd)
+    fn.check_status(DEV)
+    for k in ("dH", "dA", "dB", "dgamma", "dbeta"):
+        assert_out_close(got[k], np64(un[k]), f"regrouped vs unfused {k}")
+        assert_out_close(un[k], ref[k], f"unfused {k} vs oracle")
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+def test_postnorm_backward_regrouped_cluster_sizes(cluster):
+    try:
+        fn.set_postnorm_cluster(cluster)
+        got, ref, _ = _rg("layernorm", 264, 256, 64, 128, True, seed=35)
+    finally:
+        fn.set_postnorm_cluster(0)
+    for k in ("dH", "dA", "dB", "dgamma", "dbeta"):
+        assert_out_close(got[k], ref[k], f"cluster {cluster}: {k}")
+
+
+def test_postnorm_backward_regrouped_deterministic():
+    a, _, _ = _rg("rmsnorm", 1000, 1024, 64, 128, False, seed=37)
+    b, _, _ = _rg("rmsnorm", 1000, 1024, 64, 128, False, seed=37)
+    for k in ("dH", "dA", "dgamma", "dbeta"):
+        assert torch.equal(a[k], b[k]), f"{k} differs between two runs"

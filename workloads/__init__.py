@@ -38,13 +38,17 @@ Forms beyond the five configurations (same distributions where they apply):
   A and B and an upstream gradient dC[8192,4096] N(0,1).
 * ``postnorm_bwd``  backward of the GEMM + post-LayerNorm at cfg4_n1024_ln's
   shape: its A, B, gamma, beta and dC[16384,1024] N(0,1).
+* ``postnorm_bwd_rg``  the same backward regrouped onto the consuming layer's
+  data-gradient GEMM: cfg4_n1024_ln's A, B, gamma, beta; the consumer
+  Z = C @ W with W[1024,2048] N(0,1/sqrt(2048)) and the gradient reaching it,
+  G = dL/dZ [16384,2048] N(0,1).
 
 Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
 float32 in the order A, row scale, outlier rows, row offset, B, gamma, beta, R
 (each only where the workload has it), then rounded once to bf16 (round to
 nearest even) by ``torch.Tensor.to(torch.bfloat16)``.  gamma and beta have
 length N for a post-norm and K for a pre-norm with affine.  The backward's
-dC is drawn last.
+dC is drawn last (the regrouped backward draws G, then W, instead).
 """
 from __future__ import annotations
 
@@ -60,7 +64,7 @@ import torch
 class Workload:
     name: str
     kind: str                 # "prenorm" | "postnorm" | "prenorm_affine" | "prenorm_backward" |
-                              # "postnorm_backward" | "gemm"
+                              # "postnorm_backward" | "postnorm_regrouped_backward" | "gemm"
     M: int
     K: int
     N: int
@@ -75,6 +79,7 @@ class Workload:
     a_outlier_frac: float = 0.0       # fraction of rows of A multiplied by 100
     a_row_offset: float = 0.0         # std of a per-row offset added to A before the row scale
     residual: bool = False            # residual R[M,N] N(0,1) added before the post-norm
+    J: int = 0                        # regrouped backward: the consuming layer's output width
     description: str = ""
 
     def scaled(self, **kw) -> "Workload":
@@ -83,8 +88,12 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """2MNK per GEMM (the backward runs two: dA over N, dB over M)."""
-        return (4.0 if self.kind.endswith("_backward") else 2.0) * self.M * self.N * self.K
+        """2MNK per GEMM (the backward runs two: dA over N, dB over M; the
+        regrouped backward also the consumer's data-gradient GEMM, 2MNJ)."""
+        f = (4.0 if self.kind.endswith("_backward") else 2.0) * self.M * self.N * self.K
+        if self.kind == "postnorm_regrouped_backward":
+            f += 2.0 * self.M * self.N * self.J
+        return f
 
     @property
     def affine_len(self) -> int:
@@ -96,6 +105,13 @@ class Workload:
         """Bytes one fused launch must move: A + B + C in bf16 (+ R), gamma/beta
         (post-norm) or the folded weight's fp32 column sums and bias row
         (pre-norm with affine), and the fp32 row statistics."""
+        if self.kind == "postnorm_regrouped_backward":
+            # the fused GEMM reads G, W, C (and rstd) and writes dH and the
+            # 32-row column partials (read back by the column sum); the
+            # GEMMs read dH, B and A, dH and write dA, dB
+            M, N, K, J = self.M, self.N, self.K, self.J
+            return (2.0 * (M * J + N * J + 4 * M * N + 2 * K * N + 2 * M * K) + 4.0 * M
+                    + 2 * 8.0 * N * ((M + 31) // 32))
         if self.kind == "postnorm_backward":
             # row pass reads dC, C and writes dH; column pass reads dC, C; the
             # GEMMs read dH, B and A, dH and write dA, dB
@@ -178,6 +194,10 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
     Workload("postnorm_bwd", "postnorm_backward", M=16384, K=2048, N=1024, b_std=1.0 / 45.0, eps=1e-5,
              norm="layernorm", gamma=True, beta=True,
              description="backward (dA, dB, dgamma, dbeta) of GEMM + post-LayerNorm, A[16384,2048] @ B[2048,1024]"),
+    Workload("postnorm_bwd_rg", "postnorm_regrouped_backward", M=16384, K=2048, N=1024, b_std=1.0 / 45.0,
+             eps=1e-5, norm="layernorm", gamma=True, beta=True, J=2048,
+             description="backward (dA, dB, dgamma, dbeta) of GEMM + post-LayerNorm, A[16384,2048] @ B[2048,1024], "
+                         "regrouped onto the consumer's data-gradient GEMM G[16384,2048] @ W[1024,2048]^T"),
 ]}
 
 
@@ -219,15 +239,18 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         beta = np.float32(0.1) * rng.standard_normal(n_aff, dtype=np.float32)
     if w.residual:
         r = rng.standard_normal((w.M, w.N), dtype=np.float32)
-    dc = None
-    if w.kind.endswith("_backward"):
+    dc = g_up = w_up = None
+    if w.kind == "postnorm_regrouped_backward":
+        g_up = rng.standard_normal((w.M, w.J), dtype=np.float32)
+        w_up = rng.standard_normal((w.N, w.J), dtype=np.float32) * np.float32(1.0 / math.sqrt(w.J))
+    elif w.kind.endswith("_backward"):
         dc = rng.standard_normal((w.M, w.N), dtype=np.float32)
 
     def bf16(x):
         return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
 
     return {"A": bf16(a), "B": bf16(b), "gamma": bf16(gamma), "beta": bf16(beta), "R": bf16(r), "dC": bf16(dc),
-            "row_scale": row_scale, "outliers": outl, "row_offset": row_offset}
+            "G": bf16(g_up), "W": bf16(w_up), "row_scale": row_scale, "outliers": outl, "row_offset": row_offset}
 
 
 def make_rows_inputs(w: Workload, rows: np.ndarray, seed: int = 0) -> dict:
