@@ -587,9 +587,24 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool PAIRS = PRE && !POST && !CLUSTER && !SPILL;
   constexpr int RUN = 4;
   const int full_rounds = PAIRS && ngroups > 1 ? total / (RUN * ncl) : 0;
+  // The A^T GEMMs (a weight gradient: a reduction over the long M) take
+  // their tiles in bands of BAND_W column groups.  Each tile streams a column
+  // slab of A (K x 128) and of B (K x BN) from end to end; in row-major order
+  // a wave of tiles spans every column group and reads every B slab from DRAM
+  // again.  In bands, a wave covers about grid / BAND_W row blocks of one band
+  // and the next wave the band's remaining row blocks, whose B slabs are the
+  // same and can still be in L2.
+  constexpr int BAND_W = 8;
+  auto band = [&](int u) -> int {
+    if (!AT || ngroups <= BAND_W || u >= total) return u;
+    const int per = num_m * BAND_W;
+    const int b = u / per, r = u % per;
+    const int w = min(BAND_W, ngroups - b * BAND_W);
+    return (r / w) * ngroups + b * BAND_W + r % w;
+  };
   auto tile_of = [&](int k) -> int {
     if (k < RUN * full_rounds) return RUN * ((k / RUN) * ncl + cid) + (k % RUN);
-    return RUN * full_rounds * ncl + cid + (k - RUN * full_rounds) * ncl;
+    return band(RUN * full_rounds * ncl + cid + (k - RUN * full_rounds) * ncl);
   };
   // The per-row statistics multiply by 1/N and 1/K (correctly rounded
   // reciprocals: exact, as a division would be, whenever N and K are powers
