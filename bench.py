@@ -68,7 +68,7 @@ GROUPS = {
     "cfg5": ["cfg5"],
     "res": ["res_ln_n128", "res_rms_n1024"],
     "preaff": ["preln_affine", "prerms_gamma"],
-    "bwd": ["prenorm_bwd", "postnorm_bwd", "postnorm_bwd_rg"],
+    "bwd": ["prenorm_bwd", "postnorm_bwd", "postnorm_bwd_rg", "postnorm_bwd_rg_n4096"],
 }
 GROUP_TEXT = {
     "main": "the five configurations, one fused launch of each sub-workload per step: Lazy Pre-RMSNorm GEMM "
@@ -86,7 +86,8 @@ GROUP_TEXT = {
     "preaff": "pre-norm with affine folded into B + GEMM, A[8192,4096] @ B[4096,4096]: LayerNorm(gamma, beta), "
               "RMSNorm(gamma)",
     "bwd": "backward of the Lazy Pre-RMSNorm GEMM, A[8192,4096] @ B[4096,4096], and of GEMM + post-LayerNorm, "
-           "A[16384,2048] @ B[2048,1024]",
+           "A[16384,2048] @ B[2048,1024]: from a given dC, and regrouped onto the consuming layer's data-gradient "
+           "GEMM G[16384,2048] @ W^T (also at N = 4096)",
 }
 KERNEL_SOURCES = ["fused_gemm.cuh", "ptx.cuh", "fused_launch.cuh", "rownorm.cu"]
 

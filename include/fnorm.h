@@ -293,7 +293,9 @@ fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf1
  *   gets an epilogue fusion).  dC is the accumulator of one fused GEMM and is
  *   never written: its epilogue rebuilds h_hat = (C - beta) / gamma from the
  *   forward output, takes the norm backward's two row sums (exchanged between
- *   the CTAs of a cluster for rows wider than 256 columns), writes dH, and
+ *   the CTAs of a cluster for rows of 257 to 1024 columns, grid-wide through
+ *   the workspace for wider rows, as fnorm_gemm_postnorm_ws does with the
+ *   forward's statistics), writes dH, and
  *   writes per-32-row column partials of dC * h_hat and dC, which a
  *   fixed-order column sum turns into dgamma and dbeta (deterministic).  Then
  *   dA = dH @ B^T and dB = A^T @ dH as in fnorm_gemm_postnorm_backward.
@@ -309,10 +311,15 @@ fnorm_status_t fnorm_gemm_postnorm_backward(const fnorm_bf16* A, const fnorm_bf1
  *   dH: [M,N] bf16 output (always needed): receives dH.
  *   part: fp32 workspace of 2 * N * ceil(M / 32) values, needed with dgamma or
  *   dbeta.
- *   Rows of up to 1024 columns (FNORM_ERR_UNSUPPORTED beyond: take fnorm_gemm_ex
- *   and fnorm_gemm_postnorm_backward); a cluster size forced through
- *   fnorm_set_postnorm_cluster must be 1, 2 or 4 and leave at most 256 columns
- *   per CTA.
+ *   workspace, workspace_bytes: the grid exchange's workspace for rows of more
+ *   than 1024 columns, exactly as fnorm_gemm_postnorm_ws's (sized by
+ *   fnorm_postnorm_workspace_size(M, N), zero-filled before its first use,
+ *   left zeroed by every call, calls sharing it ordered); without one such
+ *   rows are FNORM_ERR_UNSUPPORTED.  Ignored (may be NULL) for narrower rows.
+ *   A row of more 256-column tiles than the device has SMs, or more than 2^21
+ *   rows with N > 1024, is FNORM_ERR_UNSUPPORTED.  A cluster size forced
+ *   through fnorm_set_postnorm_cluster must be 1, 2 or 4 and leave at most 256
+ *   columns per CTA.
  */
 fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const fnorm_bf16* W, int64_t J,
                                                      int trans_w, const fnorm_bf16* A, const fnorm_bf16* B,
@@ -320,7 +327,8 @@ fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const
                                                      const fnorm_bf16* gamma, const fnorm_bf16* beta,
                                                      const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
                                                      float* dgamma, float* dbeta, fnorm_bf16* dH, float* part,
-                                                     int64_t M, int64_t N, int64_t K, void* stream);
+                                                     void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                                                     int64_t K, void* stream);
 
 /*
  * fnorm_gemm_add_postnorm — C = norm(A @ B + R) * gamma + beta: a residual

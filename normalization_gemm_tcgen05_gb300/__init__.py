@@ -87,8 +87,8 @@ _SIGNATURES = {
     "fnorm_gemm_postnorm_backward": (_c_status, [_p, _p, _p, _p, ctypes.c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                                  _i64, _i64, _i64, _p]),
     "fnorm_gemm_postnorm_backward_regrouped": (_c_status, [_p, _p, _i64, ctypes.c_int, _p, _p, _p, ctypes.c_int,
-                                                           _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64,
-                                                           _p]),
+                                                           _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, ctypes.c_size_t,
+                                                           _i64, _i64, _i64, _p]),
     "fnorm_gemm_add_postnorm": (_c_status, [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _f32,
                                             _p, _p, _p]),
     "fnorm_fold_prenorm_affine": (_c_status, [_p, _i64, _i64, _p, _p, _p, _p, _p, _p]),
@@ -429,12 +429,16 @@ def gemm_postnorm_backward(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dC
 def gemm_postnorm_backward_regrouped(G: torch.Tensor, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                                      C: torch.Tensor, rstd: torch.Tensor, norm="layernorm",
                                      gamma: Optional[torch.Tensor] = None, beta: Optional[torch.Tensor] = None,
-                                     trans_w: bool = False, need=("dA", "dB", "dgamma", "dbeta")) -> dict:
+                                     trans_w: bool = False, need=("dA", "dB", "dgamma", "dbeta"),
+                                     workspace: bool = True) -> dict:
     """gemm_postnorm_backward with the output gradient produced by the
     consuming layer's GEMM inside the same fused kernel: dC = G @ W^T for a
     consumer Z = C @ W (W [N, J]), or dC = G @ W with ``trans_w`` for a
-    consumer Z = C @ W^T (W [J, N]).  G is dL/dZ [M, J].  Returns a dict with
-    the gradients named in ``need`` and "dH"."""
+    consumer Z = C @ W^T (W [J, N]).  G is dL/dZ [M, J].  Rows of more than
+    1024 columns exchange their row sums through the stream's grid-exchange
+    workspace (the one gemm_postnorm uses); ``workspace=False`` passes none
+    (such rows are then refused).  Returns a dict with the gradients named in
+    ``need`` and "dH"."""
     M, N, K = _ab(A, B)
     _mat(G, "G")
     _mat(W, "W")
@@ -460,10 +464,11 @@ def gemm_postnorm_backward_regrouped(G: torch.Tensor, W: torch.Tensor, A: torch.
     out["dH"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     part = torch.empty(2 * N * ((M + 31) // 32), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
+        ws = _workspace(M, N, dev) if workspace and N > 1024 else None
         _check(lib().fnorm_gemm_postnorm_backward_regrouped(
             _ptr(G), _ptr(W), J, 1 if trans_w else 0, _ptr(A), _ptr(B), _ptr(C), _NORMS[norm], _ptr(gamma),
             _ptr(beta), _ptr(rstd), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dgamma"]), _ptr(out["dbeta"]),
-            _ptr(out["dH"]), _ptr(part), M, N, K, _stream(dev)))
+            _ptr(out["dH"]), _ptr(part), _ptr(ws), 0 if ws is None else ws.numel(), M, N, K, _stream(dev)))
     return out
 
 

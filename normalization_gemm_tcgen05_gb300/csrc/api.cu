@@ -586,7 +586,8 @@ fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const
                                                      const fnorm_bf16* gamma, const fnorm_bf16* beta,
                                                      const float* rstd, fnorm_bf16* dA, fnorm_bf16* dB,
                                                      float* dgamma, float* dbeta, fnorm_bf16* dH, float* part,
-                                                     int64_t M, int64_t N, int64_t K, void* stream) {
+                                                     void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                                                     int64_t K, void* stream) {
   clear_error();
   FN_TRY(check_mnk(M, N, K));
   if (J < 8 || J > kMaxDim || J % 8 != 0) return bad("J must be a multiple of 8 in [8, 2^31)");
@@ -597,14 +598,29 @@ fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const
   FN_TRY(check_ptr(dgamma, "dgamma", 4, true));
   FN_TRY(check_ptr(dbeta, "dbeta", 4, true));
   // rows of up to 256 columns in one CTA's tile; up to 1024 over a cluster
-  // of 2 or 4 CTAs of 256 columns (the exchange of the two row sums)
+  // of 2 or 4 CTAs of 256 columns (the two row sums exchanged through
+  // distributed shared memory); wider rows in one-CTA tiles of 256 columns
+  // with the row sums exchanged grid-wide through the caller's workspace
   const int forced = forced_postnorm_cluster();
+  const bool gx = forced == 0 && N > 1024;
   const int c = forced != 0 ? forced : (N <= 256 ? 1 : (N <= 512 ? 2 : 4));
-  if ((c != 1 && c != 2 && c != 4) || (N + c - 1) / c > 256) {
-    set_error("the regrouped post-norm backward covers rows of up to 1024 columns (a cluster of up to 4 CTAs of 256 "
-              "columns); N = %lld%s: use fnorm_gemm_ex and fnorm_gemm_postnorm_backward",
-              (long long)N, forced != 0 ? " with the forced cluster size" : "");
+  if (!gx && ((c != 1 && c != 2 && c != 4) || (N + c - 1) / c > 256)) {
+    set_error("a cluster size forced to %d does not fit the regrouped post-norm backward of %lld columns (1, 2 or 4 "
+              "CTAs of at most 256 columns)", c, (long long)N);
     return FNORM_ERR_UNSUPPORTED;
+  }
+  GxScratch gxs{};
+  if (gx) {
+    if (workspace == nullptr) {
+      set_error("rows of %lld columns: the regrouped post-norm backward exchanges their row sums grid-wide and needs "
+                "a workspace of fnorm_postnorm_workspace_size(M, N) bytes", (long long)N);
+      return FNORM_ERR_UNSUPPORTED;
+    }
+    if ((M + 127) / 128 > kGxMaxRowBlocks) {
+      set_error("the regrouped post-norm backward's grid exchange takes at most %d row blocks of 128", kGxMaxRowBlocks);
+      return FNORM_ERR_UNSUPPORTED;
+    }
+    FN_TRY(gx_scratch_from(workspace, workspace_bytes, M, N, &gxs));
   }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool cols = dgamma != nullptr || dbeta != nullptr;
@@ -633,11 +649,23 @@ fnorm_status_t fnorm_gemm_postnorm_backward_regrouped(const fnorm_bf16* G, const
   FN_TRY(check_ptr(rstd, "rstd", 4, false));
   FN_TRY(check_ptr(dH, "dH", 16, false));
   FN_TRY(check_ptr(part, "part", 16, !cols));
+  if (gx) {
+    // one CTA per tile of a row at least (no CTA may hold two tiles of the
+    // row block it waits on)
+    DeviceInfo dev;
+    FN_TRY(current_device(&dev));
+    if ((N + 255) / 256 > dev.num_sms) {
+      set_error("a row of %lld columns has more 256-column tiles than the device has SMs (%d)", (long long)N,
+                dev.num_sms);
+      return FNORM_ERR_UNSUPPORTED;
+    }
+  }
   // dC = G @ op(W)^T in the accumulator: W [N, J] is the B^T operand, W [J, N] the plain one
   FusedLaunch L = base_launch(G, W, dH, M, N, J, stream);
   L.mode = MODE_POST | MODE_NBWD | (norm == FNORM_LAYERNORM ? MODE_LN : 0) | (trans_w ? 0 : MODE_BT);
-  L.cluster = c;
-  L.bn = (c == 1 && N <= 128) ? 128 : 256;
+  L.cluster = gx ? 1 : c;
+  L.bn = (!gx && c == 1 && N <= 128) ? 128 : 256;
+  L.gx = gx ? &gxs : nullptr;
   L.gamma = gamma;
   L.beta = beta;
   L.X = C;

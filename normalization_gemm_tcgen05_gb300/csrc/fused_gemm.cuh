@@ -159,7 +159,8 @@ __host__ __device__ constexpr int pow2_at_least(int x, int lo) {
 // element (SSN: pre-norm row sums, SS1N: pre-LayerNorm shifted sums, NSN:
 // spill-layout handoff, NBR: resident-B k-blocks), so each kernel carries
 // only what it needs.
-template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR, int GW, int GI>
+template <int STAGES_, int GB, int CLMAX, int SSN, int SS1N, int NSN, int NPART, int HD, int NBR, int GW, int GI,
+          int GWI>
 struct Aux {
   uint64_t full[STAGES_];
   uint64_t empty[STAGES_];
@@ -192,7 +193,8 @@ struct Aux {
   // resident grid exchange: each epilogue warp's gamma/beta for the columns
   // of its half of the current tile (tiles change column group)
   alignas(16) float wgam[GW > 1 ? 8 : 1][GW];
-  alignas(16) float wbet[GW > 1 ? 8 : 1][GW];
+  alignas(16) float wbet[GW > 1 ? 8 : 1][GW];  // (post-norm backward: -beta / gamma)
+  alignas(16) float wigam[GWI > 1 ? 8 : 1][GWI];  // post-norm backward: 1 / gamma
   float2 xstat[2][CLMAX > 0 ? CLMAX : 1][128];
 };
 
@@ -239,7 +241,8 @@ struct KCfg {
   static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
   static constexpr int GB = (POST && !SPILL && !GX) ? BN : 1;  // gamma/beta kept in shared memory
   static constexpr int GW = GX ? HALF : 1;  // grid exchange: per-warp gamma/beta of a half tile
-  static constexpr int GI = NBWD ? BN : 1;   // post-norm backward: 1 / gamma
+  static constexpr int GI = (NBWD && !GX) ? BN : 1;    // post-norm backward: 1 / gamma of the CTA's slice
+  static constexpr int GWI = (NBWD && GX) ? HALF : 1;  // post-norm backward, grid exchange: per warp
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);  // two accumulator buffers
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BK * BNS * 2;
@@ -257,7 +260,8 @@ struct KCfg {
   static constexpr int NPART = PRE_LN ? 2 : 1;
   static constexpr int AUX_WARPS = AUXW ? 4 * NPART : 0;
   static constexpr uint32_t AUX_BYTES =
-      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1), GW, GI>) + 15) / 16 * 16;
+      (sizeof(Aux<kMaxStages, GB, CLMAX, SSN, SS1N, NSN, NPART, HDEPTH, (BRES ? KB_MAX : 1), GW, GI, GWI>) + 15) /
+      16 * 16;
   // epilogue staging: 8 warps x STG_BUFS store boxes.  One box per warp when
   // that buys a pipeline stage and either the ring is below 4 stages, or a
   // warp stores only one box per tile (64-column tiles), so that nothing
@@ -293,8 +297,9 @@ struct KCfg {
   static_assert(!RES || (POST && !PRE), "the residual serves the post-norm");
   static_assert(!(BT || AT || DGRAD) || ((!POST || (NBWD && !AT && !DGRAD)) && !BRES && !AFF && !RES),
                 "backward operand layouts serve the plain and lazy GEMMs and the post-norm backward");
-  static_assert(!NBWD || (POST && !PRE && !RES && !SPILL && !GX && !BRES && !MCB && !CTA2 && HALF <= 128),
-                "post-norm backward: resident tiles (one CTA or a cluster), X values of a half tile in registers");
+  static_assert(!NBWD || (POST && !PRE && !RES && !SPILL && !BRES && !MCB && !CTA2 && HALF <= 128),
+                "post-norm backward: resident tiles (one CTA, a cluster or the grid exchange), X values of a half "
+                "tile in registers");
   static_assert(!DGRAD || (BT && !AT && !PRE), "the dgrad: B^T operand, per-row coefficients from memory");
   static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
   static_assert(!CTA2 || (BN == 256 && !POST && !BRES && !RES && !BT && !AT && !DGRAD),
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr int CG = Cfg::CG, RB = Cfg::RB;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   using AuxT = Aux<STAGES, Cfg::GB, Cfg::CLMAX, Cfg::SSN, Cfg::SS1N, Cfg::NSN, Cfg::NPART, Cfg::HDEPTH,
-                   (Cfg::BRES ? Cfg::KB_MAX : 1), Cfg::GW, Cfg::GI>;
+                   (Cfg::BRES ? Cfg::KB_MAX : 1), Cfg::GW, Cfg::GI, Cfg::GWI>;
   constexpr int HD = Cfg::HDEPTH;
 
   extern __shared__ uint8_t smem_raw[];
@@ -1118,9 +1123,27 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       // flight (fewer where the norm warps leave fewer registers).
       // LayerNorm in two passes over them, without a division per step:
       // mean = sum_q n_q mean_q / N, then M2 = sum_q (M2_q + n_q (mean_q - mean)^2).
-      constexpr int XB = Cfg::AUXW ? 8 : 32;
+      constexpr int XB = (Cfg::AUXW || NBWD) ? 8 : 32;
       const float2* src = p.gx_part + static_cast<size_t>(rb) * ngroups * Cfg::BM + row;
       auto nq = [&](int qq) { return static_cast<float>(min(max(N - qq * cta_cols, 0), cta_cols)); };
+      if (NBWD) {
+        // the norm backward's two row sums: plain sums, in tile order
+        float a0 = 0.0f, a1 = 0.0f;
+        for (int q0 = 0; q0 < ngroups; q0 += XB) {
+          float2 v[XB];
+#pragma unroll
+          for (int u = 0; u < XB; ++u)
+            v[u] = q0 + u < ngroups ? __ldcg(src + static_cast<size_t>(q0 + u) * Cfg::BM) : make_float2(0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < XB; ++u) {
+            a0 += v[u].x;
+            a1 += v[u].y;
+          }
+        }
+        part0 = a0;
+        part1 = a1;
+        return true;
+      }
       float acc = 0.0f;  // LayerNorm: sum n_q mean_q; RMSNorm: sum of squares
       float2 v[XB];
       for (int q0 = 0; q0 < ngroups; q0 += XB) {
@@ -1353,13 +1376,33 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         // grid exchange: this warp's gamma/beta of the tile into its own
         // shared-memory slice (read back as float4 broadcasts after the
         // exchange; the previous tile's reads of the slice are complete)
-        if (GX) {
+        if (GX && !NBWD) {
           float* dst = (lane < 16 ? &aux->wgam[warp - 2][0] : &aux->wbet[warp - 2][0]) + (lane & 15) * 8;
           const uint32_t gw[4] = {gbv.x, gbv.y, gbv.z, gbv.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             dst[2 * e] = bf16_lo(gw[e]);
             dst[2 * e + 1] = bf16_hi(gw[e]);
+          }
+          __syncwarp();
+        } else if (GX) {
+          // post-norm backward: gamma and 1/gamma from lanes 0-15, -beta/gamma
+          // from lanes 16-31 (which take their columns' gamma from lane - 16)
+          const uint32_t gw[4] = {gbv.x, gbv.y, gbv.z, gbv.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ow[e] = __shfl_xor_sync(0xffffffffu, gw[e], 16);
+          const int o = (lane & 15) * 8;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float mine = (e & 1) ? bf16_hi(gw[e >> 1]) : bf16_lo(gw[e >> 1]);
+            const float other = (e & 1) ? bf16_hi(ow[e >> 1]) : bf16_lo(ow[e >> 1]);
+            if (lane < 16) {
+              aux->wgam[warp - 2][o + e] = mine;
+              aux->wigam[warp - 2][o + e] = __frcp_rn(mine);
+            } else {
+              aux->wbet[warp - 2][o + e] = -mine * __frcp_rn(other);
+            }
           }
           __syncwarp();
         }
@@ -1377,9 +1420,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (c * 32 >= nvh) break;
             tmem_load_batch<1>(tb + c * 32, r);
             // (gamma, 1/gamma, -beta/gamma as float4 broadcasts)
-            const float4* gm = reinterpret_cast<const float4*>(&aux->gam[h * HALF + c * 32]);
-            const float4* be = reinterpret_cast<const float4*>(&aux->bet[h * HALF + c * 32]);
-            const float4* ig = reinterpret_cast<const float4*>(&aux->igam[h * HALF + c * 32]);
+            const float4* gm = reinterpret_cast<const float4*>(GX ? &aux->wgam[warp - 2][c * 32]
+                                                                  : &aux->gam[h * HALF + c * 32]);
+            const float4* be = reinterpret_cast<const float4*>(GX ? &aux->wbet[warp - 2][c * 32]
+                                                                  : &aux->bet[h * HALF + c * 32]);
+            const float4* ig = reinterpret_cast<const float4*>(GX ? &aux->wigam[warp - 2][c * 32]
+                                                                  : &aux->igam[h * HALF + c * 32]);
             float va[32];
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
@@ -1425,6 +1471,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               break;
             }
             ++xit;
+          } else if (GX) {
+            if (!gx_exchange(part0, part1, m0, g)) {
+              ok = false;
+              break;
+            }
           }
           // dH = rstd * (dh - mean_n(dh) - h_hat * mean_n(dh * h_hat))
           mean = LN ? part0 * inv_N() : 0.0f;
@@ -1492,9 +1543,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int col0 = c0h + c * 32;
             if (col0 >= N) break;
             tmem_load_batch<1>(tb + c * 32, r);
-            const float4* gm = reinterpret_cast<const float4*>(&aux->gam[h * HALF + c * 32]);
-            const float4* be = reinterpret_cast<const float4*>(&aux->bet[h * HALF + c * 32]);
-            const float4* ig = reinterpret_cast<const float4*>(&aux->igam[h * HALF + c * 32]);
+            const float4* gm = reinterpret_cast<const float4*>(GX ? &aux->wgam[ew][c * 32]
+                                                                  : &aux->gam[h * HALF + c * 32]);
+            const float4* be = reinterpret_cast<const float4*>(GX ? &aux->wbet[ew][c * 32]
+                                                                  : &aux->bet[h * HALF + c * 32]);
+            const float4* ig = reinterpret_cast<const float4*>(GX ? &aux->wigam[ew][c * 32]
+                                                                  : &aux->igam[h * HALF + c * 32]);
             uint32_t w[16];
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {

@@ -6,8 +6,10 @@
 // epilogue writes dH and the column partials of dgamma and dbeta.  Rows of up
 // to 256 columns sit in one CTA's tile, rows of up to 1024 over a cluster of
 // 2 or 4 CTAs with the two row sums exchanged through distributed shared
-// memory.  The consumer's weight is read as stored: W [N, J] as the B^T
-// operand (K-major), or W [J, N] as the plain B operand.
+// memory, wider rows in resident 256-column tiles with the row sums exchanged
+// grid-wide through the caller's workspace (a cooperative launch).  The
+// consumer's weight is read as stored: W [N, J] as the B^T operand (K-major),
+// or W [J, N] as the plain B operand.
 #include "fused_launch.cuh"
 
 namespace fnorm {
@@ -29,6 +31,11 @@ fnorm_status_t by_norm(const FusedLaunch& L) {
 
 template <int X>
 fnorm_status_t by_layout(const FusedLaunch& L) {
+  if (L.gx != nullptr) {
+    if (L.cluster == 1 && L.bn == 256) return by_norm<256, X | MODE_GX, 0>(L);
+    set_error("internal: the grid-exchange post-norm backward takes one-CTA tiles of 256 columns");
+    return FNORM_ERR_UNSUPPORTED;
+  }
   if (L.cluster == 1 && L.bn == 128) return by_norm<128, X, 0>(L);
   if (L.cluster == 1 && L.bn == 256) return by_norm<256, X, 0>(L);
   if (L.cluster > 1 && L.bn == 256) return by_norm<256, X | MODE_CLUSTER, 4>(L);
@@ -38,7 +45,7 @@ fnorm_status_t by_layout(const FusedLaunch& L) {
 }  // namespace
 
 fnorm_status_t launch_fused_norm_backward(const FusedLaunch& L) {
-  if (L.spill || L.bres || L.gx != nullptr) {
+  if (L.spill || L.bres) {
     set_error("internal: unexpected post-norm backward plan");
     return FNORM_ERR_UNSUPPORTED;
   }

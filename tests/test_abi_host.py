@@ -168,16 +168,19 @@ def test_regrouped_backward_rejects_bad_arguments(L):
     W = FAKE
 
     def call(G=FAKE, J=64, trans_w=0, norm=1, dA=FAKE, dB=FAKE, dgamma=None, dbeta=None, dH=FAKE, part=None,
-             M=128, N=256, K=64):
-        return h(G, W, J, trans_w, FAKE, FAKE, FAKE, norm, None, None, FAKE, dA, dB, dgamma, dbeta, dH, part, M, N,
-                 K, None)
+             ws=None, ws_bytes=0, M=128, N=256, K=64):
+        return h(G, W, J, trans_w, FAKE, FAKE, FAKE, norm, None, None, FAKE, dA, dB, dgamma, dbeta, dH, part, ws,
+                 ws_bytes, M, N, K, None)
 
     assert call(J=60) == 1 and b"J" in L.fnorm_last_error()
     assert call(trans_w=2) == 1
     assert call(norm=3) == 1
     assert call(N=60) == 1
-    # rows wider than a cluster of 4 x 256 columns: refused before any device work
-    assert call(N=1032) == 2 and b"1024" in L.fnorm_last_error()
+    # rows wider than a cluster of 4 x 256 columns exchange grid-wide: without a
+    # workspace they are refused, with too small a one it is an argument error,
+    # both before any device work
+    assert call(N=1032) == 2 and b"workspace" in L.fnorm_last_error()
+    assert call(N=4096, ws=FAKE, ws_bytes=1024) == 1 and b"workspace" in L.fnorm_last_error()
     assert call(M=100) == 1 and b"multiple of 8" in L.fnorm_last_error()    # dB reads dH transposed
     assert call(dH=None) == 1 and b"dH" in L.fnorm_last_error()
     assert call(dgamma=FAKE) == 1 and b"part" in L.fnorm_last_error()

@@ -258,7 +258,12 @@ RG = [("layernorm", 256, 64, 256, 128, False),   # one CTA, 128-column tile, hal
       ("rmsnorm", 384, 512, 256, 264, False),    # a cluster of 2
       ("layernorm", 1000, 1024, 128, 256, True),  # a cluster of 4, ragged M
       ("rmsnorm", 136, 1000, 64, 64, False),     # a cluster of 4, ragged N
-      ("layernorm", 8, 8, 8, 8, False)]
+      ("layernorm", 8, 8, 8, 8, False),
+      # wider rows: the row sums exchanged grid-wide through the workspace
+      ("layernorm", 264, 2048, 64, 128, False),
+      ("rmsnorm", 300, 4096, 128, 256, True),
+      ("layernorm", 128 * 20 + 5, 8192, 64, 64, False),  # 21 row blocks x 32 tiles: several waves
+      ("rmsnorm", 520, 1032, 64, 72, True)]      # one tile past a cluster's reach, a ragged last tile
 
 
 @pytest.mark.parametrize("norm,M,N,K,J,trans_w", RG, ids=lambda v: str(v))
@@ -308,3 +313,15 @@ def test_postnorm_backward_regrouped_deterministic():
     b, _, _ = _rg("rmsnorm", 1000, 1024, 64, 128, False, seed=37)
     for k in ("dH", "dA", "dgamma", "dbeta"):
         assert torch.equal(a[k], b[k]), f"{k} differs between two runs"
+
+
+def test_postnorm_backward_regrouped_wide_rows_need_a_workspace():
+    w = WORKLOADS["cfg2_n128"].scaled(M=128, N=2048, K=64)
+    d = make_inputs(w, 39)
+    A, B = d["A"].to(DEV), d["B"].to(DEV)
+    C, st = fn.gemm_postnorm(A, B, "layernorm", return_stats=True)
+    G = torch.randn(128, 64, device=DEV).to(torch.bfloat16)
+    W = torch.randn(2048, 64, device=DEV).to(torch.bfloat16)
+    with pytest.raises(fn.FnormError) as e:
+        fn.gemm_postnorm_backward_regrouped(G, W, A, B, C, st["rstd"], "layernorm", workspace=False)
+    assert e.value.status == fn.UNSUPPORTED and "workspace" in str(e.value)

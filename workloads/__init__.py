@@ -42,6 +42,7 @@ Forms beyond the five configurations (same distributions where they apply):
   data-gradient GEMM: cfg4_n1024_ln's A, B, gamma, beta; the consumer
   Z = C @ W with W[1024,2048] N(0,1/sqrt(2048)) and the gradient reaching it,
   G = dL/dZ [16384,2048] N(0,1).
+* ``postnorm_bwd_rg_n4096``  the same at cfg4_n4096_ln's shape: W[4096,2048].
 
 Random numbers come from ``numpy.random.default_rng(seed)`` (PCG64), drawn in
 float32 in the order A, row scale, outlier rows, row offset, B, gamma, beta, R
@@ -198,6 +199,11 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
              eps=1e-5, norm="layernorm", gamma=True, beta=True, J=2048,
              description="backward (dA, dB, dgamma, dbeta) of GEMM + post-LayerNorm, A[16384,2048] @ B[2048,1024], "
                          "regrouped onto the consumer's data-gradient GEMM G[16384,2048] @ W[1024,2048]^T"),
+    Workload("postnorm_bwd_rg_n4096", "postnorm_regrouped_backward", M=16384, K=2048, N=4096, b_std=1.0 / 45.0,
+             eps=1e-5, norm="layernorm", gamma=True, beta=True, J=2048,
+             description="backward (dA, dB, dgamma, dbeta) of GEMM + post-LayerNorm, A[16384,2048] @ B[2048,4096], "
+                         "regrouped onto the consumer's data-gradient GEMM G[16384,2048] @ W[4096,2048]^T "
+                         "(row sums exchanged grid-wide)"),
 ]}
 
 
