@@ -325,3 +325,26 @@ def test_postnorm_backward_regrouped_wide_rows_need_a_workspace():
     with pytest.raises(fn.FnormError) as e:
         fn.gemm_postnorm_backward_regrouped(G, W, A, B, C, st["rstd"], "layernorm", workspace=False)
     assert e.value.status == fn.UNSUPPORTED and "workspace" in str(e.value)
+
+
+@pytest.mark.parametrize("name", ["postnorm_bwd", "postnorm_bwd_rg", "postnorm_bwd_rg_n4096"])
+def test_postnorm_backward_full_size(name):
+    # the bench's post-norm backward workloads in their launch configuration,
+    # every gradient element against the oracle at full size
+    w = WORKLOADS[name]
+    d = make_inputs(w, 0)
+    Ad, Bd, gd, bd = d["A"].to(DEV), d["B"].to(DEV), d["gamma"].to(DEV), d["beta"].to(DEV)
+    C, st = fn.gemm_postnorm(Ad, Bd, w.norm, gd, bd, w.eps, return_stats=True)
+    g64, b64 = to_f64(d["gamma"]), to_f64(d["beta"])
+    if w.kind == "postnorm_backward":
+        got = fn.gemm_postnorm_backward(Ad, Bd, C, d["dC"].to(DEV), st["rstd"], w.norm, gd, bd)
+        fn.check_status(DEV)
+        ref = oracle.gemm_postnorm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(d["dC"]), w.norm, g64, b64, w.eps)
+    else:
+        got = fn.gemm_postnorm_backward_regrouped(d["G"].to(DEV), d["W"].to(DEV), Ad, Bd, C, st["rstd"], w.norm, gd,
+                                                  bd)
+        fn.check_status(DEV)
+        ref = oracle.gemm_postnorm_backward_regrouped(to_f64(d["G"]), to_f64(d["W"]), to_f64(d["A"]),
+                                                      to_f64(d["B"]), w.norm, g64, b64, w.eps)
+    for k in ("dH", "dA", "dB", "dgamma", "dbeta"):
+        assert_out_close(got[k], ref[k], f"{name} {k} (every element)")
