@@ -170,6 +170,7 @@ struct Aux {
   uint64_t ss_full[2];
   uint64_t ss_empty[2];
   uint64_t xbar[2];
+  uint64_t gxbar[2];  // grid exchange: the polling lane's "row block complete" to the other epilogue warps
   uint64_t nstat_full[HD];   // epilogue -> normaliser handoff, HD deep
   uint64_t nstat_empty[HD];
   uint64_t ebar[4][2];  // bounded barrier of the two epilogue warps of each TMEM lane quarter
@@ -178,7 +179,6 @@ struct Aux {
   uint64_t rload;           // the first residual tile, loaded by TMA (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort_flag;
-  int gx_ready;  // grid exchange: tiles whose row block the polling lane has seen complete
   int gx_last;   // grid exchange: this CTA finished last
   int nstat_m0[HD];
   int nstat_c0[HD];
@@ -639,6 +639,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->ss_full[b]), 4 * Cfg::NPART);
       mbar_init(smem_u32(&aux->ss_empty[b]), kEpiWarps);
       mbar_init(smem_u32(&aux->xbar[b]), 1);
+      mbar_init(smem_u32(&aux->gxbar[b]), 1);
       for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&aux->ebar[qq][b]), kEpiWarps / 4);
     }
     if (lane >= 2 && lane < 2 + HD) {
@@ -650,7 +651,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
       mbar_init(smem_u32(&aux->teardown), 1);
       mbar_init(smem_u32(&aux->rload), kEpiWarps);
       aux->abort_flag = 0;
-      aux->gx_ready = 0;
     }
     fence_mbar_init();
   }
@@ -1095,30 +1095,37 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     // warps publish the tile's statistics for its 128 rows and each counts
     // in on the row block's counter (4 arrivals per tile, atomic adds); one
     // lane of the CTA polls the counter until every tile of the row block
-    // has arrived and passes that on through shared memory (one poller per
-    // CTA keeps the counter's L2 line quiet for the arrivals); then every
-    // warp combines all the tiles' statistics in tile order (the same
-    // arithmetic in every tile of the row, so every tile derives the same
-    // mean and rstd).  xk counts this CTA's exchanges.  False if a wait gave
-    // up.
+    // has arrived and passes that on through an mbarrier, on which the other
+    // epilogue warps sleep rather than spin (one poller per CTA keeps the
+    // counter's L2 line quiet for the arrivals, and sleeping waiters leave
+    // the issue slots to the producer and MMA warps); then every warp
+    // combines all the tiles' statistics in tile order (the same arithmetic
+    // in every tile of the row, so every tile derives the same mean and
+    // rstd).  xk counts this CTA's exchanges; exchange k completes phase k/2
+    // of barrier k%2 (a warp cannot be two exchanges behind the poller: the
+    // halves meet in combine_halves before every exchange).  False if a wait
+    // gave up.
     int xk = 0;
     auto gx_exchange = [&](float& part0, float& part1, int m0_, int g_) -> bool {
       const int rb = m0_ / Cfg::BM;
       if (h == 0) p.gx_part[(static_cast<size_t>(rb) * ngroups + g_) * Cfg::BM + row] = make_float2(part0, part1);
       __syncwarp();
       if (h == 0 && lane == 0) grid_arrive(p.gx_cnt + rb);
-      bool ready = true;
+      const uint32_t gxb = smem_u32(&aux->gxbar[xk & 1]);
+      const uint32_t gxpar = static_cast<uint32_t>(xk >> 1) & 1u;
       ++xk;
-      if (lane == 0) {
-        if (warp == 2) {
+      if (warp == 2) {
+        bool ready = true;
+        if (lane == 0) {
           ready = grid_wait_eq(wc, p.gx_cnt + rb, static_cast<unsigned long long>(4 * ngroups), kSiteGrid);
-          if (ready) flag_release(&aux->gx_ready, xk);
-        } else {
-          ready = wait_flag_ge(wc, &aux->gx_ready, xk, kSiteGrid);
+          // (the arrive releases at CTA scope what this lane acquired at GPU scope)
+          if (ready) mbar_arrive(gxb);
         }
+        if (!__all_sync(0xffffffffu, ready)) return false;
+        __syncwarp();  // lane 0's acquire orders every lane's loads below
+      } else if (!mbar_wait_warp(wc, gxb, gxpar, kSiteGrid)) {
+        return false;
       }
-      if (!__all_sync(0xffffffffu, ready)) return false;
-      __syncwarp();  // lane 0's acquire orders every lane's loads below
       // Combine the tiles' statistics in tile order, XB per batch of loads in
       // flight (fewer where the norm warps leave fewer registers).
       // LayerNorm in two passes over them, without a division per step:

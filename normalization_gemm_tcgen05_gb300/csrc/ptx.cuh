@@ -149,31 +149,6 @@ __device__ __forceinline__ bool grid_wait_eq(const WaitCtx& w, const unsigned lo
   }
 }
 
-// Hand a value to the other warps of the CTA through a shared-memory word,
-// releasing (at CTA scope) everything this thread has seen, including what
-// it acquired at GPU scope.
-__device__ __forceinline__ void flag_release(int* flag, int v) {
-  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(flag)), "r"(v) : "memory");
-}
-
-// Wait (one lane; bounded) until the shared-memory word `flag` reads at
-// least v, with acquire loads at CTA scope (pairs with flag_release).
-__device__ __forceinline__ bool wait_flag_ge(const WaitCtx& w, const int* flag, int v, uint32_t site) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 0;; ++i) {
-    int x;
-    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(x) : "r"(smem_u32(flag)) : "memory");
-    if (x >= v) return true;
-    if ((i & 63u) == 63u) {
-      if (*w.abort_flag) return false;
-      if (global_timer_ns() - t0 > w.limit_ns) {
-        record_timeout(w, site);
-        return false;
-      }
-    }
-  }
-}
-
 // Warp-collective wait: every lane waits (and so acquires), then the lanes
 // vote, so a timeout is seen by the whole warp and no lane runs ahead into a
 // .sync.aligned instruction or a __syncwarp the others never reach.
