@@ -351,3 +351,16 @@ def test_postnorm_backward_full_size(name):
                                                       to_f64(d["B"]), w.norm, g64, b64, w.eps)
     for k in ("dH", "dA", "dB", "dgamma", "dbeta"):
         assert_out_close(got[k], ref[k], f"{name} {k} (every element)")
+
+
+def test_postnorm_backward_regrouped_empty_batch():
+    # M = 0: dB, dgamma and dbeta are zero, nothing else is touched
+    A = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    B = torch.randn(64, 256, device=DEV).to(torch.bfloat16)
+    C = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    G = torch.empty(0, 128, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(256, 128, device=DEV).to(torch.bfloat16)
+    got = fn.gemm_postnorm_backward_regrouped(G, W, A, B, C, torch.empty(0, device=DEV), "layernorm")
+    fn.check_status(DEV)
+    assert got["dA"].shape == (0, 64) and torch.all(got["dB"] == 0)
+    assert torch.all(got["dgamma"] == 0) and torch.all(got["dbeta"] == 0)
