@@ -454,6 +454,42 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     fn.check_status(DEV)
 
 
+def test_grid_exchange_timeout_is_reported_and_context_survives():
+    # The grid exchange's counter of row block 0 starts at 1 instead of 0, so
+    # it can never read its target: the polling lane's bounded wait runs out,
+    # every CTA stops, the call reports a timeout, the last CTA still zeroes
+    # the counters, and the context and the workspace stay usable.
+    M, N, K = 256, 2048, 64
+    w, d = _case("cfg4_n4096_ln", 37, M=M, N=N, K=K)
+    A, B = _dev(d["A"]), _dev(d["B"])
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    size = fn.postnorm_workspace_size(M, N)
+    ws = torch.zeros(size, dtype=torch.uint8, device=DEV)
+    ws[256:264].view(torch.int64).fill_(1)  # the first row block's counter, after the 256-byte header
+
+    def call():
+        st = fn.lib().fnorm_gemm_postnorm_ws(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, 1, None, None,
+                                             w.eps, 0, 1e-6, None, None, None, ws.data_ptr(), size,
+                                             torch.cuda.current_stream(DEV).cuda_stream)
+        assert st == 0
+
+    fn.set_wait_limit_ns(20_000_000)
+    try:
+        call()
+        with pytest.raises(fn.FnormError) as e:
+            fn.check_status(DEV)
+        assert e.value.status == fn.TIMEOUT
+    finally:
+        fn.set_wait_limit_ns(0)
+    fn.check_status(DEV)                            # cleared
+    assert torch.count_nonzero(ws[:256 + 8 * 2]) == 0  # the finish count and both row blocks' counters were
+                                                    # zeroed on the way out
+    call()                                          # the same workspace serves the next call
+    fn.check_status(DEV)
+    ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", None, None, w.eps)
+    assert_out_close(C, ref["C"], "grid exchange after a timeout")
+
+
 def test_stream_and_graph_capture():
     # calls run on the caller's stream and replay from a CUDA graph
     w, d = _case("cfg2_n128", 31, M=512, N=128, K=1024)
