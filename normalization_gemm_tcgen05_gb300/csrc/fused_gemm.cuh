@@ -592,24 +592,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
   constexpr bool PAIRS = PRE && !POST && !CLUSTER && !SPILL;
   constexpr int RUN = 4;
   const int full_rounds = PAIRS && ngroups > 1 ? total / (RUN * ncl) : 0;
-  // The A^T GEMMs (a weight gradient: a reduction over the long M) take
-  // their tiles in bands of BAND_W column groups.  Each tile streams a column
-  // slab of A (K x 128) and of B (K x BN) from end to end; in row-major order
-  // a wave of tiles spans every column group and reads every B slab from DRAM
-  // again.  In bands, a wave covers about grid / BAND_W row blocks of one band
-  // and the next wave the band's remaining row blocks, whose B slabs are the
-  // same and can still be in L2.
-  constexpr int BAND_W = 8;
-  auto band = [&](int u) -> int {
-    if (!AT || ngroups <= BAND_W || u >= total) return u;
-    const int per = num_m * BAND_W;
-    const int b = u / per, r = u % per;
-    const int w = min(BAND_W, ngroups - b * BAND_W);
-    return (r / w) * ngroups + b * BAND_W + r % w;
-  };
   auto tile_of = [&](int k) -> int {
     if (k < RUN * full_rounds) return RUN * ((k / RUN) * ncl + cid) + (k % RUN);
-    return band(RUN * full_rounds * ncl + cid + (k - RUN * full_rounds) * ncl);
+    return RUN * full_rounds * ncl + cid + (k - RUN * full_rounds) * ncl;
   };
   // The per-row statistics multiply by 1/N and 1/K (correctly rounded
   // reciprocals: exact, as a division would be, whenever N and K are powers
@@ -719,7 +704,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         for (int s = 0; s < S && ok; ++s) {
           // (CTA pair: this CTA's half of the tile's B columns)
           const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + (CTA2 ? prank * Cfg::BNS : 0);
-          for (int kb = 0; kb < num_kb; ++kb) {
+          for (int kj = 0; kj < num_kb; ++kj) {
+            // The A^T GEMMs (weight gradients: a reduction over the long M)
+            // walk the reduction backwards on every other tile of the CTA,
+            // i.e. every other wave of the grid.  Each tile streams a column
+            // slab of A and of B from end to end, so a wave that starts where
+            // the previous one ended finds those k-blocks still in L2 (the
+            // MMA's accumulate flag follows the loop order, not kb)
+            const int kb = (AT && (k & 1)) ? num_kb - 1 - kj : kj;
             // (CTA pair: the stage is released by rank 0's MMA commit)
             if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
               ok = false;

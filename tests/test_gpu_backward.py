@@ -129,9 +129,11 @@ def test_prenorm_backward_full_size():
 # ----------------------------------------------------------------------------
 @pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", [(256, 128, 512), (200, 72, 136), (128, 520, 64), (1000, 256, 1000),
-                                   # A^T with more than 8 column groups: tiles in bands of 8, the
-                                   # last band narrower (12 groups; 17 groups, a band of one)
-                                   (1160, 2824, 136), (640, 4104, 64)],
+                                   # A^T with more than 8 column groups (12, 17)
+                                   (1160, 2824, 136), (640, 4104, 64),
+                                   # A^T with more tiles than SMs (160): second tiles walk the
+                                   # reduction backwards, starting on the ragged last k-block
+                                   (2048, 2560, 200)],
                          ids=lambda v: str(v))
 def test_gemm_transposed(M, N, K, ta, tb):
     rng = np.random.default_rng(M + N + K + 2 * ta + tb)
