@@ -153,8 +153,14 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
  *   and count in on the row block's counter; each tile then combines all of
  *   them in tile order (so every tile of a row derives the same statistics)
  *   and normalises itself straight from the fp32 accumulator.  Nothing is
- *   written to C before it is normalised.  The kernel is a cooperative launch
- *   (all its CTAs co-resident); a row of more tiles than the device has SMs
+ *   written to C before it is normalised.  All CTAs of the kernel must be
+ *   resident at once: the grid never exceeds what the device holds at a
+ *   time.  For more than one row block the tiles of two neighbouring row
+ *   blocks share B over a 2-CTA cluster (fnorm_set_b_multicast), a plain
+ *   cluster launch whose CTAs are all resident once the kernels before it in
+ *   the stream have finished; work on other streams that holds SMs past the
+ *   wait limit makes the call end in FNORM_ERR_TIMEOUT.  The one-CTA form is
+ *   a cooperative launch.  A row of more tiles than the device has SMs
  *   (N > 256 * SMs) or more than 2^21 rows take fnorm_gemm_postnorm's spill
  *   layout instead, as do rows of at most 1024 columns, which need no
  *   workspace.
@@ -448,8 +454,11 @@ fnorm_status_t fnorm_rmsnorm_backward(const fnorm_bf16* dY, const fnorm_bf16* X,
 /*
  * fnorm_check_status — synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns FNORM_ERR_TIMEOUT if a kernel
- * gave up on a bounded wait since the last check, FNORM_ERR_CUDA if the
- * stream reported an error, else FNORM_OK.
+ * gave up on a bounded wait since the last check; FNORM_ERR_CUDA if the
+ * stream reported an error, or if a clustered kernel ran in a cluster of
+ * another size than it was launched with (it then returns at once and
+ * writes nothing: profilers that replay a cooperative launch drop its
+ * clusters); else FNORM_OK.
  */
 fnorm_status_t fnorm_check_status(void* stream);
 
@@ -511,8 +520,7 @@ fnorm_status_t fnorm_set_pair_mma(int mode);
  * into both CTAs' shared memory with one TMA multicast (a third less read
  * from L2 per SM).  mode: 1 = whenever the tile is 256 columns wide and B is
  * not resident; 0 = never; -1 = automatic, the default (the same, for more
- * than one row block, except the grid exchange of fnorm_gemm_postnorm_ws,
- * which keeps one-CTA tiles unless the mode is 1).  It changes the schedule, not the arithmetic: every
+ * than one row block).  It changes the schedule, not the arithmetic: every
  * output is the same sum in the same order as with one-CTA tiles.
  * Process-wide.  Any other mode returns FNORM_ERR_INVALID_ARG.
  */
@@ -527,6 +535,17 @@ fnorm_status_t fnorm_set_b_multicast(int mode);
  * to [1e3, 1e10].
  */
 fnorm_status_t fnorm_debug_wait_timeout(uint64_t limit_ns, void* stream);
+
+/*
+ * fnorm_debug_cluster_shape — self test of the check every clustered kernel
+ * makes at entry.  Launches a small kernel that expects clusters of two CTAs
+ * in clusters of `cluster` CTAs (1 or 2; anything else is
+ * FNORM_ERR_INVALID_ARG).  With 2 the check passes; with 1 it records the
+ * mismatch in the device status word, which fnorm_check_status(stream) then
+ * reports as FNORM_ERR_CUDA.  The kernel performs no cluster operation
+ * either way.
+ */
+fnorm_status_t fnorm_debug_cluster_shape(int cluster, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fnorm_version(void);

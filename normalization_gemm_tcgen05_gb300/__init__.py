@@ -42,7 +42,7 @@ __all__ = [
     "gemm_add_postnorm",
     "fold_prenorm_affine", "prenorm_gemm", "add_rownorm", "rmsnorm",
     "layernorm", "check_status", "set_wait_limit_ns", "postnorm_plan", "set_postnorm_cluster", "set_pair_mma", "set_b_multicast",
-    "debug_wait_timeout", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
+    "debug_wait_timeout", "debug_cluster_shape", "last_error", "version", "RMSNORM", "LAYERNORM", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -104,6 +104,7 @@ _SIGNATURES = {
     "fnorm_set_pair_mma": (_c_status, [ctypes.c_int]),
     "fnorm_set_b_multicast": (_c_status, [ctypes.c_int]),
     "fnorm_debug_wait_timeout": (_c_status, [ctypes.c_uint64, _p]),
+    "fnorm_debug_cluster_shape": (_c_status, [ctypes.c_int, _p]),
     "fnorm_version": (ctypes.c_int, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -641,6 +642,13 @@ def set_b_multicast(mode: int) -> None:
     """When 256-column tiles share B over a 2-CTA cluster (TMA multicast): -1 automatic, 0 never,
     1 always (see fnorm_set_b_multicast)."""
     _check(lib().fnorm_set_b_multicast(int(mode)))
+
+
+def debug_cluster_shape(cluster: int, device=None) -> None:
+    """Launch the cluster-shape self test (see fnorm_debug_cluster_shape)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().fnorm_debug_cluster_shape(int(cluster), _stream(dev)))
 
 
 def debug_wait_timeout(limit_ns: int = 50_000_000, device=None) -> None:

@@ -605,6 +605,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
   const WaitCtx wc{p.wait_limit_ns, p.status, &aux->abort_flag};
 
+  // a clustered kernel run in a cluster of any other size only reports it
+  if ((CLUSTER || PAIR) && !cluster_shape_ok(static_cast<uint32_t>(PAIR ? 2 : C), p.status)) return;
+
   // ---------------- set-up ----------------
   if (warp == 0) {
     // the barriers, initialised by the 32 lanes of warp 0 in parallel

@@ -105,15 +105,23 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if (pdl_enabled() && !Cfg::GX) {
+  // The grid exchange waits on other CTAs, so all of them must be resident at
+  // once: the grid never exceeds what the device holds at a time (one CTA
+  // per SM, or the co-resident clusters).  The one-CTA form is a cooperative
+  // launch, which also guarantees it.  The clustered form (B multicast) is a
+  // plain cluster launch: profilers replay a cooperative launch of clusters
+  // without its clusters.  Its CTAs are all resident once any kernel before
+  // it has finished (which its first global access waits for anyway), and a
+  // wait that still runs out is reported as a timeout.
+  constexpr bool kCoop = Cfg::GX && !Cfg::PAIR;
+  if (pdl_enabled() && !kCoop) {
     // the kernel's set-up may overlap the previous grid; its first global
     // access waits for that grid (griddepcontrol.wait)
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
     ++cfg.numAttrs;
   }
-  if (Cfg::GX) {
-    // the grid exchange waits on other CTAs: all of them must be resident
+  if (kCoop) {
     attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
     attr[cfg.numAttrs].val.cooperative = 1;
     ++cfg.numAttrs;
@@ -166,12 +174,11 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tr, p);
   if (e != cudaSuccess && Cfg::GX && Cfg::PAIR &&
-      (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration ||
-       e == cudaErrorCooperativeLaunchTooLarge)) {
-    // a cooperative launch of clusters refused before anything ran: the
-    // caller takes the one-CTA grid exchange
+      (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration)) {
+    // a clustered grid exchange refused before anything ran: the caller
+    // takes the one-CTA grid exchange
     (void)cudaGetLastError();
-    set_error("cooperative launch of a clustered grid exchange not available: %s", cudaGetErrorString(e));
+    set_error("clustered grid exchange not available: %s", cudaGetErrorString(e));
     return FNORM_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");

@@ -135,5 +135,6 @@ fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const floa
 fnorm_status_t launch_fused_transposed(const FusedLaunch& L);   // plain GEMM with A^T and/or B^T operands
 
 fnorm_status_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+fnorm_status_t launch_cluster_shape_selftest(int cluster, cudaStream_t stream);
 
 }  // namespace fnorm

@@ -15,6 +15,9 @@ namespace fnorm {
 // --------------------------------------------------------------------------
 enum : uint32_t {
   kStatusTimeout = 1u,
+  // a clustered kernel found itself in a cluster of another size and did
+  // nothing (a launch path that dropped the cluster shape)
+  kStatusClusterShape = 2u,
   // bits 8..15: role that timed out first (see WaitSite)
 };
 
@@ -445,6 +448,24 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
+// True if this CTA runs in a cluster of `want` CTAs.  Otherwise thread 0
+// records kStatusClusterShape in the status word and the caller must return
+// before any cluster operation: a multicast, remote arrival or cluster
+// barrier would address CTAs that do not exist.  (Profilers that replay a
+// cooperative launch run it without its clusters.)  Every CTA of a grid sees
+// the same size, so the whole grid takes the same branch.
+__device__ __forceinline__ bool cluster_shape_ok(uint32_t want, uint32_t* status) {
+  if (cluster_nctarank() == want) return true;
+  if (threadIdx.x == 0 && status != nullptr) atomicOr(status, kStatusClusterShape);
+  return false;
 }
 
 // whole-cluster barrier; not .aligned, so threads of a warp may reach it apart

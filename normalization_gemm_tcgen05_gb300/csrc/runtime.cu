@@ -193,6 +193,35 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* status, unsigned long lon
   __syncthreads();
 }
 
+// --------------------------------------------------------------------------
+// self test of the cluster-shape check: a kernel that expects clusters of two
+// CTAs, launched in clusters of `cluster` CTAs; it performs no cluster
+// operation of any kind, whatever the check answers
+// --------------------------------------------------------------------------
+__global__ void cluster_shape_selftest_kernel(uint32_t* status) {
+  if (!cluster_shape_ok(2u, status)) return;
+}
+
+fnorm_status_t launch_cluster_shape_selftest(int cluster, cudaStream_t stream) {
+  DeviceInfo dev;
+  fnorm_status_t st = current_device(&dev);
+  if (st != FNORM_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(4, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_shape_selftest_kernel, dev.status);
+  if (e != cudaSuccess) return cuda_fail(e, "cluster_shape_selftest_kernel launch");
+  return FNORM_OK;
+}
+
 fnorm_status_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
   DeviceInfo dev;
   fnorm_status_t st = current_device(&dev);
@@ -216,6 +245,11 @@ fnorm_status_t read_and_clear_status(cudaStream_t stream) {
     const uint32_t zero = 0;
     e = cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    if (word & kStatusClusterShape) {
+      set_error("a clustered kernel ran in a cluster of another size and wrote nothing (status 0x%08x); "
+                "a launch path dropped its cluster shape", word);
+      return FNORM_ERR_CUDA;
+    }
     static const char* sites[] = {"?", "TMA producer", "MMA issuer", "epilogue", "norm warps",
                                   "cluster statistics exchange", "teardown drain", "self test"};
     const uint32_t site = (word >> 8) & 0xFFu;

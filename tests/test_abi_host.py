@@ -317,6 +317,11 @@ def test_wait_limit_setter(L):
     assert L.fnorm_set_wait_limit_ns(0) == 0
 
 
+def test_cluster_shape_self_test_rejects_bad_sizes(L):
+    for bad in (0, 3, -1, 8):
+        assert L.fnorm_debug_cluster_shape(bad, None) == 1
+
+
 def test_product_path_has_no_fallback():
     # the binding must fail loudly when the library cannot be loaded
     import normalization_gemm_tcgen05_gb300 as fn

@@ -454,6 +454,25 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     fn.check_status(DEV)
 
 
+def test_cluster_shape_check_is_reported_and_context_survives():
+    # every clustered kernel first checks that it runs in clusters of the size
+    # it expects (a launch path can drop the cluster shape: profilers replay
+    # a cooperative launch without its clusters); a mismatch is recorded and
+    # the kernel returns before any cluster operation
+    fn.debug_cluster_shape(2, DEV)                  # the expected shape: nothing recorded
+    fn.check_status(DEV)
+    fn.debug_cluster_shape(1, DEV)                  # clusters of one CTA where two are expected
+    with pytest.raises(fn.FnormError) as e:
+        fn.check_status(DEV)
+    assert e.value.status == fn.CUDA_ERROR
+    assert "cluster" in str(e.value)
+    fn.check_status(DEV)                            # cleared
+    w, d = _case("cfg1", 31, M=384, N=256, K=64)    # a clustered GEMM (B multicast) still runs
+    C = fn.gemm(_dev(d["A"]), _dev(d["B"]))
+    assert_out_close(C, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])))
+    fn.check_status(DEV)
+
+
 def test_grid_exchange_timeout_is_reported_and_context_survives():
     # The grid exchange's counter of row block 0 starts at 1 instead of 0, so
     # it can never read its target: the polling lane's bounded wait runs out,
