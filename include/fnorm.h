@@ -512,9 +512,11 @@ fnorm_status_t fnorm_set_postnorm_cluster(int cluster_size);
 fnorm_status_t fnorm_set_pair_mma(int mode);
 
 /*
- * fnorm_set_b_multicast — choose when fnorm_gemm, fnorm_lazy_prenorm_gemm,
- * fnorm_prenorm_gemm and the grid exchange of fnorm_gemm_postnorm_ws share
- * B between the two CTAs of a 2-CTA cluster along M: the CTAs compute the
+ * fnorm_set_b_multicast — choose when fnorm_gemm, fnorm_gemm_ex,
+ * fnorm_lazy_prenorm_gemm, fnorm_prenorm_gemm, the plain GEMMs of the
+ * backward entry points (dA, dB) and the grid exchange of
+ * fnorm_gemm_postnorm_ws share B between the two CTAs of a 2-CTA cluster
+ * along M: the CTAs compute the
  * tiles of two neighbouring 128-row blocks at the same 256 columns, each
  * with its own one-CTA MMAs, and each loads half of every k-block's B tile
  * into both CTAs' shared memory with one TMA multicast (a third less read

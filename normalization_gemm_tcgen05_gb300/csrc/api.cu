@@ -220,7 +220,7 @@ fnorm_status_t fnorm_gemm_ex(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf1
   FusedLaunch L = base_launch(A, B, C, M, N, K, stream);
   L.mode = (trans_a ? MODE_AT : 0) | (trans_b ? MODE_BT : 0);
   L.bn = fill_tile_n(M, N);
-  return launch_fused_transposed(L);
+  return want_mcb(M, L.bn, false) ? launch_fused_transposed_mcb(L) : launch_fused_transposed(L);
 }
 
 fnorm_status_t fnorm_lazy_prenorm_gemm(const fnorm_bf16* A, const fnorm_bf16* B, fnorm_bf16* C, int64_t M,
@@ -517,14 +517,14 @@ fnorm_status_t fnorm_lazy_prenorm_gemm_backward(const fnorm_bf16* A, const fnorm
     L.bn = fill_tile_n(M, K);
     L.X = A;
     L.rowcoef = rowcoef;
-    FN_TRY(launch_fused_backward(L));
+    FN_TRY(want_mcb(M, L.bn, false) ? launch_fused_transposed_mcb(L) : launch_fused_backward(L));
   }
   if (dB != nullptr) {
     // dB [K,N] = A^T @ dCs: a GEMM over M reading A^T straight from A
     FusedLaunch L = base_launch(A, dCs, dB, K, N, M, stream);
     L.mode = MODE_AT;
     L.bn = fill_tile_n(K, N);
-    FN_TRY(launch_fused_transposed(L));
+    FN_TRY(want_mcb(K, L.bn, false) ? launch_fused_transposed_mcb(L) : launch_fused_transposed(L));
   }
   return FNORM_OK;
 }

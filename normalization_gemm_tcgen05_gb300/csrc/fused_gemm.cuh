@@ -125,6 +125,7 @@ struct FusedParams {
   int M, N, K;
   int cluster;      // CTAs per cluster along N (1 without MODE_CLUSTER)
   int slices;       // S: BN-column slices per CTA and row block (1 unless MODE_SPILL)
+  int wave;         // tiles of one wave of one-CTA tiles (the SM count): the A^T GEMMs' k order
   float eps, pre_eps;
   const __nv_bfloat16* gamma;
   const __nv_bfloat16* beta;
@@ -195,7 +196,7 @@ struct Aux {
   alignas(16) float wgam[GW > 1 ? 8 : 1][GW];
   alignas(16) float wbet[GW > 1 ? 8 : 1][GW];  // (post-norm backward: -beta / gamma)
   alignas(16) float wigam[GWI > 1 ? 8 : 1][GWI];  // post-norm backward: 1 / gamma
-  float2 xstat[2][CLMAX > 0 ? CLMAX : 1][128];
+  float2 xstat[2][CLMAX > 0 ? CLMAX : 1][CLMAX > 0 ? 128 : 1];  // cluster exchange: the C CTAs' partials
 };
 
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
@@ -304,9 +305,9 @@ struct KCfg {
   static_assert(!DGRAD || HALF <= 128, "the dgrad holds a half tile of X in registers");
   static_assert(!CTA2 || (BN == 256 && !POST && !BRES && !RES && !BT && !AT && !DGRAD),
                 "two-CTA MMA: 256-column tiles of the plain and lazy pre-norm GEMMs");
-  static_assert(!MCB || (!CTA2 && (BN == 128 || BN == 256) && !CLUSTER && !SPILL && !BRES && !RES && !BT && !AT &&
-                         !DGRAD && (!POST || GX)),
-                "B multicast: the plain, lazy pre-norm and grid-exchange post-norm GEMMs");
+  static_assert(!MCB || (!CTA2 && (BN == 128 || BN == 256) && !CLUSTER && !SPILL && !BRES && !RES && (!POST || GX)),
+                "B multicast: the plain, transposed, lazy pre-norm, dgrad and grid-exchange post-norm GEMMs "
+                "(not the post-norm backward)");
 };
 
 // Spill layout: normalise in place `nrows` rows (r0..) of one 256-column slice
@@ -668,7 +669,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           tma_prefetch_l2_2d(&tmA, kb * BK, m0);
         }
         if (BT) {
-          tma_prefetch_l2_2d(&tmB, kb * BK, n0);
+          // (B multicast: this CTA's half of the B^T rows, the box it loads)
+          tma_prefetch_l2_2d(&tmB, kb * BK, n0 + (MCB ? prank * (BN / 2) : 0));
         } else {
           for (int c = 0; c < Cfg::BNS / 64; ++c) tma_prefetch_l2_2d(&tmB, n0 + c * 64, kb * BK);
         }
@@ -707,14 +709,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         for (int s = 0; s < S && ok; ++s) {
           // (CTA pair: this CTA's half of the tile's B columns)
           const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + (CTA2 ? prank * Cfg::BNS : 0);
+          // The A^T GEMMs (weight gradients: a reduction over the long M)
+          // walk the reduction backwards on every other wave of one-CTA
+          // tiles.  Each tile streams a column slab of A and of B from end to
+          // end, so a wave that starts where the previous one ended finds
+          // those k-blocks still in L2.  The direction is a function of the
+          // output tile alone (the wave of the even row block of its 256-row
+          // pair), so that both CTAs of a B-multicast pair walk the same
+          // k-blocks and every schedule sums each output in the same order
+          // (the MMA's accumulate flag follows the loop order, not kb).
+          const bool back = AT && ((((m0 / 256) * 2 * ngroups + t % ngroups) / p.wave) & 1);
           for (int kj = 0; kj < num_kb; ++kj) {
-            // The A^T GEMMs (weight gradients: a reduction over the long M)
-            // walk the reduction backwards on every other tile of the CTA,
-            // i.e. every other wave of the grid.  Each tile streams a column
-            // slab of A and of B from end to end, so a wave that starts where
-            // the previous one ended finds those k-blocks still in L2 (the
-            // MMA's accumulate flag follows the loop order, not kb)
-            const int kb = (AT && (k & 1)) ? num_kb - 1 - kj : kj;
+            const int kb = back ? num_kb - 1 - kj : kj;
             // (CTA pair: the stage is released by rank 0's MMA commit)
             if (!mbar_wait(wc, smem_u32(&aux->empty[stage]), phase ^ 1u, kSiteProducer)) {
               ok = false;
@@ -750,7 +756,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               const uint32_t sb = sa + A_BYTES;
               if (BT) {
                 // B^T: one K-major box of [BN n-rows x 64 k] from the [N, K] array
-                tma_load_2d(sb, &tmB, kb * BK, n0, full);
+                // (B multicast: this CTA's half of its rows, a [BN/2 x 64]
+                // box, into both CTAs at the same offset)
+                if (MCB)
+                  tma_load_2d_mc(sb + static_cast<uint32_t>(prank * (BN / 2) * 128), &tmB, kb * BK,
+                                 n0 + prank * (BN / 2), full, 0x3);
+                else
+                  tma_load_2d(sb, &tmB, kb * BK, n0, full);
               } else {
 #pragma unroll
                 for (int c = 0; c < Cfg::BNS / 64; ++c) {
@@ -962,30 +974,34 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     // in rank order; half 0 pushes, both halves wait and combine; returns
     // false if the wait gave up
     auto exchange = [&](float& part0, float& part1, int g, int xit) -> bool {
-      const int xp = xit & 1;
-      const uint32_t xb = smem_u32(&aux->xbar[xp]);
-      if (etid == 0) mbar_arrive_expect_tx(xb, static_cast<uint32_t>(C) * 128u * 8u);
-      if (h == 0) {
-        const uint32_t mine = smem_u32(&aux->xstat[xp][rank][row]);
-        for (int r2 = 0; r2 < C; ++r2) st_async_f32x2(mapa_shared(mine, r2), part0, part1, mapa_shared(xb, r2));
-      }
-      if (!mbar_wait_warp<true>(wc, xb, static_cast<uint32_t>(xit >> 1) & 1u, kSiteExchange)) return false;
-      float n_acc = 0.0f, m_acc = 0.0f, q_acc = 0.0f;
-      for (int r2 = 0; r2 < C; ++r2) {
-        const float2 v = aux->xstat[xp][r2][row];
-        const int nq = min(max(N - (g * C + r2) * cta_cols, 0), cta_cols);
-        if (NBWD) {
-          m_acc += v.x;
-          q_acc += v.y;
-        } else if (LN) {
-          combine_mean_m2(m_acc, q_acc, n_acc, v.x, v.y, static_cast<float>(nq));
-        } else {
-          q_acc += v.x;
+      if constexpr (!CLUSTER) {
+        return true;  // (no cluster: nothing to exchange, no exchange buffers)
+      } else {
+        const int xp = xit & 1;
+        const uint32_t xb = smem_u32(&aux->xbar[xp]);
+        if (etid == 0) mbar_arrive_expect_tx(xb, static_cast<uint32_t>(C) * 128u * 8u);
+        if (h == 0) {
+          const uint32_t mine = smem_u32(&aux->xstat[xp][rank][row]);
+          for (int r2 = 0; r2 < C; ++r2) st_async_f32x2(mapa_shared(mine, r2), part0, part1, mapa_shared(xb, r2));
         }
+        if (!mbar_wait_warp<true>(wc, xb, static_cast<uint32_t>(xit >> 1) & 1u, kSiteExchange)) return false;
+        float n_acc = 0.0f, m_acc = 0.0f, q_acc = 0.0f;
+        for (int r2 = 0; r2 < C; ++r2) {
+          const float2 v = aux->xstat[xp][r2][row];
+          const int nq = min(max(N - (g * C + r2) * cta_cols, 0), cta_cols);
+          if (NBWD) {
+            m_acc += v.x;
+            q_acc += v.y;
+          } else if (LN) {
+            combine_mean_m2(m_acc, q_acc, n_acc, v.x, v.y, static_cast<float>(nq));
+          } else {
+            q_acc += v.x;
+          }
+        }
+        part0 = (LN || NBWD) ? m_acc : q_acc;
+        part1 = q_acc;
+        return true;
       }
-      part0 = (LN || NBWD) ? m_acc : q_acc;
-      part1 = q_acc;
-      return true;
     };
 
     // residual: write R of iteration it2's tile into its accumulator buffer

@@ -30,7 +30,8 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
 
   // A [M,K] in [128 x 64] boxes (A^T source [K,M]: [64 x 64] boxes); B [K,N]
   // in [64 x 64] boxes, MN-major for the MMA (B^T source [N,K]: [BN x 64]
-  // boxes, K-major); C [M,N] in [32 x 32] store boxes (64-byte rows)
+  // boxes, K-major; with B multicast each CTA loads half of them, [BN/2 x 64]);
+  // C [M,N] in [32 x 32] store boxes (64-byte rows)
   CUtensorMap ta, tb, tc;
   if (Cfg::AT)
     st = encode_tmap_bf16_2d(&ta, L.A, (uint64_t)L.M, (uint64_t)L.K, (uint64_t)L.M * 2, 64, Cfg::BK,
@@ -40,7 +41,8 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
                              CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FNORM_OK) return st;
   if (Cfg::BT)
-    st = encode_tmap_bf16_2d(&tb, L.B, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.K * 2, Cfg::BK, Cfg::BN,
+    st = encode_tmap_bf16_2d(&tb, L.B, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.K * 2, Cfg::BK,
+                             Cfg::MCB ? Cfg::BN / 2 : Cfg::BN,
                              CU_TENSOR_MAP_SWIZZLE_128B);
   else
     st = encode_tmap_bf16_2d(&tb, L.B, (uint64_t)L.N, (uint64_t)L.K, (uint64_t)L.N * 2, 64, Cfg::BK,
@@ -64,6 +66,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.K = L.K;
   p.cluster = Cfg::CLUSTER ? L.cluster : 1;
   p.slices = Cfg::SPILL ? L.slices : 1;
+  p.wave = dev.num_sms;
   p.eps = L.eps;
   p.pre_eps = L.pre_eps;
   p.gamma = static_cast<const __nv_bfloat16*>(L.gamma);

@@ -133,6 +133,7 @@ fnorm_status_t launch_postnorm_backward_rows(const void* dC, const void* C, cons
 fnorm_status_t launch_rmsnorm_backward(const void* dY, const void* X, const float* rstd, void* dX, int M, int N,
                                        cudaStream_t stream);
 fnorm_status_t launch_fused_transposed(const FusedLaunch& L);   // plain GEMM with A^T and/or B^T operands
+fnorm_status_t launch_fused_transposed_mcb(const FusedLaunch& L);  // the same and the dgrad, B multicast
 
 fnorm_status_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 fnorm_status_t launch_cluster_shape_selftest(int cluster, cudaStream_t stream);

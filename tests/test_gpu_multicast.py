@@ -1,7 +1,9 @@
 """B shared by a 2-CTA cluster along M (TMA multicast): the same arithmetic as
 the one-CTA tiles, so every output and statistic must agree bit for bit, on
 row-block counts that pair up and on odd ones (the second CTA of the last
-cluster then has no rows), and match the fp64 oracle.
+cluster then has no rows), and match the fp64 oracle.  The forward GEMMs, the
+grid exchange, the transposed-operand GEMMs (B^T loaded as two half boxes,
+one per CTA) and the backward entry points.
 """
 import numpy as np
 import pytest
@@ -112,6 +114,37 @@ def test_grid_exchange_multicast_with_pre():
                                to_f64(d["beta"]), w.eps, pre_rmsnorm=True, pre_eps=w.pre_eps)
     assert_out_close(r1[0], ref["C"], "grid exchange with pre-norm C")
     assert_rstd_close(r1[1]["pre_rstd"], ref["pre_rstd"], "pre rstd")
+
+
+# The transposed-operand GEMMs, from their row-major sources: (M, N, K,
+# trans_a, trans_b), 256-column tiles, even and odd row-block counts, ragged K
+TRANSPOSED = [(2048, 4096, 320, True, False), (1288, 2560, 200, False, True), (1288, 2560, 136, True, True),
+              (1032, 3072, 64, True, False)]
+
+
+@pytest.mark.parametrize("M,N,K,ta,tb", TRANSPOSED, ids=lambda v: str(v))
+def test_transposed_gemm_multicast(M, N, K, ta, tb):
+    w = WORKLOADS["cfg3"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K), a_row_scale=False)
+    d = make_inputs(w, M + N + K + ta + 2 * tb)
+    A = (d["A"].t().contiguous() if ta else d["A"]).to(DEV)
+    B = (d["B"].t().contiguous() if tb else d["B"]).to(DEV)
+    c0, c1 = _both(lambda: fn.gemm_ex(A, B, trans_a=ta, trans_b=tb))
+    _equal(c0, c1, "transposed gemm")
+    assert_out_close(c1, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])), f"gemm_ex {M}x{N}x{K} {ta} {tb}")
+
+
+def test_lazy_prenorm_backward_multicast():
+    # dgrad [1288 x 2560] and wgrad [2560 x 1024]: both on 256-column tiles
+    M, N, K = 1288, 1024, 2560
+    w = WORKLOADS["prenorm_bwd"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+    d = make_inputs(w, 83)
+    Ad, Bd, dCd = d["A"].to(DEV), d["B"].to(DEV), d["dC"].to(DEV)
+    C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+    r0, r1 = _both(lambda: fn.lazy_prenorm_gemm_backward(Ad, Bd, C, dCd, rstd))
+    _equal(r0, r1, "lazy prenorm backward")
+    rA, rB, _ = oracle.lazy_prenorm_gemm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(d["dC"]), w.eps)
+    assert_out_close(r1[0], rA, "lazy prenorm backward dA")
+    assert_out_close(r1[1], rB, "lazy prenorm backward dB")
 
 
 def test_multicast_setter_rejects_bad_modes():
