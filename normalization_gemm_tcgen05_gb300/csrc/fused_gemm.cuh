@@ -269,12 +269,17 @@ struct KCfg {
   // waits on the single buffer within a tile (a narrow tile streams A at a
   // rate set by the bytes its ring keeps in flight), or the tile is a CTA
   // pair's (six stages measured 160 us against 169 us for five on an
-  // 8192 x 4096 x 4096 GEMM).
+  // 8192 x 4096 x 4096 GEMM).  Not for the post-norm backward's grid
+  // exchange, whose tiles are bound by an epilogue that stores as much as it
+  // reads: at 16384 x 4096 x 2048 its kernel took 212-215 us with two
+  // buffers and three stages, 252 us with one and four, 228 us with three or
+  // four buffers and three stages.
   static constexpr int stages_with(int bufs) {
     return (int)((kSmemLimit - 1024 - BRES_BYTES - kEpiWarps * bufs * kBoxBytes - AUX_BYTES) / STAGE_BYTES);
   }
   static constexpr int STG_BUFS =
-      ((stages_with(2) < 4 || NCH == 1 || CTA2) && stages_with(1) > stages_with(2) && stages_with(2) < kMaxStages)
+      ((stages_with(2) < 4 || NCH == 1 || CTA2) && stages_with(1) > stages_with(2) && stages_with(2) < kMaxStages &&
+       !(NBWD && GX))
           ? 1
           : 2;
   static constexpr uint32_t STG_BYTES = kEpiWarps * STG_BUFS * kBoxBytes;
@@ -893,8 +898,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     auto store_box = [&](const uint32_t (&w)[16], int col0, int m0) {
       const uint32_t sbase = stg + sbuf * kBoxBytes;
       if (lane == 0) {
-        if (Cfg::STG_BUFS == 2) bulk_wait_read<1>();  // the store that used this buffer has read it
-        else bulk_wait_read<0>();
+        // the store that last used this buffer, STG_BUFS stores ago, has read it
+        bulk_wait_read<Cfg::STG_BUFS - 1>();
       }
       __syncwarp();
       // row `lane` of the box: 16-byte chunk ch sits at chunk (ch ^ ((row >> 1) & 3))
@@ -912,7 +917,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (m0 + q * 32 < M) tma_store_2d(&tmC, sbase, col0, m0 + q * 32);
         bulk_commit();
       }
-      if (Cfg::STG_BUFS == 2) sbuf ^= 1u;
+      sbuf = sbuf + 1u == static_cast<uint32_t>(Cfg::STG_BUFS) ? 0u : sbuf + 1u;
     };
 
     // give an accumulator buffer back to the MMA issuer (CTA pair: on rank 0's

@@ -2,7 +2,8 @@
 
 Shapes are drawn at random (ragged M from 1 row up, N and K any multiple of 8)
 so that they land in every layout class: one CTA per row, resident clusters,
-the grid-wide exchange, resident B, ragged tails of every tile dimension.
+the grid-wide exchange, resident B, B multicast over 2-CTA clusters, the
+transposed operands, ragged tails of every tile dimension.
 Every output element and every row statistic is compared; the draws are
 fixed by the seeds, so a failure reproduces.
 """
@@ -26,15 +27,16 @@ def _shapes(seed, n):
             for _ in range(n)]
 
 
-FORMS = ["gemm", "prenorm", "post_ln", "post_rms", "pre_post_ln", "res_rms", "preaff_ln", "regrouped_ln"]
+FORMS = ["gemm", "prenorm", "post_ln", "post_rms", "pre_post_ln", "res_rms", "preaff_ln", "regrouped_ln", "gemm_ex",
+         "prenorm_bwd"]
 CASES = [(form, M, N, K) for i, form in enumerate(FORMS) for (M, N, K) in _shapes(100 + i, 12)]
 
 # the opt-in paths: two-CTA MMA, B multicast off and forced on, forced cluster sizes
 KNOBS = [("pair", 1), ("mcb", 0), ("mcb", 1), ("cluster", 2), ("cluster", 4)]
 KNOB_CASES = [(knob, v, form, M, N, K) for j, (knob, v) in enumerate(KNOBS)
-              for i, form in enumerate(("gemm", "prenorm", "post_ln", "post_rms"))
+              for i, form in enumerate(("gemm", "prenorm", "post_ln", "post_rms", "gemm_ex"))
               for (M, N, K) in _shapes(200 + 10 * j + i, 2)
-              if not (knob == "cluster" and form in ("gemm", "prenorm"))]
+              if not (knob == "cluster" and form in ("gemm", "prenorm", "gemm_ex"))]
 
 
 def _dev(t):
@@ -106,6 +108,27 @@ def _run(form, M, N, K):
         Cr, _, _ = oracle.prenorm_affine_gemm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", to_f64(d["gamma"]),
                                               to_f64(d["beta"]), w.eps)
         assert_out_close(C, Cr, what)
+    elif form == "gemm_ex":
+        # op(A) from an A^T source ([K, M]; M a multiple of 8) and/or op(B) from a B^T source ([N, K])
+        ta, tb = bool((seed >> 1) & 1) and M % 8 == 0, bool((seed >> 2) & 1)
+        w = WORKLOADS["cfg3"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K), a_row_scale=False)
+        d = make_inputs(w, seed)
+        A = d["A"].t().contiguous() if ta else d["A"]
+        B = d["B"].t().contiguous() if tb else d["B"]
+        C = fn.gemm_ex(_dev(A), _dev(B), trans_a=ta, trans_b=tb)
+        fn.check_status(DEV)
+        assert_out_close(C, oracle.gemm(to_f64(d["A"]), to_f64(d["B"])), f"{what} trans_a={ta} trans_b={tb}")
+    elif form == "prenorm_bwd":
+        w = WORKLOADS["prenorm_bwd"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+        d = make_inputs(w, seed)
+        Ad, Bd = _dev(d["A"]), _dev(d["B"])
+        C, rstd = fn.lazy_prenorm_gemm(Ad, Bd, w.eps, return_rstd=True)
+        dA, dB = fn.lazy_prenorm_gemm_backward(Ad, Bd, C, _dev(d["dC"]), rstd, need_dB=M % 8 == 0)
+        fn.check_status(DEV)
+        rA, rB, _ = oracle.lazy_prenorm_gemm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(d["dC"]), w.eps)
+        assert_out_close(dA, rA, what + " dA")
+        if dB is not None:
+            assert_out_close(dB, rB, what + " dB")
     else:
         J = 8 * (1 + (seed % 97))
         trans_w = bool(seed & 1)
