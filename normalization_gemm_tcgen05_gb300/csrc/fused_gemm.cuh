@@ -125,7 +125,7 @@ struct FusedParams {
   int M, N, K;
   int cluster;      // CTAs per cluster along N (1 without MODE_CLUSTER)
   int slices;       // S: BN-column slices per CTA and row block (1 unless MODE_SPILL)
-  int wave;         // tiles of one wave of one-CTA tiles (the SM count): the A^T GEMMs' k order
+  int wave;         // 256-row units of one wave of 2-CTA clusters (half the SMs): the A^T GEMMs' k order
   float eps, pre_eps;
   const __nv_bfloat16* gamma;
   const __nv_bfloat16* beta;
@@ -715,15 +715,16 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           // (CTA pair: this CTA's half of the tile's B columns)
           const int n0 = ((t % ngroups) * C + rank) * cta_cols + s * BN + (CTA2 ? prank * Cfg::BNS : 0);
           // The A^T GEMMs (weight gradients: a reduction over the long M)
-          // walk the reduction backwards on every other wave of one-CTA
-          // tiles.  Each tile streams a column slab of A and of B from end to
-          // end, so a wave that starts where the previous one ended finds
-          // those k-blocks still in L2.  The direction is a function of the
-          // output tile alone (the wave of the even row block of its 256-row
-          // pair), so that both CTAs of a B-multicast pair walk the same
-          // k-blocks and every schedule sums each output in the same order
-          // (the MMA's accumulate flag follows the loop order, not kb).
-          const bool back = AT && ((((m0 / 256) * 2 * ngroups + t % ngroups) / p.wave) & 1);
+          // walk the reduction backwards on every other wave of B-multicast
+          // clusters, their default schedule.  Each tile streams a column
+          // slab of A and of B from end to end, so a wave that starts where
+          // the previous one ended finds those k-blocks still in L2.  The
+          // direction is a function of the output tile alone (the wave that
+          // its 256-row unit and column group fall in), so that both CTAs of
+          // a pair walk the same k-blocks and one-CTA tiles sum each output
+          // in the same order (the MMA's accumulate flag follows the loop
+          // order, not kb).
+          const bool back = AT && ((((m0 / 256) * ngroups + t % ngroups) / p.wave) & 1);
           for (int kj = 0; kj < num_kb; ++kj) {
             const int kb = back ? num_kb - 1 - kj : kj;
             // (CTA pair: the stage is released by rank 0's MMA commit)

@@ -66,7 +66,7 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.K = L.K;
   p.cluster = Cfg::CLUSTER ? L.cluster : 1;
   p.slices = Cfg::SPILL ? L.slices : 1;
-  p.wave = dev.num_sms;
+  p.wave = dev.num_sms / 2 > 0 ? dev.num_sms / 2 : 1;
   p.eps = L.eps;
   p.pre_eps = L.pre_eps;
   p.gamma = static_cast<const __nv_bfloat16*>(L.gamma);
