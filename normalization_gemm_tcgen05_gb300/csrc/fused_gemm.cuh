@@ -453,20 +453,30 @@ __device__ __forceinline__ void scale_pack(const uint32_t (&r)[32], float a, uin
 }
 
 // Lazy pre-norm with folded affine: y = u * a + (colsum_n * c + bias_n) for
-// one 32-column subtile of which `nvalid` columns lie inside the row
-// (c = -mean * rstd for LayerNorm, 0 for RMSNorm).  colsum/bias are fp32,
-// 16-byte aligned, read as float4 broadcasts (every lane reads the same
-// columns); N is a multiple of 8, so a group of 4 is wholly in or out.
+// one 32-column subtile (c = -mean * rstd for LayerNorm, 0 for RMSNorm), whose
+// column sums and bias are held by the warp's lanes, four columns each (lane
+// l: columns 4l .. 4l + 3 of the half tile, zero past N), not read from
+// memory per subtile: column j of the subtile comes from lane src0 + j / 4 by
+// a shuffle.  Every lane of the warp must call it.
 template <bool HAS_CS>
-__device__ __forceinline__ void prenorm_pack(const uint32_t (&r)[32], float a, float c, const float* cs,
-                                             const float* bias, int nvalid, uint32_t (&w)[16]) {
+__device__ __forceinline__ void prenorm_pack_lanes(const uint32_t (&r)[32], float a, float c, const float4& cs4,
+                                                   const float4& bi4, bool has_bias, int src0, uint32_t (&w)[16]) {
   const uint64_t aa = f2(a, a), cc = f2(c, c);
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
+    const int src = src0 + (j >> 2);
     float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bb = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < nvalid) {
-      if (HAS_CS) sc = __ldg(reinterpret_cast<const float4*>(cs + j));
-      if (bias != nullptr) bb = __ldg(reinterpret_cast<const float4*>(bias + j));
+    if (HAS_CS) {
+      sc.x = __shfl_sync(0xffffffffu, cs4.x, src);
+      sc.y = __shfl_sync(0xffffffffu, cs4.y, src);
+      sc.z = __shfl_sync(0xffffffffu, cs4.z, src);
+      sc.w = __shfl_sync(0xffffffffu, cs4.w, src);
+    }
+    if (has_bias) {
+      bb.x = __shfl_sync(0xffffffffu, bi4.x, src);
+      bb.y = __shfl_sync(0xffffffffu, bi4.y, src);
+      bb.z = __shfl_sync(0xffffffffu, bi4.z, src);
+      bb.w = __shfl_sync(0xffffffffu, bi4.w, src);
     }
     const uint64_t y01 = f2_fma(f2u(r[j], r[j + 1]), aa, f2_fma(f2(sc.x, sc.y), cc, f2(bb.x, bb.y)));
     const uint64_t y23 = f2_fma(f2u(r[j + 2], r[j + 3]), aa, f2_fma(f2(sc.z, sc.w), cc, f2(bb.z, bb.w)));
@@ -1229,6 +1239,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
           if (lane >= 16) gbv = make_uint4(0u, 0u, 0u, 0u);
           if (src != nullptr && col < N) gbv = __ldg(reinterpret_cast<const uint4*>(src + col));
         }
+        // pre-norm with folded affine: this half's column sums and bias, four
+        // columns per lane, loaded while the tile's MMAs run (the epilogue
+        // hands them to the lanes by shuffles)
+        float4 cs4 = make_float4(0.f, 0.f, 0.f, 0.f), bi4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (AFF) {
+          const int col = c0h + 4 * lane;
+          if (4 * lane < HALF && col < N) {
+            if (PRE_LN) cs4 = __ldg(reinterpret_cast<const float4*>(p.colsum + col));
+            if (p.bias != nullptr) bi4 = __ldg(reinterpret_cast<const float4*>(p.bias + col));
+          }
+        }
         // dgrad, post-norm backward: this half's X values (and the forward
         // rstd of the row), loaded while the tile's MMAs run
         uint4 xv[(DGRAD || NBWD) ? NCH : 1][4];
@@ -1623,8 +1644,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
               } else if (AFF) {
                 // lazy pre-norm with folded affine: y = rstd * (u - mean * colsum_n) + bias_n
-                prenorm_pack<PRE_LN>(r[b], pre, -pre_mean * pre, p.colsum + col0,
-                                     p.bias == nullptr ? nullptr : p.bias + col0, N - col0, w);
+                prenorm_pack_lanes<PRE_LN>(r[b], pre, -pre_mean * pre, cs4, bi4, p.bias != nullptr, c * 8, w);
               } else {
                 scale_pack<PRE>(r[b], pre, w);
               }
