@@ -237,9 +237,12 @@ struct KCfg {
   static constexpr int NCH = HALF / 32;        // 32-column subtiles per half
   // 32-column subtiles loaded from TMEM per wait: the whole half when the
   // register budget allows (320 threads: 168 registers), else two (448
-  // threads: 128 registers; cluster exchange code needs the room too)
+  // threads: 128 registers; cluster exchange code needs the room too), or
+  // one where two do not divide the half (192-column tiles: three subtiles)
   static constexpr int LDB = (DGRAD || NBWD) ? 1  // (these also hold their X values)
-                             : (AUXW || ((CLUSTER || GX) && NCH > 2)) ? (NCH < 2 ? NCH : 2) : NCH;
+                             : (AUXW || ((CLUSTER || GX) && NCH > 2)) ? (NCH < 2 ? NCH : (NCH % 2 == 0 ? 2 : 1))
+                                                                       : NCH;
+  static_assert(NCH % LDB == 0, "the TMEM load batches cover the half tile exactly");
   static constexpr bool KEEP = (LDB == NCH);  // one TMEM read serves statistics and output
   static constexpr int CLMAX = CLUSTER ? CLMAX_ : 0;  // largest cluster the exchange buffers hold
   static constexpr int GB = (POST && !SPILL && !GX) ? BN : 1;  // gamma/beta kept in shared memory

@@ -152,6 +152,20 @@ def test_pre_and_post_in_one_kernel(norm):
     _post(w, d, norm, pre=True)
 
 
+# every one-CTA tile width with the norm warps present (pre-RMS + post-norm):
+# 64, 128, 192 (three 32-column subtiles per half, loaded one at a time) and
+# 256 columns, full and ragged
+PRE_POST1 = [64, 120, 128, 136, 184, 192, 200, 256]
+
+
+@pytest.mark.parametrize("N", PRE_POST1)
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+def test_pre_and_post_every_tile_width(norm, N):
+    w, d = _case("cfg5", 14 + N, M=1809, N=N, K=1312, b_std=1.0 / np.sqrt(1312))
+    assert fn.postnorm_plan(N)[0] == 1
+    _post(w, d, norm, pre=True)
+
+
 # ----------------------------------------------------------------------------
 # GEMM + post-norm over a cluster along N (DSMEM row-statistics exchange)
 # ----------------------------------------------------------------------------
