@@ -3,7 +3,9 @@
 Shapes are drawn at random (ragged M from 1 row up, N and K any multiple of 8)
 so that they land in every layout class: one CTA per row, resident clusters,
 the grid-wide exchange, resident B, B multicast over 2-CTA clusters, the
-transposed operands, ragged tails of every tile dimension.
+transposed operands, ragged tails of every tile dimension.  Every entry point
+of the path is drawn: the fused forward forms, the backward entry points, the
+allocation-free post-norm and the standalone comparison norms.
 Every output element and every row statistic is compared; the draws are
 fixed by the seeds, so a failure reproduces.
 """
@@ -28,7 +30,7 @@ def _shapes(seed, n):
 
 
 FORMS = ["gemm", "prenorm", "post_ln", "post_rms", "pre_post_ln", "res_rms", "preaff_ln", "regrouped_ln", "gemm_ex",
-         "prenorm_bwd"]
+         "prenorm_bwd", "postnorm_bwd", "rownorm", "add_rownorm", "noalloc_ln"]
 CASES = [(form, M, N, K) for i, form in enumerate(FORMS) for (M, N, K) in _shapes(100 + i, 12)]
 
 # the opt-in paths: two-CTA MMA, B multicast off and forced on, forced cluster sizes
@@ -129,6 +131,63 @@ def _run(form, M, N, K):
         assert_out_close(dA, rA, what + " dA")
         if dB is not None:
             assert_out_close(dB, rB, what + " dB")
+    elif form == "postnorm_bwd":
+        # the post-norm backward from a given dC (the unfused comparison path)
+        norm = "layernorm" if seed & 1 else "rmsnorm"
+        w = WORKLOADS["cfg4_n1024_ln" if norm == "layernorm" else "cfg4_n1024_rms"].scaled(M=M, N=N, K=K,
+                                                                                          b_std=1.0 / np.sqrt(K))
+        d = make_inputs(w, seed)
+        Ad, Bd, gd, bd = _dev(d["A"]), _dev(d["B"]), _dev(d["gamma"]), _dev(d["beta"])
+        dC = torch.from_numpy(np.random.default_rng(seed + 1).standard_normal((M, N), dtype=np.float32)).to(torch.bfloat16)
+        C, st = fn.gemm_postnorm(Ad, Bd, norm, gd, bd, w.eps, return_stats=True)
+        need = ("dA", "dB", "dgamma", "dbeta") if M % 8 == 0 else ("dA", "dgamma", "dbeta")
+        got = fn.gemm_postnorm_backward(Ad, Bd, C, _dev(dC), st["rstd"], norm, gd, bd, need=need)
+        fn.check_status(DEV)
+        ref = oracle.gemm_postnorm_backward(to_f64(d["A"]), to_f64(d["B"]), to_f64(dC), norm, to_f64(d["gamma"]),
+                                            to_f64(d["beta"]), w.eps)
+        for k in need + ("dH",):
+            assert_out_close(got[k], ref[k], f"{what} {norm} {k}")
+    elif form in ("rownorm", "add_rownorm"):
+        # the standalone norms (the unfused comparison kernels): M rows of N columns
+        norm = "layernorm" if seed & 1 else "rmsnorm"
+        rng = np.random.default_rng(seed)
+        X = torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32) * 3 + 0.5).to(torch.bfloat16)
+        R = torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32)).to(torch.bfloat16)
+        g = torch.from_numpy(1 + 0.1 * rng.standard_normal(N, dtype=np.float32)).to(torch.bfloat16)
+        b = torch.from_numpy(0.1 * rng.standard_normal(N, dtype=np.float32)).to(torch.bfloat16)
+        eps = 1e-5
+        if form == "rownorm":
+            if norm == "layernorm":
+                Y, st = fn.layernorm(_dev(X), _dev(g), _dev(b), eps, return_stats=True)
+                ref, mr, rr = oracle.layernorm(to_f64(X), to_f64(g), to_f64(b), eps)
+            else:
+                Y, rstd = fn.rmsnorm(_dev(X), _dev(g), eps, return_rstd=True)
+                st = {"rstd": rstd}
+                ref, rr = oracle.rmsnorm(to_f64(X), to_f64(g), None, eps)
+        else:
+            Y, st = fn.add_rownorm(_dev(X), _dev(R), norm, _dev(g), _dev(b) if norm == "layernorm" else None, eps,
+                                   return_stats=True)
+            S = to_f64(X) + to_f64(R)
+            if norm == "layernorm":
+                ref, mr, rr = oracle.layernorm(S, to_f64(g), to_f64(b), eps)
+            else:
+                ref, rr = oracle.rmsnorm(S, to_f64(g), None, eps)
+        fn.check_status(DEV)
+        assert_out_close(Y, ref, f"{what} {norm}")
+        assert_rstd_close(st["rstd"], rr, f"{what} {norm} rstd")
+    elif form == "noalloc_ln":
+        # the allocation-free entry point (its fixed grid-exchange workspace for rows past 1024 columns)
+        w = WORKLOADS["cfg4_n4096_ln"].scaled(M=M, N=N, K=K, b_std=1.0 / np.sqrt(K))
+        d = make_inputs(w, seed)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        rstd = torch.empty(M, dtype=torch.float32, device=DEV)
+        fn.gemm_postnorm_noalloc(_dev(d["A"]), _dev(d["B"]), out, "layernorm", _dev(d["gamma"]), _dev(d["beta"]), w.eps,
+                                 rstd_out=rstd)
+        fn.check_status(DEV)
+        ref = oracle.gemm_postnorm(to_f64(d["A"]), to_f64(d["B"]), "layernorm", to_f64(d["gamma"]), to_f64(d["beta"]),
+                                   w.eps)
+        assert_out_close(out, ref["C"], what)
+        assert_rstd_close(rstd, ref["rstd"], what + " rstd")
     else:
         J = 8 * (1 + (seed % 97))
         trans_w = bool(seed & 1)
