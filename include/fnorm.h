@@ -159,8 +159,13 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
  *   blocks share B over a 2-CTA cluster (fnorm_set_b_multicast), a plain
  *   cluster launch whose CTAs are all resident once the kernels before it in
  *   the stream have finished; work on other streams that holds SMs past the
- *   wait limit makes the call end in FNORM_ERR_TIMEOUT.  The one-CTA form is
- *   a cooperative launch.  A row of more tiles than the device has SMs
+ *   wait limit makes the call end in FNORM_ERR_TIMEOUT.  In particular, two
+ *   such calls running at the same time on different streams of one device
+ *   can each hold part of the GPU and wait for each other until that limit:
+ *   callers that overlap wide-row post-norms across streams should select
+ *   the one-CTA form with fnorm_set_b_multicast(0).  The one-CTA form is a
+ *   cooperative launch, which the driver starts only when all of its CTAs
+ *   fit.  A row of more tiles than the device has SMs
  *   (N > 256 * SMs) or more than 2^21 rows take fnorm_gemm_postnorm's spill
  *   layout instead, as do rows of at most 1024 columns, which need no
  *   workspace.
