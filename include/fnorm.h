@@ -154,18 +154,18 @@ fnorm_status_t fnorm_gemm_postnorm(const fnorm_bf16* A, const fnorm_bf16* B, fno
  *   them in tile order (so every tile of a row derives the same statistics)
  *   and normalises itself straight from the fp32 accumulator.  Nothing is
  *   written to C before it is normalised.  All CTAs of the kernel must be
- *   resident at once: the grid never exceeds what the device holds at a
- *   time.  For more than one row block the tiles of two neighbouring row
- *   blocks share B over a 2-CTA cluster (fnorm_set_b_multicast), a plain
- *   cluster launch whose CTAs are all resident once the kernels before it in
- *   the stream have finished; work on other streams that holds SMs past the
- *   wait limit makes the call end in FNORM_ERR_TIMEOUT.  In particular, two
- *   such calls running at the same time on different streams of one device
- *   can each hold part of the GPU and wait for each other until that limit:
- *   callers that overlap wide-row post-norms across streams should select
- *   the one-CTA form with fnorm_set_b_multicast(0).  The one-CTA form is a
- *   cooperative launch, which the driver starts only when all of its CTAs
- *   fit.  A row of more tiles than the device has SMs
+ *   resident at once, so it is a cooperative launch, which the driver
+ *   starts only when all of its CTAs fit; for more than one row block the
+ *   tiles of two neighbouring row blocks share B over a 2-CTA cluster
+ *   (fnorm_set_b_multicast).  Profilers that replay a cooperative launch of
+ *   clusters run it without its clusters; the kernel then writes nothing
+ *   and fnorm_check_status reports FNORM_ERR_CUDA.  With the environment
+ *   variable FNORM_PLAIN_GX_LAUNCH=1 (read once per process) the clustered
+ *   form is a plain cluster launch instead, which profilers replay as
+ *   launched; its CTAs are all resident once the kernels before it in the
+ *   stream have finished, but work on other streams that holds SMs past the
+ *   wait limit (another such call, for instance) makes it end in
+ *   FNORM_ERR_TIMEOUT.  A row of more tiles than the device has SMs
  *   (N > 256 * SMs) or more than 2^21 rows take fnorm_gemm_postnorm's spill
  *   layout instead, as do rows of at most 1024 columns, which need no
  *   workspace.

@@ -28,10 +28,10 @@
 //         of a row block, on any CTAs of the grid, publish their per-row
 //         partial statistics to a global workspace and count in on the row
 //         block's counter, then each combines all of them in tile order and
-//         normalises its tile from tensor memory (all CTAs resident at once:
-//         a cooperative launch, or a grid of the co-resident 2-CTA clusters
-//         that share B; the other accumulator buffer keeps the tensor cores
-//         busy meanwhile);
+//         normalises its tile from tensor memory (a cooperative launch, all
+//         CTAs resident at once, of one CTA per SM or of the co-resident
+//         2-CTA clusters that share B; the other accumulator buffer keeps the
+//         tensor cores busy meanwhile);
 //   * both at once: norm(rmsnorm(A) @ B);
 //   * residual: norm(A @ B + R), R written into the accumulator before the
 //     tile's MMAs accumulate onto it;
@@ -99,7 +99,7 @@ enum : int {
   MODE_AT = 1024,     // A operand MN-major: read from a row-major [K, M] array (A^T of an [M, K] matrix)
   MODE_DGRAD = 4096,  // RMSNorm backward epilogue: y = u + c[m] * X[m, n]
   // post-norm of rows wider than a cluster holds: the row statistics are
-  // exchanged grid-wide through global memory (all CTAs resident), each
+  // exchanged grid-wide through global memory (a cooperative launch), each
   // CTA keeping one 256-column tile in tensor memory while the row block's
   // other tiles, on any CTAs of the grid, publish theirs
   MODE_GX = 8192,

@@ -110,21 +110,23 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   cfg.numAttrs = 0;
   // The grid exchange waits on other CTAs, so all of them must be resident at
   // once: the grid never exceeds what the device holds at a time (one CTA
-  // per SM, or the co-resident clusters).  The one-CTA form is a cooperative
-  // launch, which also guarantees it.  The clustered form (B multicast) is a
-  // plain cluster launch: profilers replay a cooperative launch of clusters
-  // without its clusters.  Its CTAs are all resident once any kernel before
-  // it has finished (which its first global access waits for anyway), and a
-  // wait that still runs out is reported as a timeout.
-  constexpr bool kCoop = Cfg::GX && !Cfg::PAIR;
-  if (pdl_enabled() && !kCoop) {
+  // per SM, or the co-resident clusters), and the launch is cooperative, so
+  // that the driver starts it only when all of its CTAs fit, whatever runs
+  // on other streams.  FNORM_PLAIN_GX_LAUNCH=1 makes the clustered form (B
+  // multicast) a plain cluster launch with programmatic stream
+  // serialisation: profilers replay a cooperative launch of clusters without
+  // its clusters (the kernel then reports the mismatch and does nothing).  A
+  // plain launch's CTAs are all resident once the kernels before it in the
+  // stream have finished, unless work on other streams holds SMs.
+  const bool coop = Cfg::GX && !(Cfg::PAIR && plain_cluster_grid_exchange());
+  if (pdl_enabled() && !coop) {
     // the kernel's set-up may overlap the previous grid; its first global
     // access waits for that grid (griddepcontrol.wait)
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
     ++cfg.numAttrs;
   }
-  if (kCoop) {
+  if (coop) {
     attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
     attr[cfg.numAttrs].val.cooperative = 1;
     ++cfg.numAttrs;
@@ -177,7 +179,8 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tr, p);
   if (e != cudaSuccess && Cfg::GX && Cfg::PAIR &&
-      (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration)) {
+      (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration ||
+       e == cudaErrorCooperativeLaunchTooLarge)) {
     // a clustered grid exchange refused before anything ran: the caller
     // takes the one-CTA grid exchange
     (void)cudaGetLastError();

@@ -30,6 +30,10 @@ int forced_postnorm_cluster();
 // programmatic dependent launch for every kernel of the library (environment
 // variable FNORM_PDL=0 turns it off)
 bool pdl_enabled();
+// FNORM_PLAIN_GX_LAUNCH=1: the clustered grid exchange as a plain cluster
+// launch instead of a cooperative one (for profilers that replay a
+// cooperative launch without its clusters)
+bool plain_cluster_grid_exchange();
 
 // 2-D row-major bf16 tensor map: `inner` elements per row (contiguous),
 // `outer` rows, `pitch_bytes` between rows; box of box_inner x box_outer.

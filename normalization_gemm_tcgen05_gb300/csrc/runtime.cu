@@ -132,6 +132,14 @@ bool pdl_enabled() {
   return on;
 }
 
+bool plain_cluster_grid_exchange() {
+  static const bool on = [] {
+    const char* v = getenv("FNORM_PLAIN_GX_LAUNCH");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
 // --------------------------------------------------------------------------
 // tensor maps
 // --------------------------------------------------------------------------
@@ -247,7 +255,8 @@ fnorm_status_t read_and_clear_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
     if (word & kStatusClusterShape) {
       set_error("a clustered kernel ran in a cluster of another size and wrote nothing (status 0x%08x); "
-                "a launch path dropped its cluster shape", word);
+                "a launch path dropped its cluster shape (profilers replay a cooperative launch of clusters "
+                "without them: set FNORM_PLAIN_GX_LAUNCH=1 when profiling)", word);
       return FNORM_ERR_CUDA;
     }
     static const char* sites[] = {"?", "TMA producer", "MMA issuer", "epilogue", "norm warps",
