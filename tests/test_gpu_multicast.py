@@ -147,6 +147,44 @@ def test_lazy_prenorm_backward_multicast():
     assert_out_close(r1[1], rB, "lazy prenorm backward dB")
 
 
+_PLAIN_GX_CHILD = """
+import sys, torch
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import normalization_gemm_tcgen05_gb300 as fn
+from workloads import WORKLOADS, make_inputs
+w = WORKLOADS["cfg4_n4096_ln"].scaled(M=1300, N=2048, K=192)
+d = make_inputs(w, 97)
+dev = torch.device("cuda", 0)
+C, st = fn.gemm_postnorm(d["A"].to(dev), d["B"].to(dev), "layernorm", d["gamma"].to(dev), d["beta"].to(dev), w.eps,
+                         return_stats=True)
+fn.check_status(dev)
+torch.save({{"C": C.cpu(), "rstd": st["rstd"].cpu(), "mean": st["mean"].cpu()}}, {out!r})
+"""
+
+
+def test_plain_cluster_grid_exchange_launch_matches(tmp_path):
+    # FNORM_PLAIN_GX_LAUNCH=1 (read once per process, so in a child process)
+    # launches the clustered grid exchange as a plain cluster launch, for
+    # profilers; the kernel is the same, so the results are bit for bit the
+    # default cooperative launch's
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = str(tmp_path / "plain.pt")
+    code = _PLAIN_GX_CHILD.format(root=root, tests=os.path.join(root, "tests"), out=out)
+    env = dict(os.environ, FNORM_PLAIN_GX_LAUNCH="1")
+    subprocess.run([sys.executable, "-c", code], env=env, check=True, timeout=600)
+    plain = torch.load(out)
+    w = WORKLOADS["cfg4_n4096_ln"].scaled(M=1300, N=2048, K=192)
+    d = make_inputs(w, 97)
+    C, st = fn.gemm_postnorm(d["A"].to(DEV), d["B"].to(DEV), "layernorm", d["gamma"].to(DEV), d["beta"].to(DEV),
+                             w.eps, return_stats=True)
+    fn.check_status(DEV)
+    assert torch.equal(C.cpu(), plain["C"]), "plain cluster launch differs from the cooperative launch"
+    assert torch.equal(st["rstd"].cpu(), plain["rstd"]) and torch.equal(st["mean"].cpu(), plain["mean"])
+
+
 def test_multicast_setter_rejects_bad_modes():
     for bad in (2, -2):
         with pytest.raises(fn.FnormError):
