@@ -36,7 +36,12 @@
  *     are launched with programmatic stream serialisation: their set-up may
  *     overlap the previous kernel in the stream, and every global memory
  *     access waits for that kernel to complete (environment variable
- *     FNORM_PDL=0 turns this off).
+ *     FNORM_PDL=0 turns this off), except the cooperative grid exchange.
+ *   - Profiling: profilers that replay a cooperative launch of clusters run
+ *     it without its clusters; set FNORM_PLAIN_GX_LAUNCH=1 when profiling
+ *     wide-row post-norms (fnorm_gemm_postnorm_ws).  Every clustered kernel
+ *     checks its cluster size first, so a mismatch is reported
+ *     (fnorm_check_status: FNORM_ERR_CUDA), never run.
  *   - A call returns FNORM_OK once its kernels are enqueued.  Argument errors
  *     return FNORM_ERR_INVALID_ARG and launch nothing; shapes the kernels do
  *     not implement return FNORM_ERR_UNSUPPORTED; CUDA launch errors return
