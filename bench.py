@@ -24,10 +24,11 @@ Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and torch.cuda.synchronize() on both sides and timed
 with CUDA events on the launching stream.  For the per-sub-workload
 comparison (latency_hidden) each leg (the fused call and the unfused pieces it
-is compared with) is then timed so in three rounds, the legs of a
-sub-workload back to back within a round, and reports its median round: the
-GPU runs at its power cap on the long legs, and legs compared with one
-another then see the same clocks.  Inputs and outputs rotate over R
+is compared with) is then timed so in six rounds, the legs of a
+sub-workload back to back within a round, in reverse order every other round,
+and reports its median round: the GPU runs at its power cap on the long legs,
+and legs compared with one another then see the same clocks (the alternating
+order cancels a drift of the clock within a round).  Inputs and outputs rotate over R
 copies whose total exceeds 2x the L2 cache, so no step reads what the previous
 one left in L2.  Under torchrun every rank runs the same per-GPU workload (weak
 scaling, independent replicas: rows of the path never interact) and the time
@@ -500,8 +501,10 @@ def time_graphs(graphs, stream, world: int, device) -> float:
 # For latency_hidden every leg of every sub-workload is then timed in ROUNDS
 # rounds, the legs of a sub-workload back to back within a round (so the
 # fused kernel and the unfused pieces it is compared with run in the same
-# thermal and power state of the GPU), and each leg reports its median round.
-ROUNDS = 3
+# thermal and power state of the GPU), in reverse order every other round (so
+# a drift of the clock within a round favours no leg), and each leg reports
+# its median round.
+ROUNDS = 6
 
 
 def run_ours(args, names, world, rank, local):
@@ -530,9 +533,9 @@ def run_ours(args, names, world, rank, local):
     rounds = [[[] for _ in range(5)] for _ in cases]
     with ClockSampler(local) as clk:
         step_t = [time_graphs(legs[k][0], stream, world, device) for k in range(len(cases))]
-        for _ in range(ROUNDS):
+        for r in range(ROUNDS):
             for k in range(len(cases)):
-                for j in range(5):
+                for j in (range(5) if r % 2 == 0 else range(4, -1, -1)):
                     rounds[k][j].append(time_graphs(legs[k][j], stream, world, device))
     del legs
     fn.check_status(device)
@@ -596,7 +599,8 @@ def run_ours(args, names, world, rank, local):
                    "sub_workloads": names, "l2": f"inputs/outputs rotate over >= 2x L2 ({l2 >> 20} MiB)",
                    "timing": f"CUDA graphs of K launches, CUDA events on the launching stream: the step once; "
                              f"for latency_hidden each leg of each sub-workload in {ROUNDS} rounds, the legs of a "
-                             f"sub-workload back to back in a round, the median round reported",
+                             f"sub-workload back to back in a round, in reverse order every other round, the "
+                             f"median round reported",
                    "parallelism": f"{world} independent replica(s)"},
         "roofline": roof,
         "latency_hidden": hidden,
