@@ -24,11 +24,12 @@ Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and torch.cuda.synchronize() on both sides and timed
 with CUDA events on the launching stream.  For the per-sub-workload
 comparison (latency_hidden) each leg (the fused call and the unfused pieces it
-is compared with) is then timed so in six rounds, the legs of a
-sub-workload back to back within a round, in reverse order every other round,
-and reports its median round: the GPU runs at its power cap on the long legs,
-and legs compared with one another then see the same clocks (the alternating
-order cancels a drift of the clock within a round).  Inputs and outputs rotate over R
+is compared with) is then timed as a graph of min(K, 20) launches in six
+rounds, the legs of a sub-workload back to back within a round, in reverse
+order every other round, and reports its median round: the GPU runs at its
+power cap on the long legs, and legs compared with one another then see the
+same clocks (short legs, and the alternating order, keep a drift of the clock
+within a round from favouring one leg).  Inputs and outputs rotate over R
 copies whose total exceeds 2x the L2 cache, so no step reads what the previous
 one left in L2.  Under torchrun every rank runs the same per-GPU workload (weak
 scaling, independent replicas: rows of the path never interact) and the time
@@ -503,8 +504,12 @@ def time_graphs(graphs, stream, world: int, device) -> float:
 # fused kernel and the unfused pieces it is compared with run in the same
 # thermal and power state of the GPU), in reverse order every other round (so
 # a drift of the clock within a round favours no leg), and each leg reports
-# its median round.
+# its median round.  The legs are graphs of LEG_LAUNCHES launches whatever K
+# is: a leg of a few hundred launches runs long enough for the clock to settle
+# differently under the power cap from one leg to the next, which the
+# comparison of per-launch times should not see.
 ROUNDS = 6
+LEG_LAUNCHES = 20
 
 
 def run_ours(args, names, world, rank, local):
@@ -528,16 +533,18 @@ def run_ours(args, names, world, rank, local):
     torch.cuda.synchronize()
     fn.check_status(device)
 
-    legs = [[build_graphs(f, K, stream) for f in (c.fused, c.gemm_only, c.norm_only, c.unfused_pipeline,
-                                                  c.cublas_gemm)] for c in cases]
+    KL = min(K, LEG_LAUNCHES)
+    steps = [build_graphs(c.fused, K, stream) for c in cases]
+    legs = [[build_graphs(f, KL, stream) for f in (c.fused, c.gemm_only, c.norm_only, c.unfused_pipeline,
+                                                   c.cublas_gemm)] for c in cases]
     rounds = [[[] for _ in range(5)] for _ in cases]
     with ClockSampler(local) as clk:
-        step_t = [time_graphs(legs[k][0], stream, world, device) for k in range(len(cases))]
+        step_t = [time_graphs(steps[k], stream, world, device) for k in range(len(cases))]
         for r in range(ROUNDS):
             for k in range(len(cases)):
                 for j in (range(5) if r % 2 == 0 else range(4, -1, -1)):
                     rounds[k][j].append(time_graphs(legs[k][j], stream, world, device))
-    del legs
+    del legs, steps
     fn.check_status(device)
     med = [[statistics.median(rounds[k][j]) for j in range(5)] for k in range(len(cases))]
     fused_t, gemm_t, norm_t, pipe_t, cub_t = ([med[k][j] for k in range(len(cases))] for j in range(5))
@@ -573,8 +580,8 @@ def run_ours(args, names, world, rank, local):
 
     hidden = {}
     for k, c in enumerate(cases):
-        tf, tg, tn, tp = fused_t[k] / K, gemm_t[k] / K, norm_t[k] / K, pipe_t[k] / K
-        tc = cub_t[k] / K
+        tf, tg, tn, tp = fused_t[k] / KL, gemm_t[k] / KL, norm_t[k] / KL, pipe_t[k] / KL
+        tc = cub_t[k] / KL
         b_k, a_k, p_k, _ = roofline_of(c.w, tf)
         hidden[c.w.name] = {
             "t_fused_us": round(tf * 1e6, 3), "t_gemm_us": round(tg * 1e6, 3), "t_norm_us": round(tn * 1e6, 3),
@@ -597,10 +604,10 @@ def run_ours(args, names, world, rank, local):
         "data": "synthetic: seeded inputs with the workload table's shapes and distributions",
         "config": {"workload": args.workload + ": " + GROUP_TEXT.get(args.workload, ""),
                    "sub_workloads": names, "l2": f"inputs/outputs rotate over >= 2x L2 ({l2 >> 20} MiB)",
-                   "timing": f"CUDA graphs of K launches, CUDA events on the launching stream: the step once; "
-                             f"for latency_hidden each leg of each sub-workload in {ROUNDS} rounds, the legs of a "
-                             f"sub-workload back to back in a round, in reverse order every other round, the "
-                             f"median round reported",
+                   "timing": f"CUDA graphs, CUDA events on the launching stream: the step once, K launches; "
+                             f"for latency_hidden each leg of each sub-workload as a graph of {KL} launches in "
+                             f"{ROUNDS} rounds, the legs of a sub-workload back to back in a round, in reverse "
+                             f"order every other round, the median round reported",
                    "parallelism": f"{world} independent replica(s)"},
         "roofline": roof,
         "latency_hidden": hidden,
