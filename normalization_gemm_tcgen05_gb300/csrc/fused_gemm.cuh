@@ -128,6 +128,7 @@ struct FusedParams {
   int cluster;      // CTAs per cluster along N (1 without MODE_CLUSTER)
   int slices;       // S: BN-column slices per CTA and row block (1 unless MODE_SPILL)
   int wave;         // 256-row units of one wave of 2-CTA clusters (half the SMs): the A^T GEMMs' k order
+  int l2_hints;     // the backward GEMMs' L2 policy: 0 none, 1 A evict_first, 2 and B evict_last
   float eps, pre_eps;
   const __nv_bfloat16* gamma;
   const __nv_bfloat16* beta;
@@ -723,6 +724,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (issuer) tma_load_2d(dst, m, c0, c1, bar);
         else tma_load_2d_pair(dst, m, c0, c1, bar);
       };
+      // The backward's GEMMs (the A^T weight gradients and the Lazy Pre-Norm
+      // data gradient) stream each A slab through one wave of tiles only,
+      // while every wave reads all of B.  With more than one wave their A
+      // loads go first out of L2, and B, where it fits, last, so that B
+      // stays for the next wave (l2_hints; evict_normal is the default).
+      constexpr bool HINT = AT || DGRAD;
+      const uint64_t pol_a = !HINT ? 0 : p.l2_hints >= 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_b = !HINT ? 0 : p.l2_hints >= 2 ? l2_policy_evict_last() : l2_policy_evict_normal();
       bool ok = true;
       for (int k = 0, t = tile_of(0); t < total && ok; t = tile_of(++k)) {
         const int m0 = (t / ngroups) * RB + prank * Cfg::BM;
@@ -768,8 +777,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
               load_pair(sa, &tmA, kb * BK, m0, full);
             } else if (AT) {
               // A^T: two MN-major chunks of [64 k-rows x 64 m] from the [K, M] array
-              tma_load_2d(sa, &tmA, m0, kb * BK, full);
-              tma_load_2d(sa + BK * 128, &tmA, m0 + 64, kb * BK, full);
+              tma_load_2d_hint(sa, &tmA, m0, kb * BK, full, pol_a);
+              tma_load_2d_hint(sa + BK * 128, &tmA, m0 + 64, kb * BK, full, pol_a);
+            } else if (HINT) {
+              tma_load_2d_hint(sa, &tmA, kb * BK, m0, full, pol_a);
             } else {
               tma_load_2d(sa, &tmA, kb * BK, m0, full);
             }
@@ -779,9 +790,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 // B^T: one K-major box of [BN n-rows x 64 k] from the [N, K] array
                 // (B multicast: this CTA's half of its rows, a [BN/2 x 64]
                 // box, into both CTAs at the same offset)
-                if (MCB)
+                if (MCB && HINT)
+                  tma_load_2d_mc_hint(sb + static_cast<uint32_t>(prank * (BN / 2) * 128), &tmB, kb * BK,
+                                      n0 + prank * (BN / 2), full, 0x3, pol_b);
+                else if (MCB)
                   tma_load_2d_mc(sb + static_cast<uint32_t>(prank * (BN / 2) * 128), &tmB, kb * BK,
                                  n0 + prank * (BN / 2), full, 0x3);
+                else if (HINT)
+                  tma_load_2d_hint(sb, &tmB, kb * BK, n0, full, pol_b);
                 else
                   tma_load_2d(sb, &tmB, kb * BK, n0, full);
               } else {
@@ -792,8 +808,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                   } else if (MCB) {
                     // this CTA's half of the tile's B boxes, into both CTAs
                     // (same offset; each CTA's full barrier counts all of B)
-                    if (c / (BN >= 128 ? BN / 128 : 1) == prank)
-                      tma_load_2d_mc(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, 0x3);
+                    if (c / (BN >= 128 ? BN / 128 : 1) == prank) {
+                      if (HINT)
+                        tma_load_2d_mc_hint(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, 0x3, pol_b);
+                      else
+                        tma_load_2d_mc(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, 0x3);
+                    }
+                  } else if (HINT) {
+                    tma_load_2d_hint(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full, pol_b);
                   } else {
                     tma_load_2d(sb + c * (BK * 128), &tmB, n0 + c * 64, kb * BK, full);
                   }

@@ -67,6 +67,14 @@ fnorm_status_t launch_cfg(const FusedLaunch& L) {
   p.cluster = Cfg::CLUSTER ? L.cluster : 1;
   p.slices = Cfg::SPILL ? L.slices : 1;
   p.wave = dev.num_sms / 2 > 0 ? dev.num_sms / 2 : 1;
+  {
+    // the backward GEMMs' L2 policy: none within one wave of tiles (no later
+    // wave re-reads B); else A evict_first, and B evict_last where it fits
+    // in half of L2
+    const int64_t tiles = (static_cast<int64_t>(L.M) + Cfg::BM - 1) / Cfg::BM *
+                          ((static_cast<int64_t>(L.N) + Cfg::BN - 1) / Cfg::BN);
+    p.l2_hints = tiles <= dev.num_sms ? 0 : static_cast<int64_t>(L.K) * L.N * 2 <= (int64_t{64} << 20) ? 2 : 1;
+  }
   p.eps = L.eps;
   p.pre_eps = L.pre_eps;
   p.gamma = static_cast<const __nv_bfloat16*>(L.gamma);
